@@ -1,0 +1,149 @@
+/*
+ * libfp8kv -- fp8 (E4M3) paged KV cache: quantise-on-append and single-query
+ * (decode) grouped-query attention, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources the operations follow (the FP8 KV-cache web pages):
+ *   [G] gpusmith.com, "FP8 KV Cache Quantization: Capacity Gains and Accuracy
+ *       Risk": "What FP8 KV changes" (E4M3, 1 byte/element, max normal 448),
+ *       "Scales and calibration" (divide by a per-tensor scale, then cast),
+ *       "Attention backend interactions" (the kernel must read fp8 directly,
+ *       dequantisation fused), "Why the KV cache sets long-context capacity"
+ *       (paged, block-granular cache).
+ *   [P] particula.tech, "KV Cache Quantization: What FP8 and q8_0 Cost in
+ *       Accuracy", opening section (partial results accumulate in real FP32
+ *       registers).
+ *   [V] phantomic12 summary of the vLLM FP8 KV-cache blog: "ACCURACY AT LONG
+ *       CONTEXT" (the P.V contraction runs over the context, >= 100K tokens),
+ *       "DECODE COST" (sliding windows of 128 and 512).
+ *
+ * Conventions for every entry point:
+ *   - All pointers except `stream` are DEVICE pointers owned by the caller.
+ *     The library allocates nothing, keeps no state between calls, and is
+ *     safe to call from several host threads.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  Nothing is synchronised.
+ *   - Invalid arguments return an error status and launch nothing.  A failed
+ *     launch returns FP8KV_ERR_CUDA.  Faults during execution surface at the
+ *     caller's next synchronisation, as for any CUDA kernel.
+ *   - bf16 means IEEE bfloat16 stored as 2-byte little-endian values.
+ */
+#ifndef FP8KV_H_
+#define FP8KV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8KV_OK = 0,
+    FP8KV_ERR_INVALID_ARG = 1, /* null pointer, bad size, non-finite/<=0 scale, misalignment */
+    FP8KV_ERR_UNSUPPORTED = 2, /* shape outside the supported set (see below)                */
+    FP8KV_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the required size         */
+    FP8KV_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed                 */
+    FP8KV_ERR_TIMEOUT = 5      /* a kernel gave up a bounded wait (read via fp8kv_read_error) */
+} fp8kv_status;
+
+/* Static, human-readable name of a status code. */
+const char* fp8kv_status_string(fp8kv_status status);
+
+/*
+ * Quantise-on-append [G "Scales and calibration"; G "What FP8 KV changes"].
+ *
+ * For every token t < num_tokens, kv head h and dim i:
+ *     code = E4M3( fp32(k_new[t][h][i]) / k_scale )     (same for V)
+ * with one IEEE fp32 division followed by one round-to-nearest-even,
+ * saturating-finite conversion (|x| >= 448 -> +-448, NaN -> NaN).  The code
+ * is written at slot s = slot_mapping[t] = block * block_size + offset:
+ *     k_cache[block][h][offset][i] = code.
+ *
+ *   k_new, v_new   bf16 [num_tokens][num_kv_heads][head_dim], contiguous,
+ *                  16-byte aligned
+ *   slot_mapping   int64 [num_tokens]; a negative slot skips the token (padding);
+ *                  a slot >= num_blocks * block_size is out of range and is
+ *                  skipped too (nothing is written for it)
+ *   k_cache,       uint8 E4M3 [num_blocks][num_kv_heads][block_size][head_dim]
+ *   v_cache        (one page = one (block, head) pair = block_size*head_dim
+ *                  contiguous bytes), 16-byte aligned
+ *   k_scale,       per-tensor scales, finite and > 0
+ *   v_scale
+ * Supported: head_dim % 16 == 0 and 16 <= head_dim <= 1024; block_size >= 1.
+ * num_tokens == 0 is a no-op.
+ */
+fp8kv_status fp8kv_quant_append(const void* k_new, const void* v_new,
+                                const int64_t* slot_mapping, int64_t num_tokens,
+                                uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks,
+                                int block_size, int num_kv_heads, int head_dim,
+                                float k_scale, float v_scale, void* stream);
+
+/*
+ * Workspace bytes fp8kv_paged_decode needs for this problem on the CURRENT
+ * device (the split-context plan depends on its SM count).  Returns 0 if the
+ * arguments are invalid or no device is available.
+ */
+size_t fp8kv_paged_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int max_seq_len, int block_size,
+                                         int window);
+
+/*
+ * Zero-fills a workspace (asynchronously on `stream`).  A workspace must be
+ * zero-filled once before its first fp8kv_paged_decode call; every call that
+ * completes leaves it ready for the next one.  Calls that share one workspace
+ * must be ordered (same stream or explicit dependencies).
+ */
+fp8kv_status fp8kv_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Reads (and clears) the workspace's error word: 0 = no error, otherwise an
+ * fp8kv_status (FP8KV_ERR_TIMEOUT, or FP8KV_ERR_INVALID_ARG for an
+ * out-of-range block id met on the device).  Synchronises `stream`.
+ */
+fp8kv_status fp8kv_read_error(void* workspace, uint32_t* code, void* stream);
+
+/*
+ * Paged fp8 decode attention [G "Attention backend interactions";
+ * V "ACCURACY AT LONG CONTEXT"; P opening section].
+ *
+ * For batch b, query head h (kv head hk = h / g, g = num_q_heads/num_kv_heads),
+ * with L = seq_lens[b] (the current token included) and the attended keys
+ * t in [lo, L), lo = (window > 0 && L > window) ? L - window : 0:
+ *     k^_t = decode(k_cache[page(t)][hk][t % bs][:]) * k_scale
+ *     v^_t = decode(v_cache[page(t)][hk][t % bs][:]) * v_scale
+ *     s_t  = sm_scale * sum_i q[b][h][i] * k^_t[i]
+ *     out[b][h][:] = sum_t exp(s_t - max s) v^_t / sum_t exp(s_t - max s)
+ * page(t) = block_tables[b][t / block_size].  Scores, the softmax and P.V are
+ * accumulated in FP32; split-context partial results are merged in FP32; the
+ * result is rounded to bf16 (RNE).  L == 0 writes zeros.
+ *
+ *   q              bf16 [batch][num_q_heads][head_dim], contiguous, 16-B aligned
+ *   k_cache,       uint8 E4M3 [num_blocks][num_kv_heads][block_size][head_dim],
+ *   v_cache        16-byte aligned (the layout fp8kv_quant_append writes)
+ *   block_tables   int32 [batch][max_blocks_per_seq]; entries past a sequence's
+ *                  last page are never read; an entry outside [0, num_blocks)
+ *                  is replaced by block 0 and reported via fp8kv_read_error
+ *   seq_lens       int32 [batch] on the device; each must satisfy
+ *                  0 <= seq_lens[b] <= min(max_seq_len, max_blocks_per_seq*block_size)
+ *   max_seq_len    host-side upper bound of seq_lens (sizes the split plan)
+ *   sm_scale       softmax scale (usually 1/sqrt(head_dim)); finite
+ *   window         <= 0: full attention; > 0: attend the last `window` keys
+ *   out            bf16 [batch][num_q_heads][head_dim], 16-byte aligned
+ *   workspace      >= fp8kv_paged_decode_workspace_size(...) bytes, 256-B
+ *                  aligned, zero-filled before first use (fp8kv_workspace_init)
+ * Supported: head_dim in {64, 128, 256}; block_size == 16;
+ *            g in {1, 2, 4, 8}; num_blocks * num_kv_heads < 2^31.
+ */
+fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                int64_t num_blocks, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* seq_lens,
+                                int max_seq_len, int batch, int num_q_heads, int num_kv_heads,
+                                int head_dim, int block_size, float k_scale, float v_scale,
+                                float sm_scale, int window, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8KV_H_ */
