@@ -1,0 +1,479 @@
+#!/usr/bin/env python
+"""fp8 paged decode attention benchmark (libfp8kv on GB300).
+
+One step = one decode step of one attention layer: fp8kv_quant_append of
+every sequence's newest K/V row into the paged E4M3 cache, then
+fp8kv_paged_decode over the whole cache (all steps of the hot path).  The
+default workload is the Llama-3.1-8B serving batch (32 q / 8 kv heads,
+head_dim 128, batch 8, contexts uniform in 18000..22000, block_size 16,
+shuffled physical blocks).
+
+Printed (rank 0, one JSON line): whole-step algorithmic GB/s and us/step, the
+roofline of the decode call against the measured HBM peak, an end-to-end
+number through host (pinned) buffers, SM clocks sampled during the timed
+region, and the CPU oracle timed on the host cores.
+
+Timing: W warm-up steps, then K timed steps; L2 is flushed (a 256 MiB device
+write) before every timed step, outside the events; CUDA events on the stream
+the library launches on; barrier + synchronize around the region; max over
+ranks.  With --gpus N > 1 (torchrun) every rank runs an independent replica
+(the path does not exchange data between GPUs).
+
+--impl reference times the CPU oracle (the only other implementation of this
+path) on the host cores, one bounded sample of the same workload per step.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from fp8_kv_cache_fp8kv_gb300 import accounting, workload  # noqa: E402
+
+METRIC = "fp8 paged decode attention: achieved HBM GB/s and % of GB300 peak; µs/decode step"
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 256 << 20
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["fp8kv", "reference"], default="fp8kv")
+    p.add_argument("--config", default="llama31_8b_b8_20k", choices=list(workload.CONFIGS))
+    p.add_argument("--window", type=int, default=None, help="default: the workload's first window")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    a = p.parse_args(argv)
+    a.warmup = max(3, a.warmup)
+    a.steps = max(1, a.steps)
+    return a
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, ws
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x, ws):
+    """Maximum of a float over ranks (every rank gets it)."""
+    if ws <= 1:
+        return float(x)
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- measurement helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBps", "hbm"):
+            if key in d:
+                return float(d[key]), "measured (MEASURED_PEAKS.json)"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 100 ms in a thread."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 5:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        scope = "during timed region"
+        if not inside:
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            inside = [p for _, p in near]
+            scope = "nearest samples (timed region shorter than the 100 ms sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "scope": "nvidia-smi unavailable"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "scope": scope}
+
+
+def traffic_for(kernel_key):
+    """DRAM bytes per launch recorded from an ncu capture of this kernel, if the
+    kernel source is unchanged since (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(kernel_key)
+    if not ent:
+        return None
+    if ent.get("source_sha256") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_kv_cache_fp8kv_gb300", "csrc")
+    for name in ("paged_decode.cu", "ptx.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# ---------------------------------------------------------------- the CUDA path
+
+class DecodeStep:
+    """Device state of one workload and one decode step through the C ABI."""
+
+    def __init__(self, w, window, device):
+        from fp8_kv_cache_fp8kv_gb300 import binding as fk
+        self.fk = fk
+        fk.load(build_if_missing=True)
+        s = w.shape
+        self.w, self.window, self.dev = w, window, device
+        shape = (w.num_blocks, s.num_kv_heads, workload.BLOCK_SIZE, s.head_dim)
+        self.k_cache = torch.zeros(shape, dtype=torch.uint8, device=device)
+        self.v_cache = torch.zeros(shape, dtype=torch.uint8, device=device)
+        fk.fp8kv_quant_append(w.k.to(device), w.v.to(device), w.slot_mapping.to(device),
+                              self.k_cache, self.v_cache, w.k_scale, w.v_scale)
+        rows = w.new_token_rows()
+        self.h_q = w.q.contiguous()
+        self.h_k_new = w.k[rows].contiguous()
+        self.h_v_new = w.v[rows].contiguous()
+        self.h_slots = w.slot_mapping[rows].contiguous()
+        self.q = self.h_q.to(device)
+        self.k_new = self.h_k_new.to(device)
+        self.v_new = self.h_v_new.to(device)
+        self.slots = self.h_slots.to(device)
+        self.block_tables = w.block_tables.to(device)
+        self.seq_lens = w.seq_lens.to(device)
+        self.out = torch.empty_like(self.q)
+        self.ws = fk.alloc_workspace(w.q.shape[0], s.num_q_heads, s.num_kv_heads, s.head_dim,
+                                     w.max_seq_len, 16, window, device=device)
+        torch.cuda.synchronize()
+
+    def append(self, k_new=None, v_new=None, slots=None):
+        self.fk.fp8kv_quant_append(self.k_new if k_new is None else k_new,
+                                   self.v_new if v_new is None else v_new,
+                                   self.slots if slots is None else slots,
+                                   self.k_cache, self.v_cache, self.w.k_scale, self.w.v_scale)
+
+    def decode(self, q=None, out=None):
+        self.fk.fp8kv_paged_decode(self.q if q is None else q, self.k_cache, self.v_cache,
+                                   self.block_tables, self.seq_lens, self.w.max_seq_len,
+                                   self.w.k_scale, self.w.v_scale, self.w.sm_scale, self.window,
+                                   self.out if out is None else out, self.ws)
+
+
+def run_fp8kv(args, rank, ws):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = workload.make_workload(args.config, seed=args.seed)
+    s = w.shape
+    window = s.windows[0] if args.window is None else args.window
+    lens = w.seq_lens.tolist()
+    B = len(lens)
+    dec_bytes = accounting.decode_bytes(lens, s.num_q_heads, s.num_kv_heads, s.head_dim, window)
+    app_bytes = accounting.append_bytes(B, s.num_kv_heads, s.head_dim)
+    step_bytes = dec_bytes + app_bytes
+    st = DecodeStep(w, window, dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    clocks = ClockSampler(torch.cuda.current_device()) if not args.no_clocks else None
+    if clocks:
+        clocks.start()
+    for _ in range(args.warmup):
+        st.append()
+        st.decode()
+    torch.cuda.synchronize()
+    assert st.fk.fp8kv_read_error(st.ws) == 0
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        st.append()
+        ev[i][1].record(stream)
+        st.decode()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    t_wall1 = time.time()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    app_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    total_ms = reduce_max(sum(step_ms), ws)
+    dec_mean = reduce_max(statistics.fmean(dec_ms), ws)
+    clk = clocks.summary(t_wall0, t_wall1) if clocks else None
+    if clocks:
+        clocks.stop()
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(st, args, ws, step_bytes, flush)
+
+    ms_per_step = total_ms / K
+    value = ws * step_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_src = measured_peaks()
+    achieved = dec_bytes / (dec_mean * 1e-3) / 1e9
+    key = "paged_decode/%s/w%d" % (args.config, window)
+    traffic = traffic_for(key)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "us_per_step": round(ms_per_step * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) bf16, per-tensor amax/448 E4M3 scales, shuffled 16-token pages)",
+        "config": {"workload": args.config, "batch": B, "num_q_heads": s.num_q_heads,
+                   "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": 16,
+                   "seq_lens": "uniform %d..%d" % (s.len_lo, s.len_hi), "total_tokens": int(sum(lens)),
+                   "window": window, "kv_cache": "e4m3, per-tensor k/v scales",
+                   "step": "quant_append(B new tokens) + paged_decode",
+                   "l2": "flushed before every timed step (256 MiB device write, outside the events)",
+                   "parallelism": "replicas" if ws > 1 else "1 gpu",
+                   "input_sha256": w.digest()[:16]},
+        "step_bytes": step_bytes, "decode_us": round(dec_mean * 1e3, 3),
+        "append_us": round(statistics.fmean(app_ms) * 1e3, 3),
+        "roofline": {"kernel": "fp8kv_paged_decode (split-context decode + in-kernel split merge)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": dec_bytes},
+        "gpu_launches": 2 * K,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, window, dec_bytes + app_bytes)
+    return line
+
+
+def measure_e2e(st, args, ws, step_bytes, flush):
+    """Same step through the public API from pinned host buffers: H2D of the
+    step's inputs (q, new K/V rows, their slots), append + decode, D2H of out."""
+    h_q = st.h_q.pin_memory()
+    h_k = st.h_k_new.pin_memory()
+    h_v = st.h_v_new.pin_memory()
+    h_s = st.h_slots.pin_memory()
+    h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    d_q, d_k, d_v, d_s = (torch.empty_like(t) for t in (st.q, st.k_new, st.v_new, st.slots))
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_s))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def one():
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_s.copy_(h_s, non_blocking=True)
+        st.append(d_k, d_v, d_s)
+        st.decode(q=d_q)
+        h_out.copy_(st.out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    K = args.steps
+    times = []
+    barrier(ws)
+    for _ in range(K):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        one()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(time.perf_counter() - t0)
+    barrier(ws)
+    mean_s = reduce_max(statistics.fmean(times), ws)
+    return {"value": round(ws * step_bytes / mean_s / 1e9, 2), "unit": "GB/s",
+            "us_per_step": round(mean_s * 1e6, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "timer": "host wall clock per step incl. H2D, kernels, D2H and the stream sync"}
+
+
+# ---------------------------------------------------------------- the CPU oracle
+
+def oracle_sample_step(w, window, kc, vc, seqs, nthreads):
+    """One decode step of the oracle restricted to sequences `seqs`: quantise
+    their newest K/V row, then fp64 attention over their caches."""
+    import oracle
+    rows = w.new_token_rows()[seqs]
+    oracle.quantize_bf16(workload.bf16_bits(w.k[rows]), w.k_scale)
+    oracle.quantize_bf16(workload.bf16_bits(w.v[rows]), w.v_scale)
+    lens = w.seq_lens.numpy()[seqs]
+    starts = w.seq_starts.numpy()[seqs]
+    idx = np.concatenate([np.arange(s, s + L) for s, L in zip(starts, lens)])
+    return oracle.decode_attention(workload.bf16_bits(w.q[seqs]), kc[idx], vc[idx], lens,
+                                   w.k_scale, w.v_scale, w.sm_scale, window, nthreads=nthreads)
+
+
+def oracle_codes(w):
+    import oracle
+    return (oracle.quantize_bf16(workload.bf16_bits(w.k), w.k_scale),
+            oracle.quantize_bf16(workload.bf16_bits(w.v), w.v_scale))
+
+
+def cpu_baseline(w, window, step_bytes_full):
+    import oracle
+    kc, vc = oracle_codes(w)
+    n = oracle.max_threads()
+    B = w.q.shape[0]
+    seqs = np.arange(B)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle_sample_step(w, window, kc, vc, seqs, n)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el * n >= 10.0 or reps >= 3:
+            break
+    per = el / reps
+    return {"value": round(step_bytes_full / per / 1e9, 4), "unit": "GB/s", "cores": n, "kind": "oracle",
+            "us_per_step": round(per * 1e6, 1),
+            "sample": "%d full decode step(s) of %s (all %d sequences): E4M3 quantisation of the new rows + "
+                      "fp64 two-pass attention, OpenMP over (sequence, head)" % (reps, w.shape.name, B)}
+
+
+def run_reference(args, rank, ws):
+    import oracle
+    w = workload.make_workload(args.config, seed=args.seed)
+    s = w.shape
+    window = s.windows[0] if args.window is None else args.window
+    lens = w.seq_lens.numpy()
+    kc, vc = oracle_codes(w)
+    n = oracle.max_threads()
+    B = len(lens)
+    times, nbytes = [], []
+    for i in range(args.warmup + args.steps):
+        seqs = np.array([i % B])
+        t0 = time.perf_counter()
+        oracle_sample_step(w, window, kc, vc, seqs, n)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            nbytes.append(accounting.decode_bytes(lens[seqs], s.num_q_heads, s.num_kv_heads, s.head_dim, window)
+                          + accounting.append_bytes(1, s.num_kv_heads, s.head_dim))
+    tot = sum(times)
+    value = sum(nbytes) / tot / 1e9
+    sample = ("one sequence of %s per step (cycling through the %d sequences): E4M3 quantisation of its new "
+              "row + fp64 attention over its cache" % (args.config, B))
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.config, "window": window, "batch": B},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, ws = dist_setup(args)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, ws)), flush=True)
+        return 0
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl fp8kv")
+    line = run_fp8kv(args, rank, ws)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,163 @@
+"""Thin ctypes binding over libfp8kv (argument marshalling only).
+
+Each function carries the C entry point's name and forwards torch tensors'
+device pointers and sizes to it; every step of the computation runs in the
+library's CUDA kernels.  There is no fallback: if the shared library is
+missing or a call returns an error status, a RuntimeError is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+STATUS = {0: "FP8KV_OK", 1: "FP8KV_ERR_INVALID_ARG", 2: "FP8KV_ERR_UNSUPPORTED",
+          3: "FP8KV_ERR_WORKSPACE", 4: "FP8KV_ERR_CUDA", 5: "FP8KV_ERR_TIMEOUT"}
+
+
+class Fp8kvError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__("%s failed: %s (%d)" % (fn, STATUS.get(code, "?"), code))
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Loads libfp8kv.so (building it first only when asked)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError("libfp8kv.so is not built (%s); run __graft_entry__.build()" % path)
+        _build.build()
+    lib = ctypes.CDLL(path)
+    P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.fp8kv_status_string.restype = ctypes.c_char_p
+    lib.fp8kv_status_string.argtypes = [I]
+    lib.fp8kv_quant_append.restype = I
+    lib.fp8kv_quant_append.argtypes = [P, P, P, I64, P, P, I64, I, I, I, F, F, P]
+    lib.fp8kv_paged_decode_workspace_size.restype = SZ
+    lib.fp8kv_paged_decode_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.fp8kv_workspace_init.restype = I
+    lib.fp8kv_workspace_init.argtypes = [P, SZ, P]
+    lib.fp8kv_read_error.restype = I
+    lib.fp8kv_read_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
+    lib.fp8kv_paged_decode.restype = I
+    lib.fp8kv_paged_decode.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
+    _lib = lib
+    return lib
+
+
+def header_symbols() -> list:
+    """Function names declared in include/fp8kv.h."""
+    hdr = os.path.join(_build.INCLUDE, "fp8kv.h")
+    text = open(hdr).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)   # drop comments
+    return sorted(set(re.findall(r"\b(fp8kv_[a-z0-9_]+)\s*\(", text)))
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(fn, code):
+    if code != 0:
+        raise Fp8kvError(fn, code)
+
+
+def _dev(t, dtype, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def fp8kv_status_string(code: int) -> str:
+    return load().fp8kv_status_string(int(code)).decode()
+
+
+def fp8kv_quant_append(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, stream=None):
+    """k_new, v_new: bf16 [T, Hkv, D]; slot_mapping: int64 [T];
+    k_cache, v_cache: uint8 [num_blocks, Hkv, block_size, D]."""
+    nb, hkv, bs, d = k_cache.shape
+    T = k_new.shape[0]
+    if tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d):
+        raise ValueError("k_new/v_new must be [T, Hkv, D] matching the cache")
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or slot_mapping.numel() != T:
+        raise ValueError("cache or slot_mapping shape mismatch")
+    code = load().fp8kv_quant_append(
+        _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _dev(slot_mapping, torch.int64, "slot_mapping"), T,
+        _dev(k_cache, torch.uint8, "k_cache"), _dev(v_cache, torch.uint8, "v_cache"),
+        nb, bs, hkv, d, float(k_scale), float(v_scale), _stream(stream))
+    _check("fp8kv_quant_append", code)
+
+
+def fp8kv_paged_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                                      block_size=16, window=0) -> int:
+    n = load().fp8kv_paged_decode_workspace_size(int(batch), int(num_q_heads), int(num_kv_heads),
+                                                 int(head_dim), int(max_seq_len), int(block_size),
+                                                 int(window))
+    if n == 0:
+        raise Fp8kvError("fp8kv_paged_decode_workspace_size", 1)
+    return int(n)
+
+
+def fp8kv_workspace_init(workspace, stream=None):
+    _check("fp8kv_workspace_init", load().fp8kv_workspace_init(
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def fp8kv_read_error(workspace, stream=None) -> int:
+    code = ctypes.c_uint32(0)
+    _check("fp8kv_read_error", load().fp8kv_read_error(
+        _dev(workspace, torch.uint8, "workspace"), ctypes.byref(code), _stream(stream)))
+    return int(code.value)
+
+
+def alloc_workspace(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, block_size=16,
+                    window=0, device=None, stream=None):
+    """Allocates (through torch) and zero-fills a workspace for these sizes."""
+    n = fp8kv_paged_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                                          block_size, window)
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    fp8kv_workspace_init(ws, stream)
+    return ws
+
+
+def fp8kv_paged_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale, v_scale,
+                       sm_scale, window, out, workspace, stream=None):
+    """q, out: bf16 [B, Hq, D]; caches uint8 [num_blocks, Hkv, bs, D];
+    block_tables int32 [B, max_blocks]; seq_lens int32 [B]."""
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if d2 != d or tuple(out.shape) != (B, hq, d) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch between q, out and the caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.numel() != B:
+        raise ValueError("block_tables must be [B, max_blocks] and seq_lens [B]")
+    code = load().fp8kv_paged_decode(
+        _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.uint8, "k_cache"),
+        _dev(v_cache, torch.uint8, "v_cache"), nb, _dev(block_tables, torch.int32, "block_tables"),
+        block_tables.shape[1], _dev(seq_lens, torch.int32, "seq_lens"), int(max_seq_len), B, hq, hkv,
+        d, bs, float(k_scale), float(v_scale), float(sm_scale), int(window),
+        _dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream))
+    _check("fp8kv_paged_decode", code)

@@ -108,6 +108,10 @@ static float bf16_bits_to_float(uint16_t h) {
 
 /* Quantise-on-append: code = e4m3(fp32(x) / scale), with an fp32 IEEE divide. */
 void oracle_quantize_bf16(const uint16_t* x, int64_t n, float scale, uint8_t* out) {
+    /* every element is independent; threads only split the index range */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int64_t i = 0; i < n; ++i) {
         float xf = bf16_bits_to_float(x[i]);
         float y = xf / scale;

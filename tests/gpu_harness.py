@@ -1,0 +1,67 @@
+"""Shared GPU-test plumbing: put a seeded workload into a paged device cache
+through fp8kv_quant_append, run fp8kv_paged_decode, and fetch what the oracle
+needs to check them."""
+import numpy as np
+import torch
+
+import oracle
+from fp8_kv_cache_fp8kv_gb300 import binding as fk
+from fp8_kv_cache_fp8kv_gb300 import workload
+
+
+class Paged:
+    def __init__(self, w: workload.Workload, fill_byte=None, device="cuda", extra_blocks=0,
+                 seed=0):
+        s = w.shape
+        self.w = w
+        self.num_blocks = w.num_blocks + extra_blocks
+        shape = (self.num_blocks, s.num_kv_heads, workload.BLOCK_SIZE, s.head_dim)
+        if fill_byte is None:
+            g = torch.Generator(device=device).manual_seed(seed + 99)
+            self.k_cache = torch.randint(0, 256, shape, dtype=torch.uint8, device=device, generator=g)
+            self.v_cache = torch.randint(0, 256, shape, dtype=torch.uint8, device=device, generator=g)
+        else:
+            self.k_cache = torch.full(shape, fill_byte, dtype=torch.uint8, device=device)
+            self.v_cache = torch.full(shape, fill_byte, dtype=torch.uint8, device=device)
+        self.q = w.q.to(device)
+        self.block_tables = w.block_tables.to(device)
+        self.seq_lens = w.seq_lens.to(device)
+
+    def append_all(self):
+        w = self.w
+        if w.k.shape[0] == 0:
+            return
+        fk.fp8kv_quant_append(w.k.to("cuda"), w.v.to("cuda"), w.slot_mapping.to("cuda"),
+                              self.k_cache, self.v_cache, w.k_scale, w.v_scale)
+
+    def gathered_codes(self):
+        """Cache codes of every logical token, [T, Hkv, D] (host)."""
+        kc = self.k_cache.cpu()
+        vc = self.v_cache.cpu()
+        sm = self.w.slot_mapping
+        blk, off = sm // workload.BLOCK_SIZE, sm % workload.BLOCK_SIZE
+        return kc[blk, :, off, :].numpy(), vc[blk, :, off, :].numpy()
+
+    def decode(self, window=0, max_seq_len=None, block_tables=None, out=None):
+        s = self.w.shape
+        B = self.q.shape[0]
+        mx = self.w.max_seq_len if max_seq_len is None else max_seq_len
+        bt = self.block_tables if block_tables is None else block_tables
+        ws = fk.alloc_workspace(B, s.num_q_heads, s.num_kv_heads, s.head_dim, mx, 16, window)
+        out = torch.empty((B, s.num_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda") if out is None else out
+        fk.fp8kv_paged_decode(self.q, self.k_cache, self.v_cache, bt, self.seq_lens, mx,
+                              self.w.k_scale, self.w.v_scale, self.w.sm_scale, window, out, ws)
+        torch.cuda.synchronize()
+        err = fk.fp8kv_read_error(ws)
+        return out, err
+
+
+def oracle_codes(w):
+    kc = oracle.quantize_bf16(workload.bf16_bits(w.k), w.k_scale)
+    vc = oracle.quantize_bf16(workload.bf16_bits(w.v), w.v_scale)
+    return kc, vc
+
+
+def oracle_out(w, kc, vc, window):
+    return oracle.decode_attention(workload.bf16_bits(w.q), kc, vc, w.seq_lens.numpy(), w.k_scale,
+                                   w.v_scale, w.sm_scale, window, nthreads=oracle.max_threads())

@@ -1,0 +1,85 @@
+"""The C ABI without a GPU: the library builds, loads, exports every function
+include/fp8kv.h declares, and rejects bad arguments with a status code before
+touching the device."""
+import ctypes
+
+import pytest
+
+from fp8_kv_cache_fp8kv_gb300 import binding as fk
+from fp8_kv_cache_fp8kv_gb300 import build as fbuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fbuild.build()
+    return fk.load()
+
+
+def test_every_header_symbol_is_exported(lib):
+    names = fk.header_symbols()
+    assert {"fp8kv_quant_append", "fp8kv_paged_decode", "fp8kv_paged_decode_workspace_size",
+            "fp8kv_workspace_init", "fp8kv_read_error", "fp8kv_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in fk.STATUS.items():
+        assert fk.fp8kv_status_string(code) == name
+    assert fk.fp8kv_status_string(99) == "FP8KV_ERR_UNKNOWN"
+
+
+FAKE = ctypes.c_void_p(0x10000)      # never dereferenced: every call below fails validation first
+MISALIGNED = ctypes.c_void_p(0x10001)
+
+
+def _decode(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, nb=100, bt=FAKE, mb=8, sl=FAKE, msl=128, B=2, hq=32, hkv=8, d=128,
+             bs=16, ks=0.01, vs=0.01, sm=0.088, win=0, out=FAKE, ws=FAKE, wsb=1 << 20)
+    a.update(kw)
+    return lib.fp8kv_paged_decode(a["q"], a["k"], a["v"], a["nb"], a["bt"], a["mb"], a["sl"], a["msl"],
+                                  a["B"], a["hq"], a["hkv"], a["d"], a["bs"], a["ks"], a["vs"], a["sm"],
+                                  a["win"], a["out"], a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), 2), (dict(d=512), 2), (dict(bs=32), 2), (dict(hq=128, hkv=8), 2),
+    (dict(hq=30, hkv=8), 1), (dict(ks=0.0), 1), (dict(vs=float("nan")), 1), (dict(sm=float("inf")), 1),
+    (dict(q=None), 1), (dict(out=None), 1), (dict(bt=None), 1), (dict(q=MISALIGNED), 1),
+    (dict(k=MISALIGNED), 1), (dict(mb=4, msl=128), 1), (dict(B=-1), 1), (dict(nb=0), 1),
+    (dict(nb=1 << 31), 2), (dict(B=70000), 1),
+])
+def test_decode_rejects_bad_arguments(lib, kw, code):
+    assert _decode(lib, **kw) == code
+
+
+def test_decode_empty_batch_is_a_no_op(lib):
+    assert _decode(lib, B=0, q=None, out=None) == 0
+
+
+def _append(lib, **kw):
+    a = dict(k=FAKE, v=FAKE, sm=FAKE, T=4, kc=FAKE, vc=FAKE, nb=10, bs=16, hkv=8, d=128, ks=0.5, vs=0.5)
+    a.update(kw)
+    return lib.fp8kv_quant_append(a["k"], a["v"], a["sm"], a["T"], a["kc"], a["vc"], a["nb"], a["bs"],
+                                  a["hkv"], a["d"], a["ks"], a["vs"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=24), 2), (dict(d=2048), 2), (dict(ks=-1.0), 1), (dict(vs=float("inf")), 1),
+    (dict(kc=None), 1), (dict(k=None), 1), (dict(sm=None), 1), (dict(k=MISALIGNED), 1),
+    (dict(T=-3), 1), (dict(nb=0), 1), (dict(hkv=0), 1),
+])
+def test_append_rejects_bad_arguments(lib, kw, code):
+    assert _append(lib, **kw) == code
+
+
+def test_append_zero_tokens_is_a_no_op(lib):
+    assert _append(lib, T=0, k=None, v=None, sm=None) == 0
+
+
+def test_workspace_calls_validate(lib):
+    assert lib.fp8kv_workspace_init(None, 16, None) == 1
+    assert lib.fp8kv_workspace_init(MISALIGNED, 16, None) == 1
+    assert lib.fp8kv_read_error(None, None, None) == 1
+    assert lib.fp8kv_paged_decode_workspace_size(2, 30, 8, 128, 100, 16, 0) == 0
+    assert lib.fp8kv_paged_decode_workspace_size(2, 32, 8, 96, 100, 16, 0) == 0

@@ -1,0 +1,194 @@
+"""GPU parity: libfp8kv (through its C ABI) against the CPU oracle.
+
+Cache codes must match bit for bit; attention outputs must meet
+max|err| <= 8e-3 and mean|err| <= 1e-3 against the fp64 oracle evaluated on
+the same codes.  Small cases span several pages, splits and ragged tails; the
+full-size cases run every workload at the size and in the launch
+configuration the benchmark times, comparing every output element.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_kv_cache_fp8kv_gb300 import binding as fk
+from fp8_kv_cache_fp8kv_gb300 import workload
+from tests._tol import assert_attn_close
+from tests.gpu_harness import Paged, oracle_codes, oracle_out
+
+pytestmark = pytest.mark.gpu
+
+
+def _as_f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+# ------------------------------------------------------------ quant_append
+
+@pytest.mark.parametrize("scale", [1.0, 0.0123, 3.7, float(np.float32(2.75 / 448))])
+def test_quant_append_every_bf16_pattern_bit_exact(scale):
+    d, hkv = 128, 2
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    T = 65536 // (d * hkv)
+    x = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).reshape(T, hkv, d)
+    y = torch.from_numpy(np.roll(bits, 12345).view(np.int16).copy()).view(torch.bfloat16).reshape(T, hkv, d)
+    nb = T // 16 + 3
+    perm = torch.randperm(nb * 16, generator=torch.Generator().manual_seed(1))[:T].to(torch.int64)
+    kc = torch.zeros((nb, hkv, 16, d), dtype=torch.uint8, device="cuda")
+    vc = torch.zeros_like(kc)
+    fk.fp8kv_quant_append(x.cuda(), y.cuda(), perm.cuda(), kc, vc, scale, scale * 2)
+    torch.cuda.synchronize()
+    gk = kc.cpu()[perm // 16, :, perm % 16, :].numpy()
+    gv = vc.cpu()[perm // 16, :, perm % 16, :].numpy()
+    for got, src, s in ((gk, x, scale), (gv, y, scale * 2)):
+        ref = oracle.quantize_bf16(workload.bf16_bits(src), s)
+        srcf = src.float().numpy()
+        nan = np.isnan(srcf)
+        assert np.array_equal(got[~nan], ref[~nan])
+        assert np.all((got[nan] & 0x7F) == 0x7F)
+
+
+def test_quant_append_skips_padding_and_out_of_range_slots():
+    d, hkv, nb = 64, 1, 4
+    x = torch.randn((5, hkv, d)).to(torch.bfloat16)
+    slots = torch.tensor([3, -1, nb * 16, 17, nb * 16 + 100], dtype=torch.int64)
+    kc = torch.full((nb, hkv, 16, d), 0xAB, dtype=torch.uint8, device="cuda")
+    vc = kc.clone()
+    fk.fp8kv_quant_append(x.cuda(), x.cuda(), slots.cuda(), kc, vc, 0.01, 0.01)
+    torch.cuda.synchronize()
+    flat = kc.cpu().reshape(nb * 16, d)  # hkv == 1: slot index = row
+    ref = oracle.quantize_bf16(workload.bf16_bits(x), 0.01).reshape(5, d)
+    assert np.array_equal(flat[3].numpy(), ref[0]) and np.array_equal(flat[17].numpy(), ref[3])
+    untouched = [r for r in range(nb * 16) if r not in (3, 17)]
+    assert bool((flat[untouched] == 0xAB).all())
+
+
+# ------------------------------------------------------------ decode, small cases
+
+SMALL = [
+    # (base config, lengths, windows)
+    ("llama31_8b_b1_4k", [1, 15, 16, 17, 33, 100, 0, 1000], (0, 1, 5, 16, 17, 100)),
+    ("llama31_8b_b8_20k", [2999, 1234, 16, 4097], (0, 128)),
+    ("gptoss20b_b8_16k", [1, 63, 64, 65, 700, 2500], (0, 128, 7)),
+    ("gemma4e2b_b16_8k32k", [1, 17, 511, 512, 513, 3000], (0, 512, 33)),
+    ("llama33_70b_needle_128k", [3000, 40], (0, 16)),
+]
+
+
+@pytest.mark.parametrize("base,lens,windows", SMALL)
+def test_decode_small_cases_match_oracle(base, lens, windows):
+    shape = workload.small_shape(base, batch=len(lens), len_lo=1, len_hi=1, needle_margin=None)
+    w = workload.make_workload(shape, seed=3, lens=lens)
+    pc = Paged(w)
+    pc.append_all()
+    kc, vc = oracle_codes(w)
+    gk, gv = pc.gathered_codes()
+    assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
+    for win in windows:
+        out, err = pc.decode(window=win)
+        assert err == 0
+        assert_attn_close(_as_f64(out), oracle_out(w, kc, vc, win), f"{base} window={win}")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_decode_every_supported_head_layout(d, g):
+    hkv = 2
+    shape = workload.LayerShape(f"t{d}_{g}", hkv * g, hkv, d, 3, 1, 1, (0,))
+    w = workload.make_workload(shape, seed=g * 1000 + d, lens=[777, 16, 35])
+    pc = Paged(w)
+    pc.append_all()
+    kc, vc = oracle_codes(w)
+    for win in (0, 50):
+        out, err = pc.decode(window=win)
+        assert err == 0
+        assert_attn_close(_as_f64(out), oracle_out(w, kc, vc, win), f"d={d} g={g} window={win}")
+
+
+def test_unwritten_nan_slots_never_leak():
+    # Every byte of the cache starts as the NaN code; only written slots may count.
+    shape = workload.small_shape("llama31_8b_b8_20k", batch=3, len_lo=1, len_hi=1)
+    w = workload.make_workload(shape, seed=4, lens=[33, 1, 250])
+    pc = Paged(w, fill_byte=0x7F, extra_blocks=4)
+    pc.append_all()
+    kc, vc = oracle_codes(w)
+    for win in (0, 3, 20):
+        out, err = pc.decode(window=win)
+        assert err == 0 and torch.isfinite(out.float()).all()
+        assert_attn_close(_as_f64(out), oracle_out(w, kc, vc, win), f"nan-filled window={win}")
+
+
+def test_result_independent_of_physical_placement():
+    shape = workload.small_shape("llama31_8b_b8_20k", batch=2, len_lo=1, len_hi=1)
+    w = workload.make_workload(shape, seed=5, lens=[1500, 333])
+    a = Paged(w)
+    a.append_all()
+    out_a, _ = a.decode()
+    # the same logical cache under the identity block table
+    ident = torch.zeros_like(w.block_tables)
+    slots = []
+    base = 0
+    for b, L in enumerate(w.seq_lens.tolist()):
+        nb = (L + 15) // 16
+        ident[b, :nb] = torch.arange(base, base + nb, dtype=torch.int32)
+        t = torch.arange(L)
+        slots.append((ident[b, t // 16].to(torch.int64) * 16 + t % 16))
+        base += nb
+    w2 = workload.Workload(**{**w.__dict__, "block_tables": ident, "slot_mapping": torch.cat(slots)})
+    b_ = Paged(w2)
+    b_.append_all()
+    out_b, _ = b_.decode()
+    assert torch.equal(out_a, out_b)
+
+
+def test_split_plan_does_not_change_the_result():
+    shape = workload.small_shape("llama33_70b_needle_128k", batch=2, len_lo=1, len_hi=1, needle_margin=None)
+    w = workload.make_workload(shape, seed=6, lens=[5000, 4100])
+    pc = Paged(w)
+    pc.append_all()
+    out1, _ = pc.decode()
+    wide = torch.zeros((2, 4 * w.max_blocks_per_seq), dtype=torch.int32, device="cuda")
+    wide[:, :w.max_blocks_per_seq] = pc.block_tables
+    out2, _ = pc.decode(max_seq_len=4 * 16 * w.max_blocks_per_seq, block_tables=wide)
+    kc, vc = oracle_codes(w)
+    ref = oracle_out(w, kc, vc, 0)
+    assert_attn_close(_as_f64(out1), ref, "plan 1")
+    assert_attn_close(_as_f64(out2), ref, "plan 2")
+    assert float((out1.float() - out2.float()).abs().max()) <= 2 ** -7
+
+
+def test_out_of_range_block_id_is_reported_not_faulted():
+    shape = workload.small_shape("llama31_8b_b8_20k", batch=1, len_lo=1, len_hi=1)
+    w = workload.make_workload(shape, seed=7, lens=[40])
+    pc = Paged(w)
+    pc.append_all()
+    bad = pc.block_tables.clone()
+    bad[0, 1] = pc.num_blocks + 5
+    _, err = pc.decode(block_tables=bad)
+    assert err == 1  # FP8KV_ERR_INVALID_ARG
+    _, err2 = pc.decode()
+    assert err2 == 0
+
+
+# ------------------------------------------------------------ full-size workloads
+
+@pytest.mark.parametrize("name", list(workload.CONFIGS))
+def test_full_size_workloads_match_oracle(name):
+    w = workload.make_workload(name, seed=0)
+    pc = Paged(w)
+    pc.append_all()
+    kc, vc = oracle_codes(w)
+    gk, gv = pc.gathered_codes()
+    assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
+    for win in w.shape.windows:
+        out, err = pc.decode(window=win)
+        assert err == 0
+        ref = oracle_out(w, kc, vc, win)
+        assert_attn_close(_as_f64(out), ref, f"{name} window={win}")
+        if w.needle_pos is not None:
+            vh = oracle.e4m3_decode(vc[w.needle_pos]) * w.v_scale
+            g = w.shape.group
+            expect = np.stack([vh[h // g] for h in range(w.shape.num_q_heads)])
+            assert_attn_close(_as_f64(out)[0], expect, f"{name} needle row")
