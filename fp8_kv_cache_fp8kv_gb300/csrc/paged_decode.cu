@@ -122,7 +122,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         const DecodeArgs a) {
     using Gm = Geo<D>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned ring (the swizzle pattern is a function of address
+    // bits 4..9); offsetting the shared array keeps the address space known.
+    uint8_t* ring = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(ring + kStages * kStageBytes);
     uint64_t* empty_bar = full_bar + kStages;
     int32_t* blk = reinterpret_cast<int32_t*>(empty_bar + kStages);
@@ -266,7 +268,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
     for (int mt = 0; mt < Gm::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-    const uint32_t ring_s = smem_u32(ring);
     for (int st = warp; st < n_stages; st += kNCW) {
         const int slot = st % kStages;
         if (!mbar_wait_bounded(&full_bar[slot], (st / kStages) & 1, kWaitLimitNs)) {
