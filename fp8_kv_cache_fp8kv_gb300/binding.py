@@ -55,6 +55,8 @@ def load(build_if_missing: bool = False):
     lib.fp8kv_read_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     lib.fp8kv_paged_decode.restype = I
     lib.fp8kv_paged_decode.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
+    lib.fp8kv_paged_decode_noalloc.restype = I
+    lib.fp8kv_paged_decode_noalloc.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P]
     _lib = lib
     return lib
 
@@ -161,3 +163,23 @@ def fp8kv_paged_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len,
         _dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"),
         workspace.numel(), _stream(stream))
     _check("fp8kv_paged_decode", code)
+
+
+def fp8kv_paged_decode_noalloc(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale, v_scale,
+                               sm_scale, window, out, stream=None):
+    """Same as fp8kv_paged_decode without a workspace: for callers that cannot
+    allocate device memory, the library's fixed 8 MiB device array holds the
+    split-merge scratch.  Calls that overlap on the GPU race on that array."""
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if d2 != d or tuple(out.shape) != (B, hq, d) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch between q, out and the caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.numel() != B:
+        raise ValueError("block_tables must be [B, max_blocks] and seq_lens [B]")
+    code = load().fp8kv_paged_decode_noalloc(
+        _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.uint8, "k_cache"),
+        _dev(v_cache, torch.uint8, "v_cache"), nb, _dev(block_tables, torch.int32, "block_tables"),
+        block_tables.shape[1], _dev(seq_lens, torch.int32, "seq_lens"), int(max_seq_len), B, hq, hkv,
+        d, bs, float(k_scale), float(v_scale), float(sm_scale), int(window),
+        _dev(out, torch.bfloat16, "out"), _stream(stream))
+    _check("fp8kv_paged_decode_noalloc", code)

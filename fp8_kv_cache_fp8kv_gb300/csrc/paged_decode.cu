@@ -701,6 +701,67 @@ extern "C" fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache
     return e == cudaSuccess ? FP8KV_OK : FP8KV_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- allocation-free variant
+//
+// Some callers cannot allocate device memory at the point where they decode:
+// a serving engine that reserved nearly all HBM up front for its own paged-KV
+// pool (so a late cudaMalloc fails or fragments that pool), host code running
+// under a no-allocation rule (a fixed-budget or real-time loop, a plugin inside
+// a framework that owns every device buffer), or a language binding with no
+// CUDA allocator at hand.  For them the split-merge scratch lives in a
+// fixed-size device array that is part of the library image itself.
+
+namespace fp8kv {
+
+// 8 MiB covers every workload shape exercised here (the largest, 16 x 32K
+// tokens at head_dim 256, needs about 5 MiB).  Every device that loads the
+// library holds this array until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+// Device address of the array on the current device, looked up once per device
+// (host code only sees a host-side stand-in for the symbol).
+static void* static_scratch_address() {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+}  // namespace fp8kv
+
+extern "C" fp8kv_status fp8kv_paged_decode_noalloc(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                                   int64_t num_blocks, const int32_t* block_tables,
+                                                   int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len,
+                                                   int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                                   int block_size, float k_scale, float v_scale, float sm_scale,
+                                                   int window, void* out, void* stream) {
+    if (batch < 0 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads != 0 || max_seq_len < 0)
+        return FP8KV_ERR_INVALID_ARG;
+    if (!supported(head_dim, block_size, num_q_heads / num_kv_heads)) return FP8KV_ERR_UNSUPPORTED;
+    if (batch == 0) return FP8KV_OK;
+    int sms = 0;
+    if (device_sms(&sms) != 0) return FP8KV_ERR_CUDA;
+    const Plan p = make_plan(batch, num_kv_heads, head_dim, max_seq_len, window, sms);
+    const WsLayout w = ws_layout(batch, num_q_heads, num_kv_heads, head_dim, p);
+    if (w.total > kStaticScratchBytes) return FP8KV_ERR_WORKSPACE;  // problem too large for the fixed array
+    void* scratch = static_scratch_address();
+    if (scratch == nullptr) return FP8KV_ERR_CUDA;
+    // The array keeps the previous call's contents: the error word and the
+    // split counters must start at zero.
+    if (cudaMemsetAsync(scratch, 0, w.ml, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8KV_ERR_CUDA;
+    return fp8kv_paged_decode(q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
+                              max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale, v_scale,
+                              sm_scale, window, out, scratch, kStaticScratchBytes, stream);
+}
+
 extern "C" fp8kv_status fp8kv_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FP8KV_ERR_INVALID_ARG;
     return cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess

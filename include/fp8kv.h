@@ -18,8 +18,9 @@
  *
  * Conventions for every entry point:
  *   - All pointers except `stream` are DEVICE pointers owned by the caller.
- *     The library allocates nothing, keeps no state between calls, and is
- *     safe to call from several host threads.
+ *     The library allocates nothing and keeps no state between calls (the one
+ *     exception is the fixed scratch array of fp8kv_paged_decode_noalloc).
+ *     The entry points are safe to call from several host threads.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
  *     legacy default stream).  Nothing is synchronised.
  *   - Invalid arguments return an error status and launch nothing.  A failed
@@ -141,6 +142,37 @@ fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache, const uin
                                 int head_dim, int block_size, float k_scale, float v_scale,
                                 float sm_scale, int window, void* out, void* workspace,
                                 size_t workspace_bytes, void* stream);
+
+/*
+ * Allocation-free paged decode.  This entry point has no counterpart on the
+ * pages: it exists for callers that cannot allocate device memory when they
+ * decode -- e.g. a serving engine that reserved nearly all HBM for its own
+ * paged KV pool, host code under a no-allocation rule, or a binding without a
+ * CUDA allocator -- and so cannot provide the workspace fp8kv_paged_decode
+ * takes.  It computes exactly what fp8kv_paged_decode computes, with the same
+ * arguments minus the workspace.
+ *
+ * Scratch: a fixed 8 MiB array compiled into the library (every device that
+ * loads the library keeps it until the process exits).  The call allocates
+ * nothing and calls no allocating routine; it clears the array's error word
+ * and split counters (cudaMemsetAsync on `stream`) and then runs the decode.
+ *   - A problem whose split-merge scratch would exceed 8 MiB is rejected with
+ *     FP8KV_ERR_WORKSPACE before anything is launched.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current (cudaGetSymbolAddress); make that first call before
+ *     any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (different
+ *     streams without ordering, or different host threads) race and corrupt
+ *     each other's results.  Order them.
+ *   - Device-side errors (an out-of-range block id) are not reported by this
+ *     variant; use fp8kv_paged_decode with a workspace to read them.
+ */
+fp8kv_status fp8kv_paged_decode_noalloc(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                        int64_t num_blocks, const int32_t* block_tables,
+                                        int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len,
+                                        int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                        int block_size, float k_scale, float v_scale, float sm_scale,
+                                        int window, void* out, void* stream);
 
 #ifdef __cplusplus
 }
