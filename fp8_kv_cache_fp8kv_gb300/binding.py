@@ -183,3 +183,53 @@ def fp8kv_paged_decode_noalloc(q, k_cache, v_cache, block_tables, seq_lens, max_
         d, bs, float(k_scale), float(v_scale), float(sm_scale), int(window),
         _dev(out, torch.bfloat16, "out"), _stream(stream))
     _check("fp8kv_paged_decode_noalloc", code)
+
+
+class PreparedCall:
+    """A validated C call with its marshalled arguments kept, for callers that
+    issue the same call repeatedly (decode loops): each invocation is just the
+    C function call.  The tensors must stay alive and unchanged in shape."""
+
+    def __init__(self, name, fn, args):
+        self.name, self.fn, self.args = name, fn, args
+
+    def __call__(self):
+        code = self.fn(*self.args)
+        if code != 0:
+            raise Fp8kvError(self.name, code)
+
+
+def prepare_quant_append(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, stream=None):
+    nb, hkv, bs, d = k_cache.shape
+    T = k_new.shape[0]
+    if tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d):
+        raise ValueError("k_new/v_new must be [T, Hkv, D] matching the cache")
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or slot_mapping.numel() != T:
+        raise ValueError("cache or slot_mapping shape mismatch")
+    lib = load()
+    args = (_dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+            _dev(slot_mapping, torch.int64, "slot_mapping"), ctypes.c_int64(T),
+            _dev(k_cache, torch.uint8, "k_cache"), _dev(v_cache, torch.uint8, "v_cache"),
+            ctypes.c_int64(nb), ctypes.c_int(bs), ctypes.c_int(hkv), ctypes.c_int(d),
+            ctypes.c_float(k_scale), ctypes.c_float(v_scale), _stream(stream))
+    return PreparedCall("fp8kv_quant_append", lib.fp8kv_quant_append, args)
+
+
+def prepare_paged_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale, v_scale,
+                         sm_scale, window, out, workspace, stream=None):
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if d2 != d or tuple(out.shape) != (B, hq, d) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch between q, out and the caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.numel() != B:
+        raise ValueError("block_tables must be [B, max_blocks] and seq_lens [B]")
+    lib = load()
+    I = ctypes.c_int
+    args = (_dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.uint8, "k_cache"),
+            _dev(v_cache, torch.uint8, "v_cache"), ctypes.c_int64(nb),
+            _dev(block_tables, torch.int32, "block_tables"), I(block_tables.shape[1]),
+            _dev(seq_lens, torch.int32, "seq_lens"), I(max_seq_len), I(B), I(hq), I(hkv), I(d), I(bs),
+            ctypes.c_float(k_scale), ctypes.c_float(v_scale), ctypes.c_float(sm_scale), I(window),
+            _dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"),
+            ctypes.c_size_t(workspace.numel()), _stream(stream))
+    return PreparedCall("fp8kv_paged_decode", lib.fp8kv_paged_decode, args)

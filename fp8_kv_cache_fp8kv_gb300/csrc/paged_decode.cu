@@ -11,26 +11,30 @@
 // LONG CONTEXT": the P.V contraction runs over the context length), and an
 // optional sliding window (same summary, "DECODE COST": windows 128, 512).
 //
-// How (one CTA = one (split of the context, kv head, sequence)):
-//  * All g query heads of a kv head share the CTA, so every cache byte is read
-//    from HBM once.  Decode attention is bandwidth-bound (2g flop per fp8
-//    byte), so the kernel is built around streaming pages at HBM speed.
+// How (persistent CTAs over a flattened, evenly split page list):
+//  * All g query heads of a kv head are handled together, so every cache byte
+//    is read from HBM once.  Decode attention is bandwidth-bound (2g flop per
+//    fp8 byte), so the kernel is built around streaming pages at HBM speed.
+//  * The attended pages of every (sequence, kv head) unit are laid end to end
+//    and cut into one equal contiguous range per CTA (2 CTAs per SM), so all
+//    CTAs finish together whatever the mix of sequence lengths.  A CTA walks
+//    the units its range overlaps ("segments").
 //  * One producer warp streams K and V pages with TMA tensor copies (128-byte
 //    or 64-byte swizzle, evict-first L2 policy) into a ring of shared-memory
-//    stages guarded by mbarriers.  Four consumer warps each own every fourth
-//    stage and keep their own online-softmax state.
+//    stages guarded by mbarriers, reading block ids 32 pages ahead.  Four
+//    consumer warps each own every fourth stage.
 //  * Per stage a consumer warp converts codes to f16 (exact) and runs the
 //    score contraction S^T = K Q^T and the value contraction O^T += V^T P^T on
-//    the tensor cores (mma m16n8k16, fp32 accumulators): with g <= 8 the
-//    query heads form the n=8 side, so no tensor-core work is padded for g=8.
-//    FP32 CUDA cores alone cannot keep up with HBM at g=8 on this part (2g
-//    flop per byte at ~7 TB/s exceeds their FMA rate).  The stage's P.V tile
-//    is then added into separate FP32 registers (O = O*alpha + tile), so the
-//    long contraction is summed in IEEE FP32, not inside the MMA.
+//    the tensor cores (mma m16n8k16, fp32 accumulators): the g <= 8 query
+//    heads form the n=8 side.  FP32 CUDA cores alone cannot keep up with HBM
+//    at g=8 on this part (2g flop per byte at ~7 TB/s exceeds their FMA
+//    rate).  The stage's P.V tile is then added into separate FP32 registers
+//    (O = O*alpha + tile), so the long contraction is summed in IEEE FP32,
+//    not inside the MMA.
 //  * The softmax max/sum use warp shuffles; P is rounded to f16 for the MMA.
-//  * Warps are merged in shared memory; splits of one (sequence, kv head) are
-//    merged in FP32 by the last CTA to finish (an atomic counter in the
-//    workspace; no CTA ever waits for another).
+//  * At the end of a segment the four warps merge through shared memory; a
+//    unit split over several CTAs is merged in FP32 by the last of them to
+//    finish (an atomic counter in the workspace; no CTA waits for another).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -49,11 +53,12 @@ namespace fp8kv {
 constexpr int kBS = 16;                    // tokens per page (block_size)
 constexpr int kNCW = 4;                    // consumer warps per CTA
 constexpr int kThreads = (kNCW + 1) * 32;  // + one producer warp
-constexpr int kStages = 12;                // ring slots; a multiple of kNCW
 constexpr int kStageHalf = 4096;           // K bytes (and V bytes) per stage
 constexpr int kStageBytes = 2 * kStageHalf;
-constexpr int kMaxPagesPerSplit = 512;
 constexpr int kCtasPerSm = 2;
+constexpr int kMaxBatch = 512;             // sequences per launch; larger batches run in chunks
+constexpr int kMaxMergeSplits = 1024;      // CTAs per launch are capped at this (the merge keeps one weight each)
+constexpr int kMinPagesPerCta = 16;
 constexpr uint64_t kWaitLimitNs = 500000000ull;  // 0.5 s: far beyond any legitimate wait
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -63,16 +68,15 @@ struct DecodeArgs {
     const int32_t* seq_lens;
     uint16_t* out;              // bf16 [B, Hq, D]
     uint32_t* err;              // workspace error word
-    int32_t* counters;          // [B*Hkv]
-    float2* part_ml;            // [B*Hkv, max_splits, 8]  (max, sum) in log2 units
-    float* part_o;              // [B*Hkv, max_splits, G, D]
+    int2* unit_meta;            // [B*Hkv] (first partial slot, partial count) of each unit
+    float2* part_ml;            // [B*Hkv + ctas][8]     (max, sum) in log2 units
+    float* part_o;              // [B*Hkv + ctas][G][D]  unnormalised partial outputs
     int64_t num_blocks;
     int max_blocks_per_seq;
     int max_seq_len;
+    int batch;
     int num_q_heads;
     int num_kv_heads;
-    int pages_per_split;
-    int max_splits;
     int window;
     float score_scale;          // sm_scale * k_scale * log2(e)
     float v_scale;
@@ -91,8 +95,18 @@ struct Geo {
     static constexpr int KSH = KW / 4;                  // k-steps per box
     static constexpr int VW = ROWB / 8;                 // V bytes a thread reads per token per box
     static constexpr int MTH = VW / 2;                  // m-tiles per box
+    static constexpr int STAGES = D == 256 ? 8 : 12;    // ring slots (a multiple of kNCW)
+    static constexpr int XW = MT * 4 + 4;               // per-lane words exchanged in the warp merge
     static_assert(PPS >= 1 && PPS * PAGE == kStageHalf, "stage must hold whole pages");
+    static_assert(STAGES % kNCW == 0, "every consumer warp owns whole ring slots");
+    static_assert(32 % PPS == 0, "a 32-page block-id batch holds whole stages");
 };
+
+template <int D>
+constexpr size_t smem_bytes() {
+    return 1024 + Geo<D>::STAGES * kStageBytes + 2 * Geo<D>::XW * 32 * sizeof(float) +
+           2 * Geo<D>::STAGES * sizeof(uint64_t) + (2 * kMaxBatch + 1 + 4 + 32) * sizeof(int32_t);
+}
 
 // Byte offset of (row r, byte o) inside one TMA box written with the 128-byte
 // (rows of 128 B) or 64-byte (rows of 64 B) swizzle: the 16-byte chunk index
@@ -116,404 +130,643 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float x) {
     return *reinterpret_cast<uint16_t*>(&h);
 }
 
+// Per-sequence geometry: the attended keys of a length-L sequence are
+// [first_token, L); they occupy pages first_token/16 .. (L-1)/16.
+__device__ __forceinline__ int clamp_len(int L, int max_len) { return L < 0 ? 0 : (L > max_len ? max_len : L); }
+__device__ __forceinline__ int first_token(int L, int window) { return (window > 0 && L > window) ? L - window : 0; }
+__device__ __forceinline__ int attended_pages(int L, int window) {
+    return L > 0 ? (L - 1) / kBS - first_token(L, window) / kBS + 1 : 0;
+}
+
+// Work of one launch: the attended pages of every (sequence, kv head) unit,
+// laid end to end (unit u = b*Hkv + hk holds pages [Hkv*pre[b] + hk*n_b,
+// ... + n_b)), split into equal contiguous ranges, one per CTA.  A CTA walks
+// the units its range overlaps; each overlap is one "segment".
+struct Walker {
+    int b, hk, n;       // sequence, kv head, pages per unit of this sequence
+    int64_t base;       // global index of the unit's first page
+    int64_t g;          // global index of the segment's first page
+};
+
+__device__ __forceinline__ void walk_start(Walker& w, const int32_t* pre, int B, int Hkv, int64_t s) {
+    int lo = 0, hi = B - 1;  // largest b with Hkv*pre[b] <= s (it has pages, since s < total)
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<int64_t>(Hkv) * pre[mid] <= s) lo = mid; else hi = mid - 1;
+    }
+    w.b = lo;
+    w.n = pre[lo + 1] - pre[lo];
+    const int64_t off = s - static_cast<int64_t>(Hkv) * pre[lo];
+    w.hk = static_cast<int>(off / w.n);
+    w.base = static_cast<int64_t>(Hkv) * pre[lo] + static_cast<int64_t>(w.hk) * w.n;
+    w.g = s;
+}
+
+// Next unit (only called while the CTA's range continues past this unit).
+__device__ __forceinline__ void walk_next(Walker& w, const int32_t* pre, int Hkv) {
+    if (++w.hk == Hkv) {
+        w.hk = 0;
+        do { ++w.b; } while (pre[w.b + 1] == pre[w.b]);
+        w.n = pre[w.b + 1] - pre[w.b];
+    }
+    w.base = static_cast<int64_t>(Hkv) * pre[w.b] + static_cast<int64_t>(w.hk) * w.n;
+    w.g = w.base;
+}
+
+// CTA whose range holds global page p (ranges: [c*P/C, (c+1)*P/C)).
+__device__ __forceinline__ int cta_of(int64_t p, int64_t P, int C) {
+    return static_cast<int>(((p + 1) * C - 1) / P);
+}
+
+__device__ __forceinline__ int load_block_id(const int32_t* row, int lane, int count, int64_t num_blocks,
+                                             uint32_t* err) {
+    int id = 0;
+    if (lane < count) {
+        id = __ldg(row + lane);
+        if (id < 0 || id >= num_blocks) {
+            report(err, FP8KV_ERR_INVALID_ARG);
+            id = 0;
+        }
+    }
+    return id;
+}
+
+// Query fragments of one (sequence, kv head): the B operand of the score MMA,
+// pre-scaled per head by a power of two so the f16 copy is exact (largest |q|
+// in [2^14, 2^15)); cs[j] scales the raw score of head 2*tig+j back and into
+// log2 units.
+template <int D, int G>
+__device__ __forceinline__ void load_query(const DecodeArgs& a, int b, int hk, int gid, int tig,
+                                           uint32_t (&qf)[Geo<D>::KS][2], float (&cs)[2]) {
+    using Gm = Geo<D>;
+    uint32_t qw[Gm::HALVES][Gm::KSH][2];
+    float qmax = 0.f;
+#pragma unroll
+    for (int hh = 0; hh < Gm::HALVES; ++hh) {
+#pragma unroll
+        for (int c = 0; c < Gm::KW / 8; ++c) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (gid < G)
+                v = __ldg(reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.num_q_heads + hk * G + gid) * D +
+                                                         hh * 128 + tig * Gm::KW) + c);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                qw[hh][c * 2 + e / 2][e % 2] = w4[e];
+                qmax = fmaxf(qmax, fmaxf(fabsf(bf16_to_f32(w4[e] & 0xFFFF)), fabsf(bf16_to_f32(w4[e] >> 16))));
+            }
+        }
+    }
+    qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
+    qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
+    int shift = 0;
+    if (qmax > 0.f) {
+        const int e = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFF) - 127;
+        shift = max(-100, min(100, 14 - e));
+    }
+    const float up = __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
+#pragma unroll
+    for (int hh = 0; hh < Gm::HALVES; ++hh)
+#pragma unroll
+        for (int kk = 0; kk < Gm::KSH; ++kk)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const uint32_t w = qw[hh][kk][e];
+                qf[hh * Gm::KSH + kk][e] = pack_f16x2(bf16_to_f32(w & 0xFFFF) * up, bf16_to_f32(w >> 16) * up);
+            }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int sh = __shfl_sync(0xffffffffu, shift, (2 * tig + j) * 4);
+        cs[j] = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+    }
+}
+
+// Folds state (m2, l2, o2) into (m, l, o): the FP32 softmax-merge identity.
+template <int MT>
+__device__ __forceinline__ void combine(float (&m)[2], float (&l)[2], float (&o)[MT][4], const float (&m2)[2],
+                                        const float (&l2)[2], const float (&o2)[MT][4]) {
+    float f1[2], f2[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float M = fmaxf(m[j], m2[j]);
+        const float Mu = M == -INFINITY ? 0.f : M;
+        f1[j] = fast_exp2(m[j] - Mu);
+        f2[j] = fast_exp2(m2[j] - Mu);
+        l[j] = l[j] * f1[j] + l2[j] * f2[j];
+        m[j] = M;
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        o[mt][0] = o[mt][0] * f1[0] + o2[mt][0] * f2[0];
+        o[mt][1] = o[mt][1] * f1[1] + o2[mt][1] * f2[1];
+        o[mt][2] = o[mt][2] * f1[0] + o2[mt][2] * f2[0];
+        o[mt][3] = o[mt][3] * f1[1] + o2[mt][3] * f2[1];
+    }
+}
+
+template <int MT>
+__device__ __forceinline__ void publish(float* x, int lane, const float (&m)[2], const float (&l)[2],
+                                        const float (&o)[MT][4]) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) x[(mt * 4 + r) * 32 + lane] = o[mt][r];
+    x[(MT * 4 + 0) * 32 + lane] = m[0];
+    x[(MT * 4 + 1) * 32 + lane] = m[1];
+    x[(MT * 4 + 2) * 32 + lane] = l[0];
+    x[(MT * 4 + 3) * 32 + lane] = l[1];
+}
+
+template <int MT>
+__device__ __forceinline__ void absorb(const float* x, int lane, float (&m)[2], float (&l)[2], float (&o)[MT][4]) {
+    float m2[2], l2[2], o2[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) o2[mt][r] = x[(mt * 4 + r) * 32 + lane];
+    m2[0] = x[(MT * 4 + 0) * 32 + lane];
+    m2[1] = x[(MT * 4 + 1) * 32 + lane];
+    l2[0] = x[(MT * 4 + 2) * 32 + lane];
+    l2[1] = x[(MT * 4 + 3) * 32 + lane];
+    combine<MT>(m, l, o, m2, l2, o2);
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeArgs a) {
     using Gm = Geo<D>;
+    constexpr int S = Gm::STAGES;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned ring (the swizzle pattern is a function of address
     // bits 4..9); offsetting the shared array keeps the address space known.
     uint8_t* ring = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* full_bar = reinterpret_cast<uint64_t*>(ring + kStages * kStageBytes);
-    uint64_t* empty_bar = full_bar + kStages;
-    int32_t* blk = reinterpret_cast<int32_t*>(empty_bar + kStages);
-    int* flag = blk + kMaxPagesPerSplit;
+    float* xbuf = reinterpret_cast<float*>(ring + S * kStageBytes);  // [2][XW][32]
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(xbuf + 2 * Gm::XW * 32);
+    uint64_t* empty_bar = full_bar + S;
+    int32_t* pre = reinterpret_cast<int32_t*>(empty_bar + S);        // [kMaxBatch + 1] page prefix
+    int32_t* lens = pre + kMaxBatch + 1;                             // [kMaxBatch] clamped lengths
+    volatile int* flag = reinterpret_cast<volatile int*>(lens + kMaxBatch);  // [1] abort
+    int32_t* ids = lens + kMaxBatch + 4;                             // [32] block ids for the producer
 
-    const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // The merge kernel that follows may start now; it waits for this grid's
+    // completion (and memory) before reading anything.
+    griddep_launch_dependents();
     // A previous CTA gave up a wait: skip the work, the call is already failed.
     if (*reinterpret_cast<volatile uint32_t*>(a.err) == FP8KV_ERR_TIMEOUT) return;
-    int L = a.seq_lens[b];
-    if (L < 0 || L > a.max_seq_len) {  // outside the caller's contract: clamp and report
-        if (split == 0 && hk == 0 && threadIdx.x == 0) report(a.err, FP8KV_ERR_INVALID_ARG);
-        L = L < 0 ? 0 : a.max_seq_len;
-    }
-    const int lo = (a.window > 0 && L > a.window) ? L - a.window : 0;
-    const int first_pg = lo / kBS;
-    const int n_pages = L > 0 ? (L - 1) / kBS - first_pg + 1 : 0;
-    const int nsplit = n_pages > 0 ? (n_pages + a.pages_per_split - 1) / a.pages_per_split : 1;
-    if (split >= nsplit) return;
-    const int hq0 = hk * G;
-    uint16_t* out_bh = a.out + (static_cast<int64_t>(b) * a.num_q_heads + hq0) * D;
-    if (n_pages == 0) {
-        for (int i = tid; i < G * D; i += kThreads) out_bh[i] = 0;
-        return;
-    }
-    const int pg_begin = first_pg + split * a.pages_per_split;
-    const int npg = min(a.pages_per_split, first_pg + n_pages - pg_begin);
-    const int n_stages = (npg + Gm::PPS - 1) / Gm::PPS;
+    const int B = a.batch, Hkv = a.num_kv_heads, C = gridDim.x, c = blockIdx.x;
 
-    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq + pg_begin;
-    for (int i = tid; i < npg; i += kThreads) {
-        int id = __ldg(bt + i);
-        if (id < 0 || id >= a.num_blocks) {
-            report(a.err, FP8KV_ERR_INVALID_ARG);
-            id = 0;
+    // ---- attended pages per sequence and their exclusive prefix
+    if (warp == 0) {
+        int run = 0;
+        for (int b0 = 0; b0 < B; b0 += 32) {
+            const int b = b0 + lane;
+            int n = 0;
+            if (b < B) {
+                const int Lraw = __ldg(a.seq_lens + b);
+                if (Lraw < 0 || Lraw > a.max_seq_len) report(a.err, FP8KV_ERR_INVALID_ARG);
+                lens[b] = clamp_len(Lraw, a.max_seq_len);
+                n = attended_pages(lens[b], a.window);
+            }
+            int x = n;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += y;
+            }
+            if (b < B) pre[b] = run + x - n;
+            run += __shfl_sync(0xffffffffu, x, 31);
         }
-        blk[i] = id;
+        if (lane == 0) pre[B] = run;
     }
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
         }
+        flag[1] = 0;
         fence_barrier_init();
     }
     __syncthreads();
 
+    const int64_t P = static_cast<int64_t>(Hkv) * pre[B];
+    // sequences with nothing to attend (length 0) produce zeros; the grid
+    // before this one (on the stream) may still be using the outputs
+    bool has_empty = false;
+    for (int b = c; b < B && !has_empty; b += C) has_empty = pre[b + 1] == pre[b];
+    if (has_empty) griddep_wait();
+    for (int b = c; b < B && has_empty; b += C) {
+        if (pre[b + 1] == pre[b]) {
+            uint16_t* ob = a.out + static_cast<int64_t>(b) * a.num_q_heads * D;
+            for (int i = tid; i < a.num_q_heads * D; i += kThreads) ob[i] = 0;
+            for (int hk = tid; hk < Hkv; hk += kThreads) a.unit_meta[b * Hkv + hk] = make_int2(0, 0);
+        }
+    }
+    const int Ce = static_cast<int>(P < C ? P : C);  // CTAs with work: every one gets >= 1 page
+    if (c >= Ce) return;
+    const int64_t s = static_cast<int64_t>(c) * P / Ce;
+    const int64_t e = static_cast<int64_t>(c + 1) * P / Ce;
+
     if (warp == kNCW) {
         // ------------------------------------------------------------ producer
+        // Lane 0 alone issues the copies; once per 32 pages the warp hands it
+        // the next 32 block ids through shared memory, and loads the 32 after
+        // those into registers while lane 0 works.
         if (lane == 0) {
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
-            const uint64_t pol = l2_policy_evict_first();
-            int issued = 0;
-            for (int st = 0; st < n_stages; ++st) {
-                const int slot = st % kStages;
-                if (st >= kStages &&
-                    !mbar_wait_bounded(&empty_bar[slot], ((st / kStages) & 1) ^ 1, kWaitLimitNs)) {
-                    report(a.err, FP8KV_ERR_TIMEOUT);
-                    break;
-                }
-                const int p0 = st * Gm::PPS;
-                const int np = min(Gm::PPS, npg - p0);
-                mbar_arrive_expect_tx(&full_bar[slot], static_cast<uint32_t>(np * 2 * Gm::PAGE));
-                uint8_t* kst = ring + slot * kStageBytes;
-                uint8_t* vst = kst + kStageHalf;
-                for (int p = 0; p < np; ++p) {
-                    const int id = blk[p0 + p];
+        }
+        const uint64_t pol = l2_policy_evict_first();
+        int st = 0;
+        bool ok = true;
+        Walker w;
+        walk_start(w, pre, B, Hkv, s);
+        // The cache may have been written by the kernel just before this one
+        // (an append); everything above overlapped it, reads start here.
+        griddep_wait();
+        while (ok) {
+            const int64_t seg_end = min(e, w.base + w.n);
+            const int lp0 = static_cast<int>(w.g - w.base);
+            const int np_seg = static_cast<int>(seg_end - w.g);
+            const int L = lens[w.b];
+            const int32_t* row = a.block_tables + static_cast<int64_t>(w.b) * a.max_blocks_per_seq +
+                                 first_token(L, a.window) / kBS + lp0;
+            int nxt = load_block_id(row, lane, np_seg, a.num_blocks, a.err);
+            for (int p0 = 0; p0 < np_seg; p0 += 32) {
+                const int cur = nxt;
+                __syncwarp();  // lane 0 is done with the previous batch
+                ids[lane] = cur;
+                nxt = load_block_id(row + p0 + 32, lane, np_seg - p0 - 32, a.num_blocks, a.err);
+                __syncwarp();
+                if (lane == 0) {
+                    const int nb = min(32, np_seg - p0);
+                    for (int q = 0; q < nb && ok; q += Gm::PPS) {
+                        const int np = min(Gm::PPS, nb - q);
+                        const int slot = st % S;
+                        if (flag[1] || (st >= S && !mbar_wait_bounded(&empty_bar[slot], ((st / S) & 1) ^ 1,
+                                                                       kWaitLimitNs))) {
+                            report(a.err, FP8KV_ERR_TIMEOUT);
+                            flag[1] = 1;
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full_bar[slot], static_cast<uint32_t>(np * 2 * Gm::PAGE));
+                        uint8_t* kst = ring + slot * kStageBytes;
+                        uint8_t* vst = kst + kStageHalf;
+                        for (int p = 0; p < np; ++p) {
+                            const int id = ids[q + p];
 #pragma unroll
-                    for (int h = 0; h < Gm::HALVES; ++h) {
-                        tma_load_4d(kst + p * Gm::PAGE + h * Gm::BOX, &tmK, &full_bar[slot], h * 128, 0, hk, id, pol);
-                        tma_load_4d(vst + p * Gm::PAGE + h * Gm::BOX, &tmV, &full_bar[slot], h * 128, 0, hk, id, pol);
+                            for (int h = 0; h < Gm::HALVES; ++h) {
+                                tma_load_4d(kst + p * Gm::PAGE + h * Gm::BOX, &tmK, &full_bar[slot], h * 128, 0,
+                                            w.hk, id, pol);
+                                tma_load_4d(vst + p * Gm::PAGE + h * Gm::BOX, &tmV, &full_bar[slot], h * 128, 0,
+                                            w.hk, id, pol);
+                            }
+                        }
+                        ++st;
                     }
                 }
-                issued = st + 1;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
             }
-            // Only after a failed wait can copies still be in flight while
-            // consumers have stopped waiting: drain them (bounded) before exit.
-            if (issued < n_stages) {
-                for (int st = issued > kStages ? issued - kStages : 0; st < issued; ++st)
-                    mbar_wait_bounded(&full_bar[st % kStages], (st / kStages) & 1, kWaitLimitNs);
-            }
+            if (!ok || seg_end >= e) break;
+            walk_next(w, pre, Hkv);
+        }
+        // Only after a failed wait can copies still be in flight while the
+        // consumers have stopped waiting: drain them (bounded) before exit.
+        if (!ok && lane == 0) {
+            for (int t = st > S ? st - S : 0; t < st; ++t)
+                mbar_wait_bounded(&full_bar[t % S], (t / S) & 1, kWaitLimitNs);
         }
         return;
     }
 
     // ---------------------------------------------------------------- consumers
     const int gid = lane >> 2, tig = lane & 3;
-
-    // Query fragments (B operand of the score MMA), pre-scaled per head by a
-    // power of two so the f16 copy is exact; the score is scaled back later.
     uint32_t qf[Gm::KS][2];
     float cs[2];
-    {
-        uint32_t qw[Gm::HALVES][Gm::KSH][2];
-        float qmax = 0.f;
-#pragma unroll
-        for (int hh = 0; hh < Gm::HALVES; ++hh) {
-#pragma unroll
-            for (int c = 0; c < Gm::KW / 8; ++c) {  // KW dims = 2*KW bytes of bf16 = KW/8 uint4
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (gid < G)
-                    v = __ldg(reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.num_q_heads + hq0 + gid) * D +
-                                                             hh * 128 + tig * Gm::KW) + c);
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    qw[hh][c * 2 + e / 2][e % 2] = w4[e];
-                    qmax = fmaxf(qmax, fmaxf(fabsf(bf16_to_f32(w4[e] & 0xFFFF)), fabsf(bf16_to_f32(w4[e] >> 16))));
-                }
-            }
-        }
-        qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
-        qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
-        // shift so that the largest |q| of the head lands in [2^14, 2^15)
-        int shift = 0;
-        if (qmax > 0.f) {
-            const int e = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFF) - 127;
-            shift = max(-100, min(100, 14 - e));
-        }
-        const float up = __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
-#pragma unroll
-        for (int hh = 0; hh < Gm::HALVES; ++hh)
-#pragma unroll
-            for (int kk = 0; kk < Gm::KSH; ++kk)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const uint32_t w = qw[hh][kk][e];
-                    qf[hh * Gm::KSH + kk][e] = pack_f16x2(bf16_to_f32(w & 0xFFFF) * up, bf16_to_f32(w >> 16) * up);
-                }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int sh = __shfl_sync(0xffffffffu, shift, (2 * tig + j) * 4);
-            cs[j] = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
-        }
-    }
-
-    float m[2] = {-INFINITY, -INFINITY};
-    float l[2] = {0.f, 0.f};
+    float m[2], l[2];
     float o[Gm::MT][4];
+    int st_base = 0;
+    Walker w;
+    walk_start(w, pre, B, Hkv, s);
+    while (true) {
+        const int64_t seg_end = min(e, w.base + w.n);
+        const int lp0 = static_cast<int>(w.g - w.base);
+        const int np_seg = static_cast<int>(seg_end - w.g);
+        const int nst = (np_seg + Gm::PPS - 1) / Gm::PPS;
+        const int L = lens[w.b];
+        const int lo = first_token(L, a.window);
+        const int pg_first = lo / kBS + lp0;  // page index (in the sequence) of the segment's first page
+        load_query<D, G>(a, w.b, w.hk, gid, tig, qf, cs);
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
 #pragma unroll
-    for (int mt = 0; mt < Gm::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        for (int mt = 0; mt < Gm::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-    for (int st = warp; st < n_stages; st += kNCW) {
-        const int slot = st % kStages;
-        if (!mbar_wait_bounded(&full_bar[slot], (st / kStages) & 1, kWaitLimitNs)) {
-            report(a.err, FP8KV_ERR_TIMEOUT);
-            break;
-        }
-        const int p0 = st * Gm::PPS;
-        const int np = min(Gm::PPS, npg - p0);
-        const uint8_t* kst = ring + slot * kStageBytes;
-        const uint8_t* vst = kst + kStageHalf;
-        const int tok_base = (pg_begin + p0) * kBS;
-
-        // ---- scores S^T[token][head] = K Q^T
-        float s[Gm::PPS][4];
-#pragma unroll
-        for (int p = 0; p < Gm::PPS; ++p) {
-            s[p][0] = s[p][1] = s[p][2] = s[p][3] = 0.f;
-            if (p < np) {
-#pragma unroll
-                for (int hh = 0; hh < Gm::HALVES; ++hh) {
-                    const uint8_t* box = kst + p * Gm::PAGE + hh * Gm::BOX;
-                    uint32_t w0[Gm::KSH], w1[Gm::KSH];
-#pragma unroll
-                    for (int c = 0; c < Gm::KW / 16; ++c) {
-                        const uint4 x = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(gid, tig * Gm::KW + 16 * c));
-                        const uint4 y = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(gid + 8, tig * Gm::KW + 16 * c));
-                        w0[4 * c + 0] = x.x; w0[4 * c + 1] = x.y; w0[4 * c + 2] = x.z; w0[4 * c + 3] = x.w;
-                        w1[4 * c + 0] = y.x; w1[4 * c + 1] = y.y; w1[4 * c + 2] = y.z; w1[4 * c + 3] = y.w;
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < Gm::KSH; ++kk) {
-                        uint32_t af[4];
-                        e4m3x4_to_f16x2x2(w0[kk], af[0], af[2]);
-                        e4m3x4_to_f16x2x2(w1[kk], af[1], af[3]);
-                        mma_16816(s[p], af, qf[hh * Gm::KSH + kk][0], qf[hh * Gm::KSH + kk][1], s[p]);
-                    }
-                }
+        for (int i = (warp - st_base % kNCW + kNCW) % kNCW; i < nst; i += kNCW) {
+            const int st = st_base + i;
+            const int slot = st % S;
+            if (flag[1]) break;
+            if (!mbar_wait_bounded(&full_bar[slot], (st / S) & 1, kWaitLimitNs)) {
+                report(a.err, FP8KV_ERR_TIMEOUT);
+                flag[1] = 1;
+                break;
             }
-        }
+            const int p0 = i * Gm::PPS;
+            const int np = min(Gm::PPS, np_seg - p0);
+            const uint8_t* kst = ring + slot * kStageBytes;
+            const uint8_t* vst = kst + kStageHalf;
+            const int tok_base = (pg_first + p0) * kBS;
 
-        // ---- mask, scale to log2 units, stage maximum
-        float mx[2] = {-INFINITY, -INFINITY};
+            // ---- scores S^T[token][head] = K Q^T
+            float sc[Gm::PPS][4];
 #pragma unroll
-        for (int p = 0; p < Gm::PPS; ++p)
+            for (int p = 0; p < Gm::PPS; ++p) {
+                sc[p][0] = sc[p][1] = sc[p][2] = sc[p][3] = 0.f;
+                if (p < np) {
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int tok = tok_base + p * kBS + gid + 8 * e;
-                const bool valid = (p < np) && tok >= lo && tok < L;
+                    for (int hh = 0; hh < Gm::HALVES; ++hh) {
+                        const uint8_t* box = kst + p * Gm::PAGE + hh * Gm::BOX;
+                        uint32_t w0[Gm::KSH], w1[Gm::KSH];
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const float t = valid ? s[p][2 * e + j] * cs[j] : -INFINITY;
-                    s[p][2 * e + j] = t;
-                    mx[j] = fmaxf(mx[j], t);
-                }
-            }
-        float alpha[2], muse[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
-            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
-            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
-            const float mn = fmaxf(m[j], mx[j]);
-            muse[j] = mn == -INFINITY ? 0.f : mn;
-            alpha[j] = fast_exp2(m[j] - muse[j]);
-            m[j] = mn;
-        }
-
-        // ---- probabilities -> f16 B fragments of the value MMA
-        uint32_t pb[Gm::PPS][2];
-        float lsum[2] = {0.f, 0.f};
-#pragma unroll
-        for (int p = 0; p < Gm::PPS; ++p) {
-            const float p00 = fast_exp2(s[p][0] - muse[0]);
-            const float p01 = fast_exp2(s[p][1] - muse[1]);
-            const float p10 = fast_exp2(s[p][2] - muse[0]);
-            const float p11 = fast_exp2(s[p][3] - muse[1]);
-            lsum[0] += p00 + p10;
-            lsum[1] += p01 + p11;
-            pb[p][0] = movmatrix_trans(pack_f16x2(p00, p01));
-            pb[p][1] = movmatrix_trans(pack_f16x2(p10, p11));
-        }
-        l[0] = l[0] * alpha[0] + lsum[0];
-        l[1] = l[1] * alpha[1] + lsum[1];
-
-        // ---- P.V tile of this stage: O^T[dim][head] = V^T P^T
-        float ot[Gm::MT][4];
-#pragma unroll
-        for (int mt = 0; mt < Gm::MT; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
-#pragma unroll
-        for (int p = 0; p < Gm::PPS; ++p) {
-            if (p < np) {
-                const int t0 = tok_base + p * kBS;
-                const bool edge = t0 < lo || t0 + kBS > L;
-#pragma unroll
-                for (int hh = 0; hh < Gm::HALVES; ++hh) {
-                    const uint8_t* box = vst + p * Gm::PAGE + hh * Gm::BOX;
-                    uint32_t v[4][Gm::VW / 4];
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int row = 2 * tig + (r & 1) + 8 * (r >> 1);
-                        if constexpr (Gm::VW == 16) {
-                            const uint4 x = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(row, gid * 16));
-                            v[r][0] = x.x; v[r][1] = x.y; v[r][2] = x.z; v[r][3] = x.w;
-                        } else {
-                            const uint2 x = *reinterpret_cast<const uint2*>(box + swz<Gm::ROWB>(row, gid * 8));
-                            v[r][0] = x.x; v[r][1] = x.y;
+                        for (int cc = 0; cc < Gm::KW / 16; ++cc) {
+                            const uint4 x = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(gid, tig * Gm::KW + 16 * cc));
+                            const uint4 y = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(gid + 8, tig * Gm::KW + 16 * cc));
+                            w0[4 * cc + 0] = x.x; w0[4 * cc + 1] = x.y; w0[4 * cc + 2] = x.z; w0[4 * cc + 3] = x.w;
+                            w1[4 * cc + 0] = y.x; w1[4 * cc + 1] = y.y; w1[4 * cc + 2] = y.z; w1[4 * cc + 3] = y.w;
                         }
-                        if (edge) {
-                            const int tok = t0 + row;
-                            if (tok < lo || tok >= L) {
 #pragma unroll
-                                for (int w = 0; w < Gm::VW / 4; ++w) v[r][w] = 0u;  // never let stale NaN codes meet p = 0
+                        for (int kk = 0; kk < Gm::KSH; ++kk) {
+                            uint32_t af[4];
+                            e4m3x4_to_f16x2x2(w0[kk], af[0], af[2]);
+                            e4m3x4_to_f16x2x2(w1[kk], af[1], af[3]);
+                            mma_16816(sc[p], af, qf[hh * Gm::KSH + kk][0], qf[hh * Gm::KSH + kk][1], sc[p]);
+                        }
+                    }
+                }
+            }
+
+            // ---- mask, scale to log2 units, stage maximum
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int p = 0; p < Gm::PPS; ++p)
+#pragma unroll
+                for (int e2 = 0; e2 < 2; ++e2) {
+                    const int tok = tok_base + p * kBS + gid + 8 * e2;
+                    const bool valid = (p < np) && tok >= lo && tok < L;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const float t = valid ? sc[p][2 * e2 + j] * cs[j] : -INFINITY;
+                        sc[p][2 * e2 + j] = t;
+                        mx[j] = fmaxf(mx[j], t);
+                    }
+                }
+            float alpha[2], muse[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
+                mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
+                mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
+                const float mn = fmaxf(m[j], mx[j]);
+                muse[j] = mn == -INFINITY ? 0.f : mn;
+                alpha[j] = fast_exp2(m[j] - muse[j]);
+                m[j] = mn;
+            }
+
+            // ---- probabilities -> f16 B fragments of the value MMA
+            uint32_t pb[Gm::PPS][2];
+            float lsum[2] = {0.f, 0.f};
+#pragma unroll
+            for (int p = 0; p < Gm::PPS; ++p) {
+                const float p00 = fast_exp2(sc[p][0] - muse[0]);
+                const float p01 = fast_exp2(sc[p][1] - muse[1]);
+                const float p10 = fast_exp2(sc[p][2] - muse[0]);
+                const float p11 = fast_exp2(sc[p][3] - muse[1]);
+                lsum[0] += p00 + p10;
+                lsum[1] += p01 + p11;
+                pb[p][0] = movmatrix_trans(pack_f16x2(p00, p01));
+                pb[p][1] = movmatrix_trans(pack_f16x2(p10, p11));
+            }
+            l[0] = l[0] * alpha[0] + lsum[0];
+            l[1] = l[1] * alpha[1] + lsum[1];
+
+            // ---- P.V tile of this stage: O^T[dim][head] = V^T P^T
+            float ot[Gm::MT][4];
+#pragma unroll
+            for (int mt = 0; mt < Gm::MT; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
+#pragma unroll
+            for (int p = 0; p < Gm::PPS; ++p) {
+                if (p < np) {
+                    const int t0 = tok_base + p * kBS;
+                    const bool edge = t0 < lo || t0 + kBS > L;
+#pragma unroll
+                    for (int hh = 0; hh < Gm::HALVES; ++hh) {
+                        const uint8_t* box = vst + p * Gm::PAGE + hh * Gm::BOX;
+                        uint32_t v[4][Gm::VW / 4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const int row = 2 * tig + (r & 1) + 8 * (r >> 1);
+                            if constexpr (Gm::VW == 16) {
+                                const uint4 x = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(row, gid * 16));
+                                v[r][0] = x.x; v[r][1] = x.y; v[r][2] = x.z; v[r][3] = x.w;
+                            } else {
+                                const uint2 x = *reinterpret_cast<const uint2*>(box + swz<Gm::ROWB>(row, gid * 8));
+                                v[r][0] = x.x; v[r][1] = x.y;
+                            }
+                            if (edge) {
+                                const int tok = t0 + row;
+                                if (tok < lo || tok >= L) {
+#pragma unroll
+                                    for (int ww = 0; ww < Gm::VW / 4; ++ww) v[r][ww] = 0u;  // never let stale NaN codes meet p = 0
+                                }
                             }
                         }
-                    }
 #pragma unroll
-                    for (int mtl = 0; mtl < Gm::MTH; ++mtl) {
-                        const uint32_t sel = (mtl & 1) ? 0x7362u : 0x5140u;
-                        const uint32_t x01 = byte_perm(v[0][mtl >> 1], v[1][mtl >> 1], sel);
-                        const uint32_t x23 = byte_perm(v[2][mtl >> 1], v[3][mtl >> 1], sel);
-                        uint32_t af[4];
-                        e4m3x4_to_f16x2x2(x01, af[0], af[1]);
-                        e4m3x4_to_f16x2x2(x23, af[2], af[3]);
-                        mma_16816(ot[hh * Gm::MTH + mtl], af, pb[p][0], pb[p][1], ot[hh * Gm::MTH + mtl]);
+                        for (int mtl = 0; mtl < Gm::MTH; ++mtl) {
+                            const uint32_t sel = (mtl & 1) ? 0x7362u : 0x5140u;
+                            const uint32_t x01 = byte_perm(v[0][mtl >> 1], v[1][mtl >> 1], sel);
+                            const uint32_t x23 = byte_perm(v[2][mtl >> 1], v[3][mtl >> 1], sel);
+                            uint32_t af[4];
+                            e4m3x4_to_f16x2x2(x01, af[0], af[1]);
+                            e4m3x4_to_f16x2x2(x23, af[2], af[3]);
+                            mma_16816(ot[hh * Gm::MTH + mtl], af, pb[p][0], pb[p][1], ot[hh * Gm::MTH + mtl]);
+                        }
                     }
                 }
             }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[slot]);
 
-        // ---- fold the tile into the FP32 accumulators
+            // ---- fold the tile into the FP32 accumulators
 #pragma unroll
-        for (int mt = 0; mt < Gm::MT; ++mt) {
-            o[mt][0] = fmaf(o[mt][0], alpha[0], ot[mt][0]);
-            o[mt][1] = fmaf(o[mt][1], alpha[1], ot[mt][1]);
-            o[mt][2] = fmaf(o[mt][2], alpha[0], ot[mt][2]);
-            o[mt][3] = fmaf(o[mt][3], alpha[1], ot[mt][3]);
+            for (int mt = 0; mt < Gm::MT; ++mt) {
+                o[mt][0] = fmaf(o[mt][0], alpha[0], ot[mt][0]);
+                o[mt][1] = fmaf(o[mt][1], alpha[1], ot[mt][1]);
+                o[mt][2] = fmaf(o[mt][2], alpha[0], ot[mt][2]);
+                o[mt][3] = fmaf(o[mt][3], alpha[1], ot[mt][3]);
+            }
         }
-    }
+        st_base += nst;
 
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        l[j] += __shfl_xor_sync(0xffffffffu, l[j], 4);
-        l[j] += __shfl_xor_sync(0xffffffffu, l[j], 8);
-        l[j] += __shfl_xor_sync(0xffffffffu, l[j], 16);
-    }
-
-    // ---------------------------------------------------------------- merge warps
-    consumer_sync();  // every consumer is done with the ring: reuse it
-    float* Ow = reinterpret_cast<float*>(ring);   // [kNCW][8][D]
-    float* mw = Ow + kNCW * 8 * D;                // [kNCW][8]
-    float* lw = mw + kNCW * 8;
-#pragma unroll
-    for (int mt = 0; mt < Gm::MT; ++mt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int dim = (mt / Gm::MTH) * 128 + Gm::VW * gid + 2 * (mt % Gm::MTH) + e;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) Ow[(warp * 8 + 2 * tig + j) * D + dim] = o[mt][2 * e + j];
-        }
-    if (gid == 0) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            mw[warp * 8 + 2 * tig + j] = m[j];
-            lw[warp * 8 + 2 * tig + j] = l[j];
+            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 4);
+            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 8);
+            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 16);
         }
-    }
-    consumer_sync();
 
-    const int bh = b * a.num_kv_heads + hk;
-    const int64_t part = static_cast<int64_t>(bh) * a.max_splits + split;
-    for (int idx = tid; idx < G * D; idx += kNCW * 32) {
-        const int h = idx / D, i = idx - h * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kNCW; ++w) M = fmaxf(M, mw[w * 8 + h]);
-        const float Mu = M == -INFINITY ? 0.f : M;
-        float O = 0.f, Lh = 0.f;
-#pragma unroll
-        for (int w = 0; w < kNCW; ++w) {
-            const float f = fast_exp2(mw[w * 8 + h] - Mu);
-            O += Ow[(w * 8 + h) * D + i] * f;
-            Lh += lw[w * 8 + h] * f;
-        }
-        if (nsplit == 1) {
-            out_bh[idx] = f32_to_bf16(Lh > 0.f ? O * a.v_scale / Lh : 0.f);
-        } else {
-            a.part_o[part * G * D + idx] = O;
-            if (i == 0) a.part_ml[part * 8 + h] = make_float2(M, Lh);
-        }
-    }
-    if (nsplit == 1) return;
+        // ---- merge the four warps' states into warp 0 (tree through smem)
+        if (warp >= 2) publish<Gm::MT>(xbuf + (warp - 2) * Gm::XW * 32, lane, m, l, o);
+        consumer_sync();
+        if (warp < 2) absorb<Gm::MT>(xbuf + warp * Gm::XW * 32, lane, m, l, o);
+        consumer_sync();
+        if (warp == 1) publish<Gm::MT>(xbuf, lane, m, l, o);
+        consumer_sync();
+        if (warp == 0) absorb<Gm::MT>(xbuf, lane, m, l, o);
 
-    // ---------------------------------------------------------------- merge splits
-    __threadfence();
-    consumer_sync();
-    if (tid == 0) {
-        const int old = atomicAdd(&a.counters[bh], 1);
-        *flag = (old == nsplit - 1);
-    }
-    consumer_sync();
-    if (!*flag) return;
-    __threadfence();
-    const int64_t base = static_cast<int64_t>(bh) * a.max_splits;
-    for (int idx = tid; idx < G * D; idx += kNCW * 32) {
-        const int h = idx / D;
-        float M = -INFINITY;
-        for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(&a.part_ml[(base + sp) * 8 + h].x));
-        const float Mu = M == -INFINITY ? 0.f : M;
-        float O = 0.f, Lh = 0.f;
-        for (int sp = 0; sp < nsplit; ++sp) {
-            const float2 ml = __ldcg(&a.part_ml[(base + sp) * 8 + h]);
-            const float f = fast_exp2(ml.x - Mu);
-            O += __ldcg(&a.part_o[(base + sp) * G * D + idx]) * f;
-            Lh += ml.y * f;
+        // ---- emit: the whole unit in this CTA -> output; else a partial
+        // that the merge kernel combines.  The CTA holding the unit's first
+        // page records where the unit's partials are.
+        const int u = w.b * Hkv + w.hk;
+        const int c_first = cta_of(w.base, P, Ce);
+        const int c_last = cta_of(w.base + w.n - 1, P, Ce);
+        const int k_u = c_last - c_first + 1;
+        if (warp == 0) {
+            if (k_u == 1) {
+                uint16_t* out_u = a.out + (static_cast<int64_t>(w.b) * a.num_q_heads + w.hk * G) * D;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int h = 2 * tig + j;
+                    const float sc_out = l[j] > 0.f ? a.v_scale / l[j] : 0.f;
+                    if (h < G) {
+#pragma unroll
+                        for (int mt = 0; mt < Gm::MT; ++mt)
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2) {
+                                const int dim = (mt / Gm::MTH) * 128 + Gm::VW * gid + 2 * (mt % Gm::MTH) + e2;
+                                out_u[h * D + dim] = f32_to_bf16(o[mt][2 * e2 + j] * sc_out);
+                            }
+                    }
+                }
+            } else {
+                const int64_t slot_idx = static_cast<int64_t>(u) + c;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int h = 2 * tig + j;
+                    if (h < G) {
+                        float* po = a.part_o + (slot_idx * G + h) * D;
+#pragma unroll
+                        for (int mt = 0; mt < Gm::MT; ++mt)
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2)
+                                po[(mt / Gm::MTH) * 128 + Gm::VW * gid + 2 * (mt % Gm::MTH) + e2] = o[mt][2 * e2 + j];
+                        if (gid == 0) a.part_ml[slot_idx * 8 + h] = make_float2(m[j], l[j]);
+                    }
+                }
+            }
+            if (c == c_first && lane == 0) a.unit_meta[u] = make_int2(u + c_first, k_u);
         }
-        out_bh[idx] = f32_to_bf16(Lh > 0.f ? O * a.v_scale / Lh : 0.f);
+        consumer_sync();  // warp 0 is done with the exchange buffer
+        if (seg_end >= e) break;
+        walk_next(w, pre, Hkv);
     }
-    if (tid == 0) a.counters[bh] = 0;  // ready for the next call
+}
+
+// Combines the partials of every (sequence, kv head) unit that was split over
+// several CTAs: one CTA per (unit, query head of the group).  Its threads split
+// the unit's partials into KS slices (8 loads in flight per thread, one online
+// softmax-merge pass), then combine the slices in shared memory.  It starts as
+// a programmatic dependent of the decode grid and waits for that grid's
+// completion before reading.
+template <int D, int G>
+__global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
+    constexpr int NG = D / 4;       // float4 groups per head: 16, 32, 64
+    constexpr int KS = 128 / NG;    // slices of the partial list: 8, 4, 2
+    __shared__ float sm_m[KS][NG], sm_l[KS][NG];
+    __shared__ float4 sm_o[KS][NG];
+    griddep_wait();
+    const int u = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int g4 = tid % NG, ks = tid / NG;
+    const int2 meta = a.unit_meta[u];
+    const int k_u = meta.y;
+    if (k_u <= 1) return;  // empty, or written directly by its only CTA
+    const int64_t s0 = meta.x;
+    float M = -INFINITY, Lh = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = ks; k0 < k_u; k0 += 8 * KS) {
+        float2 ml[8];
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int k = k0 + j * KS;
+            if (k < k_u) {
+                ml[j] = a.part_ml[(s0 + k) * 8 + h];
+                v[j] = *(reinterpret_cast<const float4*>(a.part_o + ((s0 + k) * G + h) * D) + g4);
+            } else {
+                ml[j] = make_float2(-INFINITY, 0.f);
+                v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float Mb = M;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) Mb = fmaxf(Mb, ml[j].x);
+        const float Mbu = Mb == -INFINITY ? 0.f : Mb;
+        const float r = fast_exp2(M - Mbu);
+        acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+        Lh *= r;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float f = fast_exp2(ml[j].x - Mbu);
+            acc.x += f * v[j].x; acc.y += f * v[j].y; acc.z += f * v[j].z; acc.w += f * v[j].w;
+            Lh += f * ml[j].y;
+        }
+        M = Mb;
+    }
+    sm_m[ks][g4] = M;
+    sm_l[ks][g4] = Lh;
+    sm_o[ks][g4] = acc;
+    __syncthreads();
+    if (ks != 0) return;
+    float Mt = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < KS; ++j) Mt = fmaxf(Mt, sm_m[j][g4]);
+    const float Mtu = Mt == -INFINITY ? 0.f : Mt;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float Lt = 0.f;
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {
+        const float f = fast_exp2(sm_m[j][g4] - Mtu);
+        o.x += f * sm_o[j][g4].x; o.y += f * sm_o[j][g4].y; o.z += f * sm_o[j][g4].z; o.w += f * sm_o[j][g4].w;
+        Lt += f * sm_l[j][g4];
+    }
+    const float sc_out = Lt > 0.f ? a.v_scale / Lt : 0.f;
+    const int b = u / a.num_kv_heads, hk = u - b * a.num_kv_heads;
+    uint16_t* out = a.out + (static_cast<int64_t>(b) * a.num_q_heads + hk * G + h) * D;
+    const uint32_t lo2 = f32_to_bf16(o.x * sc_out) | (static_cast<uint32_t>(f32_to_bf16(o.y * sc_out)) << 16);
+    const uint32_t hi2 = f32_to_bf16(o.z * sc_out) | (static_cast<uint32_t>(f32_to_bf16(o.w * sc_out)) << 16);
+    *reinterpret_cast<uint2*>(out + g4 * 4) = make_uint2(lo2, hi2);
 }
 
 // ---------------------------------------------------------------- host side
 
 struct Plan {
-    int pages_per_split;
-    int max_splits;
+    int batch;  // sequences per launch (batches above kMaxBatch run in chunks)
+    int ctas;   // CTAs per launch
 };
 
-int stage_pages(int D) { return kStageHalf / (kBS * D); }
-
 Plan make_plan(int batch, int num_kv_heads, int D, int max_seq_len, int window, int sms) {
-    Plan p{1, 1};
+    (void)D;
+    Plan p{std::max(1, std::min(batch, kMaxBatch)), 1};
     if (max_seq_len <= 0) return p;
-    const int all_pages = (max_seq_len + kBS - 1) / kBS;
-    int max_pages = all_pages;
-    if (window > 0 && window < max_seq_len) max_pages = std::min(all_pages, (window + kBS - 1) / kBS + 1);
-    const int64_t units = static_cast<int64_t>(batch) * num_kv_heads;
-    const int64_t target = static_cast<int64_t>(sms) * kCtasPerSm * 2;
-    int64_t splits = std::max<int64_t>(1, (target + units - 1) / units);
-    const int sp = stage_pages(D);
-    int pps = static_cast<int>((max_pages + splits - 1) / splits);
-    pps = std::max(sp, (pps + sp - 1) / sp * sp);
-    if (pps > kMaxPagesPerSplit) pps = kMaxPagesPerSplit;
-    p.pages_per_split = pps;
-    p.max_splits = (max_pages + pps - 1) / pps;
+    const int64_t all_pages = (max_seq_len + kBS - 1) / kBS;
+    int64_t max_pages = all_pages;
+    if (window > 0 && window < max_seq_len) max_pages = std::min<int64_t>(all_pages, (window + kBS - 1) / kBS + 1);
+    const int64_t pmax = static_cast<int64_t>(p.batch) * num_kv_heads * max_pages;
+    const int64_t want = (pmax + kMinPagesPerCta - 1) / kMinPagesPerCta;
+    p.ctas = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>(std::min<int64_t>(want, static_cast<int64_t>(sms) * kCtasPerSm), kMaxMergeSplits)));
     return p;
 }
 
@@ -524,20 +777,32 @@ struct WsLayout {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 WsLayout ws_layout(int batch, int num_q_heads, int num_kv_heads, int D, const Plan& p) {
-    const size_t units = static_cast<size_t>(batch) * num_kv_heads;
+    (void)batch;
+    const size_t units = static_cast<size_t>(p.batch) * num_kv_heads;
+    const size_t slots = units + p.ctas;
     const int G = num_q_heads / num_kv_heads;
     WsLayout w;
-    w.counters = 256;
-    w.ml = w.counters + align256(units * sizeof(int32_t));
-    w.o = w.ml + align256(units * p.max_splits * 8 * sizeof(float2));
-    w.total = w.o + align256(units * p.max_splits * G * D * sizeof(float));
+    w.counters = 256;  // per-unit (first slot, count) metadata
+    w.ml = w.counters + align256(units * sizeof(int2));
+    w.o = w.ml + align256(slots * 8 * sizeof(float2));
+    w.total = w.o + align256(slots * G * D * sizeof(float));
     return w;
 }
 
+// SM count of the current device (queried once per device).
 int device_sms(int* sms) {
+    static std::atomic<int> cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) {
+            *sms = c;
+            return 0;
+        }
+    }
     if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    if (dev >= 0 && dev < 64) cache[dev].store(*sms, std::memory_order_relaxed);
     return 0;
 }
 
@@ -561,7 +826,7 @@ EncodeTiledFn encode_fn() {
 
 // The cache as a 4-D tensor {D, 16 tokens, kv heads, blocks} of bytes; one box
 // is one page (or one 128-byte-wide half of a D=256 page).
-bool make_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int Hkv, int D) {
+bool encode_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int Hkv, int D) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(kBS),
@@ -576,12 +841,45 @@ bool make_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int Hk
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t smem_bytes() {
-    return 1024 + kStages * kStageBytes + 2 * kStages * sizeof(uint64_t) + kMaxPagesPerSplit * sizeof(int32_t) + 64;
+// Encoding a tensor map is pure host work on its arguments; the last few
+// (pointer, shape) -> map results are kept so repeated decode calls over the
+// same cache skip it.
+bool make_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int Hkv, int D) {
+    struct Entry {
+        const void* base;
+        int64_t num_blocks;
+        int Hkv, D;
+        CUtensorMap map;
+    };
+    constexpr int kEntries = 8;
+    static std::mutex mu;
+    static Entry entries[kEntries];
+    static int used = 0, next = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i) {
+            const Entry& e = entries[i];
+            if (e.base == base && e.num_blocks == num_blocks && e.Hkv == Hkv && e.D == D) {
+                *m = e.map;
+                return true;
+            }
+        }
+    }
+    if (!encode_cache_map(m, base, num_blocks, Hkv, D)) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    Entry& e = entries[next];
+    e.base = base;
+    e.num_blocks = num_blocks;
+    e.Hkv = Hkv;
+    e.D = D;
+    e.map = *m;
+    next = (next + 1) % kEntries;
+    if (used < kEntries) ++used;
+    return true;
 }
 
 template <int D, int G>
-cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArgs& a, int batch, int Hkv,
+cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArgs& a, int ctas,
                    cudaStream_t stream) {
     // The shared-memory opt-in is per device; remember which devices have it.
     static std::atomic<uint64_t> done_mask{0};
@@ -591,26 +889,42 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
     if (bit == 0 || !(done_mask.load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(paged_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem_bytes()));
+                                 static_cast<int>(smem_bytes<D>()));
         if (e != cudaSuccess) return e;
         done_mask.fetch_or(bit, std::memory_order_release);
     }
+    // Both grids may start before the previous work on the stream ends; each
+    // waits (griddepcontrol.wait) before touching what that work wrote.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.max_splits, Hkv, batch);
+    cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes();
+    cfg.dynamicSmemBytes = smem_bytes<D>();
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G>, mk, mv, a);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G>, mk, mv, a);
+    if (e != cudaSuccess || ctas == 1) return e;  // one CTA: every unit is written directly
+    cudaLaunchConfig_t mcfg = {};
+    mcfg.gridDim = dim3(a.batch * a.num_kv_heads, G);
+    mcfg.blockDim = dim3(128);
+    mcfg.dynamicSmemBytes = 0;
+    mcfg.stream = stream;
+    mcfg.attrs = attr;
+    mcfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&mcfg, merge_kernel<D, G>, a);
 }
 
 template <int D>
-cudaError_t launch_g(int G, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArgs& a, int batch, int Hkv,
+cudaError_t launch_g(int G, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArgs& a, int ctas,
                      cudaStream_t s) {
     switch (G) {
-        case 1: return launch<D, 1>(mk, mv, a, batch, Hkv, s);
-        case 2: return launch<D, 2>(mk, mv, a, batch, Hkv, s);
-        case 4: return launch<D, 4>(mk, mv, a, batch, Hkv, s);
-        case 8: return launch<D, 8>(mk, mv, a, batch, Hkv, s);
+        case 1: return launch<D, 1>(mk, mv, a, ctas, s);
+        case 2: return launch<D, 2>(mk, mv, a, ctas, s);
+        case 4: return launch<D, 4>(mk, mv, a, ctas, s);
+        case 8: return launch<D, 8>(mk, mv, a, ctas, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -653,6 +967,10 @@ extern "C" fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache
     if (num_blocks >= (INT64_C(1) << 31) || num_blocks * num_kv_heads >= (INT64_C(1) << 31))
         return FP8KV_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(max_blocks_per_seq) * block_size < max_seq_len) return FP8KV_ERR_INVALID_ARG;
+    // total (sequence, kv head, page) triples of one launch must stay far inside int64 index math
+    if (static_cast<int64_t>(std::min(batch, kMaxBatch)) * num_kv_heads * ((max_seq_len + kBS - 1) / kBS + 1) >=
+        (INT64_C(1) << 40))
+        return FP8KV_ERR_UNSUPPORTED;
     if (batch == 0) return FP8KV_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out) return FP8KV_ERR_INVALID_ARG;
     if (!a16(q) || !a16(k_cache) || !a16(v_cache) || !a16(out)) return FP8KV_ERR_INVALID_ARG;
@@ -660,8 +978,8 @@ extern "C" fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache
         return FP8KV_ERR_INVALID_ARG;
     int sms = 0;
     if (device_sms(&sms) != 0) return FP8KV_ERR_CUDA;
-    const Plan p = make_plan(batch, num_kv_heads, head_dim, max_seq_len, window, sms);
-    const WsLayout w = ws_layout(batch, num_q_heads, num_kv_heads, head_dim, p);
+    const WsLayout w = ws_layout(batch, num_q_heads, num_kv_heads, head_dim,
+                                 make_plan(batch, num_kv_heads, head_dim, max_seq_len, window, sms));
     if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return FP8KV_ERR_WORKSPACE;
 
@@ -671,34 +989,39 @@ extern "C" fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache
         return FP8KV_ERR_CUDA;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    DecodeArgs a;
-    a.q = static_cast<const uint16_t*>(q);
-    a.block_tables = block_tables;
-    a.seq_lens = seq_lens;
-    a.out = static_cast<uint16_t*>(out);
-    a.err = reinterpret_cast<uint32_t*>(ws);
-    a.counters = reinterpret_cast<int32_t*>(ws + w.counters);
-    a.part_ml = reinterpret_cast<float2*>(ws + w.ml);
-    a.part_o = reinterpret_cast<float*>(ws + w.o);
-    a.num_blocks = num_blocks;
-    a.max_blocks_per_seq = max_blocks_per_seq;
-    a.max_seq_len = max_seq_len;
-    a.num_q_heads = num_q_heads;
-    a.num_kv_heads = num_kv_heads;
-    a.pages_per_split = p.pages_per_split;
-    a.max_splits = p.max_splits;
-    a.window = window > 0 ? window : 0;
-    a.score_scale = sm_scale * k_scale * kLog2e;
-    a.v_scale = v_scale;
-
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    switch (head_dim) {
-        case 64: e = launch_g<64>(G, mk, mv, a, batch, num_kv_heads, s); break;
-        case 128: e = launch_g<128>(G, mk, mv, a, batch, num_kv_heads, s); break;
-        default: e = launch_g<256>(G, mk, mv, a, batch, num_kv_heads, s); break;
+    // Batches above kMaxBatch sequences run as consecutive launches on the
+    // stream; each leaves the workspace counters at zero for the next.
+    for (int b0 = 0; b0 < batch; b0 += kMaxBatch) {
+        const int nb = std::min(kMaxBatch, batch - b0);
+        const Plan p = make_plan(nb, num_kv_heads, head_dim, max_seq_len, window, sms);
+        DecodeArgs a;
+        a.q = static_cast<const uint16_t*>(q) + static_cast<int64_t>(b0) * num_q_heads * head_dim;
+        a.block_tables = block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq;
+        a.seq_lens = seq_lens + b0;
+        a.out = static_cast<uint16_t*>(out) + static_cast<int64_t>(b0) * num_q_heads * head_dim;
+        a.err = reinterpret_cast<uint32_t*>(ws);
+        a.unit_meta = reinterpret_cast<int2*>(ws + w.counters);
+        a.part_ml = reinterpret_cast<float2*>(ws + w.ml);
+        a.part_o = reinterpret_cast<float*>(ws + w.o);
+        a.num_blocks = num_blocks;
+        a.max_blocks_per_seq = max_blocks_per_seq;
+        a.max_seq_len = max_seq_len;
+        a.batch = nb;
+        a.num_q_heads = num_q_heads;
+        a.num_kv_heads = num_kv_heads;
+        a.window = window > 0 ? window : 0;
+        a.score_scale = sm_scale * k_scale * kLog2e;
+        a.v_scale = v_scale;
+        cudaError_t e;
+        switch (head_dim) {
+            case 64: e = launch_g<64>(G, mk, mv, a, p.ctas, s); break;
+            case 128: e = launch_g<128>(G, mk, mv, a, p.ctas, s); break;
+            default: e = launch_g<256>(G, mk, mv, a, p.ctas, s); break;
+        }
+        if (e != cudaSuccess) return FP8KV_ERR_CUDA;
     }
-    return e == cudaSuccess ? FP8KV_OK : FP8KV_ERR_CUDA;
+    return FP8KV_OK;
 }
 
 // ---------------------------------------------------------------- allocation-free variant

@@ -26,6 +26,9 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, const int64_t* __restrict__ slot_mapping,
     int64_t num_tokens, uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, int64_t num_slots,
     int num_kv_heads, int head_dim, int block_size, float k_scale, float v_scale) {
+    // A decode launched right after may start its set-up now (it waits for
+    // this grid before reading the cache).
+    griddep_launch_dependents();
     const int64_t chunks_per_row = head_dim / 16;
     const int64_t chunks_per_token = chunks_per_row * num_kv_heads;
     const int64_t per_tensor = num_tokens * chunks_per_token;
