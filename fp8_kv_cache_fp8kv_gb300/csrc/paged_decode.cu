@@ -52,7 +52,8 @@ namespace fp8kv {
 
 constexpr int kBS = 16;                    // tokens per page (block_size)
 constexpr int kNCW = 4;                    // consumer warps per CTA
-constexpr int kThreads = (kNCW + 1) * 32;  // + one producer warp
+constexpr int kNPW = 2;                    // producer warps: one issues K copies, one V copies
+constexpr int kThreads = (kNCW + kNPW) * 32;
 constexpr int kStageHalf = 4096;           // K bytes (and V bytes) per stage
 constexpr int kStageBytes = 2 * kStageHalf;
 constexpr int kCtasPerSm = 2;
@@ -105,7 +106,7 @@ struct Geo {
 template <int D>
 constexpr size_t smem_bytes() {
     return 1024 + Geo<D>::STAGES * kStageBytes + 2 * Geo<D>::XW * 32 * sizeof(float) +
-           2 * Geo<D>::STAGES * sizeof(uint64_t) + (2 * kMaxBatch + 1 + 4 + 32) * sizeof(int32_t);
+           2 * Geo<D>::STAGES * sizeof(uint64_t) + (2 * kMaxBatch + 1 + 4 + 32 * kNPW) * sizeof(int32_t);
 }
 
 // Byte offset of (row r, byte o) inside one TMA box written with the 128-byte
@@ -307,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int32_t* pre = reinterpret_cast<int32_t*>(empty_bar + S);        // [kMaxBatch + 1] page prefix
     int32_t* lens = pre + kMaxBatch + 1;                             // [kMaxBatch] clamped lengths
     volatile int* flag = reinterpret_cast<volatile int*>(lens + kMaxBatch);  // [1] abort
-    int32_t* ids = lens + kMaxBatch + 4;                             // [32] block ids for the producer
+    int32_t* ids = lens + kMaxBatch + 4;                             // [kNPW][32] block ids per producer
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // The merge kernel that follows may start now; it waits for this grid's
@@ -368,15 +369,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int64_t s = static_cast<int64_t>(c) * P / Ce;
     const int64_t e = static_cast<int64_t>(c + 1) * P / Ce;
 
-    if (warp == kNCW) {
-        // ------------------------------------------------------------ producer
-        // Lane 0 alone issues the copies; once per 32 pages the warp hands it
-        // the next 32 block ids through shared memory, and loads the 32 after
-        // those into registers while lane 0 works.
-        if (lane == 0) {
-            prefetch_tmap(&tmK);
-            prefetch_tmap(&tmV);
-        }
+    if (warp >= kNCW) {
+        // ------------------------------------------------------------ producers
+        // Two producer warps walk the same pages: the first issues the K
+        // copies (and posts each stage's byte count), the second the V copies,
+        // so their issue latencies overlap.  In each, lane 0 alone issues;
+        // once per 32 pages the warp hands it the next 32 block ids through
+        // shared memory and loads the 32 after those while lane 0 works.
+        const int pw = warp - kNCW;
+        const CUtensorMap* tm = pw == 0 ? &tmK : &tmV;
+        int32_t* my_ids = ids + pw * 32;
+        if (lane == 0) prefetch_tmap(tm);
         const uint64_t pol = l2_policy_evict_first();
         int st = 0;
         bool ok = true;
@@ -396,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             for (int p0 = 0; p0 < np_seg; p0 += 32) {
                 const int cur = nxt;
                 __syncwarp();  // lane 0 is done with the previous batch
-                ids[lane] = cur;
+                my_ids[lane] = cur;
                 nxt = load_block_id(row + p0 + 32, lane, np_seg - p0 - 32, a.num_blocks, a.err);
                 __syncwarp();
                 if (lane == 0) {
@@ -411,18 +414,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&full_bar[slot], static_cast<uint32_t>(np * 2 * Gm::PAGE));
-                        uint8_t* kst = ring + slot * kStageBytes;
-                        uint8_t* vst = kst + kStageHalf;
+                        // K and V bytes of the stage; the V copies may land first
+                        // (the phase still waits for this arrival)
+                        if (pw == 0) mbar_arrive_expect_tx(&full_bar[slot], static_cast<uint32_t>(np * 2 * Gm::PAGE));
+                        uint8_t* dst = ring + slot * kStageBytes + pw * kStageHalf;
                         for (int p = 0; p < np; ++p) {
-                            const int id = ids[q + p];
+                            const int id = my_ids[q + p];
 #pragma unroll
-                            for (int h = 0; h < Gm::HALVES; ++h) {
-                                tma_load_4d(kst + p * Gm::PAGE + h * Gm::BOX, &tmK, &full_bar[slot], h * 128, 0,
-                                            w.hk, id, pol);
-                                tma_load_4d(vst + p * Gm::PAGE + h * Gm::BOX, &tmV, &full_bar[slot], h * 128, 0,
-                                            w.hk, id, pol);
-                            }
+                            for (int h = 0; h < Gm::HALVES; ++h)
+                                tma_load_4d(dst + p * Gm::PAGE + h * Gm::BOX, tm, &full_bar[slot], h * 128, 0, w.hk,
+                                            id, pol);
                         }
                         ++st;
                     }
