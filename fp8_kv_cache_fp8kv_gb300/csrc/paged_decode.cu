@@ -314,6 +314,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // The merge kernel that follows may start now; it waits for this grid's
     // completion (and memory) before reading anything.
     griddep_launch_dependents();
+    // This grid may have started before the previous one on the stream
+    // finished (programmatic launch): wait for it before reading any input,
+    // since that grid may have produced them (q, lengths, tables, the cache).
+    griddep_wait();
     // A previous CTA gave up a wait: skip the work, the call is already failed.
     if (*reinterpret_cast<volatile uint32_t*>(a.err) == FP8KV_ERR_TIMEOUT) return;
     const int B = a.batch, Hkv = a.num_kv_heads, C = gridDim.x, c = blockIdx.x;
@@ -352,12 +356,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     __syncthreads();
 
     const int64_t P = static_cast<int64_t>(Hkv) * pre[B];
-    // sequences with nothing to attend (length 0) produce zeros; the grid
-    // before this one (on the stream) may still be using the outputs
-    bool has_empty = false;
-    for (int b = c; b < B && !has_empty; b += C) has_empty = pre[b + 1] == pre[b];
-    if (has_empty) griddep_wait();
-    for (int b = c; b < B && has_empty; b += C) {
+    // sequences with nothing to attend (length 0) produce zeros
+    for (int b = c; b < B; b += C) {
         if (pre[b + 1] == pre[b]) {
             uint16_t* ob = a.out + static_cast<int64_t>(b) * a.num_q_heads * D;
             for (int i = tid; i < a.num_q_heads * D; i += kThreads) ob[i] = 0;
@@ -383,56 +383,66 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const uint64_t pol = l2_policy_evict_first();
         int st = 0;
         bool ok = true;
+        // Batches of up to 32 pages never straddle a segment; the ids of the
+        // batch after the current one (in the same or the next segment) are
+        // loaded while lane 0 issues the current one.
         Walker w;
         walk_start(w, pre, B, Hkv, s);
-        // The cache may have been written by the kernel just before this one
-        // (an append); everything above overlapped it, reads start here.
-        griddep_wait();
-        while (ok) {
-            const int64_t seg_end = min(e, w.base + w.n);
-            const int lp0 = static_cast<int>(w.g - w.base);
-            const int np_seg = static_cast<int>(seg_end - w.g);
-            const int L = lens[w.b];
-            const int32_t* row = a.block_tables + static_cast<int64_t>(w.b) * a.max_blocks_per_seq +
-                                 first_token(L, a.window) / kBS + lp0;
-            int nxt = load_block_id(row, lane, np_seg, a.num_blocks, a.err);
-            for (int p0 = 0; p0 < np_seg; p0 += 32) {
-                const int cur = nxt;
-                __syncwarp();  // lane 0 is done with the previous batch
-                my_ids[lane] = cur;
-                nxt = load_block_id(row + p0 + 32, lane, np_seg - p0 - 32, a.num_blocks, a.err);
-                __syncwarp();
-                if (lane == 0) {
-                    const int nb = min(32, np_seg - p0);
-                    for (int q = 0; q < nb && ok; q += Gm::PPS) {
-                        const int np = min(Gm::PPS, nb - q);
-                        const int slot = st % S;
-                        if (flag[1] || (st >= S && !mbar_wait_bounded(&empty_bar[slot], ((st / S) & 1) ^ 1,
-                                                                       kWaitLimitNs))) {
-                            report(a.err, FP8KV_ERR_TIMEOUT);
-                            flag[1] = 1;
-                            ok = false;
-                            break;
-                        }
-                        // K and V bytes of the stage; the V copies may land first
-                        // (the phase still waits for this arrival)
-                        if (pw == 0) mbar_arrive_expect_tx(&full_bar[slot], static_cast<uint32_t>(np * 2 * Gm::PAGE));
-                        uint8_t* dst = ring + slot * kStageBytes + pw * kStageHalf;
-                        for (int p = 0; p < np; ++p) {
-                            const int id = my_ids[q + p];
-#pragma unroll
-                            for (int h = 0; h < Gm::HALVES; ++h)
-                                tma_load_4d(dst + p * Gm::PAGE + h * Gm::BOX, tm, &full_bar[slot], h * 128, 0, w.hk,
-                                            id, pol);
-                        }
-                        ++st;
-                    }
+        auto seg_pages = [&](const Walker& x) { return static_cast<int>(min(e, x.base + x.n) - x.g); };
+        auto seg_row = [&](const Walker& x) {
+            return a.block_tables + static_cast<int64_t>(x.b) * a.max_blocks_per_seq +
+                   first_token(lens[x.b], a.window) / kBS + (x.g - x.base);
+        };
+        int np_seg = seg_pages(w);
+        const int32_t* row = seg_row(w);
+        int p0 = 0;
+        int nxt = load_block_id(row, lane, np_seg, a.num_blocks, a.err);
+        bool more = true;
+        while (ok && more) {
+            const int cur = nxt;
+            const int hk = w.hk;
+            const int nb = min(32, np_seg - p0);
+            __syncwarp();  // lane 0 is done with the previous batch
+            my_ids[lane] = cur;
+            p0 += 32;
+            if (p0 >= np_seg) {
+                if (min(e, w.base + w.n) >= e) {
+                    more = false;
+                } else {
+                    walk_next(w, pre, Hkv);
+                    np_seg = seg_pages(w);
+                    row = seg_row(w);
+                    p0 = 0;
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
             }
-            if (!ok || seg_end >= e) break;
-            walk_next(w, pre, Hkv);
+            nxt = more ? load_block_id(row + p0, lane, np_seg - p0, a.num_blocks, a.err) : 0;
+            __syncwarp();
+            if (lane == 0) {
+                for (int q = 0; q < nb && ok; q += Gm::PPS) {
+                    const int np = min(Gm::PPS, nb - q);
+                    const int slot = st % S;
+                    if (flag[1] || (st >= S && !mbar_wait_bounded(&empty_bar[slot], ((st / S) & 1) ^ 1,
+                                                                   kWaitLimitNs))) {
+                        report(a.err, FP8KV_ERR_TIMEOUT);
+                        flag[1] = 1;
+                        ok = false;
+                        break;
+                    }
+                    // K and V bytes of the stage; the V copies may land first
+                    // (the phase still waits for this arrival)
+                    if (pw == 0) mbar_arrive_expect_tx(&full_bar[slot], static_cast<uint32_t>(np * 2 * Gm::PAGE));
+                    uint8_t* dst = ring + slot * kStageBytes + pw * kStageHalf;
+                    for (int p = 0; p < np; ++p) {
+                        const int id = my_ids[q + p];
+#pragma unroll
+                        for (int h = 0; h < Gm::HALVES; ++h)
+                            tma_load_4d(dst + p * Gm::PAGE + h * Gm::BOX, tm, &full_bar[slot], h * 128, 0, hk, id,
+                                        pol);
+                    }
+                    ++st;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
         }
         // Only after a failed wait can copies still be in flight while the
         // consumers have stopped waiting: drain them (bounded) before exit.
@@ -461,6 +471,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int lo = first_token(L, a.window);
         const int pg_first = lo / kBS + lp0;  // page index (in the sequence) of the segment's first page
         load_query<D, G>(a, w.b, w.hk, gid, tig, qf, cs);
+        if (seg_end < e && gid < G) {  // warm L2 with the next segment's queries
+            Walker nw = w;
+            walk_next(nw, pre, Hkv);
+#pragma unroll
+            for (int hh = 0; hh < Gm::HALVES; ++hh)
+                prefetch_l2(a.q + (static_cast<int64_t>(nw.b) * a.num_q_heads + nw.hk * G + gid) * D + hh * 128 +
+                            tig * Gm::KW);
+        }
         m[0] = m[1] = -INFINITY;
         l[0] = l[1] = 0.f;
 #pragma unroll
@@ -681,12 +699,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 // softmax-merge pass), then combine the slices in shared memory.  It starts as
 // a programmatic dependent of the decode grid and waits for that grid's
 // completion before reading.
+constexpr int kMergeThreads = 256;
+
 template <int D, int G>
-__global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
-    constexpr int NG = D / 4;       // float4 groups per head: 16, 32, 64
-    constexpr int KS = 128 / NG;    // slices of the partial list: 8, 4, 2
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a) {
+    constexpr int NG = D / 4;                // float4 groups per head: 16, 32, 64
+    constexpr int KS = kMergeThreads / NG;   // slices of the partial list: 16, 8, 4
     __shared__ float sm_m[KS][NG], sm_l[KS][NG];
     __shared__ float4 sm_o[KS][NG];
+    griddep_launch_dependents();  // the next call's set-up may overlap this merge
     griddep_wait();
     const int u = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     const int g4 = tid % NG, ks = tid / NG;
@@ -910,7 +931,7 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     if (e != cudaSuccess || ctas == 1) return e;  // one CTA: every unit is written directly
     cudaLaunchConfig_t mcfg = {};
     mcfg.gridDim = dim3(a.batch * a.num_kv_heads, G);
-    mcfg.blockDim = dim3(128);
+    mcfg.blockDim = dim3(kMergeThreads);
     mcfg.dynamicSmemBytes = 0;
     mcfg.stream = stream;
     mcfg.attrs = attr;

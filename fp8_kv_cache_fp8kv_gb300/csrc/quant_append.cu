@@ -26,9 +26,13 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, const int64_t* __restrict__ slot_mapping,
     int64_t num_tokens, uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, int64_t num_slots,
     int num_kv_heads, int head_dim, int block_size, float k_scale, float v_scale) {
-    // A decode launched right after may start its set-up now (it waits for
-    // this grid before reading the cache).
+    // A decode launched right after may get resident now (it waits for this
+    // grid before reading anything).
     griddep_launch_dependents();
+    // This grid may have started before the previous one on the stream
+    // finished (programmatic launch): that grid may have produced the inputs
+    // or still read the cache, so wait for it before touching either.
+    griddep_wait();
     const int64_t chunks_per_row = head_dim / 16;
     const int64_t chunks_per_token = chunks_per_row * num_kv_heads;
     const int64_t per_tensor = num_tokens * chunks_per_token;
@@ -97,11 +101,18 @@ extern "C" fp8kv_status fp8kv_quant_append(const void* k_new, const void* v_new,
     int64_t blocks = (items + threads - 1) / threads;
     const int64_t cap = static_cast<int64_t>(sms) * 8;
     if (blocks > cap) blocks = cap;
+    // May get resident while the previous grid on the stream finishes; the
+    // kernel waits for it (griddepcontrol.wait) before touching memory.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = static_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     const cudaError_t err = cudaLaunchKernelEx(
         &cfg, fp8kv::quant_append_kernel, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
         slot_mapping, num_tokens, k_cache, v_cache, num_blocks * block_size, num_kv_heads, head_dim, block_size,

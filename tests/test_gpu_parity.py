@@ -192,3 +192,24 @@ def test_full_size_workloads_match_oracle(name):
             g = w.shape.group
             expect = np.stack([vh[h // g] for h in range(w.shape.num_q_heads)])
             assert_attn_close(_as_f64(out)[0], expect, f"{name} needle row")
+
+
+def test_inputs_written_by_the_previous_kernel_are_seen():
+    """Both kernels may be launched before the previous work on the stream ends;
+    they must still read the inputs that work produced (here the new K/V rows
+    and q come out of torch kernels issued right before each call)."""
+    shape = workload.small_shape("llama31_8b_b8_20k", batch=2, len_lo=1, len_hi=1)
+    w = workload.make_workload(shape, seed=8, lens=[900, 1300])
+    pc = Paged(w, fill_byte=0)
+    k_dev = torch.zeros_like(w.k, device="cuda")
+    v_dev = torch.zeros_like(w.v, device="cuda")
+    k_dev.copy_(w.k.to("cuda").float().mul_(1.0).to(torch.bfloat16))   # produced just before the append
+    v_dev.copy_(w.v.to("cuda").float().mul_(1.0).to(torch.bfloat16))
+    fk.fp8kv_quant_append(k_dev, v_dev, w.slot_mapping.to("cuda"), pc.k_cache, pc.v_cache, w.k_scale, w.v_scale)
+    pc.q = w.q.to("cuda").float().mul_(1.0).to(torch.bfloat16)          # produced just before the decode
+    out, err = pc.decode()
+    assert err == 0
+    kc, vc = oracle_codes(w)
+    gk, gv = pc.gathered_codes()
+    assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
+    assert_attn_close(_as_f64(out), oracle_out(w, kc, vc, 0), "fresh inputs")
