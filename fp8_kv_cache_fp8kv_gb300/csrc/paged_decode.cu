@@ -65,6 +65,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeArgs {
     const uint16_t* q;          // bf16 [B, Hq, D]
+    const uint16_t* k_new;      // bf16 [B, Hkv, D] newest rows to append first, or null
+    const uint16_t* v_new;
+    uint8_t* k_cache;           // the caches (written only when appending)
+    uint8_t* v_cache;
+    float k_scale_raw;          // per-tensor scales (the append divides by them)
+    float v_scale_raw;
     const int32_t* block_tables;
     const int32_t* seq_lens;
     uint16_t* out;              // bf16 [B, Hq, D]
@@ -179,6 +185,9 @@ __device__ __forceinline__ int cta_of(int64_t p, int64_t P, int C) {
     return static_cast<int>(((p + 1) * C - 1) / P);
 }
 
+// Block id of page `lane` of a batch; an id outside [0, num_blocks) is
+// reported and returned as -1 (its page is then read from block 0 and never
+// written).
 __device__ __forceinline__ int load_block_id(const int32_t* row, int lane, int count, int64_t num_blocks,
                                              uint32_t* err) {
     int id = 0;
@@ -186,10 +195,47 @@ __device__ __forceinline__ int load_block_id(const int32_t* row, int lane, int c
         id = __ldg(row + lane);
         if (id < 0 || id >= num_blocks) {
             report(err, FP8KV_ERR_INVALID_ARG);
-            id = 0;
+            id = -1;
         }
     }
     return id;
+}
+
+// One new K or V row (D bf16 values) held by a warp: lane l owns elements
+// [l*D/32, (l+1)*D/32).
+template <int D>
+struct NewRow {
+    uint32_t w[D / 64];
+};
+
+template <int D>
+__device__ __forceinline__ void load_new_row(NewRow<D>& r, const uint16_t* src_row, int lane) {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(src_row + lane * (D / 32));
+#pragma unroll
+    for (int i = 0; i < D / 64; ++i) r.w[i] = __ldg(p + i);
+}
+
+// Quantise-on-append of the warp's row: code = E4M3_satfinite(fp32(x) / scale)
+// with one IEEE divide and one RNE conversion (the same arithmetic as the
+// quant_append kernel), stored at dst_row.
+template <int D>
+__device__ __forceinline__ void store_new_row(const NewRow<D>& r, uint8_t* dst_row, int lane, float scale) {
+    uint16_t c[D / 64];
+#pragma unroll
+    for (int i = 0; i < D / 64; ++i) {
+        const float e0 = __uint_as_float(r.w[i] << 16), e1 = __uint_as_float(r.w[i] & 0xFFFF0000u);
+        c[i] = f32x2_to_e4m3x2_satfinite(__fdiv_rn(e0, scale), __fdiv_rn(e1, scale));
+    }
+    uint8_t* dst = dst_row + lane * (D / 32);
+    if constexpr (D == 64) {
+        *reinterpret_cast<uint16_t*>(dst) = c[0];
+    } else if constexpr (D == 128) {
+        *reinterpret_cast<uint32_t*>(dst) = static_cast<uint32_t>(c[0]) | (static_cast<uint32_t>(c[1]) << 16);
+    } else {
+        *reinterpret_cast<uint2*>(dst) =
+            make_uint2(static_cast<uint32_t>(c[0]) | (static_cast<uint32_t>(c[1]) << 16),
+                       static_cast<uint32_t>(c[2]) | (static_cast<uint32_t>(c[3]) << 16));
+    }
 }
 
 // Query fragments of one (sequence, kv head): the B operand of the score MMA,
@@ -386,6 +432,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // Batches of up to 32 pages never straddle a segment; the ids of the
         // batch after the current one (in the same or the next segment) are
         // loaded while lane 0 issues the current one.
+        //
+        // With a row to append (a decode step), the producer that owns a
+        // unit's last page first writes that sequence's newest K (or V) row
+        // into the page, orders the write before its own copies
+        // (fence.proxy.async), and only then issues the page.
+        const bool appending = a.k_new != nullptr;
+        const uint16_t* new_rows = pw == 0 ? a.k_new : a.v_new;
+        uint8_t* cache = pw == 0 ? a.k_cache : a.v_cache;
+        const float scale_raw = pw == 0 ? a.k_scale_raw : a.v_scale_raw;
         Walker w;
         walk_start(w, pre, B, Hkv, s);
         auto seg_pages = [&](const Walker& x) { return static_cast<int>(min(e, x.base + x.n) - x.g); };
@@ -393,15 +448,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             return a.block_tables + static_cast<int64_t>(x.b) * a.max_blocks_per_seq +
                    first_token(lens[x.b], a.window) / kBS + (x.g - x.base);
         };
+        auto seg_reaches_end = [&](const Walker& x) { return min(e, x.base + x.n) == x.base + x.n; };
         int np_seg = seg_pages(w);
         const int32_t* row = seg_row(w);
         int p0 = 0;
         int nxt = load_block_id(row, lane, np_seg, a.num_blocks, a.err);
+        int seg_b = w.b, seg_hk = w.hk;
+        bool seg_last = appending && seg_reaches_end(w);
+        NewRow<D> nrow;
+        if (seg_last) load_new_row<D>(nrow, new_rows + (static_cast<int64_t>(w.b) * Hkv + w.hk) * D, lane);
         bool more = true;
         while (ok && more) {
             const int cur = nxt;
-            const int hk = w.hk;
+            const int hk = seg_hk;
             const int nb = min(32, np_seg - p0);
+            const bool batch_has_last = seg_last && p0 + nb == np_seg;
+            const int batch_b = seg_b;
+            const NewRow<D> batch_row = nrow;
             __syncwarp();  // lane 0 is done with the previous batch
             my_ids[lane] = cur;
             p0 += 32;
@@ -413,10 +476,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     np_seg = seg_pages(w);
                     row = seg_row(w);
                     p0 = 0;
+                    seg_b = w.b;
+                    seg_hk = w.hk;
+                    seg_last = appending && seg_reaches_end(w);
+                    if (seg_last) load_new_row<D>(nrow, new_rows + (static_cast<int64_t>(w.b) * Hkv + w.hk) * D, lane);
                 }
             }
             nxt = more ? load_block_id(row + p0, lane, np_seg - p0, a.num_blocks, a.err) : 0;
             __syncwarp();
+            if (batch_has_last) {
+                const int id = my_ids[nb - 1];
+                if (id >= 0) {
+                    const int L = lens[batch_b];
+                    uint8_t* dst_row = cache + ((static_cast<int64_t>(id) * Hkv + hk) * kBS + (L - 1) % kBS) * D;
+                    store_new_row<D>(batch_row, dst_row, lane, scale_raw);
+                    fence_proxy_async_global();
+                }
+                __syncwarp();
+            }
             if (lane == 0) {
                 for (int q = 0; q < nb && ok; q += Gm::PPS) {
                     const int np = min(Gm::PPS, nb - q);
@@ -433,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     if (pw == 0) mbar_arrive_expect_tx(&full_bar[slot], static_cast<uint32_t>(np * 2 * Gm::PAGE));
                     uint8_t* dst = ring + slot * kStageBytes + pw * kStageHalf;
                     for (int p = 0; p < np; ++p) {
-                        const int id = my_ids[q + p];
+                        const int id = max(my_ids[q + p], 0);
 #pragma unroll
                         for (int h = 0; h < Gm::HALVES; ++h)
                             tma_load_4d(dst + p * Gm::PAGE + h * Gm::BOX, tm, &full_bar[slot], h * 128, 0, hk, id,
@@ -971,12 +1048,14 @@ extern "C" size_t fp8kv_paged_decode_workspace_size(int batch, int num_q_heads, 
     return ws_layout(batch, num_q_heads, num_kv_heads, head_dim, p).total;
 }
 
-extern "C" fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
-                                           int64_t num_blocks, const int32_t* block_tables, int max_blocks_per_seq,
-                                           const int32_t* seq_lens, int max_seq_len, int batch, int num_q_heads,
-                                           int num_kv_heads, int head_dim, int block_size, float k_scale,
-                                           float v_scale, float sm_scale, int window, void* out, void* workspace,
-                                           size_t workspace_bytes, void* stream) {
+namespace {
+
+fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, const uint8_t* k_cache,
+                         const uint8_t* v_cache, int64_t num_blocks, const int32_t* block_tables,
+                         int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len, int batch,
+                         int num_q_heads, int num_kv_heads, int head_dim, int block_size, float k_scale,
+                         float v_scale, float sm_scale, int window, void* out, void* workspace,
+                         size_t workspace_bytes, void* stream) {
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (batch < 0 || batch > 65535 || num_kv_heads < 1 || num_kv_heads > 65535 || num_q_heads < 1 ||
         num_q_heads % num_kv_heads != 0 || max_seq_len < 0 || num_blocks < 1 || max_blocks_per_seq < 0)
@@ -996,6 +1075,8 @@ extern "C" fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache
     if (batch == 0) return FP8KV_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out) return FP8KV_ERR_INVALID_ARG;
     if (!a16(q) || !a16(k_cache) || !a16(v_cache) || !a16(out)) return FP8KV_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return FP8KV_ERR_INVALID_ARG;
+    if (k_new && (!a16(k_new) || !a16(v_new))) return FP8KV_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
         return FP8KV_ERR_INVALID_ARG;
     int sms = 0;
@@ -1019,6 +1100,14 @@ extern "C" fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache
         const Plan p = make_plan(nb, num_kv_heads, head_dim, max_seq_len, window, sms);
         DecodeArgs a;
         a.q = static_cast<const uint16_t*>(q) + static_cast<int64_t>(b0) * num_q_heads * head_dim;
+        a.k_new = k_new ? static_cast<const uint16_t*>(k_new) + static_cast<int64_t>(b0) * num_kv_heads * head_dim
+                        : nullptr;
+        a.v_new = v_new ? static_cast<const uint16_t*>(v_new) + static_cast<int64_t>(b0) * num_kv_heads * head_dim
+                        : nullptr;
+        a.k_cache = const_cast<uint8_t*>(k_cache);
+        a.v_cache = const_cast<uint8_t*>(v_cache);
+        a.k_scale_raw = k_scale;
+        a.v_scale_raw = v_scale;
         a.block_tables = block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq;
         a.seq_lens = seq_lens + b0;
         a.out = static_cast<uint16_t*>(out) + static_cast<int64_t>(b0) * num_q_heads * head_dim;
@@ -1044,6 +1133,31 @@ extern "C" fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache
         if (e != cudaSuccess) return FP8KV_ERR_CUDA;
     }
     return FP8KV_OK;
+}
+
+}  // namespace
+
+extern "C" fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                           int64_t num_blocks, const int32_t* block_tables, int max_blocks_per_seq,
+                                           const int32_t* seq_lens, int max_seq_len, int batch, int num_q_heads,
+                                           int num_kv_heads, int head_dim, int block_size, float k_scale,
+                                           float v_scale, float sm_scale, int window, void* out, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+    return decode_impl(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
+                       seq_lens, max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale,
+                       v_scale, sm_scale, window, out, workspace, workspace_bytes, stream);
+}
+
+extern "C" fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, uint8_t* k_cache,
+                                          uint8_t* v_cache, int64_t num_blocks, const int32_t* block_tables,
+                                          int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len,
+                                          int batch, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                          float k_scale, float v_scale, float sm_scale, int window, void* out,
+                                          void* workspace, size_t workspace_bytes, void* stream) {
+    if (batch > 0 && (!k_new || !v_new)) return FP8KV_ERR_INVALID_ARG;
+    return decode_impl(q, k_new, v_new, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
+                       max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale, v_scale,
+                       sm_scale, window, out, workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------- allocation-free variant

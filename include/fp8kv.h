@@ -144,6 +144,29 @@ fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache, const uin
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * One decode step: append, then attend [G "Scales and calibration";
+ * G "Attention backend interactions"; V "ACCURACY AT LONG CONTEXT"].
+ *
+ * Equivalent to fp8kv_quant_append of each sequence's newest row followed by
+ * fp8kv_paged_decode, in one launch (plus the split merge): for every b with
+ * L = seq_lens[b] > 0 the row k_new[b] (v_new[b]) is quantised exactly as
+ * fp8kv_quant_append does and written at token L-1 of the sequence, i.e. at
+ * page block_tables[b][(L-1)/block_size], offset (L-1) % block_size; then the
+ * attention of fp8kv_paged_decode runs over the cache including that token.
+ *
+ *   k_new, v_new   bf16 [batch][num_kv_heads][head_dim], 16-byte aligned
+ *   all other arguments as for fp8kv_paged_decode (k_cache / v_cache are
+ *   written).  Sequences of length 0 append nothing; a page whose block id is
+ *   out of range is not written (the error word reports it).
+ */
+fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, uint8_t* k_cache,
+                               uint8_t* v_cache, int64_t num_blocks, const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len,
+                               int batch, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                               float k_scale, float v_scale, float sm_scale, int window, void* out,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Allocation-free paged decode.  This entry point has no counterpart on the
  * pages: it exists for callers that cannot allocate device memory when they
  * decode -- e.g. a serving engine that reserved nearly all HBM for its own

@@ -1,6 +1,6 @@
 """Shared GPU-test plumbing: put a seeded workload into a paged device cache
-through fp8kv_quant_append, run fp8kv_paged_decode, and fetch what the oracle
-needs to check them."""
+through fp8kv_quant_append, run fp8kv_paged_decode (or the fused
+fp8kv_decode_step), and fetch what the oracle needs to check them."""
 import numpy as np
 import torch
 
@@ -33,6 +33,43 @@ class Paged:
             return
         fk.fp8kv_quant_append(w.k.to("cuda"), w.v.to("cuda"), w.slot_mapping.to("cuda"),
                               self.k_cache, self.v_cache, w.k_scale, w.v_scale)
+
+    def append_history(self):
+        """Append every token except each sequence's newest one."""
+        w = self.w
+        keep = torch.ones(w.k.shape[0], dtype=torch.bool)
+        L = w.seq_lens.to(torch.int64)
+        keep[w.new_token_rows()[L > 0]] = False
+        if int(keep.sum()) == 0:
+            return
+        fk.fp8kv_quant_append(w.k[keep].to("cuda"), w.v[keep].to("cuda"), w.slot_mapping[keep].to("cuda"),
+                              self.k_cache, self.v_cache, w.k_scale, w.v_scale)
+
+    def new_rows(self):
+        """bf16 [B, Hkv, D]: each sequence's newest K and V row (zeros where empty)."""
+        w = self.w
+        s = w.shape
+        B = w.seq_lens.shape[0]
+        kn = torch.zeros((B, s.num_kv_heads, s.head_dim), dtype=torch.bfloat16)
+        vn = torch.zeros_like(kn)
+        L = w.seq_lens.to(torch.int64)
+        nz = L > 0
+        kn[nz] = w.k[w.new_token_rows()[nz]]
+        vn[nz] = w.v[w.new_token_rows()[nz]]
+        return kn.to("cuda"), vn.to("cuda")
+
+    def step(self, window=0, out=None):
+        """One fused decode step over a cache holding the history only."""
+        s = self.w.shape
+        B = self.q.shape[0]
+        mx = self.w.max_seq_len
+        kn, vn = self.new_rows()
+        ws = fk.alloc_workspace(B, s.num_q_heads, s.num_kv_heads, s.head_dim, mx, 16, window)
+        out = torch.empty((B, s.num_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda") if out is None else out
+        fk.fp8kv_decode_step(self.q, kn, vn, self.k_cache, self.v_cache, self.block_tables, self.seq_lens, mx,
+                             self.w.k_scale, self.w.v_scale, self.w.sm_scale, window, out, ws)
+        torch.cuda.synchronize()
+        return out, fk.fp8kv_read_error(ws)
 
     def gathered_codes(self):
         """Cache codes of every logical token, [T, Hkv, D] (host)."""

@@ -17,7 +17,7 @@ def lib():
 
 def test_every_header_symbol_is_exported(lib):
     names = fk.header_symbols()
-    assert {"fp8kv_quant_append", "fp8kv_paged_decode", "fp8kv_paged_decode_workspace_size",
+    assert {"fp8kv_quant_append", "fp8kv_paged_decode", "fp8kv_decode_step", "fp8kv_paged_decode_workspace_size",
             "fp8kv_workspace_init", "fp8kv_read_error", "fp8kv_status_string"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
@@ -55,6 +55,27 @@ def test_decode_rejects_bad_arguments(lib, kw, code):
 
 def test_decode_empty_batch_is_a_no_op(lib):
     assert _decode(lib, B=0, q=None, out=None) == 0
+
+
+def _step(lib, **kw):
+    a = dict(q=FAKE, kn=FAKE, vn=FAKE, k=FAKE, v=FAKE, nb=100, bt=FAKE, mb=8, sl=FAKE, msl=128, B=2, hq=32, hkv=8,
+             d=128, bs=16, ks=0.01, vs=0.01, sm=0.088, win=0, out=FAKE, ws=FAKE, wsb=1 << 20)
+    a.update(kw)
+    return lib.fp8kv_decode_step(a["q"], a["kn"], a["vn"], a["k"], a["v"], a["nb"], a["bt"], a["mb"], a["sl"],
+                                 a["msl"], a["B"], a["hq"], a["hkv"], a["d"], a["bs"], a["ks"], a["vs"], a["sm"],
+                                 a["win"], a["out"], a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kn=None), 1), (dict(vn=None), 1), (dict(kn=MISALIGNED), 1), (dict(vn=MISALIGNED), 1),
+    (dict(d=96), 2), (dict(ks=0.0), 1), (dict(q=None), 1), (dict(mb=4, msl=128), 1),
+])
+def test_decode_step_rejects_bad_arguments(lib, kw, code):
+    assert _step(lib, **kw) == code
+
+
+def test_decode_step_empty_batch_is_a_no_op(lib):
+    assert _step(lib, B=0, q=None, kn=None, vn=None, out=None) == 0
 
 
 def _append(lib, **kw):

@@ -172,6 +172,56 @@ def test_out_of_range_block_id_is_reported_not_faulted():
     assert err2 == 0
 
 
+# ------------------------------------------------------------ fused decode step
+
+STEP_CASES = [
+    ("llama31_8b_b1_4k", [1, 15, 16, 17, 33, 100, 0, 1000], (0, 1, 17)),
+    ("llama31_8b_b8_20k", [2999, 1234, 16, 4097], (0, 128)),
+    ("gptoss20b_b8_16k", [1, 63, 64, 65, 700], (0, 7)),
+    ("gemma4e2b_b16_8k32k", [1, 17, 513, 3000], (0, 33)),
+    ("llama33_70b_needle_128k", [3000, 40], (0,)),
+]
+
+
+@pytest.mark.parametrize("base,lens,windows", STEP_CASES)
+def test_decode_step_equals_append_then_decode(base, lens, windows):
+    """The fused step writes the same cache bytes and returns the same outputs,
+    bit for bit, as the append kernel followed by the decode kernel."""
+    shape = workload.small_shape(base, batch=len(lens), len_lo=1, len_hi=1, needle_margin=None)
+    w = workload.make_workload(shape, seed=11, lens=lens)
+    kc, vc = oracle_codes(w)
+    for win in windows:
+        sep = Paged(w, seed=win)
+        sep.append_all()
+        out_sep, err_sep = sep.decode(window=win)
+        fused = Paged(w, seed=win)          # same garbage in unwritten slots
+        fused.append_history()
+        out_f, err_f = fused.step(window=win)
+        assert err_sep == 0 and err_f == 0
+        assert torch.equal(fused.k_cache, sep.k_cache) and torch.equal(fused.v_cache, sep.v_cache)
+        assert torch.equal(out_f, out_sep), f"{base} window={win}"
+        assert_attn_close(_as_f64(out_f), oracle_out(w, kc, vc, win), f"step {base} window={win}")
+
+
+def test_decode_step_writes_only_the_newest_slot():
+    shape = workload.small_shape("llama31_8b_b8_20k", batch=3, len_lo=1, len_hi=1)
+    w = workload.make_workload(shape, seed=12, lens=[40, 16, 0])
+    pc = Paged(w, fill_byte=0xAB, extra_blocks=2)
+    before_k, before_v = pc.k_cache.clone(), pc.v_cache.clone()
+    _, err = pc.step()
+    assert err == 0
+    kc, vc = oracle_codes(w)
+    sm = w.slot_mapping
+    changed = {int(sm[r]) for r in w.new_token_rows()[w.seq_lens > 0].tolist()}
+    for cache, before, codes in ((pc.k_cache, before_k, kc), (pc.v_cache, before_v, vc)):
+        flat = cache.cpu().permute(0, 2, 1, 3).reshape(-1, shape.num_kv_heads, shape.head_dim)
+        ref = before.cpu().permute(0, 2, 1, 3).reshape(-1, shape.num_kv_heads, shape.head_dim).clone()
+        for r in w.new_token_rows()[w.seq_lens > 0].tolist():
+            ref[int(sm[r])] = torch.from_numpy(codes[r])
+        assert torch.equal(flat, ref)
+    assert len(changed) == 2
+
+
 # ------------------------------------------------------------ full-size workloads
 
 @pytest.mark.parametrize("name", list(workload.CONFIGS))
@@ -192,6 +242,14 @@ def test_full_size_workloads_match_oracle(name):
             g = w.shape.group
             expect = np.stack([vh[h // g] for h in range(w.shape.num_q_heads)])
             assert_attn_close(_as_f64(out)[0], expect, f"{name} needle row")
+        # the fused step the benchmark times: same bytes, same outputs
+        fused = Paged(w)
+        fused.append_history()
+        out_f, err_f = fused.step(window=win)
+        assert err_f == 0
+        assert torch.equal(fused.k_cache, pc.k_cache) and torch.equal(fused.v_cache, pc.v_cache)
+        assert torch.equal(out_f, out), f"{name} window={win} fused step"
+        del fused
 
 
 def test_inputs_written_by_the_previous_kernel_are_seen():
