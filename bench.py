@@ -266,6 +266,11 @@ class DecodeStep:
         self._decode = fk.prepare_paged_decode(self.q, self.k_cache, self.v_cache, self.block_tables,
                                                self.seq_lens, w.max_seq_len, w.k_scale, w.v_scale,
                                                w.sm_scale, window, self.out, self.ws)
+        self._decode_engine = {
+            e: fk.prepare_paged_decode(self.q, self.k_cache, self.v_cache, self.block_tables, self.seq_lens,
+                                       w.max_seq_len, w.k_scale, w.v_scale, w.sm_scale, window, self.out,
+                                       self.ws, engine=e)
+            for e in (fk.ENGINE_TENSOR_CORES, fk.ENGINE_CUDA_CORES)}
         self._step = fk.prepare_decode_step(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
                                             self.block_tables, self.seq_lens, w.max_seq_len, w.k_scale,
                                             w.v_scale, w.sm_scale, window, self.out, self.ws)
@@ -275,6 +280,9 @@ class DecodeStep:
 
     def decode(self):
         self._decode()
+
+    def decode_engine(self, engine):
+        self._decode_engine[engine]()
 
     def step(self):
         """The decode step: every sequence's newest row appended, then attended."""
@@ -340,6 +348,22 @@ def run_fp8kv(args, rank, ws):
     dec_ms = [dec_ms[2 * i].elapsed_time(dec_ms[2 * i + 1]) for i in range(K)]
     app_ms = [app_ms[2 * i].elapsed_time(app_ms[2 * i + 1]) for i in range(K)]
     dec_mean = reduce_max(statistics.fmean(dec_ms), ws)
+    # the two contraction engines of the decode call, back to back
+    eng_us = {}
+    for name, eng in (("tensor_cores", st.fk.ENGINE_TENSOR_CORES), ("cuda_cores", st.fk.ENGINE_CUDA_CORES)):
+        for _ in range(3):
+            st.decode_engine(eng)
+        evs = []
+        for i in range(K):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            st.decode_engine(eng)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        assert st.fk.fp8kv_read_error(st.ws) == 0
+        eng_us[name + "_us"] = round(reduce_max(statistics.fmean(a.elapsed_time(b) for a, b in evs), ws) * 1e3, 3)
     if clocks:
         clocks.stop()
 
@@ -371,6 +395,7 @@ def run_fp8kv(args, rank, ws):
                    "input_sha256": w.digest()[:16]},
         "step_bytes": step_bytes, "paged_decode_us": round(dec_mean * 1e3, 3),
         "quant_append_us": round(statistics.fmean(app_ms) * 1e3, 3),
+        "paged_decode_engines": eng_us,
         "roofline": {"kernel": "fp8kv_decode_step call: flattened split-context decode kernel with the "
                                "append fused in + split-merge kernel",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

@@ -55,6 +55,8 @@ def load(build_if_missing: bool = False):
     lib.fp8kv_read_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     lib.fp8kv_paged_decode.restype = I
     lib.fp8kv_paged_decode.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
+    lib.fp8kv_paged_decode_engine.restype = I
+    lib.fp8kv_paged_decode_engine.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P, I]
     lib.fp8kv_decode_step.restype = I
     lib.fp8kv_decode_step.argtypes = [P, P, P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
     lib.fp8kv_paged_decode_noalloc.restype = I
@@ -167,6 +169,18 @@ def fp8kv_paged_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len,
     _check("fp8kv_paged_decode", code)
 
 
+# fp8kv_engine
+ENGINE_DEFAULT, ENGINE_TENSOR_CORES, ENGINE_CUDA_CORES = 0, 1, 2
+
+
+def fp8kv_paged_decode_engine(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale, v_scale,
+                              sm_scale, window, out, workspace, engine, stream=None):
+    """fp8kv_paged_decode with the contraction engine chosen explicitly
+    (ENGINE_TENSOR_CORES or ENGINE_CUDA_CORES; ENGINE_DEFAULT = the library's)."""
+    prepare_paged_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale, v_scale, sm_scale,
+                         window, out, workspace, stream, engine=engine)()
+
+
 def fp8kv_paged_decode_noalloc(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale, v_scale,
                                sm_scale, window, out, stream=None):
     """Same as fp8kv_paged_decode without a workspace: for callers that cannot
@@ -218,7 +232,7 @@ def prepare_quant_append(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, 
 
 
 def prepare_paged_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale, v_scale,
-                         sm_scale, window, out, workspace, stream=None):
+                         sm_scale, window, out, workspace, stream=None, engine=None):
     B, hq, d = q.shape
     nb, hkv, bs, d2 = k_cache.shape
     if d2 != d or tuple(out.shape) != (B, hq, d) or tuple(v_cache.shape) != tuple(k_cache.shape):
@@ -234,7 +248,9 @@ def prepare_paged_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_le
             ctypes.c_float(k_scale), ctypes.c_float(v_scale), ctypes.c_float(sm_scale), I(window),
             _dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"),
             ctypes.c_size_t(workspace.numel()), _stream(stream))
-    return PreparedCall("fp8kv_paged_decode", lib.fp8kv_paged_decode, args)
+    if engine is None:
+        return PreparedCall("fp8kv_paged_decode", lib.fp8kv_paged_decode, args)
+    return PreparedCall("fp8kv_paged_decode_engine", lib.fp8kv_paged_decode_engine, args + (I(engine),))
 
 
 def _decode_step_args(q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale, v_scale,

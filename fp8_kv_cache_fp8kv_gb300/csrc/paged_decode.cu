@@ -109,10 +109,13 @@ struct Geo {
     static_assert(32 % PPS == 0, "a 32-page block-id batch holds whole stages");
 };
 
-template <int D>
+// The CUDA-core consumers also keep the segment's f16 queries ([G][D]) and
+// their shifts ([8]) in shared memory.
+template <int D, int G, bool SIMT>
 constexpr size_t smem_bytes() {
     return 1024 + Geo<D>::STAGES * kStageBytes + 2 * Geo<D>::XW * 32 * sizeof(float) +
-           2 * Geo<D>::STAGES * sizeof(uint64_t) + (2 * kMaxBatch + 1 + 4 + 32 * kNPW) * sizeof(int32_t);
+           2 * Geo<D>::STAGES * sizeof(uint64_t) + (2 * kMaxBatch + 1 + 4 + 32 * kNPW) * sizeof(int32_t) +
+           (SIMT ? 16 + G * D * sizeof(uint16_t) + 8 * sizeof(int) : 0);
 }
 
 // Byte offset of (row r, byte o) inside one TMA box written with the 128-byte
@@ -338,7 +341,431 @@ __device__ __forceinline__ void absorb(const float* x, int lane, float (&m)[2], 
     combine<MT>(m, l, o, m2, l2, o2);
 }
 
+// ---------------------------------------------------------------- CUDA-core consumers
+//
+// The same split-context flash-decoding step with both contractions on the
+// CUDA cores: every score and every P.V sum is an FP32 fma chain of exact f16
+// products (K, V and P are f16-exact: E4M3 codes, the f16-rounded
+// probabilities; q is the same power-of-two-scaled f16 copy the tensor-core
+// consumers use).  Scores: lane = token (D = 256: two lanes per token, one per
+// 128-dim half), q broadcast from shared memory.  P.V: lane = D/32 output
+// dims, the stage's probabilities broadcast from shared memory.
 template <int D, int G>
+struct SimtGeo {
+    using Gm = Geo<D>;
+    static constexpr int TS = Gm::PPS * kBS;              // tokens per stage: 64, 32, 16
+    static constexpr int TPL = TS >= 32 ? TS / 32 : 1;     // tokens per lane in the score pass
+    static constexpr int DSPLIT = TS >= 32 ? 1 : 32 / TS;  // lanes sharing one token (D = 256: 2)
+    static constexpr int DPL = D / 32;                     // output dims per lane in the value pass
+    static constexpr int CH = Gm::ROWB / 16;               // 16-byte chunks per box row
+    static constexpr int XW = G * DPL + 2;                 // words per lane in the warp merge
+    static constexpr int PSM = TS * G * 2;                 // bytes of one warp's f16 probabilities
+    static_assert(XW <= Gm::XW, "merge state fits the exchange buffer");
+    static_assert(kNCW * PSM <= 2 * Gm::XW * 32 * 4, "probabilities fit the exchange buffer");
+    static_assert(DSPLIT == 1 || DSPLIT == Gm::HALVES, "split lanes cover one 128-dim box each");
+};
+
+template <int N>
+__device__ __forceinline__ void load_f16s(const uint8_t* p, uint16_t (&h)[N]) {
+    if constexpr (N == 1) {
+        h[0] = *reinterpret_cast<const uint16_t*>(p);
+    } else if constexpr (N == 2) {
+        const uint32_t x = *reinterpret_cast<const uint32_t*>(p);
+        h[0] = x & 0xFFFF; h[1] = x >> 16;
+    } else if constexpr (N == 4) {
+        const uint2 x = *reinterpret_cast<const uint2*>(p);
+        h[0] = x.x & 0xFFFF; h[1] = x.x >> 16; h[2] = x.y & 0xFFFF; h[3] = x.y >> 16;
+    } else {
+        const uint4 x = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { h[2 * i] = w[i] & 0xFFFF; h[2 * i + 1] = w[i] >> 16; }
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void store_f16s(uint8_t* p, const float (&v)[N]) {
+    if constexpr (N == 1) {
+        const __half h = __float2half_rn(v[0]);
+        *reinterpret_cast<uint16_t*>(p) = *reinterpret_cast<const uint16_t*>(&h);
+    } else if constexpr (N == 2) {
+        *reinterpret_cast<uint32_t*>(p) = pack_f16x2(v[0], v[1]);
+    } else if constexpr (N == 4) {
+        *reinterpret_cast<uint2*>(p) = make_uint2(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]));
+    } else {
+        *reinterpret_cast<uint4*>(p) = make_uint4(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]),
+                                                  pack_f16x2(v[4], v[5]), pack_f16x2(v[6], v[7]));
+    }
+}
+
+template <int G, int DPL>
+__device__ __forceinline__ void simt_combine(float (&m)[G], float (&l)[G], float (&o)[G][DPL], const float (&m2)[G],
+                                             const float (&l2)[G], const float (&o2)[G][DPL]) {
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+        const float M = fmaxf(m[j], m2[j]);
+        const float Mu = M == -INFINITY ? 0.f : M;
+        const float f1 = fast_exp2(m[j] - Mu), f2 = fast_exp2(m2[j] - Mu);
+        l[j] = l[j] * f1 + l2[j] * f2;
+        m[j] = M;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) o[j][d] = o[j][d] * f1 + o2[j][d] * f2;
+    }
+}
+
+// Lane-major exchange of a warp's (m, l, o); m and l are warp-uniform and go
+// one head per lane.
+template <int G, int DPL>
+__device__ __forceinline__ void simt_publish(float* x, int lane, const float (&m)[G], const float (&l)[G],
+                                             const float (&o)[G][DPL]) {
+#pragma unroll
+    for (int j = 0; j < G; ++j)
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) x[(j * DPL + d) * 32 + lane] = o[j][d];
+#pragma unroll
+    for (int j = 0; j < G; ++j)
+        if (lane == j) {
+            x[(G * DPL) * 32 + j] = m[j];
+            x[(G * DPL + 1) * 32 + j] = l[j];
+        }
+}
+
+template <int G, int DPL>
+__device__ __forceinline__ void simt_absorb(const float* x, int lane, float (&m)[G], float (&l)[G],
+                                            float (&o)[G][DPL]) {
+    float m2[G], l2[G], o2[G][DPL];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) o2[j][d] = x[(j * DPL + d) * 32 + lane];
+        m2[j] = x[(G * DPL) * 32 + j];
+        l2[j] = x[(G * DPL + 1) * 32 + j];
+    }
+    simt_combine<G, DPL>(m, l, o, m2, l2, o2);
+}
+
+// Byte offset, inside one V page, of the D/32 codes lane `lane` reads from a
+// row whose swizzle phase is k (the row's address bits 7-9 for 128-byte rows,
+// 7-8 for 64-byte rows), minus the row start.
+template <int D>
+__device__ __forceinline__ int simt_v_offset(int lane, int k) {
+    using Gm = Geo<D>;
+    const int o = D == 256 ? (lane % 16) * 8 : lane * (D / 32);   // offset inside the box row
+    const int box = D == 256 ? (lane / 16) * Gm::BOX : 0;
+    return box + ((((o >> 4) ^ k) << 4) | (o & 15));
+}
+
+// One token of the P.V pass: o[j][d] += P[j] * V[d] for the lane's D/32 dims.
+template <int D, int G>
+__device__ __forceinline__ void simt_pv_row(const uint8_t* vrow, const uint8_t* prow, float (&o)[G][D / 32]) {
+    constexpr int DPL = D / 32;
+    uint32_t vh[DPL / 2];
+    if constexpr (DPL == 2) {
+        vh[0] = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(vrow));
+    } else if constexpr (DPL == 4) {
+        e4m3x4_to_f16x2x2(*reinterpret_cast<const uint32_t*>(vrow), vh[0], vh[1]);
+    } else {
+        const uint2 c8 = *reinterpret_cast<const uint2*>(vrow);
+        e4m3x4_to_f16x2x2(c8.x, vh[0], vh[1]);
+        e4m3x4_to_f16x2x2(c8.y, vh[2], vh[3]);
+    }
+    uint16_t ph[G];
+    load_f16s<G>(prow, ph);
+#pragma unroll
+    for (int j = 0; j < G; ++j)
+#pragma unroll
+        for (int k = 0; k < DPL / 2; ++k) fma_f16x2_f16_f32(o[j][2 * k], o[j][2 * k + 1], vh[k], ph[j]);
+}
+
+// Shared state of one CTA that the consumer warps read.
+struct CtaView {
+    uint8_t* ring;
+    float* xbuf;
+    uint64_t* full_bar;
+    uint64_t* empty_bar;
+    const int32_t* pre;
+    const int32_t* lens;
+    volatile int* flag;
+    uint16_t* qsm;   // [G][D] f16 scaled queries of the current segment
+    int* qsh;        // [G] their power-of-two shifts
+    int64_t s, e, P;
+    int Ce, c;
+};
+
+template <int D, int G>
+__device__ __forceinline__ void simt_consumers(const DecodeArgs& a, const CtaView& v, int warp, int lane) {
+    using Gm = Geo<D>;
+    using Sg = SimtGeo<D, G>;
+    constexpr int S = Gm::STAGES;
+    constexpr int DPL = Sg::DPL;
+    const int B = a.batch, Hkv = a.num_kv_heads;
+    uint8_t* psm = reinterpret_cast<uint8_t*>(v.xbuf) + warp * Sg::PSM;  // this warp's probabilities
+    float m[G], l[G], o[G][DPL], cs[G];
+    constexpr int NK = Gm::ROWB == 128 ? 8 : 4;  // swizzle phases of a box row
+    int vo[NK];
+#pragma unroll
+    for (int k = 0; k < NK; ++k) vo[k] = simt_v_offset<D>(lane, k);
+    int st_base = 0;
+    Walker w;
+    walk_start(w, v.pre, B, Hkv, v.s);
+    while (true) {
+        const int64_t seg_end = min(v.e, w.base + w.n);
+        const int lp0 = static_cast<int>(w.g - w.base);
+        const int np_seg = static_cast<int>(seg_end - w.g);
+        const int nst = (np_seg + Gm::PPS - 1) / Gm::PPS;
+        const int L = v.lens[w.b];
+        const int lo = first_token(L, a.window);
+        const int pg_first = lo / kBS + lp0;
+
+        // ---- the segment's queries -> scaled f16 in shared memory (one warp per head)
+        for (int j = warp; j < G; j += kNCW) {
+            const uint16_t* src = a.q + (static_cast<int64_t>(w.b) * a.num_q_heads + w.hk * G + j) * D + lane * DPL;
+            float x[DPL];
+            if constexpr (DPL == 2) {
+                const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(src));
+                x[0] = bf16_to_f32(u & 0xFFFF); x[1] = bf16_to_f32(u >> 16);
+            } else if constexpr (DPL == 4) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
+                x[0] = bf16_to_f32(u.x & 0xFFFF); x[1] = bf16_to_f32(u.x >> 16);
+                x[2] = bf16_to_f32(u.y & 0xFFFF); x[3] = bf16_to_f32(u.y >> 16);
+            } else {
+                const uint4 u = __ldg(reinterpret_cast<const uint4*>(src));
+                const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) { x[2 * i] = bf16_to_f32(ww[i] & 0xFFFF); x[2 * i + 1] = bf16_to_f32(ww[i] >> 16); }
+            }
+            float qmax = 0.f;
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) qmax = fmaxf(qmax, fabsf(x[d]));
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+            int shift = 0;
+            if (qmax > 0.f) {
+                const int ex = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFF) - 127;
+                shift = max(-100, min(100, 14 - ex));
+            }
+            const float up = __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) x[d] *= up;
+            store_f16s<DPL>(reinterpret_cast<uint8_t*>(v.qsm + j * D + lane * DPL), x);
+            if (lane == 0) v.qsh[j] = shift;
+        }
+        if (seg_end < v.e) {  // warm L2 with the next segment's queries
+            Walker nw = w;
+            walk_next(nw, v.pre, Hkv);
+            if (lane < G * D * 2 / 128)
+                prefetch_l2(reinterpret_cast<const uint8_t*>(a.q + (static_cast<int64_t>(nw.b) * a.num_q_heads + nw.hk * G) * D) +
+                            lane * 128);
+        }
+        consumer_sync();
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            cs[j] = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - v.qsh[j]) << 23);
+            m[j] = -INFINITY;
+            l[j] = 0.f;
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) o[j][d] = 0.f;
+        }
+
+        for (int i = (warp - st_base % kNCW + kNCW) % kNCW; i < nst; i += kNCW) {
+            const int st = st_base + i;
+            const int slot = st % S;
+            if (v.flag[1]) break;
+            if (!mbar_wait_bounded(&v.full_bar[slot], (st / S) & 1, kWaitLimitNs)) {
+                report(a.err, FP8KV_ERR_TIMEOUT);
+                v.flag[1] = 1;
+                break;
+            }
+            const int p0 = i * Gm::PPS;
+            const int np = min(Gm::PPS, np_seg - p0);
+            const uint8_t* kst = v.ring + slot * kStageBytes;
+            const uint8_t* vst = kst + kStageHalf;
+            const int tok_base = (pg_first + p0) * kBS;
+
+            // ---- scores: s[t][j] = sum_d K[t][d] q_j[d]
+            float sc[Sg::TPL][G];
+            {
+                const int hb = Sg::DSPLIT == 1 ? 0 : lane / Sg::TS;
+                float acc[Sg::TPL][G][2];
+#pragma unroll
+                for (int t = 0; t < Sg::TPL; ++t)
+#pragma unroll
+                    for (int j = 0; j < G; ++j) acc[t][j][0] = acc[t][j][1] = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < Sg::CH; ++cc) {
+                    uint4 x[Sg::TPL];
+#pragma unroll
+                    for (int t = 0; t < Sg::TPL; ++t) {
+                        const int tl = Sg::DSPLIT == 1 ? t * 32 + lane : lane % Sg::TS;
+                        const uint8_t* box = kst + (tl / kBS) * Gm::PAGE + hb * Gm::BOX;
+                        x[t] = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(tl % kBS, 16 * cc));
+                    }
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        const uint16_t* qj = v.qsm + j * D + hb * 128 + 16 * cc;
+                        const uint4 qa = *reinterpret_cast<const uint4*>(qj);
+                        const uint4 qb = *reinterpret_cast<const uint4*>(qj + 8);
+#pragma unroll
+                        for (int t = 0; t < Sg::TPL; ++t) {
+                            uint32_t k0, k1, k2, k3, k4, k5, k6, k7;
+                            e4m3x4_to_f16x2x2(x[t].x, k0, k1);
+                            e4m3x4_to_f16x2x2(x[t].y, k2, k3);
+                            e4m3x4_to_f16x2x2(x[t].z, k4, k5);
+                            e4m3x4_to_f16x2x2(x[t].w, k6, k7);
+                            fma_f16x2_f32(acc[t][j][0], acc[t][j][1], k0, qa.x);
+                            fma_f16x2_f32(acc[t][j][0], acc[t][j][1], k1, qa.y);
+                            fma_f16x2_f32(acc[t][j][0], acc[t][j][1], k2, qa.z);
+                            fma_f16x2_f32(acc[t][j][0], acc[t][j][1], k3, qa.w);
+                            fma_f16x2_f32(acc[t][j][0], acc[t][j][1], k4, qb.x);
+                            fma_f16x2_f32(acc[t][j][0], acc[t][j][1], k5, qb.y);
+                            fma_f16x2_f32(acc[t][j][0], acc[t][j][1], k6, qb.z);
+                            fma_f16x2_f32(acc[t][j][0], acc[t][j][1], k7, qb.w);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < Sg::TPL; ++t)
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        float sv = acc[t][j][0] + acc[t][j][1];
+                        if constexpr (Sg::DSPLIT == 2) sv += __shfl_xor_sync(0xffffffffu, sv, 16);
+                        sc[t][j] = sv;
+                    }
+            }
+
+            // ---- mask, scale to log2 units, stage maximum
+            float mx[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j) mx[j] = -INFINITY;
+#pragma unroll
+            for (int t = 0; t < Sg::TPL; ++t) {
+                const int tl = Sg::DSPLIT == 1 ? t * 32 + lane : lane % Sg::TS;
+                const int tok = tok_base + tl;
+                const bool valid = tl < np * kBS && tok >= lo && tok < L;
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    sc[t][j] = valid ? sc[t][j] * cs[j] : -INFINITY;
+                    mx[j] = fmaxf(mx[j], sc[t][j]);
+                }
+            }
+            float alpha[G], muse[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], off));
+                const float mn = fmaxf(m[j], mx[j]);
+                muse[j] = mn == -INFINITY ? 0.f : mn;
+                alpha[j] = fast_exp2(m[j] - muse[j]);
+                m[j] = mn;
+            }
+
+            // ---- probabilities -> f16 in this warp's shared slice; each lane's
+            // share of l moves to the new maximum first
+#pragma unroll
+            for (int j = 0; j < G; ++j) l[j] *= alpha[j];
+            __syncwarp();  // the previous stage's readers are done with the slice
+#pragma unroll
+            for (int t = 0; t < Sg::TPL; ++t) {
+                const int tl = Sg::DSPLIT == 1 ? t * 32 + lane : lane % Sg::TS;
+                float pr[G];
+#pragma unroll
+                for (int j = 0; j < G; ++j) pr[j] = fast_exp2(sc[t][j] - muse[j]);
+                if (Sg::DSPLIT == 1 || lane < Sg::TS) {
+#pragma unroll
+                    for (int j = 0; j < G; ++j) l[j] += pr[j];
+                    store_f16s<G>(psm + tl * G * 2, pr);
+                }
+            }
+            __syncwarp();
+
+            // ---- P.V: o[j][d] += sum_t P[t][j] V[t][d] over the stage's valid tokens
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) o[j][d] *= alpha[j];
+            const int t_lo = max(lo - tok_base, 0);
+            const int t_hi = min(L - tok_base, np * kBS);
+            if (t_lo == 0 && t_hi == np * kBS) {
+                // every token of the stage attended: fully unrolled rows with
+                // the swizzled lane offsets taken from vo[]
+#pragma unroll
+                for (int p = 0; p < Gm::PPS; ++p) {
+                    if (p < np) {
+#pragma unroll
+                        for (int r = 0; r < kBS; ++r)
+                            simt_pv_row<D, G>(vst + p * Gm::PAGE + r * Gm::ROWB + vo[Gm::ROWB == 128 ? (r & 7) : ((r >> 1) & 3)],
+                                              psm + (p * kBS + r) * G * 2, o);
+                    }
+                }
+            } else {
+#pragma unroll 2
+                for (int t = t_lo; t < t_hi; ++t) {
+                    const int r = t % kBS;
+                    simt_pv_row<D, G>(vst + (t / kBS) * Gm::PAGE + r * Gm::ROWB +
+                                          simt_v_offset<D>(lane, Gm::ROWB == 128 ? (r & 7) : ((r >> 1) & 3)),
+                                      psm + t * G * 2, o);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&v.empty_bar[slot]);
+        }
+        st_base += nst;
+
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) l[j] += __shfl_xor_sync(0xffffffffu, l[j], off);
+
+        // ---- merge the four warps' states into warp 0 (the exchange buffer
+        // also holds the probability slices: every warp leaves its stages first)
+        consumer_sync();
+        if (warp >= 2) simt_publish<G, DPL>(v.xbuf + (warp - 2) * Sg::XW * 32, lane, m, l, o);
+        consumer_sync();
+        if (warp < 2) simt_absorb<G, DPL>(v.xbuf + warp * Sg::XW * 32, lane, m, l, o);
+        consumer_sync();
+        if (warp == 1) simt_publish<G, DPL>(v.xbuf, lane, m, l, o);
+        consumer_sync();
+        if (warp == 0) simt_absorb<G, DPL>(v.xbuf, lane, m, l, o);
+
+        // ---- emit (as the tensor-core consumers do)
+        const int u = w.b * Hkv + w.hk;
+        const int c_first = cta_of(w.base, v.P, v.Ce);
+        const int c_last = cta_of(w.base + w.n - 1, v.P, v.Ce);
+        const int k_u = c_last - c_first + 1;
+        if (warp == 0) {
+            if (k_u == 1) {
+                uint16_t* out_u = a.out + (static_cast<int64_t>(w.b) * a.num_q_heads + w.hk * G) * D + lane * DPL;
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    const float sc_out = l[j] > 0.f ? a.v_scale / l[j] : 0.f;
+                    uint32_t pk[DPL / 2];
+#pragma unroll
+                    for (int k = 0; k < DPL / 2; ++k)
+                        pk[k] = static_cast<uint32_t>(f32_to_bf16(o[j][2 * k] * sc_out)) |
+                                (static_cast<uint32_t>(f32_to_bf16(o[j][2 * k + 1] * sc_out)) << 16);
+                    if constexpr (DPL == 2) *reinterpret_cast<uint32_t*>(out_u + j * D) = pk[0];
+                    else if constexpr (DPL == 4) *reinterpret_cast<uint2*>(out_u + j * D) = make_uint2(pk[0], pk[1]);
+                    else *reinterpret_cast<uint4*>(out_u + j * D) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            } else {
+                const int64_t slot_idx = static_cast<int64_t>(u) + v.c;
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    float* po = a.part_o + (slot_idx * G + j) * D + lane * DPL;
+#pragma unroll
+                    for (int d = 0; d < DPL; d += 2) *reinterpret_cast<float2*>(po + d) = make_float2(o[j][d], o[j][d + 1]);
+                    if (lane == 0) a.part_ml[slot_idx * 8 + j] = make_float2(m[j], l[j]);
+                }
+            }
+            if (v.c == c_first && lane == 0) a.unit_meta[u] = make_int2(u + c_first, k_u);
+        }
+        consumer_sync();  // warp 0 is done with the exchange buffer
+        if (seg_end >= v.e) break;
+        walk_next(w, v.pre, Hkv);
+    }
+}
+
+template <int D, int G, bool SIMT>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeArgs a) {
@@ -355,6 +782,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int32_t* lens = pre + kMaxBatch + 1;                             // [kMaxBatch] clamped lengths
     volatile int* flag = reinterpret_cast<volatile int*>(lens + kMaxBatch);  // [1] abort
     int32_t* ids = lens + kMaxBatch + 4;                             // [kNPW][32] block ids per producer
+    uint16_t* qsm = reinterpret_cast<uint16_t*>(                     // CUDA-core consumers: [G][D] f16 q
+        ring + ((reinterpret_cast<uint8_t*>(ids + 32 * kNPW) - ring + 15) & ~static_cast<intptr_t>(15)));
+    int* qsh = reinterpret_cast<int*>(qsm + G * D);                  // [8] q shifts
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // The merge kernel that follows may start now; it waits for this grid's
@@ -531,6 +961,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 
     // ---------------------------------------------------------------- consumers
+    if constexpr (SIMT) {
+        const CtaView v{ring, xbuf, full_bar, empty_bar, pre, lens, flag, qsm, qsh, s, e, P, Ce, c};
+        simt_consumers<D, G>(a, v, warp, lane);
+        return;
+    }
     const int gid = lane >> 2, tig = lane & 3;
     uint32_t qf[Gm::KS][2];
     float cs[2];
@@ -977,7 +1412,7 @@ bool make_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int Hk
     return true;
 }
 
-template <int D, int G>
+template <int D, int G, bool SIMT>
 cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArgs& a, int ctas,
                    cudaStream_t stream) {
     // The shared-memory opt-in is per device; remember which devices have it.
@@ -987,8 +1422,8 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
     if (bit == 0 || !(done_mask.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(paged_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem_bytes<D>()));
+        e = cudaFuncSetAttribute(paged_decode_kernel<D, G, SIMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem_bytes<D, G, SIMT>()));
         if (e != cudaSuccess) return e;
         done_mask.fetch_or(bit, std::memory_order_release);
     }
@@ -1000,11 +1435,11 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes<D>();
+    cfg.dynamicSmemBytes = smem_bytes<D, G, SIMT>();
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G>, mk, mv, a);
+    e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, SIMT>, mk, mv, a);
     if (e != cudaSuccess || ctas == 1) return e;  // one CTA: every unit is written directly
     cudaLaunchConfig_t mcfg = {};
     mcfg.gridDim = dim3(a.batch * a.num_kv_heads, G);
@@ -1016,17 +1451,20 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     return cudaLaunchKernelEx(&mcfg, merge_kernel<D, G>, a);
 }
 
-template <int D>
+template <int D, bool SIMT>
 cudaError_t launch_g(int G, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArgs& a, int ctas,
                      cudaStream_t s) {
     switch (G) {
-        case 1: return launch<D, 1>(mk, mv, a, ctas, s);
-        case 2: return launch<D, 2>(mk, mv, a, ctas, s);
-        case 4: return launch<D, 4>(mk, mv, a, ctas, s);
-        case 8: return launch<D, 8>(mk, mv, a, ctas, s);
+        case 1: return launch<D, 1, SIMT>(mk, mv, a, ctas, s);
+        case 2: return launch<D, 2, SIMT>(mk, mv, a, ctas, s);
+        case 4: return launch<D, 4, SIMT>(mk, mv, a, ctas, s);
+        case 8: return launch<D, 8, SIMT>(mk, mv, a, ctas, s);
         default: return cudaErrorInvalidValue;
     }
 }
+
+// The contraction engine a call uses when the caller leaves it open.
+bool default_is_cuda_cores(int /*head_dim*/, int /*G*/) { return false; }
 
 bool supported(int head_dim, int block_size, int G) {
     return (head_dim == 64 || head_dim == 128 || head_dim == 256) && block_size == kBS &&
@@ -1055,7 +1493,7 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
                          int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len, int batch,
                          int num_q_heads, int num_kv_heads, int head_dim, int block_size, float k_scale,
                          float v_scale, float sm_scale, int window, void* out, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+                         size_t workspace_bytes, void* stream, int engine) {
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (batch < 0 || batch > 65535 || num_kv_heads < 1 || num_kv_heads > 65535 || num_q_heads < 1 ||
         num_q_heads % num_kv_heads != 0 || max_seq_len < 0 || num_blocks < 1 || max_blocks_per_seq < 0)
@@ -1065,6 +1503,10 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         return FP8KV_ERR_INVALID_ARG;
     const int G = num_q_heads / num_kv_heads;
     if (!supported(head_dim, block_size, G)) return FP8KV_ERR_UNSUPPORTED;
+    if (engine != FP8KV_ENGINE_DEFAULT && engine != FP8KV_ENGINE_TENSOR_CORES && engine != FP8KV_ENGINE_CUDA_CORES)
+        return FP8KV_ERR_INVALID_ARG;
+    const bool simt = engine == FP8KV_ENGINE_CUDA_CORES ||
+                      (engine == FP8KV_ENGINE_DEFAULT && default_is_cuda_cores(head_dim, G));
     if (num_blocks >= (INT64_C(1) << 31) || num_blocks * num_kv_heads >= (INT64_C(1) << 31))
         return FP8KV_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(max_blocks_per_seq) * block_size < max_seq_len) return FP8KV_ERR_INVALID_ARG;
@@ -1125,10 +1567,13 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         a.score_scale = sm_scale * k_scale * kLog2e;
         a.v_scale = v_scale;
         cudaError_t e;
-        switch (head_dim) {
-            case 64: e = launch_g<64>(G, mk, mv, a, p.ctas, s); break;
-            case 128: e = launch_g<128>(G, mk, mv, a, p.ctas, s); break;
-            default: e = launch_g<256>(G, mk, mv, a, p.ctas, s); break;
+        switch (head_dim * 2 + (simt ? 1 : 0)) {
+            case 128: e = launch_g<64, false>(G, mk, mv, a, p.ctas, s); break;
+            case 129: e = launch_g<64, true>(G, mk, mv, a, p.ctas, s); break;
+            case 256: e = launch_g<128, false>(G, mk, mv, a, p.ctas, s); break;
+            case 257: e = launch_g<128, true>(G, mk, mv, a, p.ctas, s); break;
+            case 512: e = launch_g<256, false>(G, mk, mv, a, p.ctas, s); break;
+            default: e = launch_g<256, true>(G, mk, mv, a, p.ctas, s); break;
         }
         if (e != cudaSuccess) return FP8KV_ERR_CUDA;
     }
@@ -1145,7 +1590,19 @@ extern "C" fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache
                                            size_t workspace_bytes, void* stream) {
     return decode_impl(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
                        seq_lens, max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale,
-                       v_scale, sm_scale, window, out, workspace, workspace_bytes, stream);
+                       v_scale, sm_scale, window, out, workspace, workspace_bytes, stream, FP8KV_ENGINE_DEFAULT);
+}
+
+extern "C" fp8kv_status fp8kv_paged_decode_engine(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                                  int64_t num_blocks, const int32_t* block_tables,
+                                                  int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len,
+                                                  int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                                  int block_size, float k_scale, float v_scale, float sm_scale,
+                                                  int window, void* out, void* workspace, size_t workspace_bytes,
+                                                  void* stream, int engine) {
+    return decode_impl(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
+                       seq_lens, max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale,
+                       v_scale, sm_scale, window, out, workspace, workspace_bytes, stream, engine);
 }
 
 extern "C" fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, uint8_t* k_cache,
@@ -1157,7 +1614,7 @@ extern "C" fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, cons
     if (batch > 0 && (!k_new || !v_new)) return FP8KV_ERR_INVALID_ARG;
     return decode_impl(q, k_new, v_new, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                        max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale, v_scale,
-                       sm_scale, window, out, workspace, workspace_bytes, stream);
+                       sm_scale, window, out, workspace, workspace_bytes, stream, FP8KV_ENGINE_DEFAULT);
 }
 
 // ---------------------------------------------------------------- allocation-free variant

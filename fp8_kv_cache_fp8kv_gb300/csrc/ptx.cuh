@@ -1,5 +1,6 @@
 // Inline-PTX building blocks for the sm_103a kernels of libfp8kv: mbarriers,
-// TMA tensor loads, the fp8/f16 conversions and the m16n8k16 tensor-core MMA.
+// TMA tensor loads, the fp8/f16 conversions, the mixed-precision FP32 FMA of
+// the CUDA-core path and the m16n8k16 tensor-core MMA.
 // Every wait on an mbarrier is bounded in time; a wait that runs out reports
 // failure to its caller instead of spinning forever.
 #pragma once
@@ -147,6 +148,31 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// ---------------------------------------------------------------- CUDA-core FP32 accumulation
+
+// acc_lo += a.lo * b.lo, acc_hi += a.hi * b.hi for f16x2 words a, b: the
+// products of two f16 values are exact in FP32 and each sum is rounded once
+// to FP32 (mixed-precision fma, f16 operands, FP32 addend and result).
+__device__ __forceinline__ void fma_f16x2_f32(float& acc_lo, float& acc_hi, uint32_t a, uint32_t b) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %2;\n\t"
+        "mov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.f16 %1, ah, bh, %1;\n\t}"
+        : "+f"(acc_lo), "+f"(acc_hi)
+        : "r"(a), "r"(b));
+}
+
+// acc_lo += a.lo * b, acc_hi += a.hi * b for an f16x2 word a and an f16 b.
+__device__ __forceinline__ void fma_f16x2_f16_f32(float& acc_lo, float& acc_hi, uint32_t a, uint16_t b) {
+    asm("{\n\t.reg .b16 al, ah;\n\t"
+        "mov.b32 {al, ah}, %2;\n\t"
+        "fma.rn.f32.f16 %0, al, %3, %0;\n\t"
+        "fma.rn.f32.f16 %1, ah, %3, %1;\n\t}"
+        : "+f"(acc_lo), "+f"(acc_hi)
+        : "r"(a), "h"(b));
 }
 
 // ---------------------------------------------------------------- tensor cores

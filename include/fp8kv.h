@@ -15,6 +15,9 @@
  *   [V] phantomic12 summary of the vLLM FP8 KV-cache blog: "ACCURACY AT LONG
  *       CONTEXT" (the P.V contraction runs over the context, >= 100K tokens),
  *       "DECODE COST" (sliding windows of 128 and 512).
+ *   [A] phantomic12 record flops/ctx-fp8-kv-cache-long-context-accuracy:
+ *       "Arithmetic intensity" (decode attention streams the cache at about
+ *       2g flop per fp8 byte: memory-bound).
  *
  * Conventions for every entry point:
  *   - All pointers except `stream` are DEVICE pointers owned by the caller.
@@ -142,6 +145,32 @@ fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache, const uin
                                 int head_dim, int block_size, float k_scale, float v_scale,
                                 float sm_scale, int window, void* out, void* workspace,
                                 size_t workspace_bytes, void* stream);
+
+/* Which units perform the two contractions of the decode attention. */
+typedef enum {
+    FP8KV_ENGINE_DEFAULT = 0,      /* the library's choice for the shape (the faster one measured) */
+    FP8KV_ENGINE_TENSOR_CORES = 1, /* m16n8k16 f16 MMA per stage tile, folded into FP32 registers */
+    FP8KV_ENGINE_CUDA_CORES = 2    /* FP32 fma chains of exact f16 products on the CUDA cores     */
+} fp8kv_engine;
+
+/*
+ * fp8kv_paged_decode with the contraction engine chosen by the caller
+ * [P opening section (FP32 accumulation); A "Arithmetic intensity" (at M = g
+ * the contractions are small next to the bytes streamed, so either unit may
+ * keep up; the default is the one measured faster)].
+ *
+ * Same operation, arguments, workspace and errors as fp8kv_paged_decode; the
+ * engines differ only in rounding order (both accumulate in FP32 and meet the
+ * same tolerance).  An engine value outside fp8kv_engine is
+ * FP8KV_ERR_INVALID_ARG.
+ */
+fp8kv_status fp8kv_paged_decode_engine(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                       int64_t num_blocks, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* seq_lens,
+                                       int max_seq_len, int batch, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, float k_scale, float v_scale,
+                                       float sm_scale, int window, void* out, void* workspace,
+                                       size_t workspace_bytes, void* stream, int engine);
 
 /*
  * One decode step: append, then attend [G "Scales and calibration";

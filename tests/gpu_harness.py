@@ -79,15 +79,20 @@ class Paged:
         blk, off = sm // workload.BLOCK_SIZE, sm % workload.BLOCK_SIZE
         return kc[blk, :, off, :].numpy(), vc[blk, :, off, :].numpy()
 
-    def decode(self, window=0, max_seq_len=None, block_tables=None, out=None):
+    def decode(self, window=0, max_seq_len=None, block_tables=None, out=None, engine=None):
         s = self.w.shape
         B = self.q.shape[0]
         mx = self.w.max_seq_len if max_seq_len is None else max_seq_len
         bt = self.block_tables if block_tables is None else block_tables
         ws = fk.alloc_workspace(B, s.num_q_heads, s.num_kv_heads, s.head_dim, mx, 16, window)
         out = torch.empty((B, s.num_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda") if out is None else out
-        fk.fp8kv_paged_decode(self.q, self.k_cache, self.v_cache, bt, self.seq_lens, mx,
-                              self.w.k_scale, self.w.v_scale, self.w.sm_scale, window, out, ws)
+        if engine is None:
+            fk.fp8kv_paged_decode(self.q, self.k_cache, self.v_cache, bt, self.seq_lens, mx,
+                                  self.w.k_scale, self.w.v_scale, self.w.sm_scale, window, out, ws)
+        else:
+            fk.fp8kv_paged_decode_engine(self.q, self.k_cache, self.v_cache, bt, self.seq_lens, mx,
+                                         self.w.k_scale, self.w.v_scale, self.w.sm_scale, window, out, ws,
+                                         engine)
         torch.cuda.synchronize()
         err = fk.fp8kv_read_error(ws)
         return out, err

@@ -57,6 +57,23 @@ def test_decode_empty_batch_is_a_no_op(lib):
     assert _decode(lib, B=0, q=None, out=None) == 0
 
 
+def _engine(lib, engine, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, nb=100, bt=FAKE, mb=8, sl=FAKE, msl=128, B=2, hq=32, hkv=8, d=128,
+             bs=16, ks=0.01, vs=0.01, sm=0.088, win=0, out=FAKE, ws=FAKE, wsb=1 << 20)
+    a.update(kw)
+    return lib.fp8kv_paged_decode_engine(a["q"], a["k"], a["v"], a["nb"], a["bt"], a["mb"], a["sl"], a["msl"],
+                                         a["B"], a["hq"], a["hkv"], a["d"], a["bs"], a["ks"], a["vs"], a["sm"],
+                                         a["win"], a["out"], a["ws"], a["wsb"], None, engine)
+
+
+@pytest.mark.parametrize("engine,kw,code", [
+    (3, {}, 1), (-1, {}, 1), (1, dict(d=96), 2), (2, dict(d=96), 2), (2, dict(q=None), 1),
+    (2, dict(ks=0.0), 1), (1, dict(B=0, q=None, out=None), 0), (2, dict(B=0, q=None, out=None), 0),
+])
+def test_engine_entry_validates(lib, engine, kw, code):
+    assert _engine(lib, engine, **kw) == code
+
+
 def _step(lib, **kw):
     a = dict(q=FAKE, kn=FAKE, vn=FAKE, k=FAKE, v=FAKE, nb=100, bt=FAKE, mb=8, sl=FAKE, msl=128, B=2, hq=32, hkv=8,
              d=128, bs=16, ks=0.01, vs=0.01, sm=0.088, win=0, out=FAKE, ws=FAKE, wsb=1 << 20)

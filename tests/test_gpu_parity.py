@@ -77,8 +77,12 @@ SMALL = [
 ]
 
 
+ENGINES = [fk.ENGINE_TENSOR_CORES, fk.ENGINE_CUDA_CORES]
+
+
+@pytest.mark.parametrize("engine", ENGINES)
 @pytest.mark.parametrize("base,lens,windows", SMALL)
-def test_decode_small_cases_match_oracle(base, lens, windows):
+def test_decode_small_cases_match_oracle(base, lens, windows, engine):
     shape = workload.small_shape(base, batch=len(lens), len_lo=1, len_hi=1, needle_margin=None)
     w = workload.make_workload(shape, seed=3, lens=lens)
     pc = Paged(w)
@@ -87,14 +91,15 @@ def test_decode_small_cases_match_oracle(base, lens, windows):
     gk, gv = pc.gathered_codes()
     assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
     for win in windows:
-        out, err = pc.decode(window=win)
+        out, err = pc.decode(window=win, engine=engine)
         assert err == 0
-        assert_attn_close(_as_f64(out), oracle_out(w, kc, vc, win), f"{base} window={win}")
+        assert_attn_close(_as_f64(out), oracle_out(w, kc, vc, win), f"{base} window={win} engine={engine}")
 
 
+@pytest.mark.parametrize("engine", ENGINES)
 @pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("g", [1, 2, 4, 8])
-def test_decode_every_supported_head_layout(d, g):
+def test_decode_every_supported_head_layout(d, g, engine):
     hkv = 2
     shape = workload.LayerShape(f"t{d}_{g}", hkv * g, hkv, d, 3, 1, 1, (0,))
     w = workload.make_workload(shape, seed=g * 1000 + d, lens=[777, 16, 35])
@@ -102,12 +107,13 @@ def test_decode_every_supported_head_layout(d, g):
     pc.append_all()
     kc, vc = oracle_codes(w)
     for win in (0, 50):
-        out, err = pc.decode(window=win)
+        out, err = pc.decode(window=win, engine=engine)
         assert err == 0
-        assert_attn_close(_as_f64(out), oracle_out(w, kc, vc, win), f"d={d} g={g} window={win}")
+        assert_attn_close(_as_f64(out), oracle_out(w, kc, vc, win), f"d={d} g={g} window={win} engine={engine}")
 
 
-def test_unwritten_nan_slots_never_leak():
+@pytest.mark.parametrize("engine", ENGINES)
+def test_unwritten_nan_slots_never_leak(engine):
     # Every byte of the cache starts as the NaN code; only written slots may count.
     shape = workload.small_shape("llama31_8b_b8_20k", batch=3, len_lo=1, len_hi=1)
     w = workload.make_workload(shape, seed=4, lens=[33, 1, 250])
@@ -115,7 +121,7 @@ def test_unwritten_nan_slots_never_leak():
     pc.append_all()
     kc, vc = oracle_codes(w)
     for win in (0, 3, 20):
-        out, err = pc.decode(window=win)
+        out, err = pc.decode(window=win, engine=engine)
         assert err == 0 and torch.isfinite(out.float()).all()
         assert_attn_close(_as_f64(out), oracle_out(w, kc, vc, win), f"nan-filled window={win}")
 
@@ -242,6 +248,12 @@ def test_full_size_workloads_match_oracle(name):
             g = w.shape.group
             expect = np.stack([vh[h // g] for h in range(w.shape.num_q_heads)])
             assert_attn_close(_as_f64(out)[0], expect, f"{name} needle row")
+        # the CUDA-core engine on the same cache
+        out_c, err_c = pc.decode(window=win, engine=fk.ENGINE_CUDA_CORES)
+        assert err_c == 0
+        assert_attn_close(_as_f64(out_c), ref, f"{name} window={win} cuda cores")
+        if w.needle_pos is not None:
+            assert_attn_close(_as_f64(out_c)[0], expect, f"{name} needle row, cuda cores")
         # the fused step the benchmark times: same bytes, same outputs
         fused = Paged(w)
         fused.append_history()
