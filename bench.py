@@ -199,7 +199,7 @@ def traffic_for(kernel_key):
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_kv_cache_fp8kv_gb300", "csrc")
-    for name in ("paged_decode.cu", "ptx.cuh"):
+    for name in ("paged_decode.cu", "partition.cuh", "ptx.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()

@@ -19,22 +19,27 @@
 //    and cut into one equal contiguous range per CTA (2 CTAs per SM), so all
 //    CTAs finish together whatever the mix of sequence lengths.  A CTA walks
 //    the units its range overlaps ("segments").
-//  * One producer warp streams K and V pages with TMA tensor copies (128-byte
-//    or 64-byte swizzle, evict-first L2 policy) into a ring of shared-memory
-//    stages guarded by mbarriers, reading block ids 32 pages ahead.  Four
-//    consumer warps each own every fourth stage.
+//  * Two producer warps stream the pages with TMA tensor copies (128-byte or
+//    64-byte swizzle, evict-first L2 policy), one the K pages and one the V
+//    pages, into a ring of shared-memory stages guarded by mbarriers, reading
+//    block ids 32 pages ahead.  Four consumer warps each own every fourth
+//    stage.  In a decode step (fp8kv_decode_step) the producer that owns a
+//    unit's last page first quantises and writes the sequence's newest K (V)
+//    row into it, orders that write before its own copies and then loads it.
 //  * Per stage a consumer warp converts codes to f16 (exact) and runs the
 //    score contraction S^T = K Q^T and the value contraction O^T += V^T P^T on
 //    the tensor cores (mma m16n8k16, fp32 accumulators): the g <= 8 query
-//    heads form the n=8 side.  FP32 CUDA cores alone cannot keep up with HBM
-//    at g=8 on this part (2g flop per byte at ~7 TB/s exceeds their FMA
-//    rate).  The stage's P.V tile is then added into separate FP32 registers
-//    (O = O*alpha + tile), so the long contraction is summed in IEEE FP32,
-//    not inside the MMA.
+//    heads form the n=8 side.  The stage's P.V tile is then added into
+//    separate FP32 registers (O = O*alpha + tile), so the long contraction is
+//    summed in IEEE FP32, not inside the MMA.  A CUDA-core engine (FP32 fma of
+//    exact f16 products, same pipeline) exists for comparison; it is slower at
+//    every supported g and is used only when asked for.
 //  * The softmax max/sum use warp shuffles; P is rounded to f16 for the MMA.
 //  * At the end of a segment the four warps merge through shared memory; a
-//    unit split over several CTAs is merged in FP32 by the last of them to
-//    finish (an atomic counter in the workspace; no CTA waits for another).
+//    unit split over several CTAs leaves FP32 partials that a small merge
+//    kernel combines.  It is launched as a programmatic dependent: it derives
+//    the split from the lengths while the decode grid finishes, then waits for
+//    that grid and reads the partials.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -46,6 +51,7 @@
 #include <mutex>
 
 #include "fp8kv.h"
+#include "partition.cuh"
 #include "ptx.cuh"
 
 namespace fp8kv {
@@ -75,7 +81,7 @@ struct DecodeArgs {
     const int32_t* seq_lens;
     uint16_t* out;              // bf16 [B, Hq, D]
     uint32_t* err;              // workspace error word
-    int2* unit_meta;            // [B*Hkv] (first partial slot, partial count) of each unit
+    int decode_ctas;            // grid size of the decode kernel (the merge recomputes its split)
     float2* part_ml;            // [B*Hkv + ctas][8]     (max, sum) in log2 units
     float* part_o;              // [B*Hkv + ctas][G][D]  unnormalised partial outputs
     int64_t num_blocks;
@@ -183,10 +189,6 @@ __device__ __forceinline__ void walk_next(Walker& w, const int32_t* pre, int Hkv
     w.g = w.base;
 }
 
-// CTA whose range holds global page p (ranges: [c*P/C, (c+1)*P/C)).
-__device__ __forceinline__ int cta_of(int64_t p, int64_t P, int C) {
-    return static_cast<int>(((p + 1) * C - 1) / P);
-}
 
 // Block id of page `lane` of a batch; an id outside [0, num_blocks) is
 // reported and returned as -1 (its page is then read from block 0 and never
@@ -488,8 +490,9 @@ struct CtaView {
     volatile int* flag;
     uint16_t* qsm;   // [G][D] f16 scaled queries of the current segment
     int* qsh;        // [G] their power-of-two shifts
-    int64_t s, e, P;
-    int Ce, c;
+    int64_t s, e;
+    Partition part;
+    int c;
 };
 
 template <int D, int G>
@@ -729,8 +732,8 @@ __device__ __forceinline__ void simt_consumers(const DecodeArgs& a, const CtaVie
 
         // ---- emit (as the tensor-core consumers do)
         const int u = w.b * Hkv + w.hk;
-        const int c_first = cta_of(w.base, v.P, v.Ce);
-        const int c_last = cta_of(w.base + w.n - 1, v.P, v.Ce);
+        const int c_first = cta_of(v.part, w.base);
+        const int c_last = cta_of(v.part, w.base + w.n - 1);
         const int k_u = c_last - c_first + 1;
         if (warp == 0) {
             if (k_u == 1) {
@@ -757,7 +760,6 @@ __device__ __forceinline__ void simt_consumers(const DecodeArgs& a, const CtaVie
                     if (lane == 0) a.part_ml[slot_idx * 8 + j] = make_float2(m[j], l[j]);
                 }
             }
-            if (v.c == c_first && lane == 0) a.unit_meta[u] = make_int2(u + c_first, k_u);
         }
         consumer_sync();  // warp 0 is done with the exchange buffer
         if (seg_end >= v.e) break;
@@ -787,19 +789,34 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int* qsh = reinterpret_cast<int*>(qsm + G * D);                  // [8] q shifts
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // The merge kernel that follows may start now; it waits for this grid's
-    // completion (and memory) before reading anything.
-    griddep_launch_dependents();
+    // Set-up that reads no input: the ring barriers (shared memory) and the
+    // tensor-map descriptors (kernel parameters).
+    if (tid == 0) {
+        for (int st0 = 0; st0 < S; ++st0) {
+            mbar_init(&full_bar[st0], 1);
+            mbar_init(&empty_bar[st0], 1);
+        }
+        flag[1] = 0;
+        fence_barrier_init();
+    }
+    if (warp == kNCW && lane == 0) prefetch_tmap(&tmK);
+    if (warp == kNCW + 1 && lane == 0) prefetch_tmap(&tmV);
     // This grid may have started before the previous one on the stream
     // finished (programmatic launch): wait for it before reading any input,
     // since that grid may have produced them (q, lengths, tables, the cache).
     griddep_wait();
-    // A previous CTA gave up a wait: skip the work, the call is already failed.
-    if (*reinterpret_cast<volatile uint32_t*>(a.err) == FP8KV_ERR_TIMEOUT) return;
+    // The merge kernel that follows may start now: it reads the lengths (final,
+    // since every CTA of this grid is past its wait) and waits for this grid's
+    // completion before reading anything this grid writes.
+    griddep_launch_dependents();
     const int B = a.batch, Hkv = a.num_kv_heads, C = gridDim.x, c = blockIdx.x;
 
-    // ---- attended pages per sequence and their exclusive prefix
+    // ---- attended pages per sequence and their exclusive prefix; the error
+    // word is read alongside (a CTA of an earlier call that gave up a wait
+    // fails every later call until the workspace is re-initialised)
     if (warp == 0) {
+        uint32_t prev_err = 0;
+        if (lane == 0) prev_err = *reinterpret_cast<volatile uint32_t*>(a.err);
         int run = 0;
         for (int b0 = 0; b0 < B; b0 += 32) {
             const int b = b0 + lane;
@@ -819,17 +836,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (b < B) pre[b] = run + x - n;
             run += __shfl_sync(0xffffffffu, x, 31);
         }
-        if (lane == 0) pre[B] = run;
-    }
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);
+        if (lane == 0) {
+            pre[B] = run;
+            flag[2] = prev_err == FP8KV_ERR_TIMEOUT;
         }
-        flag[1] = 0;
-        fence_barrier_init();
     }
     __syncthreads();
+    if (flag[2]) return;
 
     const int64_t P = static_cast<int64_t>(Hkv) * pre[B];
     // sequences with nothing to attend (length 0) produce zeros
@@ -837,13 +850,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (pre[b + 1] == pre[b]) {
             uint16_t* ob = a.out + static_cast<int64_t>(b) * a.num_q_heads * D;
             for (int i = tid; i < a.num_q_heads * D; i += kThreads) ob[i] = 0;
-            for (int hk = tid; hk < Hkv; hk += kThreads) a.unit_meta[b * Hkv + hk] = make_int2(0, 0);
         }
     }
     const int Ce = static_cast<int>(P < C ? P : C);  // CTAs with work: every one gets >= 1 page
     if (c >= Ce) return;
-    const int64_t s = static_cast<int64_t>(c) * P / Ce;
-    const int64_t e = static_cast<int64_t>(c + 1) * P / Ce;
+    const Partition part = make_partition(P, Ce);
+    const int64_t s = range_start(part, c);
+    const int64_t e = range_start(part, c + 1);
 
     if (warp >= kNCW) {
         // ------------------------------------------------------------ producers
@@ -855,7 +868,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int pw = warp - kNCW;
         const CUtensorMap* tm = pw == 0 ? &tmK : &tmV;
         int32_t* my_ids = ids + pw * 32;
-        if (lane == 0) prefetch_tmap(tm);
         const uint64_t pol = l2_policy_evict_first();
         int st = 0;
         bool ok = true;
@@ -962,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     // ---------------------------------------------------------------- consumers
     if constexpr (SIMT) {
-        const CtaView v{ring, xbuf, full_bar, empty_bar, pre, lens, flag, qsm, qsh, s, e, P, Ce, c};
+        const CtaView v{ring, xbuf, full_bar, empty_bar, pre, lens, flag, qsm, qsh, s, e, part, c};
         simt_consumers<D, G>(a, v, warp, lane);
         return;
     }
@@ -1161,8 +1173,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // that the merge kernel combines.  The CTA holding the unit's first
         // page records where the unit's partials are.
         const int u = w.b * Hkv + w.hk;
-        const int c_first = cta_of(w.base, P, Ce);
-        const int c_last = cta_of(w.base + w.n - 1, P, Ce);
+        const int c_first = cta_of(part, w.base);
+        const int c_last = cta_of(part, w.base + w.n - 1);
         const int k_u = c_last - c_first + 1;
         if (warp == 0) {
             if (k_u == 1) {
@@ -1197,7 +1209,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     }
                 }
             }
-            if (c == c_first && lane == 0) a.unit_meta[u] = make_int2(u + c_first, k_u);
         }
         consumer_sync();  // warp 0 is done with the exchange buffer
         if (seg_end >= e) break;
@@ -1220,13 +1231,50 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a
     __shared__ float sm_m[KS][NG], sm_l[KS][NG];
     __shared__ float4 sm_o[KS][NG];
     griddep_launch_dependents();  // the next call's set-up may overlap this merge
-    griddep_wait();
     const int u = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     const int g4 = tid % NG, ks = tid / NG;
-    const int2 meta = a.unit_meta[u];
-    const int k_u = meta.y;
-    if (k_u <= 1) return;  // empty, or written directly by its only CTA
-    const int64_t s0 = meta.x;
+    // Where this unit's partials are: the decode grid's page split, recomputed
+    // from the lengths while that grid finishes (they are final: the decode
+    // CTAs trigger this grid only after their own wait).
+    __shared__ long long red[2][kMergeThreads / 32];
+    const int Hkv = a.num_kv_heads, b = u / Hkv, hk = u - b * Hkv;
+    long long before = 0, total = 0;
+    for (int i = tid; i < a.batch; i += kMergeThreads) {
+        const int n = attended_pages(clamp_len(__ldg(a.seq_lens + i), a.max_seq_len), a.window);
+        total += n;
+        before += i < b ? n : 0;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, off);
+        total += __shfl_xor_sync(0xffffffffu, total, off);
+    }
+    if ((tid & 31) == 0) {
+        red[0][tid >> 5] = before;
+        red[1][tid >> 5] = total;
+    }
+    __syncthreads();
+    before = total = 0;
+#pragma unroll
+    for (int w = 0; w < kMergeThreads / 32; ++w) {
+        before += red[0][w];
+        total += red[1][w];
+    }
+    const int nb = attended_pages(clamp_len(__ldg(a.seq_lens + b), a.max_seq_len), a.window);
+    int k_u = 0, c_first = 0;
+    if (nb > 0) {
+        const int64_t P = static_cast<int64_t>(Hkv) * total;
+        const Partition part = make_partition(P, static_cast<int>(P < a.decode_ctas ? P : a.decode_ctas));
+        const int64_t base = static_cast<int64_t>(Hkv) * before + static_cast<int64_t>(hk) * nb;
+        c_first = cta_of(part, base);
+        k_u = cta_of(part, base + nb - 1) - c_first + 1;
+    }
+    // Every CTA waits, even one with nothing to merge: this grid must not
+    // complete (and release the next grid on the stream) before the decode
+    // grid has.
+    griddep_wait();
+    if (k_u <= 1) return;  // empty (zeros), or written directly by its only CTA
+    const int64_t s0 = static_cast<int64_t>(u) + c_first;
     float M = -INFINITY, Lh = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k0 = ks; k0 < k_u; k0 += 8 * KS) {
@@ -1276,7 +1324,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a
         Lt += f * sm_l[j][g4];
     }
     const float sc_out = Lt > 0.f ? a.v_scale / Lt : 0.f;
-    const int b = u / a.num_kv_heads, hk = u - b * a.num_kv_heads;
     uint16_t* out = a.out + (static_cast<int64_t>(b) * a.num_q_heads + hk * G + h) * D;
     const uint32_t lo2 = f32_to_bf16(o.x * sc_out) | (static_cast<uint32_t>(f32_to_bf16(o.y * sc_out)) << 16);
     const uint32_t hi2 = f32_to_bf16(o.z * sc_out) | (static_cast<uint32_t>(f32_to_bf16(o.w * sc_out)) << 16);
@@ -1305,7 +1352,7 @@ Plan make_plan(int batch, int num_kv_heads, int D, int max_seq_len, int window, 
 }
 
 struct WsLayout {
-    size_t counters, ml, o, total;
+    size_t ml, o, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -1316,8 +1363,7 @@ WsLayout ws_layout(int batch, int num_q_heads, int num_kv_heads, int D, const Pl
     const size_t slots = units + p.ctas;
     const int G = num_q_heads / num_kv_heads;
     WsLayout w;
-    w.counters = 256;  // per-unit (first slot, count) metadata
-    w.ml = w.counters + align256(units * sizeof(int2));
+    w.ml = 256;  // after the header (the error word)
     w.o = w.ml + align256(slots * 8 * sizeof(float2));
     w.total = w.o + align256(slots * G * D * sizeof(float));
     return w;
@@ -1536,7 +1582,7 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // Batches above kMaxBatch sequences run as consecutive launches on the
-    // stream; each leaves the workspace counters at zero for the next.
+    // stream, reusing the workspace.
     for (int b0 = 0; b0 < batch; b0 += kMaxBatch) {
         const int nb = std::min(kMaxBatch, batch - b0);
         const Plan p = make_plan(nb, num_kv_heads, head_dim, max_seq_len, window, sms);
@@ -1554,7 +1600,7 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         a.seq_lens = seq_lens + b0;
         a.out = static_cast<uint16_t*>(out) + static_cast<int64_t>(b0) * num_q_heads * head_dim;
         a.err = reinterpret_cast<uint32_t*>(ws);
-        a.unit_meta = reinterpret_cast<int2*>(ws + w.counters);
+        a.decode_ctas = p.ctas;
         a.part_ml = reinterpret_cast<float2*>(ws + w.ml);
         a.part_o = reinterpret_cast<float*>(ws + w.o);
         a.num_blocks = num_blocks;
@@ -1670,8 +1716,8 @@ extern "C" fp8kv_status fp8kv_paged_decode_noalloc(const void* q, const uint8_t*
     if (w.total > kStaticScratchBytes) return FP8KV_ERR_WORKSPACE;  // problem too large for the fixed array
     void* scratch = static_scratch_address();
     if (scratch == nullptr) return FP8KV_ERR_CUDA;
-    // The array keeps the previous call's contents: the error word and the
-    // split counters must start at zero.
+    // The array keeps the previous call's contents: the error word must start
+    // at zero.
     if (cudaMemsetAsync(scratch, 0, w.ml, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8KV_ERR_CUDA;
     return fp8kv_paged_decode(q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                               max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale, v_scale,

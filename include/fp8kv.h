@@ -94,8 +94,9 @@ size_t fp8kv_paged_decode_workspace_size(int batch, int num_q_heads, int num_kv_
 /*
  * Zero-fills a workspace (asynchronously on `stream`).  A workspace must be
  * zero-filled once before its first fp8kv_paged_decode call; every call that
- * completes leaves it ready for the next one.  Calls that share one workspace
- * must be ordered (same stream or explicit dependencies).
+ * completes leaves it ready for the next one.  After a call that failed with
+ * FP8KV_ERR_TIMEOUT the workspace must be zero-filled again.  Calls that share one workspace must be ordered (same
+ * stream or explicit dependencies).
  */
 fp8kv_status fp8kv_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 

@@ -165,6 +165,34 @@ def test_split_plan_does_not_change_the_result():
     assert float((out1.float() - out2.float()).abs().max()) <= 2 ** -7
 
 
+def test_repeated_calls_on_one_workspace_agree():
+    """Split units are merged with per-unit counters kept in the workspace;
+    every call must leave them ready for the next one, whichever engine ran."""
+    shape = workload.small_shape("llama33_70b_needle_128k", batch=3, len_lo=1, len_hi=1, needle_margin=None)
+    w = workload.make_workload(shape, seed=9, lens=[6000, 1, 2500])
+    pc = Paged(w)
+    pc.append_all()
+    s = w.shape
+    ws = fk.alloc_workspace(3, s.num_q_heads, s.num_kv_heads, s.head_dim, w.max_seq_len)
+    outs = []
+    for engine in (None, None, fk.ENGINE_CUDA_CORES, None, fk.ENGINE_TENSOR_CORES, None):
+        out = torch.empty((3, s.num_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
+        args = (pc.q, pc.k_cache, pc.v_cache, pc.block_tables, pc.seq_lens, w.max_seq_len, w.k_scale, w.v_scale,
+                w.sm_scale, 0, out, ws)
+        if engine is None:
+            fk.fp8kv_paged_decode(*args)
+        else:
+            fk.fp8kv_paged_decode_engine(*args, engine)
+        torch.cuda.synchronize()
+        assert fk.fp8kv_read_error(ws) == 0
+        if engine is None:
+            outs.append(out)
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    kc, vc = oracle_codes(w)
+    assert_attn_close(_as_f64(outs[0]), oracle_out(w, kc, vc, 0), "repeated calls")
+
+
 def test_out_of_range_block_id_is_reported_not_faulted():
     shape = workload.small_shape("llama31_8b_b8_20k", batch=1, len_lo=1, len_hi=1)
     w = workload.make_workload(shape, seed=7, lens=[40])
