@@ -46,6 +46,10 @@ def _load():
             P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_int,
             ctypes.c_int, ctypes.c_int, P, ctypes.c_int64, P]
+        lib.oracle_decode_attention_bf16.restype = ctypes.c_int
+        lib.oracle_decode_attention_bf16.argtypes = [
+            P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_float, ctypes.c_int, ctypes.c_int, P, ctypes.c_int64, P]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -121,3 +125,30 @@ def decode_attention(q_bits, k_codes, v_codes, seq_lens, k_scale, v_scale,
         raise ValueError("oracle_decode_attention: bad arguments")
     return out
 
+
+
+def decode_attention_bf16(q_bits, k_bits, v_bits, seq_lens, sm_scale, window=0, nthreads=1) -> np.ndarray:
+    """fp64 decode attention over a bf16 cache (the comparison baseline of the
+    fp8 cache): q_bits uint16 [B, Hq, d]; k_bits, v_bits uint16 [total_tokens,
+    Hkv, d] bf16 bit patterns, sequences concatenated in logical order."""
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    kb = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    vb = np.ascontiguousarray(v_bits, dtype=np.uint16)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, d = q.shape
+    Hkv = kb.shape[1]
+    assert kb.shape[2] == d and vb.shape == kb.shape
+    starts = np.zeros(B, dtype=np.int64)
+    if B > 1:
+        starts[1:] = np.cumsum(lens.astype(np.int64))[:-1]
+    assert int(lens.sum()) <= kb.shape[0]
+    max_len = int(max(1, lens.max() if B else 1))
+    nthreads = max(1, int(nthreads))
+    scratch = np.empty(nthreads * (max_len + d), dtype=np.float64)
+    out = np.zeros((B, Hq, d), dtype=np.float64)
+    rc = _load().oracle_decode_attention_bf16(
+        _ptr(q), _ptr(kb), _ptr(vb), _ptr(starts), _ptr(lens), B, Hq, Hkv, d,
+        float(sm_scale), int(window), nthreads, _ptr(scratch), max_len, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_decode_attention_bf16: bad arguments")
+    return out

@@ -140,15 +140,37 @@ static double round_to_bits(double v, int bits) {
 }
 
 /*
+ * Where the cached K and V of one sequence live: E4M3 codes with their
+ * per-tensor scales (the fp8 cache), or bf16 values (the bf16 cache that the
+ * fp8 one is compared against).  Element i of token t, kv head hk is at
+ * t * Hkv * d + hk * d + i.
+ */
+typedef struct {
+    const uint8_t* kc;   /* E4M3 codes, or NULL */
+    const uint8_t* vc;
+    const uint16_t* kb;  /* bf16 bits, used when kc is NULL */
+    const uint16_t* vb;
+    const double* dec;   /* decoded value of each of the 256 codes */
+    double k_scale, v_scale;
+} kv_store;
+
+static double kv_key(const kv_store* s, int64_t idx) {
+    return s->kc ? s->dec[s->kc[idx]] * s->k_scale : (double)bf16_bits_to_float(s->kb[idx]);
+}
+
+static double kv_value(const kv_store* s, int64_t idx) {
+    return s->vc ? s->dec[s->vc[idx]] * s->v_scale : (double)bf16_bits_to_float(s->vb[idx]);
+}
+
+/*
  * One query head of decode attention over a contiguous (logical-order) run of
- * codes.  kc/vc point at token 0 of the sequence; token stride = Hkv * d.
+ * cached tokens; the store points at token 0 of the sequence.
  * acc_bits <= 0: fp64 accumulation (the oracle proper).  acc_bits > 0: the
  * exp-weighted sums are rounded to acc_bits significand bits after every add,
  * a deliberately broken variant that models an imprecise accumulator.
  */
-static void attend_one_head(const uint16_t* qh, const uint8_t* kc, const uint8_t* vc,
+static void attend_one_head(const uint16_t* qh, const kv_store* kv,
                             int64_t L, int window, int Hkv, int hk, int d,
-                            const double* dec, double k_scale, double v_scale,
                             double sm_scale, int acc_bits, double* sigma,
                             double* num, double* out) {
     int64_t lo = 0;
@@ -159,10 +181,10 @@ static void attend_one_head(const uint16_t* qh, const uint8_t* kc, const uint8_t
     /* pass 1: scores and their maximum */
     double mx = -INFINITY;
     for (int64_t t = lo; t < L; ++t) {
-        const uint8_t* kr = kc + t * stride + (int64_t)hk * d;
+        const int64_t kr = t * stride + (int64_t)hk * d;
         double s = 0.0;
         for (int i = 0; i < d; ++i)
-            s += (double)bf16_bits_to_float(qh[i]) * (dec[kr[i]] * k_scale);
+            s += (double)bf16_bits_to_float(qh[i]) * kv_key(kv, kr + i);
         s *= sm_scale;
         sigma[t - lo] = s;
         if (s > mx) mx = s;
@@ -172,34 +194,26 @@ static void attend_one_head(const uint16_t* qh, const uint8_t* kc, const uint8_t
     for (int i = 0; i < d; ++i) num[i] = 0.0;
     for (int64_t t = lo; t < L; ++t) {
         double w = exp(sigma[t - lo] - mx);
-        const uint8_t* vr = vc + t * stride + (int64_t)hk * d;
+        const int64_t vr = t * stride + (int64_t)hk * d;
         if (acc_bits > 0) {
             den = round_to_bits(den + w, acc_bits);
             for (int i = 0; i < d; ++i)
-                num[i] = round_to_bits(num[i] + w * (dec[vr[i]] * v_scale), acc_bits);
+                num[i] = round_to_bits(num[i] + w * kv_value(kv, vr + i), acc_bits);
         } else {
             den += w;
-            for (int i = 0; i < d; ++i) num[i] += w * (dec[vr[i]] * v_scale);
+            for (int i = 0; i < d; ++i) num[i] += w * kv_value(kv, vr + i);
         }
     }
     for (int i = 0; i < d; ++i) out[i] = num[i] / den;
 }
 
-/*
- * Decode attention for a batch.
- *   q        bf16 bits [B, Hq, d]
- *   kc, vc   E4M3 codes [total_tokens, Hkv, d]; sequence b occupies tokens
- *            [seq_start[b], seq_start[b] + seq_lens[b]) in logical order
- *   out      fp64 [B, Hq, d]
- *   scratch  fp64, at least nthreads * (max_len + d) elements
- * Returns 0 on success, -1 on bad arguments.
- */
-int oracle_decode_attention(const uint16_t* q, const uint8_t* kc, const uint8_t* vc,
-                            const int64_t* seq_start, const int32_t* seq_lens,
-                            int B, int Hq, int Hkv, int d,
-                            float k_scale, float v_scale, float sm_scale, int window,
-                            int acc_bits, int nthreads, double* scratch,
-                            int64_t max_len, double* out) {
+/* Decode attention for a batch over either store (the two entry points below). */
+static int attention_batch(const uint16_t* q, const uint8_t* kc, const uint8_t* vc, const uint16_t* kb,
+                           const uint16_t* vb, const int64_t* seq_start, const int32_t* seq_lens,
+                           int B, int Hq, int Hkv, int d,
+                           float k_scale, float v_scale, float sm_scale, int window,
+                           int acc_bits, int nthreads, double* scratch,
+                           int64_t max_len, double* out) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || nthreads <= 0) return -1;
     for (int b = 0; b < B; ++b)
         if (seq_lens[b] < 0 || seq_lens[b] > max_len) return -1;
@@ -218,14 +232,46 @@ int oracle_decode_attention(const uint16_t* q, const uint8_t* kc, const uint8_t*
         int b = (int)(u / Hq), h = (int)(u % Hq);
         double* sigma = scratch + (int64_t)tid * (max_len + d);
         double* num = sigma + max_len;
-        attend_one_head(q + ((int64_t)b * Hq + h) * d,
-                        kc + seq_start[b] * (int64_t)Hkv * d,
-                        vc + seq_start[b] * (int64_t)Hkv * d,
-                        seq_lens[b], window, Hkv, h / g, d, dec,
-                        (double)k_scale, (double)v_scale, (double)sm_scale,
-                        acc_bits, sigma, num, out + ((int64_t)b * Hq + h) * d);
+        const int64_t off = seq_start[b] * (int64_t)Hkv * d;
+        kv_store kv = {kc ? kc + off : NULL, vc ? vc + off : NULL, kb ? kb + off : NULL, vb ? vb + off : NULL,
+                       dec, (double)k_scale, (double)v_scale};
+        attend_one_head(q + ((int64_t)b * Hq + h) * d, &kv, seq_lens[b], window, Hkv, h / g, d,
+                        (double)sm_scale, acc_bits, sigma, num, out + ((int64_t)b * Hq + h) * d);
     }
     return 0;
+}
+
+/*
+ * Decode attention for a batch over an E4M3 cache.
+ *   q        bf16 bits [B, Hq, d]
+ *   kc, vc   E4M3 codes [total_tokens, Hkv, d]; sequence b occupies tokens
+ *            [seq_start[b], seq_start[b] + seq_lens[b]) in logical order
+ *   out      fp64 [B, Hq, d]
+ *   scratch  fp64, at least nthreads * (max_len + d) elements
+ * Returns 0 on success, -1 on bad arguments.
+ */
+int oracle_decode_attention(const uint16_t* q, const uint8_t* kc, const uint8_t* vc,
+                            const int64_t* seq_start, const int32_t* seq_lens,
+                            int B, int Hq, int Hkv, int d,
+                            float k_scale, float v_scale, float sm_scale, int window,
+                            int acc_bits, int nthreads, double* scratch,
+                            int64_t max_len, double* out) {
+    if (!kc || !vc) return -1;
+    return attention_batch(q, kc, vc, NULL, NULL, seq_start, seq_lens, B, Hq, Hkv, d, k_scale, v_scale,
+                           sm_scale, window, acc_bits, nthreads, scratch, max_len, out);
+}
+
+/*
+ * The same attention over a bf16 cache (kb, vb: bf16 bits [total_tokens, Hkv,
+ * d]); no scales.
+ */
+int oracle_decode_attention_bf16(const uint16_t* q, const uint16_t* kb, const uint16_t* vb,
+                                 const int64_t* seq_start, const int32_t* seq_lens,
+                                 int B, int Hq, int Hkv, int d, float sm_scale, int window,
+                                 int nthreads, double* scratch, int64_t max_len, double* out) {
+    if (!kb || !vb) return -1;
+    return attention_batch(q, NULL, NULL, kb, vb, seq_start, seq_lens, B, Hq, Hkv, d, 1.0f, 1.0f, sm_scale,
+                           window, 0, nthreads, scratch, max_len, out);
 }
 
 int oracle_max_threads(void) {

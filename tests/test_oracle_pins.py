@@ -353,3 +353,67 @@ def test_reduced_precision_accumulator_fails_at_128k_and_fp32_passes():
     assert mx_b > ATTN_MAX_ABS or mean_b > ATTN_MEAN_ABS
     mx_g, mean_g = attn_errors(good, ref)
     assert mx_g <= ATTN_MAX_ABS / 10 and mean_g <= ATTN_MEAN_ABS / 10
+
+
+# ------------------------------------------------------------- the bf16 cache (comparison baseline)
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv,d,window", [
+    ([37], 4, 4, 16, 0), ([1, 50, 17], 8, 2, 32, 0), ([64, 3], 8, 1, 64, 5), ([100, 0, 100], 16, 4, 128, 33),
+])
+def test_bf16_attention_matches_torch_fp64_softmax(lens, Hq, Hkv, d, window):
+    g = torch.Generator().manual_seed(21)
+    B, T = len(lens), int(sum(lens))
+    q = torch.randn((B, Hq, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((T, Hkv, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((T, Hkv, d), generator=g).to(torch.bfloat16)
+    sm = float(np.float32(1 / math.sqrt(d)))
+    got = oracle.decode_attention_bf16(_bits(q), _bits(k), _bits(v), lens, sm, window)
+    G = Hq // Hkv
+    ref = np.zeros((B, Hq, d))
+    start = 0
+    for b, L in enumerate(lens):
+        if L > 0:
+            lo = L - window if (window > 0 and L > window) else 0
+            for h in range(Hq):
+                K = k[start + lo:start + L, h // G].double()
+                V = v[start + lo:start + L, h // G].double()
+                ref[b, h] = (torch.softmax(sm * (K @ q[b, h].double()), dim=0) @ V).numpy()
+        start += L
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_bf16_and_fp8_attention_agree_on_values_both_hold_exactly():
+    """K and V drawn from E4M3 values (exact in bf16): the fp8 oracle with
+    scale 1 on their codes and the bf16 oracle on the values must agree
+    bit for bit, since both compute the same fp64 sums of the same numbers."""
+    rng = np.random.default_rng(5)
+    lens, Hq, Hkv, d = [33, 70], 8, 2, 64
+    T = sum(lens)
+    codes_k = rng.integers(0, 256, size=(T, Hkv, d)).astype(np.uint8)
+    codes_v = rng.integers(0, 256, size=(T, Hkv, d)).astype(np.uint8)
+    for c in (codes_k, codes_v):
+        c[(c & 0x7F) == 0x7F] = 0x00          # no NaN codes
+    kf = oracle.e4m3_decode(codes_k).astype(np.float32)
+    vf = oracle.e4m3_decode(codes_v).astype(np.float32)
+    kb = (kf.view(np.uint32) >> 16).astype(np.uint16)   # exact: E4M3 values have 3 mantissa bits
+    vb = (vf.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((kb.astype(np.uint32) << 16).view(np.float32), kf)
+    q = _bits(torch.randn((2, Hq, d), generator=torch.Generator().manual_seed(6)).to(torch.bfloat16))
+    for window in (0, 9):
+        a = oracle.decode_attention(q, codes_k, codes_v, lens, 1.0, 1.0, 0.125, window)
+        b = oracle.decode_attention_bf16(q, kb, vb, lens, 0.125, window)
+        assert np.array_equal(a, b)
+
+
+def test_bf16_attention_single_key_returns_its_value():
+    g = torch.Generator().manual_seed(8)
+    v = torch.randn((1, 2, 16), generator=g).to(torch.bfloat16)
+    k = torch.randn((1, 2, 16), generator=g).to(torch.bfloat16)
+    q = torch.randn((1, 4, 16), generator=g).to(torch.bfloat16)
+    out = oracle.decode_attention_bf16(_bits(q), _bits(k), _bits(v), [1], 0.3, 0)
+    for h in range(4):
+        assert np.array_equal(out[0, h], v[0, h // 2].double().numpy())
