@@ -60,6 +60,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="instead of the step: decode time against context length, fp8 cache and bf16 cache")
     a = p.parse_args(argv)
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -542,6 +544,92 @@ def run_reference(args, rank, ws):
     }
 
 
+# ---------------------------------------------------------------- context sweep
+
+SWEEP_LENS = (1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072)
+
+
+def _fit(xs, ys):
+    """Least-squares line y = slope * x + intercept."""
+    A = np.stack([np.asarray(xs, dtype=np.float64), np.ones(len(xs))], axis=1)
+    (slope, icpt), *_ = np.linalg.lstsq(A, np.asarray(ys, dtype=np.float64), rcond=None)
+    return float(slope), float(icpt)
+
+
+def run_sweep(args, rank, ws):
+    """Decode time of one Llama-3.1-8B attention layer (32 q / 8 kv heads,
+    d = 128, batch 1) against context length, for the fp8 cache
+    (fp8kv_paged_decode) and the bf16 cache (fp8kv_paged_decode_bf16): the
+    per-token cost of each and their ratio, the GB300 counterpart of the
+    fitted ITL slopes the pages compare."""
+    from fp8_kv_cache_fp8kv_gb300 import binding as fk
+    fk.load(build_if_missing=True)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    points = []
+    for L in SWEEP_LENS:
+        shape = workload.LayerShape("llama31_8b_layer_b1", 32, 8, 128, 1, L, L, (0,))
+        w = workload.make_workload(shape, seed=args.seed, lens=[L])
+        s = w.shape
+        cshape = (w.num_blocks, s.num_kv_heads, workload.BLOCK_SIZE, s.head_dim)
+        sm = w.slot_mapping.to(dev)
+        blk, off = sm // workload.BLOCK_SIZE, sm % workload.BLOCK_SIZE
+        k8 = torch.zeros(cshape, dtype=torch.uint8, device=dev)
+        v8 = torch.zeros_like(k8)
+        fk.fp8kv_quant_append(w.k.to(dev), w.v.to(dev), sm, k8, v8, w.k_scale, w.v_scale)
+        kb = torch.zeros(cshape, dtype=torch.bfloat16, device=dev)
+        vb = torch.zeros_like(kb)
+        kb[blk, :, off, :] = w.k.to(dev)
+        vb[blk, :, off, :] = w.v.to(dev)
+        q = w.q.to(dev)
+        bt = w.block_tables.to(dev)
+        lens = w.seq_lens.to(dev)
+        out = torch.empty_like(q)
+        wsp = fk.alloc_workspace(1, s.num_q_heads, s.num_kv_heads, s.head_dim, L, 16, 0, device=dev)
+        calls = {
+            "fp8": fk.prepare_paged_decode(q, k8, v8, bt, lens, L, w.k_scale, w.v_scale, w.sm_scale, 0, out, wsp),
+            "bf16": fk.prepare_paged_decode_bf16(q, kb, vb, bt, lens, L, w.sm_scale, 0, out, wsp),
+        }
+        read = {"fp8": accounting.decode_bytes([L], 32, 8, 128, 0),
+                "bf16": 2 * accounting.decode_bytes([L], 32, 8, 128, 0)}
+        rec = {"context": L}
+        for name, call in calls.items():
+            flush = L2Policy(read[name], dev)
+            for _ in range(args.warmup):
+                call()
+            torch.cuda.synchronize()
+            evs = []
+            for _ in range(args.steps):
+                flush()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+            assert fk.fp8kv_read_error(wsp) == 0
+            us = reduce_max(statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3, ws)
+            rec[name + "_us"] = round(us, 3)
+            rec[name + "_l2"] = "flushed" if flush.buf is not None else "larger than L2"
+        points.append(rec)
+        del k8, v8, kb, vb
+        torch.cuda.empty_cache()
+    fit = {}
+    for name in ("fp8", "bf16"):
+        slope, icpt = _fit([p["context"] for p in points], [p[name + "_us"] for p in points])
+        fit[name] = {"us_per_1k_tokens": round(slope * 1e3, 5), "intercept_us": round(icpt, 3)}
+    ratio = fit["fp8"]["us_per_1k_tokens"] / fit["bf16"]["us_per_1k_tokens"]
+    d_icpt = fit["fp8"]["intercept_us"] - fit["bf16"]["intercept_us"]
+    d_slope = (fit["bf16"]["us_per_1k_tokens"] - fit["fp8"]["us_per_1k_tokens"]) / 1e3
+    breakeven = round(d_icpt / d_slope) if d_icpt > 0 and d_slope > 0 else None  # None: fp8 never slower
+    return {"sweep": "paged decode time against context length, fp8 cache vs bf16 cache",
+            "config": {"workload": "llama31_8b_layer_b1", "num_q_heads": 32, "num_kv_heads": 8, "head_dim": 128,
+                       "batch": 1, "block_size": 16, "window": 0, "timer": "CUDA events per call, median of %d"
+                       % args.steps},
+            "points": points, "fit": fit, "slope_ratio_fp8_over_bf16": round(ratio, 4),
+            "breakeven_context_tokens": breakeven, "n_gpus": ws}
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -555,6 +643,11 @@ def main(argv=None):
     rank, ws = dist_setup(args)
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU for --impl fp8kv")
+    if args.sweep:
+        line = run_sweep(args, rank, ws)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return 0
     line = run_fp8kv(args, rank, ws)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -57,6 +57,8 @@ def load(build_if_missing: bool = False):
     lib.fp8kv_paged_decode.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
     lib.fp8kv_paged_decode_engine.restype = I
     lib.fp8kv_paged_decode_engine.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P, I]
+    lib.fp8kv_paged_decode_bf16.restype = I
+    lib.fp8kv_paged_decode_bf16.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, I, P, P, SZ, P]
     lib.fp8kv_decode_step.restype = I
     lib.fp8kv_decode_step.argtypes = [P, P, P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
     lib.fp8kv_paged_decode_noalloc.restype = I
@@ -287,3 +289,35 @@ def prepare_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, seq_len
     args = _decode_step_args(q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale,
                              v_scale, sm_scale, window, out, workspace, stream)
     return PreparedCall("fp8kv_decode_step", load().fp8kv_decode_step, args)
+
+
+def _decode_bf16_args(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, sm_scale, window, out,
+                      workspace, stream):
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if d2 != d or tuple(out.shape) != (B, hq, d) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch between q, out and the caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.numel() != B:
+        raise ValueError("block_tables must be [B, max_blocks] and seq_lens [B]")
+    I = ctypes.c_int
+    return (_dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.bfloat16, "k_cache"),
+            _dev(v_cache, torch.bfloat16, "v_cache"), ctypes.c_int64(nb),
+            _dev(block_tables, torch.int32, "block_tables"), I(block_tables.shape[1]),
+            _dev(seq_lens, torch.int32, "seq_lens"), I(max_seq_len), I(B), I(hq), I(hkv), I(d), I(bs),
+            ctypes.c_float(sm_scale), I(window), _dev(out, torch.bfloat16, "out"),
+            _dev(workspace, torch.uint8, "workspace"), ctypes.c_size_t(workspace.numel()), _stream(stream))
+
+
+def fp8kv_paged_decode_bf16(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, sm_scale, window, out,
+                            workspace, stream=None):
+    """The bf16-cache twin of fp8kv_paged_decode: caches bf16
+    [num_blocks, Hkv, 16, D], no scales."""
+    _check("fp8kv_paged_decode_bf16", load().fp8kv_paged_decode_bf16(*_decode_bf16_args(
+        q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, sm_scale, window, out, workspace, stream)))
+
+
+def prepare_paged_decode_bf16(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, sm_scale, window, out,
+                              workspace, stream=None):
+    args = _decode_bf16_args(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, sm_scale, window, out,
+                             workspace, stream)
+    return PreparedCall("fp8kv_paged_decode_bf16", load().fp8kv_paged_decode_bf16, args)

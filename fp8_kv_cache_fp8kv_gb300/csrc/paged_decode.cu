@@ -95,32 +95,39 @@ struct DecodeArgs {
     float v_scale;
 };
 
-template <int D>
+// Geometry of one head dimension D with ES-byte elements (1: E4M3 codes,
+// 2: bf16 for the bf16 twin).  Pages, boxes, stages and per-thread loads are
+// in bytes; k-steps and m-tiles in elements.
+template <int D, int ES = 1>
 struct Geo {
-    static constexpr int PAGE = kBS * D;                // bytes of one K (or V) page
+    static constexpr int RB = D * ES;                   // bytes of one token row of one head
+    static constexpr int PAGE = kBS * RB;               // bytes of one K (or V) page
     static constexpr int PPS = kStageHalf / PAGE;       // pages per stage: 4, 2, 1
-    static constexpr int HALVES = D >= 128 ? D / 128 : 1;
-    static constexpr int ROWB = D >= 128 ? 128 : D;     // bytes per smem row of one TMA box
+    static constexpr int HALVES = RB >= 128 ? RB / 128 : 1;
+    static constexpr int ROWB = RB >= 128 ? 128 : RB;   // bytes per smem row of one TMA box
     static constexpr int BOX = kBS * ROWB;              // bytes of one TMA box
+    static constexpr int DBOX = ROWB / ES;              // elements per box row
     static constexpr int KS = D / 16;                   // k-steps of the score MMA
     static constexpr int MT = D / 16;                   // m-tiles of the value MMA
     static constexpr int KW = ROWB / 4;                 // K bytes a thread reads per row per box
-    static constexpr int KSH = KW / 4;                  // k-steps per box
+    static constexpr int KSH = KW / (4 * ES);           // k-steps per box
     static constexpr int VW = ROWB / 8;                 // V bytes a thread reads per token per box
-    static constexpr int MTH = VW / 2;                  // m-tiles per box
-    static constexpr int STAGES = D == 256 ? 8 : 12;    // ring slots (a multiple of kNCW)
+    static constexpr int VWD = VW / ES;                 // ... in elements
+    static constexpr int MTH = VWD / 2;                 // m-tiles per box
     static constexpr int XW = MT * 4 + 4;               // per-lane words exchanged in the warp merge
+    static constexpr int STAGES = XW > 40 ? 8 : 12;     // ring slots (a multiple of kNCW)
     static_assert(PPS >= 1 && PPS * PAGE == kStageHalf, "stage must hold whole pages");
     static_assert(STAGES % kNCW == 0, "every consumer warp owns whole ring slots");
     static_assert(32 % PPS == 0, "a 32-page block-id batch holds whole stages");
+    static_assert(KSH * HALVES == KS && MTH * HALVES == MT, "boxes cover the head dimension");
 };
 
 // The CUDA-core consumers also keep the segment's f16 queries ([G][D]) and
 // their shifts ([8]) in shared memory.
-template <int D, int G, bool SIMT>
+template <int D, int G, bool SIMT, int ES = 1>
 constexpr size_t smem_bytes() {
-    return 1024 + Geo<D>::STAGES * kStageBytes + 2 * Geo<D>::XW * 32 * sizeof(float) +
-           2 * Geo<D>::STAGES * sizeof(uint64_t) + (2 * kMaxBatch + 1 + 4 + 32 * kNPW) * sizeof(int32_t) +
+    return 1024 + Geo<D, ES>::STAGES * kStageBytes + 2 * Geo<D, ES>::XW * 32 * sizeof(float) +
+           4 * Geo<D, ES>::STAGES * sizeof(uint64_t) + (2 * kMaxBatch + 1 + 4 + 32 * kNPW) * sizeof(int32_t) +
            (SIMT ? 16 + G * D * sizeof(uint16_t) + 8 * sizeof(int) : 0);
 }
 
@@ -290,6 +297,61 @@ __device__ __forceinline__ void load_query(const DecodeArgs& a, int b, int hk, i
     for (int j = 0; j < 2; ++j) {
         const int sh = __shfl_sync(0xffffffffu, shift, (2 * tig + j) * 4);
         cs[j] = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+    }
+}
+
+// bf16 twin: the g query rows of kv head hk as bf16 B fragments of the score
+// MMA (no scaling: the cache is bf16 too), in the k order that matches how a
+// thread reads its K bytes: MMA k = 2*tig + e and 2*tig + 8 + e of k-step kk
+// of box hh are elements hh*64 + tig*16 + 4*kk + e and ... + 2 + e.
+template <int D, int G>
+__device__ __forceinline__ void load_query_bf16(const DecodeArgs& a, int b, int hk, int gid, int tig,
+                                                uint32_t (&qf)[Geo<D, 2>::KS][2], float (&cs)[2]) {
+    using Gm = Geo<D, 2>;
+#pragma unroll
+    for (int hh = 0; hh < Gm::HALVES; ++hh) {
+        uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
+        if (gid < G) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                a.q + (static_cast<int64_t>(b) * a.num_q_heads + hk * G + gid) * D + hh * Gm::DBOX + tig * 16);
+            v0 = __ldg(src);
+            v1 = __ldg(src + 1);
+        }
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int kk = 0; kk < Gm::KSH; ++kk) {
+            qf[hh * Gm::KSH + kk][0] = w[2 * kk];
+            qf[hh * Gm::KSH + kk][1] = w[2 * kk + 1];
+        }
+    }
+    cs[0] = cs[1] = a.score_scale;
+}
+
+// The V bytes one thread feeds to the value MMA from one box of a page:
+// token rows 2*tig, 2*tig+1, 2*tig+8, 2*tig+9, VW bytes each at column
+// gid*VW.  Rows outside [lo, L) (or a page past the stage's last) read as
+// zero codes, so stale NaN codes never meet a zero probability.
+template <int D, int ES>
+__device__ __forceinline__ void load_v_box(const uint8_t* box, int gid, int tig, int t0, int lo, int L, bool page_ok,
+                                           uint32_t (&v)[4][Geo<D, ES>::VW / 4]) {
+    using Gm = Geo<D, ES>;
+    const bool edge = t0 < lo || t0 + kBS > L;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int row = 2 * tig + (r & 1) + 8 * (r >> 1);
+        if (page_ok) {
+            if constexpr (Gm::VW == 16) {
+                const uint4 x = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(row, gid * 16));
+                v[r][0] = x.x; v[r][1] = x.y; v[r][2] = x.z; v[r][3] = x.w;
+            } else {
+                const uint2 x = *reinterpret_cast<const uint2*>(box + swz<Gm::ROWB>(row, gid * 8));
+                v[r][0] = x.x; v[r][1] = x.y;
+            }
+        }
+        if (!page_ok || (edge && (t0 + row < lo || t0 + row >= L))) {
+#pragma unroll
+            for (int ww = 0; ww < Gm::VW / 4; ++ww) v[r][ww] = 0u;
+        }
     }
 }
 
@@ -483,8 +545,8 @@ __device__ __forceinline__ void simt_pv_row(const uint8_t* vrow, const uint8_t* 
 struct CtaView {
     uint8_t* ring;
     float* xbuf;
-    uint64_t* full_bar;
-    uint64_t* empty_bar;
+    uint64_t* full_bar;   // [S] K half of a slot landed; V: full_bar + S
+    uint64_t* empty_bar;  // [S] K half of a slot consumed; V: empty_bar + S
     const int32_t* pre;
     const int32_t* lens;
     volatile int* flag;
@@ -636,6 +698,9 @@ __device__ __forceinline__ void simt_consumers(const DecodeArgs& a, const CtaVie
                     }
             }
 
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&v.empty_bar[slot]);  // the K half is free again
+
             // ---- mask, scale to log2 units, stage maximum
             float mx[G];
 #pragma unroll
@@ -682,6 +747,11 @@ __device__ __forceinline__ void simt_consumers(const DecodeArgs& a, const CtaVie
             __syncwarp();
 
             // ---- P.V: o[j][d] += sum_t P[t][j] V[t][d] over the stage's valid tokens
+            if (!mbar_wait_bounded(&v.full_bar[S + slot], (st / S) & 1, kWaitLimitNs)) {
+                report(a.err, FP8KV_ERR_TIMEOUT);
+                v.flag[1] = 1;
+                break;
+            }
 #pragma unroll
             for (int j = 0; j < G; ++j)
 #pragma unroll
@@ -710,7 +780,7 @@ __device__ __forceinline__ void simt_consumers(const DecodeArgs& a, const CtaVie
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&v.empty_bar[slot]);
+            if (lane == 0) mbar_arrive(&v.empty_bar[S + slot]);
         }
         st_base += nst;
 
@@ -767,20 +837,29 @@ __device__ __forceinline__ void simt_consumers(const DecodeArgs& a, const CtaVie
     }
 }
 
-template <int D, int G, bool SIMT>
+template <int D, int G, bool SIMT, int ES = 1>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeArgs a) {
-    using Gm = Geo<D>;
+    static_assert(ES == 1 || !SIMT, "the bf16 twin runs on the tensor cores only");
+    using Gm = Geo<D, ES>;
+    // At d = 128 the V fragments move to registers as soon as they land (a
+    // measured gain); the accumulators of d = 256 leave no room, and at d = 64
+    // it measured slower.
+    constexpr bool kEarlyV = Gm::MT == 8;
     constexpr int S = Gm::STAGES;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned ring (the swizzle pattern is a function of address
     // bits 4..9); offsetting the shared array keeps the address space known.
     uint8_t* ring = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float* xbuf = reinterpret_cast<float*>(ring + S * kStageBytes);  // [2][XW][32]
-    uint64_t* full_bar = reinterpret_cast<uint64_t*>(xbuf + 2 * Gm::XW * 32);
-    uint64_t* empty_bar = full_bar + S;
-    int32_t* pre = reinterpret_cast<int32_t*>(empty_bar + S);        // [kMaxBatch + 1] page prefix
+    // Each ring slot holds a K half and a V half with a barrier pair each:
+    // full_bar[s] / full_bar[S + s] complete when the K / V copies land,
+    // empty_bar[s] / empty_bar[S + s] when the consumer is done with them, so
+    // the K half returns to its producer as soon as the scores are computed.
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(xbuf + 2 * Gm::XW * 32);  // [2][S]
+    uint64_t* empty_bar = full_bar + 2 * S;                                     // [2][S]
+    int32_t* pre = reinterpret_cast<int32_t*>(empty_bar + 2 * S);    // [kMaxBatch + 1] page prefix
     int32_t* lens = pre + kMaxBatch + 1;                             // [kMaxBatch] clamped lengths
     volatile int* flag = reinterpret_cast<volatile int*>(lens + kMaxBatch);  // [1] abort
     int32_t* ids = lens + kMaxBatch + 4;                             // [kNPW][32] block ids per producer
@@ -792,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // Set-up that reads no input: the ring barriers (shared memory) and the
     // tensor-map descriptors (kernel parameters).
     if (tid == 0) {
-        for (int st0 = 0; st0 < S; ++st0) {
+        for (int st0 = 0; st0 < 2 * S; ++st0) {
             mbar_init(&full_bar[st0], 1);
             mbar_init(&empty_bar[st0], 1);
         }
@@ -879,7 +958,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // unit's last page first writes that sequence's newest K (or V) row
         // into the page, orders the write before its own copies
         // (fence.proxy.async), and only then issues the page.
-        const bool appending = a.k_new != nullptr;
+        const bool appending = ES == 1 && a.k_new != nullptr;
         const uint16_t* new_rows = pw == 0 ? a.k_new : a.v_new;
         uint8_t* cache = pw == 0 ? a.k_cache : a.v_cache;
         const float scale_raw = pw == 0 ? a.k_scale_raw : a.v_scale_raw;
@@ -940,22 +1019,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int q = 0; q < nb && ok; q += Gm::PPS) {
                     const int np = min(Gm::PPS, nb - q);
                     const int slot = st % S;
-                    if (flag[1] || (st >= S && !mbar_wait_bounded(&empty_bar[slot], ((st / S) & 1) ^ 1,
+                    if (flag[1] || (st >= S && !mbar_wait_bounded(&empty_bar[pw * S + slot], ((st / S) & 1) ^ 1,
                                                                    kWaitLimitNs))) {
                         report(a.err, FP8KV_ERR_TIMEOUT);
                         flag[1] = 1;
                         ok = false;
                         break;
                     }
-                    // K and V bytes of the stage; the V copies may land first
-                    // (the phase still waits for this arrival)
-                    if (pw == 0) mbar_arrive_expect_tx(&full_bar[slot], static_cast<uint32_t>(np * 2 * Gm::PAGE));
+                    // this producer's half of the stage (K or V)
+                    mbar_arrive_expect_tx(&full_bar[pw * S + slot], static_cast<uint32_t>(np * Gm::PAGE));
                     uint8_t* dst = ring + slot * kStageBytes + pw * kStageHalf;
                     for (int p = 0; p < np; ++p) {
                         const int id = max(my_ids[q + p], 0);
 #pragma unroll
                         for (int h = 0; h < Gm::HALVES; ++h)
-                            tma_load_4d(dst + p * Gm::PAGE + h * Gm::BOX, tm, &full_bar[slot], h * 128, 0, hk, id,
+                            tma_load_4d(dst + p * Gm::PAGE + h * Gm::BOX, tm, &full_bar[pw * S + slot], h * 128, 0, hk, id,
                                         pol);
                     }
                     ++st;
@@ -967,7 +1045,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // consumers have stopped waiting: drain them (bounded) before exit.
         if (!ok && lane == 0) {
             for (int t = st > S ? st - S : 0; t < st; ++t)
-                mbar_wait_bounded(&full_bar[t % S], (t / S) & 1, kWaitLimitNs);
+                mbar_wait_bounded(&full_bar[pw * S + t % S], (t / S) & 1, kWaitLimitNs);
         }
         return;
     }
@@ -994,14 +1072,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int L = lens[w.b];
         const int lo = first_token(L, a.window);
         const int pg_first = lo / kBS + lp0;  // page index (in the sequence) of the segment's first page
-        load_query<D, G>(a, w.b, w.hk, gid, tig, qf, cs);
+        if constexpr (ES == 1)
+            load_query<D, G>(a, w.b, w.hk, gid, tig, qf, cs);
+        else
+            load_query_bf16<D, G>(a, w.b, w.hk, gid, tig, qf, cs);
         if (seg_end < e && gid < G) {  // warm L2 with the next segment's queries
             Walker nw = w;
             walk_next(nw, pre, Hkv);
 #pragma unroll
             for (int hh = 0; hh < Gm::HALVES; ++hh)
-                prefetch_l2(a.q + (static_cast<int64_t>(nw.b) * a.num_q_heads + nw.hk * G + gid) * D + hh * 128 +
-                            tig * Gm::KW);
+                prefetch_l2(a.q + (static_cast<int64_t>(nw.b) * a.num_q_heads + nw.hk * G + gid) * D +
+                            hh * Gm::DBOX + tig * (Gm::KW / ES));
         }
         m[0] = m[1] = -INFINITY;
         l[0] = l[1] = 0.f;
@@ -1023,6 +1104,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const uint8_t* vst = kst + kStageHalf;
             const int tok_base = (pg_first + p0) * kBS;
 
+            // ---- (d = 128) the stage's V fragments into registers first, and
+            // the V half back to its producer: it is not held through the
+            // scores and the softmax (a held half is one copy fewer in flight)
+            uint32_t vr[kEarlyV ? Gm::PPS : 1][kEarlyV ? Gm::HALVES : 1][4][Gm::VW / 4];
+            if constexpr (kEarlyV) {
+                if (!mbar_wait_bounded(&full_bar[S + slot], (st / S) & 1, kWaitLimitNs)) {
+                    report(a.err, FP8KV_ERR_TIMEOUT);
+                    flag[1] = 1;
+                    break;
+                }
+#pragma unroll
+                for (int p = 0; p < Gm::PPS; ++p)
+#pragma unroll
+                    for (int hh = 0; hh < Gm::HALVES; ++hh)
+                        load_v_box<D, ES>(vst + p * Gm::PAGE + hh * Gm::BOX, gid, tig, tok_base + p * kBS, lo, L,
+                                          p < np, vr[p][hh]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_bar[S + slot]);
+            }
+
             // ---- scores S^T[token][head] = K Q^T
             float sc[Gm::PPS][4];
 #pragma unroll
@@ -1032,7 +1133,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
                     for (int hh = 0; hh < Gm::HALVES; ++hh) {
                         const uint8_t* box = kst + p * Gm::PAGE + hh * Gm::BOX;
-                        uint32_t w0[Gm::KSH], w1[Gm::KSH];
+                        uint32_t w0[Gm::KW / 4], w1[Gm::KW / 4];
 #pragma unroll
                         for (int cc = 0; cc < Gm::KW / 16; ++cc) {
                             const uint4 x = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(gid, tig * Gm::KW + 16 * cc));
@@ -1043,13 +1144,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
                         for (int kk = 0; kk < Gm::KSH; ++kk) {
                             uint32_t af[4];
-                            e4m3x4_to_f16x2x2(w0[kk], af[0], af[2]);
-                            e4m3x4_to_f16x2x2(w1[kk], af[1], af[3]);
-                            mma_16816(sc[p], af, qf[hh * Gm::KSH + kk][0], qf[hh * Gm::KSH + kk][1], sc[p]);
+                            if constexpr (ES == 1) {
+                                e4m3x4_to_f16x2x2(w0[kk], af[0], af[2]);
+                                e4m3x4_to_f16x2x2(w1[kk], af[1], af[3]);
+                                mma_16816(sc[p], af, qf[hh * Gm::KSH + kk][0], qf[hh * Gm::KSH + kk][1], sc[p]);
+                            } else {
+                                af[0] = w0[2 * kk];
+                                af[2] = w0[2 * kk + 1];
+                                af[1] = w1[2 * kk];
+                                af[3] = w1[2 * kk + 1];
+                                mma_16816_bf16(sc[p], af, qf[hh * Gm::KSH + kk][0], qf[hh * Gm::KSH + kk][1], sc[p]);
+                            }
                         }
                     }
                 }
             }
+
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[slot]);  // the K half is free again
 
             // ---- mask, scale to log2 units, stage maximum
             float mx[2] = {-INFINITY, -INFINITY};
@@ -1089,58 +1201,69 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const float p11 = fast_exp2(sc[p][3] - muse[1]);
                 lsum[0] += p00 + p10;
                 lsum[1] += p01 + p11;
-                pb[p][0] = movmatrix_trans(pack_f16x2(p00, p01));
-                pb[p][1] = movmatrix_trans(pack_f16x2(p10, p11));
+                if constexpr (ES == 1) {
+                    pb[p][0] = movmatrix_trans(pack_f16x2(p00, p01));
+                    pb[p][1] = movmatrix_trans(pack_f16x2(p10, p11));
+                } else {
+                    pb[p][0] = movmatrix_trans(pack_bf16x2(p00, p01));
+                    pb[p][1] = movmatrix_trans(pack_bf16x2(p10, p11));
+                }
             }
             l[0] = l[0] * alpha[0] + lsum[0];
             l[1] = l[1] * alpha[1] + lsum[1];
 
             // ---- P.V tile of this stage: O^T[dim][head] = V^T P^T
+            if constexpr (!kEarlyV) {
+                if (!mbar_wait_bounded(&full_bar[S + slot], (st / S) & 1, kWaitLimitNs)) {
+                    report(a.err, FP8KV_ERR_TIMEOUT);
+                    flag[1] = 1;
+                    break;
+                }
+            }
             float ot[Gm::MT][4];
 #pragma unroll
             for (int mt = 0; mt < Gm::MT; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
 #pragma unroll
             for (int p = 0; p < Gm::PPS; ++p) {
                 if (p < np) {
-                    const int t0 = tok_base + p * kBS;
-                    const bool edge = t0 < lo || t0 + kBS > L;
 #pragma unroll
                     for (int hh = 0; hh < Gm::HALVES; ++hh) {
-                        const uint8_t* box = vst + p * Gm::PAGE + hh * Gm::BOX;
                         uint32_t v[4][Gm::VW / 4];
+                        if constexpr (kEarlyV) {
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            const int row = 2 * tig + (r & 1) + 8 * (r >> 1);
-                            if constexpr (Gm::VW == 16) {
-                                const uint4 x = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(row, gid * 16));
-                                v[r][0] = x.x; v[r][1] = x.y; v[r][2] = x.z; v[r][3] = x.w;
-                            } else {
-                                const uint2 x = *reinterpret_cast<const uint2*>(box + swz<Gm::ROWB>(row, gid * 8));
-                                v[r][0] = x.x; v[r][1] = x.y;
-                            }
-                            if (edge) {
-                                const int tok = t0 + row;
-                                if (tok < lo || tok >= L) {
+                            for (int r = 0; r < 4; ++r)
 #pragma unroll
-                                    for (int ww = 0; ww < Gm::VW / 4; ++ww) v[r][ww] = 0u;  // never let stale NaN codes meet p = 0
-                                }
-                            }
+                                for (int ww = 0; ww < Gm::VW / 4; ++ww) v[r][ww] = vr[p][hh][r][ww];
+                        } else {
+                            load_v_box<D, ES>(vst + p * Gm::PAGE + hh * Gm::BOX, gid, tig, tok_base + p * kBS, lo, L,
+                                              true, v);
                         }
 #pragma unroll
                         for (int mtl = 0; mtl < Gm::MTH; ++mtl) {
-                            const uint32_t sel = (mtl & 1) ? 0x7362u : 0x5140u;
-                            const uint32_t x01 = byte_perm(v[0][mtl >> 1], v[1][mtl >> 1], sel);
-                            const uint32_t x23 = byte_perm(v[2][mtl >> 1], v[3][mtl >> 1], sel);
                             uint32_t af[4];
-                            e4m3x4_to_f16x2x2(x01, af[0], af[1]);
-                            e4m3x4_to_f16x2x2(x23, af[2], af[3]);
-                            mma_16816(ot[hh * Gm::MTH + mtl], af, pb[p][0], pb[p][1], ot[hh * Gm::MTH + mtl]);
+                            if constexpr (ES == 1) {
+                                const uint32_t sel = (mtl & 1) ? 0x7362u : 0x5140u;
+                                const uint32_t x01 = byte_perm(v[0][mtl >> 1], v[1][mtl >> 1], sel);
+                                const uint32_t x23 = byte_perm(v[2][mtl >> 1], v[3][mtl >> 1], sel);
+                                e4m3x4_to_f16x2x2(x01, af[0], af[1]);
+                                e4m3x4_to_f16x2x2(x23, af[2], af[3]);
+                                mma_16816(ot[hh * Gm::MTH + mtl], af, pb[p][0], pb[p][1], ot[hh * Gm::MTH + mtl]);
+                            } else {
+                                // element pair 2*mtl of the thread's 8: tokens (2tig, 2tig+1) and (2tig+8, 2tig+9)
+                                af[0] = byte_perm(v[0][mtl], v[1][mtl], 0x5410u);
+                                af[1] = byte_perm(v[0][mtl], v[1][mtl], 0x7632u);
+                                af[2] = byte_perm(v[2][mtl], v[3][mtl], 0x5410u);
+                                af[3] = byte_perm(v[2][mtl], v[3][mtl], 0x7632u);
+                                mma_16816_bf16(ot[hh * Gm::MTH + mtl], af, pb[p][0], pb[p][1], ot[hh * Gm::MTH + mtl]);
+                            }
                         }
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[slot]);
+            if constexpr (!kEarlyV) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_bar[S + slot]);
+            }
 
             // ---- fold the tile into the FP32 accumulators
 #pragma unroll
@@ -1188,7 +1311,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         for (int mt = 0; mt < Gm::MT; ++mt)
 #pragma unroll
                             for (int e2 = 0; e2 < 2; ++e2) {
-                                const int dim = (mt / Gm::MTH) * 128 + Gm::VW * gid + 2 * (mt % Gm::MTH) + e2;
+                                const int dim = (mt / Gm::MTH) * Gm::DBOX + Gm::VWD * gid + 2 * (mt % Gm::MTH) + e2;
                                 out_u[h * D + dim] = f32_to_bf16(o[mt][2 * e2 + j] * sc_out);
                             }
                     }
@@ -1204,7 +1327,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         for (int mt = 0; mt < Gm::MT; ++mt)
 #pragma unroll
                             for (int e2 = 0; e2 < 2; ++e2)
-                                po[(mt / Gm::MTH) * 128 + Gm::VW * gid + 2 * (mt % Gm::MTH) + e2] = o[mt][2 * e2 + j];
+                                po[(mt / Gm::MTH) * Gm::DBOX + Gm::VWD * gid + 2 * (mt % Gm::MTH) + e2] = o[mt][2 * e2 + j];
                         if (gid == 0) a.part_ml[slot_idx * 8 + h] = make_float2(m[j], l[j]);
                     }
                 }
@@ -1458,7 +1581,7 @@ bool make_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int Hk
     return true;
 }
 
-template <int D, int G, bool SIMT>
+template <int D, int G, bool SIMT, int ES = 1>
 cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArgs& a, int ctas,
                    cudaStream_t stream) {
     // The shared-memory opt-in is per device; remember which devices have it.
@@ -1468,8 +1591,8 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
     if (bit == 0 || !(done_mask.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(paged_decode_kernel<D, G, SIMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem_bytes<D, G, SIMT>()));
+        e = cudaFuncSetAttribute(paged_decode_kernel<D, G, SIMT, ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem_bytes<D, G, SIMT, ES>()));
         if (e != cudaSuccess) return e;
         done_mask.fetch_or(bit, std::memory_order_release);
     }
@@ -1481,11 +1604,11 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes<D, G, SIMT>();
+    cfg.dynamicSmemBytes = smem_bytes<D, G, SIMT, ES>();
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, SIMT>, mk, mv, a);
+    e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, SIMT, ES>, mk, mv, a);
     if (e != cudaSuccess || ctas == 1) return e;  // one CTA: every unit is written directly
     cudaLaunchConfig_t mcfg = {};
     mcfg.gridDim = dim3(a.batch * a.num_kv_heads, G);
@@ -1497,14 +1620,14 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     return cudaLaunchKernelEx(&mcfg, merge_kernel<D, G>, a);
 }
 
-template <int D, bool SIMT>
+template <int D, bool SIMT, int ES = 1>
 cudaError_t launch_g(int G, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArgs& a, int ctas,
                      cudaStream_t s) {
     switch (G) {
-        case 1: return launch<D, 1, SIMT>(mk, mv, a, ctas, s);
-        case 2: return launch<D, 2, SIMT>(mk, mv, a, ctas, s);
-        case 4: return launch<D, 4, SIMT>(mk, mv, a, ctas, s);
-        case 8: return launch<D, 8, SIMT>(mk, mv, a, ctas, s);
+        case 1: return launch<D, 1, SIMT, ES>(mk, mv, a, ctas, s);
+        case 2: return launch<D, 2, SIMT, ES>(mk, mv, a, ctas, s);
+        case 4: return launch<D, 4, SIMT, ES>(mk, mv, a, ctas, s);
+        case 8: return launch<D, 8, SIMT, ES>(mk, mv, a, ctas, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -1539,7 +1662,7 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
                          int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len, int batch,
                          int num_q_heads, int num_kv_heads, int head_dim, int block_size, float k_scale,
                          float v_scale, float sm_scale, int window, void* out, void* workspace,
-                         size_t workspace_bytes, void* stream, int engine) {
+                         size_t workspace_bytes, void* stream, int engine, int es = 1) {
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (batch < 0 || batch > 65535 || num_kv_heads < 1 || num_kv_heads > 65535 || num_q_heads < 1 ||
         num_q_heads % num_kv_heads != 0 || max_seq_len < 0 || num_blocks < 1 || max_blocks_per_seq < 0)
@@ -1549,6 +1672,7 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         return FP8KV_ERR_INVALID_ARG;
     const int G = num_q_heads / num_kv_heads;
     if (!supported(head_dim, block_size, G)) return FP8KV_ERR_UNSUPPORTED;
+    if (es == 2 && head_dim == 256) return FP8KV_ERR_UNSUPPORTED;  // a bf16 page of 8 KB exceeds a stage
     if (engine != FP8KV_ENGINE_DEFAULT && engine != FP8KV_ENGINE_TENSOR_CORES && engine != FP8KV_ENGINE_CUDA_CORES)
         return FP8KV_ERR_INVALID_ARG;
     const bool simt = engine == FP8KV_ENGINE_CUDA_CORES ||
@@ -1574,9 +1698,9 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
     if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return FP8KV_ERR_WORKSPACE;
 
-    CUtensorMap mk, mv;
-    if (!make_cache_map(&mk, k_cache, num_blocks, num_kv_heads, head_dim) ||
-        !make_cache_map(&mv, v_cache, num_blocks, num_kv_heads, head_dim))
+    CUtensorMap mk, mv;  // the caches as bytes: rows of head_dim * es bytes
+    if (!make_cache_map(&mk, k_cache, num_blocks, num_kv_heads, head_dim * es) ||
+        !make_cache_map(&mv, v_cache, num_blocks, num_kv_heads, head_dim * es))
         return FP8KV_ERR_CUDA;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1613,7 +1737,10 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         a.score_scale = sm_scale * k_scale * kLog2e;
         a.v_scale = v_scale;
         cudaError_t e;
-        switch (head_dim * 2 + (simt ? 1 : 0)) {
+        if (es == 2) {
+            e = head_dim == 64 ? launch_g<64, false, 2>(G, mk, mv, a, p.ctas, s)
+                               : launch_g<128, false, 2>(G, mk, mv, a, p.ctas, s);
+        } else switch (head_dim * 2 + (simt ? 1 : 0)) {
             case 128: e = launch_g<64, false>(G, mk, mv, a, p.ctas, s); break;
             case 129: e = launch_g<64, true>(G, mk, mv, a, p.ctas, s); break;
             case 256: e = launch_g<128, false>(G, mk, mv, a, p.ctas, s); break;
@@ -1649,6 +1776,18 @@ extern "C" fp8kv_status fp8kv_paged_decode_engine(const void* q, const uint8_t* 
     return decode_impl(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
                        seq_lens, max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale,
                        v_scale, sm_scale, window, out, workspace, workspace_bytes, stream, engine);
+}
+
+extern "C" fp8kv_status fp8kv_paged_decode_bf16(const void* q, const void* k_cache, const void* v_cache,
+                                                int64_t num_blocks, const int32_t* block_tables,
+                                                int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len,
+                                                int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                                int block_size, float sm_scale, int window, void* out,
+                                                void* workspace, size_t workspace_bytes, void* stream) {
+    return decode_impl(q, nullptr, nullptr, static_cast<const uint8_t*>(k_cache), static_cast<const uint8_t*>(v_cache),
+                       num_blocks, block_tables, max_blocks_per_seq, seq_lens, max_seq_len, batch, num_q_heads,
+                       num_kv_heads, head_dim, block_size, 1.0f, 1.0f, sm_scale, window, out, workspace,
+                       workspace_bytes, stream, FP8KV_ENGINE_TENSOR_CORES, 2);
 }
 
 extern "C" fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, uint8_t* k_cache,

@@ -174,6 +174,27 @@ fp8kv_status fp8kv_paged_decode_engine(const void* q, const uint8_t* k_cache, co
                                        size_t workspace_bytes, void* stream, int engine);
 
 /*
+ * The bf16 twin of fp8kv_paged_decode: the same attention over a paged cache
+ * that stores bf16 K and V instead of E4M3 codes -- the baseline the fp8 cache
+ * is compared against [G "What FP8 KV changes" (1 byte per element against
+ * bf16's 2); V "DECODE COST" (cost per cached token, fp8 against bf16)].
+ *
+ *   k_cache, v_cache  bf16 [num_blocks][num_kv_heads][block_size][head_dim],
+ *                     16-byte aligned (no scales: the values are the cache)
+ *   all other arguments, the workspace and the errors as fp8kv_paged_decode.
+ *
+ * Scores and P.V run on the tensor cores with bf16 operands (P rounded to
+ * bf16) and FP32 accumulation, each stage's tile added into FP32 registers.
+ * Supported: head_dim in {64, 128}; block_size == 16; g in {1, 2, 4, 8}.
+ */
+fp8kv_status fp8kv_paged_decode_bf16(const void* q, const void* k_cache, const void* v_cache,
+                                     int64_t num_blocks, const int32_t* block_tables,
+                                     int max_blocks_per_seq, const int32_t* seq_lens,
+                                     int max_seq_len, int batch, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int block_size, float sm_scale, int window,
+                                     void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * One decode step: append, then attend [G "Scales and calibration";
  * G "Attention backend interactions"; V "ACCURACY AT LONG CONTEXT"].
  *

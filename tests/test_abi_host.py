@@ -74,6 +74,24 @@ def test_engine_entry_validates(lib, engine, kw, code):
     assert _engine(lib, engine, **kw) == code
 
 
+def _bf16(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, nb=100, bt=FAKE, mb=8, sl=FAKE, msl=128, B=2, hq=32, hkv=8, d=128,
+             bs=16, sm=0.088, win=0, out=FAKE, ws=FAKE, wsb=1 << 20)
+    a.update(kw)
+    return lib.fp8kv_paged_decode_bf16(a["q"], a["k"], a["v"], a["nb"], a["bt"], a["mb"], a["sl"], a["msl"],
+                                       a["B"], a["hq"], a["hkv"], a["d"], a["bs"], a["sm"], a["win"], a["out"],
+                                       a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=256), 2), (dict(d=96), 2), (dict(bs=32), 2), (dict(hq=128, hkv=8), 2), (dict(hq=30, hkv=8), 1),
+    (dict(sm=float("nan")), 1), (dict(q=None), 1), (dict(k=MISALIGNED), 1), (dict(mb=4, msl=128), 1),
+    (dict(B=0, q=None, out=None), 0),
+])
+def test_bf16_twin_validates(lib, kw, code):
+    assert _bf16(lib, **kw) == code
+
+
 def _step(lib, **kw):
     a = dict(q=FAKE, kn=FAKE, vn=FAKE, k=FAKE, v=FAKE, nb=100, bt=FAKE, mb=8, sl=FAKE, msl=128, B=2, hq=32, hkv=8,
              d=128, bs=16, ks=0.01, vs=0.01, sm=0.088, win=0, out=FAKE, ws=FAKE, wsb=1 << 20)
