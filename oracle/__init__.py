@@ -50,6 +50,10 @@ def _load():
         lib.oracle_decode_attention_bf16.argtypes = [
             P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_float, ctypes.c_int, ctypes.c_int, P, ctypes.c_int64, P]
+        lib.oracle_decode_attention_per_head.restype = ctypes.c_int
+        lib.oracle_decode_attention_per_head.argtypes = [
+            P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
+            ctypes.c_float, ctypes.c_int, ctypes.c_int, P, ctypes.c_int64, P]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -151,4 +155,44 @@ def decode_attention_bf16(q_bits, k_bits, v_bits, seq_lens, sm_scale, window=0, 
         float(sm_scale), int(window), nthreads, _ptr(scratch), max_len, _ptr(out))
     if rc != 0:
         raise ValueError("oracle_decode_attention_bf16: bad arguments")
+    return out
+
+
+def quantize_bf16_per_head(bits, scales) -> np.ndarray:
+    """E4M3 codes of bf16 bits [T, Hkv, d] with one scale per kv head: each
+    head's elements are quantised exactly as quantize_bf16 does with that
+    head's scale."""
+    x = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(x.shape, dtype=np.uint8)
+    for h in range(x.shape[1]):
+        out[:, h, :] = quantize_bf16(np.ascontiguousarray(x[:, h, :]), float(scales[h])).reshape(x.shape[0], x.shape[2])
+    return out
+
+
+def decode_attention_per_head(q_bits, k_codes, v_codes, seq_lens, k_scales, v_scales, sm_scale, window=0,
+                              nthreads=1) -> np.ndarray:
+    """fp64 decode attention over an E4M3 cache with per-kv-head scales
+    (k_scales, v_scales: [Hkv] fp32)."""
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    kc = np.ascontiguousarray(k_codes, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_codes, dtype=np.uint8)
+    ks = np.ascontiguousarray(k_scales, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scales, dtype=np.float32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, d = q.shape
+    Hkv = kc.shape[1]
+    assert kc.shape[2] == d and vc.shape == kc.shape and ks.shape == (Hkv,) and vs.shape == (Hkv,)
+    starts = np.zeros(B, dtype=np.int64)
+    if B > 1:
+        starts[1:] = np.cumsum(lens.astype(np.int64))[:-1]
+    assert int(lens.sum()) <= kc.shape[0]
+    max_len = int(max(1, lens.max() if B else 1))
+    nthreads = max(1, int(nthreads))
+    scratch = np.empty(nthreads * (max_len + d), dtype=np.float64)
+    out = np.zeros((B, Hq, d), dtype=np.float64)
+    rc = _load().oracle_decode_attention_per_head(
+        _ptr(q), _ptr(kc), _ptr(vc), _ptr(starts), _ptr(lens), B, Hq, Hkv, d, _ptr(ks), _ptr(vs),
+        float(sm_scale), int(window), nthreads, _ptr(scratch), max_len, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_decode_attention_per_head: bad arguments")
     return out

@@ -151,15 +151,22 @@ typedef struct {
     const uint16_t* kb;  /* bf16 bits, used when kc is NULL */
     const uint16_t* vb;
     const double* dec;   /* decoded value of each of the 256 codes */
-    double k_scale, v_scale;
+    double k_scale, v_scale;        /* per-tensor scales ... */
+    const float* k_head_scales;     /* ... or one per kv head ([Hkv]) when not NULL */
+    const float* v_head_scales;
+    int Hkv, d;
 } kv_store;
 
 static double kv_key(const kv_store* s, int64_t idx) {
-    return s->kc ? s->dec[s->kc[idx]] * s->k_scale : (double)bf16_bits_to_float(s->kb[idx]);
+    if (!s->kc) return (double)bf16_bits_to_float(s->kb[idx]);
+    const double sc = s->k_head_scales ? (double)s->k_head_scales[(idx / s->d) % s->Hkv] : s->k_scale;
+    return s->dec[s->kc[idx]] * sc;
 }
 
 static double kv_value(const kv_store* s, int64_t idx) {
-    return s->vc ? s->dec[s->vc[idx]] * s->v_scale : (double)bf16_bits_to_float(s->vb[idx]);
+    if (!s->vc) return (double)bf16_bits_to_float(s->vb[idx]);
+    const double sc = s->v_head_scales ? (double)s->v_head_scales[(idx / s->d) % s->Hkv] : s->v_scale;
+    return s->dec[s->vc[idx]] * sc;
 }
 
 /*
@@ -211,8 +218,8 @@ static void attend_one_head(const uint16_t* qh, const kv_store* kv,
 static int attention_batch(const uint16_t* q, const uint8_t* kc, const uint8_t* vc, const uint16_t* kb,
                            const uint16_t* vb, const int64_t* seq_start, const int32_t* seq_lens,
                            int B, int Hq, int Hkv, int d,
-                           float k_scale, float v_scale, float sm_scale, int window,
-                           int acc_bits, int nthreads, double* scratch,
+                           float k_scale, float v_scale, const float* k_head_scales, const float* v_head_scales,
+                           float sm_scale, int window, int acc_bits, int nthreads, double* scratch,
                            int64_t max_len, double* out) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || nthreads <= 0) return -1;
     for (int b = 0; b < B; ++b)
@@ -234,7 +241,7 @@ static int attention_batch(const uint16_t* q, const uint8_t* kc, const uint8_t* 
         double* num = sigma + max_len;
         const int64_t off = seq_start[b] * (int64_t)Hkv * d;
         kv_store kv = {kc ? kc + off : NULL, vc ? vc + off : NULL, kb ? kb + off : NULL, vb ? vb + off : NULL,
-                       dec, (double)k_scale, (double)v_scale};
+                       dec, (double)k_scale, (double)v_scale, k_head_scales, v_head_scales, Hkv, d};
         attend_one_head(q + ((int64_t)b * Hq + h) * d, &kv, seq_lens[b], window, Hkv, h / g, d,
                         (double)sm_scale, acc_bits, sigma, num, out + ((int64_t)b * Hq + h) * d);
     }
@@ -257,8 +264,23 @@ int oracle_decode_attention(const uint16_t* q, const uint8_t* kc, const uint8_t*
                             int acc_bits, int nthreads, double* scratch,
                             int64_t max_len, double* out) {
     if (!kc || !vc) return -1;
-    return attention_batch(q, kc, vc, NULL, NULL, seq_start, seq_lens, B, Hq, Hkv, d, k_scale, v_scale,
+    return attention_batch(q, kc, vc, NULL, NULL, seq_start, seq_lens, B, Hq, Hkv, d, k_scale, v_scale, NULL, NULL,
                            sm_scale, window, acc_bits, nthreads, scratch, max_len, out);
+}
+
+/*
+ * The same attention over an E4M3 cache with one K and one V scale per kv
+ * head (k_scales, v_scales: [Hkv]); code c of kv head h stands for
+ * decode(c) * scales[h].
+ */
+int oracle_decode_attention_per_head(const uint16_t* q, const uint8_t* kc, const uint8_t* vc,
+                                     const int64_t* seq_start, const int32_t* seq_lens,
+                                     int B, int Hq, int Hkv, int d,
+                                     const float* k_scales, const float* v_scales, float sm_scale, int window,
+                                     int nthreads, double* scratch, int64_t max_len, double* out) {
+    if (!kc || !vc || !k_scales || !v_scales) return -1;
+    return attention_batch(q, kc, vc, NULL, NULL, seq_start, seq_lens, B, Hq, Hkv, d, 1.0f, 1.0f, k_scales,
+                           v_scales, sm_scale, window, 0, nthreads, scratch, max_len, out);
 }
 
 /*
@@ -270,8 +292,8 @@ int oracle_decode_attention_bf16(const uint16_t* q, const uint16_t* kb, const ui
                                  int B, int Hq, int Hkv, int d, float sm_scale, int window,
                                  int nthreads, double* scratch, int64_t max_len, double* out) {
     if (!kb || !vb) return -1;
-    return attention_batch(q, NULL, NULL, kb, vb, seq_start, seq_lens, B, Hq, Hkv, d, 1.0f, 1.0f, sm_scale,
-                           window, 0, nthreads, scratch, max_len, out);
+    return attention_batch(q, NULL, NULL, kb, vb, seq_start, seq_lens, B, Hq, Hkv, d, 1.0f, 1.0f, NULL, NULL,
+                           sm_scale, window, 0, nthreads, scratch, max_len, out);
 }
 
 int oracle_max_threads(void) {

@@ -417,3 +417,58 @@ def test_bf16_attention_single_key_returns_its_value():
     out = oracle.decode_attention_bf16(_bits(q), _bits(k), _bits(v), [1], 0.3, 0)
     for h in range(4):
         assert np.array_equal(out[0, h], v[0, h // 2].double().numpy())
+
+
+# ------------------------------------------------------------- per-kv-head scales
+
+def _per_head_case(seed, lens, Hq, Hkv, d):
+    g = torch.Generator().manual_seed(seed)
+    B, T = len(lens), int(sum(lens))
+    q = torch.randn((B, Hq, d), generator=g).to(torch.bfloat16)
+    # heads of very different magnitude, so one scale per head matters
+    mag = torch.tensor([2.0 ** (3 * h - 4) for h in range(Hkv)]).view(1, Hkv, 1)
+    k = (torch.randn((T, Hkv, d), generator=g) * mag).to(torch.bfloat16)
+    v = (torch.randn((T, Hkv, d), generator=g) * mag).to(torch.bfloat16)
+    ks = (k.float().abs().amax(dim=(0, 2)) / 448).numpy().astype(np.float32)
+    vs = (v.float().abs().amax(dim=(0, 2)) / 448).numpy().astype(np.float32)
+    return q, k, v, ks, vs
+
+
+def test_per_head_quantize_is_per_tensor_quantize_of_each_head():
+    q, k, v, ks, vs = _per_head_case(31, [20, 7], 8, 4, 32)
+    kb = _bits(k)
+    codes = oracle.quantize_bf16_per_head(kb, ks)
+    for h in range(4):
+        assert np.array_equal(codes[:, h, :], oracle.quantize_bf16(np.ascontiguousarray(kb[:, h, :]), ks[h]))
+    # equal scales: the per-tensor codes
+    same = np.full(4, ks.max(), dtype=np.float32)
+    assert np.array_equal(oracle.quantize_bf16_per_head(kb, same), oracle.quantize_bf16(kb, float(ks.max())))
+
+
+@pytest.mark.parametrize("window", [0, 6])
+def test_per_head_attention_equals_per_tensor_attention_of_each_head(window):
+    """Each kv head (with its q group) through the per-tensor oracle, at that
+    head's scales, gives exactly the per-head oracle's output for the group."""
+    lens, Hq, Hkv, d = [25, 1, 40], 8, 4, 32
+    q, k, v, ks, vs = _per_head_case(32, lens, Hq, Hkv, d)
+    kc = oracle.quantize_bf16_per_head(_bits(k), ks)
+    vc = oracle.quantize_bf16_per_head(_bits(v), vs)
+    qb = _bits(q)
+    got = oracle.decode_attention_per_head(qb, kc, vc, lens, ks, vs, 0.2, window)
+    G = Hq // Hkv
+    for h in range(Hkv):
+        ref = oracle.decode_attention(np.ascontiguousarray(qb[:, h * G:(h + 1) * G]),
+                                      np.ascontiguousarray(kc[:, h:h + 1]), np.ascontiguousarray(vc[:, h:h + 1]),
+                                      lens, float(ks[h]), float(vs[h]), 0.2, window)
+        assert np.array_equal(got[:, h * G:(h + 1) * G], ref)
+
+
+def test_per_head_attention_with_equal_scales_is_the_per_tensor_attention():
+    lens, Hq, Hkv, d = [30, 12], 8, 2, 16
+    q, k, v, ks, vs = _per_head_case(33, lens, Hq, Hkv, d)
+    kc = oracle.quantize_bf16(_bits(k), 0.05)
+    vc = oracle.quantize_bf16(_bits(v), 0.07)
+    a = oracle.decode_attention(_bits(q), kc, vc, lens, 0.05, 0.07, 0.3, 0)
+    b = oracle.decode_attention_per_head(_bits(q), kc, vc, lens, np.full(Hkv, 0.05, np.float32),
+                                         np.full(Hkv, 0.07, np.float32), 0.3, 0)
+    assert np.array_equal(a, b)
