@@ -59,6 +59,12 @@ def load(build_if_missing: bool = False):
     lib.fp8kv_paged_decode_engine.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P, I]
     lib.fp8kv_paged_decode_bf16.restype = I
     lib.fp8kv_paged_decode_bf16.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, I, P, P, SZ, P]
+    lib.fp8kv_quant_append_per_head.restype = I
+    lib.fp8kv_quant_append_per_head.argtypes = [P, P, P, I64, P, P, I64, I, I, I, P, P, P]
+    lib.fp8kv_paged_decode_per_head.restype = I
+    lib.fp8kv_paged_decode_per_head.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, P, P, F, I, P, P, SZ, P]
+    lib.fp8kv_decode_step_per_head.restype = I
+    lib.fp8kv_decode_step_per_head.argtypes = [P, P, P, P, P, I64, P, I, P, I, I, I, I, I, I, P, P, F, I, P, P, SZ, P]
     lib.fp8kv_decode_step.restype = I
     lib.fp8kv_decode_step.argtypes = [P, P, P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
     lib.fp8kv_paged_decode_noalloc.restype = I
@@ -321,3 +327,61 @@ def prepare_paged_decode_bf16(q, k_cache, v_cache, block_tables, seq_lens, max_s
     args = _decode_bf16_args(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, sm_scale, window, out,
                              workspace, stream)
     return PreparedCall("fp8kv_paged_decode_bf16", load().fp8kv_paged_decode_bf16, args)
+
+
+# ---------------------------------------------------------------- per-kv-head scales
+
+def fp8kv_quant_append_per_head(k_new, v_new, slot_mapping, k_cache, v_cache, k_scales, v_scales, stream=None):
+    """fp8kv_quant_append with fp32 [Hkv] device scale arrays."""
+    nb, hkv, bs, d = k_cache.shape
+    T = k_new.shape[0]
+    if tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d):
+        raise ValueError("k_new/v_new must be [T, Hkv, D] matching the cache")
+    if k_scales.numel() != hkv or v_scales.numel() != hkv:
+        raise ValueError("k_scales/v_scales must have num_kv_heads entries")
+    _check("fp8kv_quant_append_per_head", load().fp8kv_quant_append_per_head(
+        _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _dev(slot_mapping, torch.int64, "slot_mapping"), ctypes.c_int64(T), _dev(k_cache, torch.uint8, "k_cache"),
+        _dev(v_cache, torch.uint8, "v_cache"), ctypes.c_int64(nb), bs, hkv, d,
+        _dev(k_scales, torch.float32, "k_scales"), _dev(v_scales, torch.float32, "v_scales"), _stream(stream)))
+
+
+def _per_head_common(q, k_cache, v_cache, block_tables, seq_lens, k_scales, v_scales):
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch between q and the caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.numel() != B:
+        raise ValueError("block_tables must be [B, max_blocks] and seq_lens [B]")
+    if k_scales.numel() != hkv or v_scales.numel() != hkv:
+        raise ValueError("k_scales/v_scales must have num_kv_heads entries")
+    return B, hq, d, nb, hkv, bs
+
+
+def fp8kv_paged_decode_per_head(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scales, v_scales,
+                                sm_scale, window, out, workspace, stream=None):
+    """fp8kv_paged_decode with fp32 [Hkv] device scale arrays."""
+    B, hq, d, nb, hkv, bs = _per_head_common(q, k_cache, v_cache, block_tables, seq_lens, k_scales, v_scales)
+    I = ctypes.c_int
+    _check("fp8kv_paged_decode_per_head", load().fp8kv_paged_decode_per_head(
+        _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.uint8, "k_cache"), _dev(v_cache, torch.uint8, "v_cache"),
+        ctypes.c_int64(nb), _dev(block_tables, torch.int32, "block_tables"), I(block_tables.shape[1]),
+        _dev(seq_lens, torch.int32, "seq_lens"), I(max_seq_len), I(B), I(hq), I(hkv), I(d), I(bs),
+        _dev(k_scales, torch.float32, "k_scales"), _dev(v_scales, torch.float32, "v_scales"),
+        ctypes.c_float(sm_scale), I(window), _dev(out, torch.bfloat16, "out"),
+        _dev(workspace, torch.uint8, "workspace"), ctypes.c_size_t(workspace.numel()), _stream(stream)))
+
+
+def fp8kv_decode_step_per_head(q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scales,
+                               v_scales, sm_scale, window, out, workspace, stream=None):
+    """fp8kv_decode_step with fp32 [Hkv] device scale arrays."""
+    B, hq, d, nb, hkv, bs = _per_head_common(q, k_cache, v_cache, block_tables, seq_lens, k_scales, v_scales)
+    I = ctypes.c_int
+    _check("fp8kv_decode_step_per_head", load().fp8kv_decode_step_per_head(
+        _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _dev(k_cache, torch.uint8, "k_cache"), _dev(v_cache, torch.uint8, "v_cache"), ctypes.c_int64(nb),
+        _dev(block_tables, torch.int32, "block_tables"), I(block_tables.shape[1]),
+        _dev(seq_lens, torch.int32, "seq_lens"), I(max_seq_len), I(B), I(hq), I(hkv), I(d), I(bs),
+        _dev(k_scales, torch.float32, "k_scales"), _dev(v_scales, torch.float32, "v_scales"),
+        ctypes.c_float(sm_scale), I(window), _dev(out, torch.bfloat16, "out"),
+        _dev(workspace, torch.uint8, "workspace"), ctypes.c_size_t(workspace.numel()), _stream(stream)))

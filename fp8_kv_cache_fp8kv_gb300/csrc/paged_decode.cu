@@ -77,6 +77,9 @@ struct DecodeArgs {
     uint8_t* v_cache;
     float k_scale_raw;          // per-tensor scales (the append divides by them)
     float v_scale_raw;
+    const float* k_scales;      // [Hkv] per-kv-head scales, or null for the per-tensor ones
+    const float* v_scales;
+    float sm_scale;
     const int32_t* block_tables;
     const int32_t* seq_lens;
     uint16_t* out;              // bf16 [B, Hq, D]
@@ -254,6 +257,16 @@ __device__ __forceinline__ void store_new_row(const NewRow<D>& r, uint8_t* dst_r
 // pre-scaled per head by a power of two so the f16 copy is exact (largest |q|
 // in [2^14, 2^15)); cs[j] scales the raw score of head 2*tig+j back and into
 // log2 units.
+// Score multiplier (sm_scale * k_scale * log2 e, multiplied in that order as
+// the host does for the per-tensor scale) and V scale of kv head hk.
+__device__ __forceinline__ float unit_score_scale(const DecodeArgs& a, int hk) {
+    return a.k_scales ? (a.sm_scale * __ldg(a.k_scales + hk)) * kLog2e : a.score_scale;
+}
+
+__device__ __forceinline__ float unit_v_scale(const DecodeArgs& a, int hk) {
+    return a.v_scales ? __ldg(a.v_scales + hk) : a.v_scale;
+}
+
 template <int D, int G>
 __device__ __forceinline__ void load_query(const DecodeArgs& a, int b, int hk, int gid, int tig,
                                            uint32_t (&qf)[Geo<D>::KS][2], float (&cs)[2]) {
@@ -296,7 +309,7 @@ __device__ __forceinline__ void load_query(const DecodeArgs& a, int b, int hk, i
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         const int sh = __shfl_sync(0xffffffffu, shift, (2 * tig + j) * 4);
-        cs[j] = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+        cs[j] = unit_score_scale(a, hk) * __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
     }
 }
 
@@ -625,7 +638,7 @@ __device__ __forceinline__ void simt_consumers(const DecodeArgs& a, const CtaVie
         consumer_sync();
 #pragma unroll
         for (int j = 0; j < G; ++j) {
-            cs[j] = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - v.qsh[j]) << 23);
+            cs[j] = unit_score_scale(a, w.hk) * __uint_as_float(static_cast<uint32_t>(127 - v.qsh[j]) << 23);
             m[j] = -INFINITY;
             l[j] = 0.f;
 #pragma unroll
@@ -810,7 +823,7 @@ __device__ __forceinline__ void simt_consumers(const DecodeArgs& a, const CtaVie
                 uint16_t* out_u = a.out + (static_cast<int64_t>(w.b) * a.num_q_heads + w.hk * G) * D + lane * DPL;
 #pragma unroll
                 for (int j = 0; j < G; ++j) {
-                    const float sc_out = l[j] > 0.f ? a.v_scale / l[j] : 0.f;
+                    const float sc_out = l[j] > 0.f ? unit_v_scale(a, w.hk) / l[j] : 0.f;
                     uint32_t pk[DPL / 2];
 #pragma unroll
                     for (int k = 0; k < DPL / 2; ++k)
@@ -961,7 +974,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const bool appending = ES == 1 && a.k_new != nullptr;
         const uint16_t* new_rows = pw == 0 ? a.k_new : a.v_new;
         uint8_t* cache = pw == 0 ? a.k_cache : a.v_cache;
-        const float scale_raw = pw == 0 ? a.k_scale_raw : a.v_scale_raw;
+        const float scale_raw = pw == 0 ? a.k_scale_raw : a.v_scale_raw;  // per-tensor; per head below
+        const float* head_scales = pw == 0 ? a.k_scales : a.v_scales;
         Walker w;
         walk_start(w, pre, B, Hkv, s);
         auto seg_pages = [&](const Walker& x) { return static_cast<int>(min(e, x.base + x.n) - x.g); };
@@ -1010,7 +1024,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 if (id >= 0) {
                     const int L = lens[batch_b];
                     uint8_t* dst_row = cache + ((static_cast<int64_t>(id) * Hkv + hk) * kBS + (L - 1) % kBS) * D;
-                    store_new_row<D>(batch_row, dst_row, lane, scale_raw);
+                    store_new_row<D>(batch_row, dst_row, lane, head_scales ? __ldg(head_scales + hk) : scale_raw);
                     fence_proxy_async_global();
                 }
                 __syncwarp();
@@ -1305,7 +1319,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int h = 2 * tig + j;
-                    const float sc_out = l[j] > 0.f ? a.v_scale / l[j] : 0.f;
+                    const float sc_out = l[j] > 0.f ? unit_v_scale(a, w.hk) / l[j] : 0.f;
                     if (h < G) {
 #pragma unroll
                         for (int mt = 0; mt < Gm::MT; ++mt)
@@ -1446,7 +1460,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a
         o.x += f * sm_o[j][g4].x; o.y += f * sm_o[j][g4].y; o.z += f * sm_o[j][g4].z; o.w += f * sm_o[j][g4].w;
         Lt += f * sm_l[j][g4];
     }
-    const float sc_out = Lt > 0.f ? a.v_scale / Lt : 0.f;
+    const float sc_out = Lt > 0.f ? unit_v_scale(a, hk) / Lt : 0.f;
     uint16_t* out = a.out + (static_cast<int64_t>(b) * a.num_q_heads + hk * G + h) * D;
     const uint32_t lo2 = f32_to_bf16(o.x * sc_out) | (static_cast<uint32_t>(f32_to_bf16(o.y * sc_out)) << 16);
     const uint32_t hi2 = f32_to_bf16(o.z * sc_out) | (static_cast<uint32_t>(f32_to_bf16(o.w * sc_out)) << 16);
@@ -1662,7 +1676,8 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
                          int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len, int batch,
                          int num_q_heads, int num_kv_heads, int head_dim, int block_size, float k_scale,
                          float v_scale, float sm_scale, int window, void* out, void* workspace,
-                         size_t workspace_bytes, void* stream, int engine, int es = 1) {
+                         size_t workspace_bytes, void* stream, int engine, int es = 1,
+                         const float* k_scales = nullptr, const float* v_scales = nullptr) {
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (batch < 0 || batch > 65535 || num_kv_heads < 1 || num_kv_heads > 65535 || num_q_heads < 1 ||
         num_q_heads % num_kv_heads != 0 || max_seq_len < 0 || num_blocks < 1 || max_blocks_per_seq < 0)
@@ -1689,6 +1704,9 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
     if (!a16(q) || !a16(k_cache) || !a16(v_cache) || !a16(out)) return FP8KV_ERR_INVALID_ARG;
     if ((k_new == nullptr) != (v_new == nullptr)) return FP8KV_ERR_INVALID_ARG;
     if (k_new && (!a16(k_new) || !a16(v_new))) return FP8KV_ERR_INVALID_ARG;
+    if ((k_scales == nullptr) != (v_scales == nullptr)) return FP8KV_ERR_INVALID_ARG;
+    if (k_scales && ((reinterpret_cast<uintptr_t>(k_scales) & 3u) || (reinterpret_cast<uintptr_t>(v_scales) & 3u)))
+        return FP8KV_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
         return FP8KV_ERR_INVALID_ARG;
     int sms = 0;
@@ -1720,6 +1738,9 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         a.v_cache = const_cast<uint8_t*>(v_cache);
         a.k_scale_raw = k_scale;
         a.v_scale_raw = v_scale;
+        a.k_scales = k_scales;
+        a.v_scales = v_scales;
+        a.sm_scale = sm_scale;
         a.block_tables = block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq;
         a.seq_lens = seq_lens + b0;
         a.out = static_cast<uint16_t*>(out) + static_cast<int64_t>(b0) * num_q_heads * head_dim;
@@ -1788,6 +1809,34 @@ extern "C" fp8kv_status fp8kv_paged_decode_bf16(const void* q, const void* k_cac
                        num_blocks, block_tables, max_blocks_per_seq, seq_lens, max_seq_len, batch, num_q_heads,
                        num_kv_heads, head_dim, block_size, 1.0f, 1.0f, sm_scale, window, out, workspace,
                        workspace_bytes, stream, FP8KV_ENGINE_TENSOR_CORES, 2);
+}
+
+extern "C" fp8kv_status fp8kv_paged_decode_per_head(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                                    int64_t num_blocks, const int32_t* block_tables,
+                                                    int max_blocks_per_seq, const int32_t* seq_lens,
+                                                    int max_seq_len, int batch, int num_q_heads, int num_kv_heads,
+                                                    int head_dim, int block_size, const float* k_scales,
+                                                    const float* v_scales, float sm_scale, int window, void* out,
+                                                    void* workspace, size_t workspace_bytes, void* stream) {
+    if (batch > 0 && (!k_scales || !v_scales)) return FP8KV_ERR_INVALID_ARG;
+    return decode_impl(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
+                       seq_lens, max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, 1.0f, 1.0f,
+                       sm_scale, window, out, workspace, workspace_bytes, stream, FP8KV_ENGINE_DEFAULT, 1, k_scales,
+                       v_scales);
+}
+
+extern "C" fp8kv_status fp8kv_decode_step_per_head(const void* q, const void* k_new, const void* v_new,
+                                                   uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks,
+                                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                                   const int32_t* seq_lens, int max_seq_len, int batch,
+                                                   int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                                   const float* k_scales, const float* v_scales, float sm_scale,
+                                                   int window, void* out, void* workspace, size_t workspace_bytes,
+                                                   void* stream) {
+    if (batch > 0 && (!k_new || !v_new || !k_scales || !v_scales)) return FP8KV_ERR_INVALID_ARG;
+    return decode_impl(q, k_new, v_new, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
+                       max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, 1.0f, 1.0f, sm_scale,
+                       window, out, workspace, workspace_bytes, stream, FP8KV_ENGINE_DEFAULT, 1, k_scales, v_scales);
 }
 
 extern "C" fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, uint8_t* k_cache,

@@ -3,7 +3,8 @@
 //
 // The operation is the one gpusmith.com, "FP8 KV Cache Quantization: Capacity
 // Gains and Accuracy Risk", describes in "Scales and calibration" (each K and
-// V tensor is divided by a per-tensor scale, then cast) with the format of
+// V tensor is divided by a scale, then cast; one scale per tensor, or one per
+// kv head for the per-attention-head granularity) with the format of
 // "What FP8 KV changes" (E4M3, 1 byte per element, maximum normal 448).  The
 // divide is one IEEE fp32 division; the cast is the hardware's
 // round-to-nearest-even, saturating-finite conversion.
@@ -25,7 +26,8 @@ namespace fp8kv {
 __global__ void __launch_bounds__(256) quant_append_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, const int64_t* __restrict__ slot_mapping,
     int64_t num_tokens, uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, int64_t num_slots,
-    int num_kv_heads, int head_dim, int block_size, float k_scale, float v_scale) {
+    int num_kv_heads, int head_dim, int block_size, float k_scale, float v_scale,
+    const float* __restrict__ k_scales, const float* __restrict__ v_scales) {
     // A decode launched right after may get resident now (it waits for this
     // grid before reading anything).
     griddep_launch_dependents();
@@ -52,7 +54,9 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
         const uint4* src = (is_v ? v_new : k_new) + 2 * j;
         const uint4 a = __ldcs(src);
         const uint4 b = __ldcs(src + 1);
-        const float s = is_v ? v_scale : k_scale;
+        // per-tensor scale, or the kv head's own one ([Hkv] arrays)
+        const float* hs = is_v ? v_scales : k_scales;
+        const float s = hs ? __ldg(hs + hk) : (is_v ? v_scale : k_scale);
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         uint32_t o[4];
 #pragma unroll
@@ -79,12 +83,17 @@ bool good_scale(float s) { return std::isfinite(s) && s > 0.0f; }
 
 }  // namespace
 
-extern "C" fp8kv_status fp8kv_quant_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
-                                           int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
-                                           int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
-                                           float k_scale, float v_scale, void* stream) {
+namespace {
+
+fp8kv_status append_impl(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t num_tokens,
+                         uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks, int block_size, int num_kv_heads,
+                         int head_dim, float k_scale, float v_scale, const float* k_scales, const float* v_scales,
+                         void* stream) {
     if (num_tokens < 0 || num_blocks < 1 || block_size < 1 || num_kv_heads < 1) return FP8KV_ERR_INVALID_ARG;
     if (!good_scale(k_scale) || !good_scale(v_scale)) return FP8KV_ERR_INVALID_ARG;
+    if ((k_scales == nullptr) != (v_scales == nullptr)) return FP8KV_ERR_INVALID_ARG;
+    if (k_scales && ((reinterpret_cast<uintptr_t>(k_scales) & 3u) || (reinterpret_cast<uintptr_t>(v_scales) & 3u)))
+        return FP8KV_ERR_INVALID_ARG;
     if (head_dim % 16 != 0 || head_dim < 16 || head_dim > 1024) return FP8KV_ERR_UNSUPPORTED;
     if (!k_cache || !v_cache || !aligned16(k_cache) || !aligned16(v_cache)) return FP8KV_ERR_INVALID_ARG;
     if (num_tokens == 0) return FP8KV_OK;
@@ -116,6 +125,26 @@ extern "C" fp8kv_status fp8kv_quant_append(const void* k_new, const void* v_new,
     const cudaError_t err = cudaLaunchKernelEx(
         &cfg, fp8kv::quant_append_kernel, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
         slot_mapping, num_tokens, k_cache, v_cache, num_blocks * block_size, num_kv_heads, head_dim, block_size,
-        k_scale, v_scale);
+        k_scale, v_scale, k_scales, v_scales);
     return err == cudaSuccess ? FP8KV_OK : FP8KV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" fp8kv_status fp8kv_quant_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                           int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
+                                           int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
+                                           float k_scale, float v_scale, void* stream) {
+    return append_impl(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, block_size, num_kv_heads,
+                       head_dim, k_scale, v_scale, nullptr, nullptr, stream);
+}
+
+extern "C" fp8kv_status fp8kv_quant_append_per_head(const void* k_new, const void* v_new,
+                                                    const int64_t* slot_mapping, int64_t num_tokens,
+                                                    uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks,
+                                                    int block_size, int num_kv_heads, int head_dim,
+                                                    const float* k_scales, const float* v_scales, void* stream) {
+    if (num_tokens > 0 && (!k_scales || !v_scales)) return FP8KV_ERR_INVALID_ARG;
+    return append_impl(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, block_size, num_kv_heads,
+                       head_dim, 1.0f, 1.0f, k_scales, v_scales, stream);
 }

@@ -147,6 +147,46 @@ fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache, const uin
                                 float sm_scale, int window, void* out, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/*
+ * Per-attention-head scales [G "Scales and calibration": per-tensor or
+ * per-attention-head k/v scales, [num_kv_heads] each].
+ *
+ * The same operations as fp8kv_quant_append, fp8kv_paged_decode and
+ * fp8kv_decode_step, with one K scale and one V scale per kv head instead of
+ * one per tensor: elements of kv head h are divided by k_scales[h]
+ * (v_scales[h]) before the cast, and its codes stand for
+ * decode(code) * scale[h] in the attention.
+ *
+ *   k_scales, v_scales  DEVICE fp32 [num_kv_heads], 4-byte aligned, finite and
+ *                       > 0 (not checked on the device: other values give
+ *                       unspecified codes and outputs); read by the kernels
+ *                       after they wait for the previous work on the stream.
+ *   all other arguments, the workspace and the errors as the per-tensor calls.
+ * With every k_scales[h] == k_scale and v_scales[h] == v_scale the results
+ * are bit-identical to the per-tensor calls.
+ */
+fp8kv_status fp8kv_quant_append_per_head(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                         int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
+                                         int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
+                                         const float* k_scales, const float* v_scales, void* stream);
+
+fp8kv_status fp8kv_paged_decode_per_head(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                         int64_t num_blocks, const int32_t* block_tables,
+                                         int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len,
+                                         int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                         int block_size, const float* k_scales, const float* v_scales,
+                                         float sm_scale, int window, void* out, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
+fp8kv_status fp8kv_decode_step_per_head(const void* q, const void* k_new, const void* v_new,
+                                        uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks,
+                                        const int32_t* block_tables, int max_blocks_per_seq,
+                                        const int32_t* seq_lens, int max_seq_len, int batch,
+                                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                        const float* k_scales, const float* v_scales, float sm_scale,
+                                        int window, void* out, void* workspace, size_t workspace_bytes,
+                                        void* stream);
+
 /* Which units perform the two contractions of the decode attention. */
 typedef enum {
     FP8KV_ENGINE_DEFAULT = 0,      /* the library's choice for the shape (the faster one measured) */

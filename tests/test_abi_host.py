@@ -113,6 +113,31 @@ def test_decode_step_empty_batch_is_a_no_op(lib):
     assert _step(lib, B=0, q=None, kn=None, vn=None, out=None) == 0
 
 
+def _decode_ph(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, nb=100, bt=FAKE, mb=8, sl=FAKE, msl=128, B=2, hq=32, hkv=8, d=128,
+             bs=16, ks=FAKE, vs=FAKE, sm=0.088, win=0, out=FAKE, ws=FAKE, wsb=1 << 20)
+    a.update(kw)
+    return lib.fp8kv_paged_decode_per_head(a["q"], a["k"], a["v"], a["nb"], a["bt"], a["mb"], a["sl"], a["msl"],
+                                           a["B"], a["hq"], a["hkv"], a["d"], a["bs"], a["ks"], a["vs"], a["sm"],
+                                           a["win"], a["out"], a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ks=None), 1), (dict(vs=None), 1), (dict(ks=ctypes.c_void_p(0x10002)), 1), (dict(d=96), 2),
+    (dict(sm=float("inf")), 1), (dict(B=0, q=None, out=None, ks=None, vs=None), 0),
+])
+def test_per_head_decode_validates(lib, kw, code):
+    assert _decode_ph(lib, **kw) == code
+
+
+def test_per_head_append_validates(lib):
+    f = lib.fp8kv_quant_append_per_head
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 10, 16, 8, 128, None, FAKE, None) == 1
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 10, 16, 8, 128, ctypes.c_void_p(0x10002), FAKE, None) == 1
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 10, 16, 8, 24, FAKE, FAKE, None) == 2
+    assert f(None, None, None, 0, FAKE, FAKE, 10, 16, 8, 128, None, None, None) == 0
+
+
 def _append(lib, **kw):
     a = dict(k=FAKE, v=FAKE, sm=FAKE, T=4, kc=FAKE, vc=FAKE, nb=10, bs=16, hkv=8, d=128, ks=0.5, vs=0.5)
     a.update(kw)
