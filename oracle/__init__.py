@@ -54,6 +54,16 @@ def _load():
         lib.oracle_decode_attention_per_head.argtypes = [
             P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
             ctypes.c_float, ctypes.c_int, ctypes.c_int, P, ctypes.c_int64, P]
+        lib.oracle_decode_codes_e5m2.restype = None
+        lib.oracle_decode_codes_e5m2.argtypes = [P, ctypes.c_int64, P]
+        lib.oracle_encode_f32_e5m2.restype = None
+        lib.oracle_encode_f32_e5m2.argtypes = [P, ctypes.c_int64, P]
+        lib.oracle_quantize_bf16_e5m2.restype = None
+        lib.oracle_quantize_bf16_e5m2.argtypes = [P, ctypes.c_int64, ctypes.c_float, P]
+        lib.oracle_decode_attention_e5m2.restype = ctypes.c_int
+        lib.oracle_decode_attention_e5m2.argtypes = [
+            P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_int, P, ctypes.c_int64, P]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -195,4 +205,56 @@ def decode_attention_per_head(q_bits, k_codes, v_codes, seq_lens, k_scales, v_sc
         float(sm_scale), int(window), nthreads, _ptr(scratch), max_len, _ptr(out))
     if rc != 0:
         raise ValueError("oracle_decode_attention_per_head: bad arguments")
+    return out
+
+
+# ---------------------------------------------------------------- E5M2
+
+def e5m2_decode(codes) -> np.ndarray:
+    """Exact fp64 value of each E5M2 code (+-inf for 0x7C / 0xFC, NaN for the
+    other exponent-31 codes)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_decode_codes_e5m2(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def e5m2_encode(values) -> np.ndarray:
+    """E5M2 code of each fp32 value: round-to-nearest-even, saturate at +-57344."""
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().oracle_encode_f32_e5m2(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def quantize_bf16_e5m2(x_bits, scale: float) -> np.ndarray:
+    """E5M2 cache codes of bf16 inputs: code = e5m2(fp32(x) / fp32(scale))."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().oracle_quantize_bf16_e5m2(_ptr(x), x.size, float(scale), _ptr(out))
+    return out
+
+
+def decode_attention_e5m2(q_bits, k_codes, v_codes, seq_lens, k_scale, v_scale, sm_scale, window=0,
+                          nthreads=1) -> np.ndarray:
+    """fp64 decode attention over an E5M2 cache (per-tensor scales)."""
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    kc = np.ascontiguousarray(k_codes, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_codes, dtype=np.uint8)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, d = q.shape
+    Hkv = kc.shape[1]
+    starts = np.zeros(B, dtype=np.int64)
+    if B > 1:
+        starts[1:] = np.cumsum(lens.astype(np.int64))[:-1]
+    assert int(lens.sum()) <= kc.shape[0] and vc.shape == kc.shape
+    max_len = int(max(1, lens.max() if B else 1))
+    nthreads = max(1, int(nthreads))
+    scratch = np.empty(nthreads * (max_len + d), dtype=np.float64)
+    out = np.zeros((B, Hq, d), dtype=np.float64)
+    rc = _load().oracle_decode_attention_e5m2(
+        _ptr(q), _ptr(kc), _ptr(vc), _ptr(starts), _ptr(lens), B, Hq, Hkv, d, float(k_scale), float(v_scale),
+        float(sm_scale), int(window), nthreads, _ptr(scratch), max_len, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_decode_attention_e5m2: bad arguments")
     return out

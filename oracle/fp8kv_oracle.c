@@ -99,6 +99,63 @@ uint8_t oracle_e4m3_encode(float y) {
     return (uint8_t)(sign | code);
 }
 
+/*
+ * E5M2 (the other FP8 format; gpusmith.com, "What FP8 KV changes": 2 mantissa
+ * bits, maximum 57,344).  Layout after the same format paper: S.EEEEE.MM,
+ * exponent bias 15, subnormals m * 2^-16, IEEE-style specials (exponent 31:
+ * mantissa 0 = infinity, otherwise NaN).
+ */
+double oracle_e5m2_decode(uint8_t c) {
+    int s = (c >> 7) & 1;
+    int e = (c >> 2) & 0x1F;
+    int m = c & 0x3;
+    double v;
+    if (e == 31) return m == 0 ? (s ? -INFINITY : INFINITY) : NAN;
+    if (e == 0)
+        v = ldexp((double)m, -16);
+    else
+        v = ldexp((double)(4 + m), e - 17);
+    return s ? -v : v;
+}
+
+/* E5M2 encoder: RNE, saturating finite magnitudes >= 57344 and infinities to
+ * +-57344 (0x7B / 0xFB); NaN maps to 0x7F; the sign of zero and of an
+ * underflow is kept. */
+uint8_t oracle_e5m2_encode(float y) {
+    uint32_t bits;
+    memcpy(&bits, &y, sizeof bits);
+    uint8_t sign = (uint8_t)((bits >> 31) << 7);
+    if (isnan(y)) return 0x7F;
+    double a = fabs((double)y);
+    if (a >= 57344.0) return (uint8_t)(sign | 0x7B);
+    if (a == 0.0) return sign;
+    int ex;
+    frexp(a, &ex);
+    int E = ex - 1;                 /* a in [2^E, 2^(E+1)) */
+    if (E < -14) E = -14;           /* subnormals share the 2^-16 quantum */
+    double quantum = ldexp(1.0, E - 2);
+    double v = round_half_even(a / quantum) * quantum;
+    if (v == 0.0) return sign;
+    uint8_t code;
+    if (v < ldexp(1.0, -14)) {
+        code = (uint8_t)(v / ldexp(1.0, -16));
+    } else {
+        int vex;
+        frexp(v, &vex);
+        int Ev = vex - 1;
+        int m = (int)(v / ldexp(1.0, Ev - 2)) - 4;     /* 0..3 */
+        code = (uint8_t)(((Ev + 15) << 2) | m);
+    }
+    return (uint8_t)(sign | code);
+}
+
+/* Quantise-on-append into E5M2: code = e5m2(fp32(x) / scale). */
+void oracle_quantize_bf16_e5m2(const uint16_t* x, int64_t n, float scale, uint8_t* out);
+
+void oracle_decode_codes_e5m2(const uint8_t* c, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e5m2_decode(c[i]);
+}
+
 static float bf16_bits_to_float(uint16_t h) {
     uint32_t u = (uint32_t)h << 16;
     float f;
@@ -117,6 +174,21 @@ void oracle_quantize_bf16(const uint16_t* x, int64_t n, float scale, uint8_t* ou
         float y = xf / scale;
         out[i] = oracle_e4m3_encode(y);
     }
+}
+
+void oracle_quantize_bf16_e5m2(const uint16_t* x, int64_t n, float scale, uint8_t* out) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t i = 0; i < n; ++i) {
+        float xf = bf16_bits_to_float(x[i]);
+        float y = xf / scale;
+        out[i] = oracle_e5m2_encode(y);
+    }
+}
+
+void oracle_encode_f32_e5m2(const float* y, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e5m2_encode(y[i]);
 }
 
 void oracle_encode_f32(const float* y, int64_t n, uint8_t* out) {
@@ -220,12 +292,12 @@ static int attention_batch(const uint16_t* q, const uint8_t* kc, const uint8_t* 
                            int B, int Hq, int Hkv, int d,
                            float k_scale, float v_scale, const float* k_head_scales, const float* v_head_scales,
                            float sm_scale, int window, int acc_bits, int nthreads, double* scratch,
-                           int64_t max_len, double* out) {
+                           int64_t max_len, double* out, int e5m2) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || nthreads <= 0) return -1;
     for (int b = 0; b < B; ++b)
         if (seq_lens[b] < 0 || seq_lens[b] > max_len) return -1;
     double dec[256];
-    for (int c = 0; c < 256; ++c) dec[c] = oracle_e4m3_decode((uint8_t)c);
+    for (int c = 0; c < 256; ++c) dec[c] = e5m2 ? oracle_e5m2_decode((uint8_t)c) : oracle_e4m3_decode((uint8_t)c);
     int g = Hq / Hkv;
     int64_t units = (int64_t)B * Hq;
 #ifdef _OPENMP
@@ -265,7 +337,18 @@ int oracle_decode_attention(const uint16_t* q, const uint8_t* kc, const uint8_t*
                             int64_t max_len, double* out) {
     if (!kc || !vc) return -1;
     return attention_batch(q, kc, vc, NULL, NULL, seq_start, seq_lens, B, Hq, Hkv, d, k_scale, v_scale, NULL, NULL,
-                           sm_scale, window, acc_bits, nthreads, scratch, max_len, out);
+                           sm_scale, window, acc_bits, nthreads, scratch, max_len, out, 0);
+}
+
+/* The same attention over an E5M2 cache (per-tensor scales). */
+int oracle_decode_attention_e5m2(const uint16_t* q, const uint8_t* kc, const uint8_t* vc,
+                                 const int64_t* seq_start, const int32_t* seq_lens,
+                                 int B, int Hq, int Hkv, int d,
+                                 float k_scale, float v_scale, float sm_scale, int window,
+                                 int nthreads, double* scratch, int64_t max_len, double* out) {
+    if (!kc || !vc) return -1;
+    return attention_batch(q, kc, vc, NULL, NULL, seq_start, seq_lens, B, Hq, Hkv, d, k_scale, v_scale, NULL, NULL,
+                           sm_scale, window, 0, nthreads, scratch, max_len, out, 1);
 }
 
 /*
@@ -280,7 +363,7 @@ int oracle_decode_attention_per_head(const uint16_t* q, const uint8_t* kc, const
                                      int nthreads, double* scratch, int64_t max_len, double* out) {
     if (!kc || !vc || !k_scales || !v_scales) return -1;
     return attention_batch(q, kc, vc, NULL, NULL, seq_start, seq_lens, B, Hq, Hkv, d, 1.0f, 1.0f, k_scales,
-                           v_scales, sm_scale, window, 0, nthreads, scratch, max_len, out);
+                           v_scales, sm_scale, window, 0, nthreads, scratch, max_len, out, 0);
 }
 
 /*
@@ -293,7 +376,7 @@ int oracle_decode_attention_bf16(const uint16_t* q, const uint16_t* kb, const ui
                                  int nthreads, double* scratch, int64_t max_len, double* out) {
     if (!kb || !vb) return -1;
     return attention_batch(q, NULL, NULL, kb, vb, seq_start, seq_lens, B, Hq, Hkv, d, 1.0f, 1.0f, NULL, NULL,
-                           sm_scale, window, 0, nthreads, scratch, max_len, out);
+                           sm_scale, window, 0, nthreads, scratch, max_len, out, 0);
 }
 
 int oracle_max_threads(void) {

@@ -472,3 +472,106 @@ def test_per_head_attention_with_equal_scales_is_the_per_tensor_attention():
     b = oracle.decode_attention_per_head(_bits(q), kc, vc, lens, np.full(Hkv, 0.05, np.float32),
                                          np.full(Hkv, 0.07, np.float32), 0.3, 0)
     assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------- E5M2 (the other FP8 format)
+
+def test_e5m2_decoder_printed_facts_and_structure():
+    """2 mantissa bits and a maximum of 57,344 (gpusmith.com, "What FP8 KV
+    changes"); IEEE-style specials; every finite value once per sign."""
+    c = np.arange(256, dtype=np.uint8)
+    d = oracle.e5m2_decode(c)
+    fin = np.isfinite(d)
+    assert d[fin].max() == 57344.0 and d[0x7B] == 57344.0 and d[0xFB] == -57344.0
+    assert np.isinf(d[0x7C]) and d[0x7C] > 0 and np.isinf(d[0xFC]) and d[0xFC] < 0
+    assert np.isnan(d[[0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF]]).all()
+    assert d[0x01] == 2.0 ** -16 and d[0x04] == 2.0 ** -14          # smallest subnormal / normal
+    pos = d[:0x7C]
+    assert np.all(np.diff(pos) > 0)                                   # monotone in code order
+    assert np.array_equal(d[0x80:0xFC], -pos)
+    # each binade [2^e, 2^(e+1)) holds exactly 4 values (2 mantissa bits)
+    for e in range(-14, 16):
+        n = np.count_nonzero((pos >= 2.0 ** e) & (pos < 2.0 ** (e + 1)))
+        assert n == 4, e
+
+
+def test_e5m2_decoder_matches_torch_float8_e5m2():
+    c = np.arange(256, dtype=np.uint8)
+    d = oracle.e5m2_decode(c)
+    t = torch.from_numpy(c.copy()).view(torch.float8_e5m2).double().numpy()
+    assert np.array_equal(np.isnan(d), np.isnan(t))
+    ok = ~np.isnan(d)
+    assert np.array_equal(d[ok], t[ok])
+
+
+def test_e5m2_encoder_roundtrip_midpoints_and_saturation():
+    c = np.arange(256, dtype=np.uint8)
+    d = oracle.e5m2_decode(c)
+    fin = np.isfinite(d)
+    assert np.array_equal(oracle.e5m2_encode(d[fin].astype(np.float32)), c[fin])
+    # midpoints between neighbours go to the even code
+    pos = np.sort(d[(d > 0) & fin])
+    mid = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
+    assert np.array_equal(mid.astype(np.float64), (pos[:-1] + pos[1:]) / 2)   # exact in fp32
+    got = oracle.e5m2_encode(mid)
+    lo = oracle.e5m2_encode(pos[:-1].astype(np.float32))
+    hi = oracle.e5m2_encode(pos[1:].astype(np.float32))
+    assert np.array_equal(got, np.where(lo % 2 == 0, lo, hi))
+    sat = np.array([57344.0, 60000.0, 61440.0, 1e30, np.inf, -61440.0, -np.inf], dtype=np.float32)
+    assert list(oracle.e5m2_encode(sat)) == [0x7B] * 5 + [0xFB] * 2
+    assert oracle.e5m2_encode(np.array([np.nan], np.float32))[0] == 0x7F
+    assert list(oracle.e5m2_encode(np.array([0.0, -0.0, 2.0 ** -18, -2.0 ** -18], np.float32))) == [0, 0x80, 0, 0x80]
+
+
+def test_e5m2_encoder_matches_brute_force_and_torch_in_range():
+    rng = np.random.default_rng(9)
+    y = (rng.standard_normal(20000) * np.exp2(rng.integers(-18, 16, 20000))).astype(np.float32)
+    y = y[np.abs(y) < 57344]
+    got = oracle.e5m2_encode(y)
+    c = np.arange(256, dtype=np.uint8)
+    d = oracle.e5m2_decode(c)
+    fin = np.isfinite(d)
+    vals, codes = d[fin], c[fin]
+    # brute force: nearest finite value, ties to the even code
+    dist = np.abs(y[:, None].astype(np.float64) - vals[None, :])
+    best = dist.min(axis=1, keepdims=True)
+    cand = np.where(dist == best, codes[None, :].astype(np.int32), 999)
+    even = np.where(cand % 2 == 0, cand, 999).min(axis=1)
+    first = cand.min(axis=1)
+    ties = (dist == best).sum(axis=1) > 1
+    want = np.where(ties, even, first).astype(np.uint8)
+    # zero: the sign of the input decides between 0x00 and 0x80
+    zero = want == 0
+    want[zero & (y < 0)] = 0x80
+    assert np.array_equal(got, want)
+    t = torch.from_numpy(y).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(got, t)
+
+
+@pytest.mark.parametrize("window", [0, 5])
+def test_e5m2_attention_matches_torch_fp64_softmax(window):
+    lens, Hq, Hkv, d = [33, 1, 60], 8, 2, 32
+    g = torch.Generator().manual_seed(41)
+    q = torch.randn((3, Hq, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((sum(lens), Hkv, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((sum(lens), Hkv, d), generator=g).to(torch.bfloat16)
+    ks = float(np.float32(k.float().abs().max() / 57344))
+    vs = float(np.float32(v.float().abs().max() / 57344))
+    kc = oracle.quantize_bf16_e5m2(_bits(k), ks)
+    vc = oracle.quantize_bf16_e5m2(_bits(v), vs)
+    # the quantiser is the encoder applied to the fp32 quotient
+    assert np.array_equal(kc, oracle.e5m2_encode((k.float() / torch.tensor(ks, dtype=torch.float32)).numpy()))
+    got = oracle.decode_attention_e5m2(_bits(q), kc, vc, lens, ks, vs, 0.25, window)
+    kh = torch.from_numpy(oracle.e5m2_decode(kc)) * ks
+    vh = torch.from_numpy(oracle.e5m2_decode(vc)) * vs
+    G = Hq // Hkv
+    ref = np.zeros_like(got)
+    start = 0
+    for b, L in enumerate(lens):
+        lo = L - window if (window > 0 and L > window) else 0
+        for h in range(Hq):
+            K = kh[start + lo:start + L, h // G]
+            V = vh[start + lo:start + L, h // G]
+            ref[b, h] = (torch.softmax(0.25 * (K @ q[b, h].double()), dim=0) @ V).numpy()
+        start += L
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-13)
