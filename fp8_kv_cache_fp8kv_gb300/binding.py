@@ -65,6 +65,12 @@ def load(build_if_missing: bool = False):
     lib.fp8kv_paged_decode_per_head.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, P, P, F, I, P, P, SZ, P]
     lib.fp8kv_decode_step_per_head.restype = I
     lib.fp8kv_decode_step_per_head.argtypes = [P, P, P, P, P, I64, P, I, P, I, I, I, I, I, I, P, P, F, I, P, P, SZ, P]
+    lib.fp8kv_quant_append_e5m2.restype = I
+    lib.fp8kv_quant_append_e5m2.argtypes = [P, P, P, I64, P, P, I64, I, I, I, F, F, P]
+    lib.fp8kv_paged_decode_e5m2.restype = I
+    lib.fp8kv_paged_decode_e5m2.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
+    lib.fp8kv_decode_step_e5m2.restype = I
+    lib.fp8kv_decode_step_e5m2.argtypes = [P, P, P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
     lib.fp8kv_decode_step.restype = I
     lib.fp8kv_decode_step.argtypes = [P, P, P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
     lib.fp8kv_paged_decode_noalloc.restype = I
@@ -385,3 +391,27 @@ def fp8kv_decode_step_per_head(q, k_new, v_new, k_cache, v_cache, block_tables, 
         _dev(k_scales, torch.float32, "k_scales"), _dev(v_scales, torch.float32, "v_scales"),
         ctypes.c_float(sm_scale), I(window), _dev(out, torch.bfloat16, "out"),
         _dev(workspace, torch.uint8, "workspace"), ctypes.c_size_t(workspace.numel()), _stream(stream)))
+
+
+# ---------------------------------------------------------------- E5M2 cache
+
+def fp8kv_quant_append_e5m2(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, stream=None):
+    """fp8kv_quant_append writing E5M2 codes."""
+    call = prepare_quant_append(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, stream)
+    _check("fp8kv_quant_append_e5m2", load().fp8kv_quant_append_e5m2(*call.args))
+
+
+def fp8kv_paged_decode_e5m2(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale, v_scale, sm_scale,
+                            window, out, workspace, stream=None):
+    """fp8kv_paged_decode over an E5M2 cache."""
+    call = prepare_paged_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale, v_scale,
+                                sm_scale, window, out, workspace, stream)
+    _check("fp8kv_paged_decode_e5m2", load().fp8kv_paged_decode_e5m2(*call.args))
+
+
+def fp8kv_decode_step_e5m2(q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale,
+                           v_scale, sm_scale, window, out, workspace, stream=None):
+    """fp8kv_decode_step over an E5M2 cache."""
+    _check("fp8kv_decode_step_e5m2", load().fp8kv_decode_step_e5m2(*_decode_step_args(
+        q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale, v_scale, sm_scale,
+        window, out, workspace, stream)))

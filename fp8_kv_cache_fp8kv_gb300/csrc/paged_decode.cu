@@ -233,13 +233,14 @@ __device__ __forceinline__ void load_new_row(NewRow<D>& r, const uint16_t* src_r
 // Quantise-on-append of the warp's row: code = E4M3_satfinite(fp32(x) / scale)
 // with one IEEE divide and one RNE conversion (the same arithmetic as the
 // quant_append kernel), stored at dst_row.
-template <int D>
+template <int D, bool E5M2 = false>
 __device__ __forceinline__ void store_new_row(const NewRow<D>& r, uint8_t* dst_row, int lane, float scale) {
     uint16_t c[D / 64];
 #pragma unroll
     for (int i = 0; i < D / 64; ++i) {
         const float e0 = __uint_as_float(r.w[i] << 16), e1 = __uint_as_float(r.w[i] & 0xFFFF0000u);
-        c[i] = f32x2_to_e4m3x2_satfinite(__fdiv_rn(e0, scale), __fdiv_rn(e1, scale));
+        c[i] = E5M2 ? f32x2_to_e5m2x2_satfinite(__fdiv_rn(e0, scale), __fdiv_rn(e1, scale))
+                    : f32x2_to_e4m3x2_satfinite(__fdiv_rn(e0, scale), __fdiv_rn(e1, scale));
     }
     uint8_t* dst = dst_row + lane * (D / 32);
     if constexpr (D == 64) {
@@ -257,6 +258,16 @@ __device__ __forceinline__ void store_new_row(const NewRow<D>& r, uint8_t* dst_r
 // pre-scaled per head by a power of two so the f16 copy is exact (largest |q|
 // in [2^14, 2^15)); cs[j] scales the raw score of head 2*tig+j back and into
 // log2 units.
+// Four FP8 codes (one 32-bit word, code 0 in the low byte) -> two f16x2:
+// codes 0,1 in lo and 2,3 in hi; exact for both formats.
+template <bool E5M2>
+__device__ __forceinline__ void codes4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    if constexpr (E5M2)
+        e5m2x4_to_f16x2x2(w, lo, hi);
+    else
+        e4m3x4_to_f16x2x2(w, lo, hi);
+}
+
 // Score multiplier (sm_scale * k_scale * log2 e, multiplied in that order as
 // the host does for the per-tensor scale) and V scale of kv head hk.
 __device__ __forceinline__ float unit_score_scale(const DecodeArgs& a, int hk) {
@@ -850,11 +861,12 @@ __device__ __forceinline__ void simt_consumers(const DecodeArgs& a, const CtaVie
     }
 }
 
-template <int D, int G, bool SIMT, int ES = 1>
+template <int D, int G, bool SIMT, int ES = 1, bool E5M2 = false>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeArgs a) {
     static_assert(ES == 1 || !SIMT, "the bf16 twin runs on the tensor cores only");
+    static_assert(!E5M2 || (ES == 1 && !SIMT), "the E5M2 cache runs on the tensor cores only");
     using Gm = Geo<D, ES>;
     // At d = 128 the V fragments move to registers as soon as they land (a
     // measured gain); the accumulators of d = 256 leave no room, and at d = 64
@@ -1024,7 +1036,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 if (id >= 0) {
                     const int L = lens[batch_b];
                     uint8_t* dst_row = cache + ((static_cast<int64_t>(id) * Hkv + hk) * kBS + (L - 1) % kBS) * D;
-                    store_new_row<D>(batch_row, dst_row, lane, head_scales ? __ldg(head_scales + hk) : scale_raw);
+                    store_new_row<D, E5M2>(batch_row, dst_row, lane, head_scales ? __ldg(head_scales + hk) : scale_raw);
                     fence_proxy_async_global();
                 }
                 __syncwarp();
@@ -1159,8 +1171,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         for (int kk = 0; kk < Gm::KSH; ++kk) {
                             uint32_t af[4];
                             if constexpr (ES == 1) {
-                                e4m3x4_to_f16x2x2(w0[kk], af[0], af[2]);
-                                e4m3x4_to_f16x2x2(w1[kk], af[1], af[3]);
+                                codes4_to_f16x2x2<E5M2>(w0[kk], af[0], af[2]);
+                                codes4_to_f16x2x2<E5M2>(w1[kk], af[1], af[3]);
                                 mma_16816(sc[p], af, qf[hh * Gm::KSH + kk][0], qf[hh * Gm::KSH + kk][1], sc[p]);
                             } else {
                                 af[0] = w0[2 * kk];
@@ -1259,8 +1271,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                                 const uint32_t sel = (mtl & 1) ? 0x7362u : 0x5140u;
                                 const uint32_t x01 = byte_perm(v[0][mtl >> 1], v[1][mtl >> 1], sel);
                                 const uint32_t x23 = byte_perm(v[2][mtl >> 1], v[3][mtl >> 1], sel);
-                                e4m3x4_to_f16x2x2(x01, af[0], af[1]);
-                                e4m3x4_to_f16x2x2(x23, af[2], af[3]);
+                                codes4_to_f16x2x2<E5M2>(x01, af[0], af[1]);
+                                codes4_to_f16x2x2<E5M2>(x23, af[2], af[3]);
                                 mma_16816(ot[hh * Gm::MTH + mtl], af, pb[p][0], pb[p][1], ot[hh * Gm::MTH + mtl]);
                             } else {
                                 // element pair 2*mtl of the thread's 8: tokens (2tig, 2tig+1) and (2tig+8, 2tig+9)
@@ -1595,7 +1607,7 @@ bool make_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int Hk
     return true;
 }
 
-template <int D, int G, bool SIMT, int ES = 1>
+template <int D, int G, bool SIMT, int ES = 1, bool E5M2 = false>
 cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArgs& a, int ctas,
                    cudaStream_t stream) {
     // The shared-memory opt-in is per device; remember which devices have it.
@@ -1605,7 +1617,7 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
     if (bit == 0 || !(done_mask.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(paged_decode_kernel<D, G, SIMT, ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(paged_decode_kernel<D, G, SIMT, ES, E5M2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem_bytes<D, G, SIMT, ES>()));
         if (e != cudaSuccess) return e;
         done_mask.fetch_or(bit, std::memory_order_release);
@@ -1622,7 +1634,7 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, SIMT, ES>, mk, mv, a);
+    e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, SIMT, ES, E5M2>, mk, mv, a);
     if (e != cudaSuccess || ctas == 1) return e;  // one CTA: every unit is written directly
     cudaLaunchConfig_t mcfg = {};
     mcfg.gridDim = dim3(a.batch * a.num_kv_heads, G);
@@ -1634,14 +1646,14 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     return cudaLaunchKernelEx(&mcfg, merge_kernel<D, G>, a);
 }
 
-template <int D, bool SIMT, int ES = 1>
+template <int D, bool SIMT, int ES = 1, bool E5M2 = false>
 cudaError_t launch_g(int G, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArgs& a, int ctas,
                      cudaStream_t s) {
     switch (G) {
-        case 1: return launch<D, 1, SIMT, ES>(mk, mv, a, ctas, s);
-        case 2: return launch<D, 2, SIMT, ES>(mk, mv, a, ctas, s);
-        case 4: return launch<D, 4, SIMT, ES>(mk, mv, a, ctas, s);
-        case 8: return launch<D, 8, SIMT, ES>(mk, mv, a, ctas, s);
+        case 1: return launch<D, 1, SIMT, ES, E5M2>(mk, mv, a, ctas, s);
+        case 2: return launch<D, 2, SIMT, ES, E5M2>(mk, mv, a, ctas, s);
+        case 4: return launch<D, 4, SIMT, ES, E5M2>(mk, mv, a, ctas, s);
+        case 8: return launch<D, 8, SIMT, ES, E5M2>(mk, mv, a, ctas, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -1677,7 +1689,7 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
                          int num_q_heads, int num_kv_heads, int head_dim, int block_size, float k_scale,
                          float v_scale, float sm_scale, int window, void* out, void* workspace,
                          size_t workspace_bytes, void* stream, int engine, int es = 1,
-                         const float* k_scales = nullptr, const float* v_scales = nullptr) {
+                         const float* k_scales = nullptr, const float* v_scales = nullptr, bool e5m2 = false) {
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (batch < 0 || batch > 65535 || num_kv_heads < 1 || num_kv_heads > 65535 || num_q_heads < 1 ||
         num_q_heads % num_kv_heads != 0 || max_seq_len < 0 || num_blocks < 1 || max_blocks_per_seq < 0)
@@ -1761,6 +1773,10 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         if (es == 2) {
             e = head_dim == 64 ? launch_g<64, false, 2>(G, mk, mv, a, p.ctas, s)
                                : launch_g<128, false, 2>(G, mk, mv, a, p.ctas, s);
+        } else if (e5m2) {
+            e = head_dim == 64 ? launch_g<64, false, 1, true>(G, mk, mv, a, p.ctas, s)
+                : head_dim == 128 ? launch_g<128, false, 1, true>(G, mk, mv, a, p.ctas, s)
+                                  : launch_g<256, false, 1, true>(G, mk, mv, a, p.ctas, s);
         } else switch (head_dim * 2 + (simt ? 1 : 0)) {
             case 128: e = launch_g<64, false>(G, mk, mv, a, p.ctas, s); break;
             case 129: e = launch_g<64, true>(G, mk, mv, a, p.ctas, s); break;
@@ -1837,6 +1853,33 @@ extern "C" fp8kv_status fp8kv_decode_step_per_head(const void* q, const void* k_
     return decode_impl(q, k_new, v_new, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                        max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, 1.0f, 1.0f, sm_scale,
                        window, out, workspace, workspace_bytes, stream, FP8KV_ENGINE_DEFAULT, 1, k_scales, v_scales);
+}
+
+extern "C" fp8kv_status fp8kv_paged_decode_e5m2(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                                int64_t num_blocks, const int32_t* block_tables,
+                                                int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len,
+                                                int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                                int block_size, float k_scale, float v_scale, float sm_scale,
+                                                int window, void* out, void* workspace, size_t workspace_bytes,
+                                                void* stream) {
+    return decode_impl(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
+                       seq_lens, max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale,
+                       v_scale, sm_scale, window, out, workspace, workspace_bytes, stream, FP8KV_ENGINE_TENSOR_CORES,
+                       1, nullptr, nullptr, true);
+}
+
+extern "C" fp8kv_status fp8kv_decode_step_e5m2(const void* q, const void* k_new, const void* v_new,
+                                               uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks,
+                                               const int32_t* block_tables, int max_blocks_per_seq,
+                                               const int32_t* seq_lens, int max_seq_len, int batch,
+                                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                               float k_scale, float v_scale, float sm_scale, int window, void* out,
+                                               void* workspace, size_t workspace_bytes, void* stream) {
+    if (batch > 0 && (!k_new || !v_new)) return FP8KV_ERR_INVALID_ARG;
+    return decode_impl(q, k_new, v_new, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
+                       max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale, v_scale,
+                       sm_scale, window, out, workspace, workspace_bytes, stream, FP8KV_ENGINE_TENSOR_CORES, 1,
+                       nullptr, nullptr, true);
 }
 
 extern "C" fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, uint8_t* k_cache,

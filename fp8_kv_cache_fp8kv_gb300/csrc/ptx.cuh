@@ -125,6 +125,22 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint
         : "r"(w));
 }
 
+// Both halves of a 32-bit word of E5M2 codes -> two f16x2.  An E5M2 code is
+// the upper byte of the f16 with the same value (same sign, 5 exponent bits
+// with bias 15, leading 2 mantissa bits), so this is a byte move.
+__device__ __forceinline__ void e5m2x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("prmt.b32 %0, %1, 0, 0x1404;" : "=r"(lo) : "r"(w));
+    asm("prmt.b32 %0, %1, 0, 0x3424;" : "=r"(hi) : "r"(w));
+}
+
+// fp32 pair -> E5M2 pair with round-to-nearest-even and saturation to
+// +-57344; `lo` lands in bits 0-7, `hi` in bits 8-15.
+__device__ __forceinline__ uint16_t f32x2_to_e5m2x2_satfinite(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // fp32 pair -> E4M3 pair with round-to-nearest-even and saturation to +-448;
 // `lo` lands in bits 0-7, `hi` in bits 8-15.
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2_satfinite(float lo, float hi) {

@@ -9,6 +9,9 @@
 // divide is one IEEE fp32 division; the cast is the hardware's
 // round-to-nearest-even, saturating-finite conversion.
 //
+// The same kernel writes E5M2 codes (the other FP8 format: 2 mantissa bits,
+// maximum 57,344, same page) when asked for them.
+//
 // HBM-bound elementwise kernel: each thread turns 16 bf16 values (32 bytes,
 // two 16-byte loads) into 16 codes (one 16-byte store).  The grid is a
 // multiple of the SM count and strides over all (token, head, 16-dim chunk)
@@ -23,6 +26,7 @@
 
 namespace fp8kv {
 
+template <bool E5M2>
 __global__ void __launch_bounds__(256) quant_append_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, const int64_t* __restrict__ slot_mapping,
     int64_t num_tokens, uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, int64_t num_slots,
@@ -65,8 +69,14 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
             const uint32_t w0 = w[2 * q], w1 = w[2 * q + 1];
             const float e0 = __uint_as_float(w0 << 16), e1 = __uint_as_float(w0 & 0xFFFF0000u);
             const float e2 = __uint_as_float(w1 << 16), e3 = __uint_as_float(w1 & 0xFFFF0000u);
-            const uint16_t lo = f32x2_to_e4m3x2_satfinite(__fdiv_rn(e0, s), __fdiv_rn(e1, s));
-            const uint16_t hi = f32x2_to_e4m3x2_satfinite(__fdiv_rn(e2, s), __fdiv_rn(e3, s));
+            uint16_t lo, hi;
+            if constexpr (E5M2) {
+                lo = f32x2_to_e5m2x2_satfinite(__fdiv_rn(e0, s), __fdiv_rn(e1, s));
+                hi = f32x2_to_e5m2x2_satfinite(__fdiv_rn(e2, s), __fdiv_rn(e3, s));
+            } else {
+                lo = f32x2_to_e4m3x2_satfinite(__fdiv_rn(e0, s), __fdiv_rn(e1, s));
+                hi = f32x2_to_e4m3x2_satfinite(__fdiv_rn(e2, s), __fdiv_rn(e3, s));
+            }
             o[q] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
         }
         uint8_t* dst = (is_v ? v_cache : k_cache) + ((blk * num_kv_heads + hk) * block_size + off) * head_dim + c * 16;
@@ -88,7 +98,7 @@ namespace {
 fp8kv_status append_impl(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t num_tokens,
                          uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks, int block_size, int num_kv_heads,
                          int head_dim, float k_scale, float v_scale, const float* k_scales, const float* v_scales,
-                         void* stream) {
+                         void* stream, bool e5m2 = false) {
     if (num_tokens < 0 || num_blocks < 1 || block_size < 1 || num_kv_heads < 1) return FP8KV_ERR_INVALID_ARG;
     if (!good_scale(k_scale) || !good_scale(v_scale)) return FP8KV_ERR_INVALID_ARG;
     if ((k_scales == nullptr) != (v_scales == nullptr)) return FP8KV_ERR_INVALID_ARG;
@@ -123,9 +133,9 @@ fp8kv_status append_impl(const void* k_new, const void* v_new, const int64_t* sl
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t err = cudaLaunchKernelEx(
-        &cfg, fp8kv::quant_append_kernel, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
-        slot_mapping, num_tokens, k_cache, v_cache, num_blocks * block_size, num_kv_heads, head_dim, block_size,
-        k_scale, v_scale, k_scales, v_scales);
+        &cfg, e5m2 ? fp8kv::quant_append_kernel<true> : fp8kv::quant_append_kernel<false>,
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, num_tokens, k_cache,
+        v_cache, num_blocks * block_size, num_kv_heads, head_dim, block_size, k_scale, v_scale, k_scales, v_scales);
     return err == cudaSuccess ? FP8KV_OK : FP8KV_ERR_CUDA;
 }
 
@@ -147,4 +157,12 @@ extern "C" fp8kv_status fp8kv_quant_append_per_head(const void* k_new, const voi
     if (num_tokens > 0 && (!k_scales || !v_scales)) return FP8KV_ERR_INVALID_ARG;
     return append_impl(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, block_size, num_kv_heads,
                        head_dim, 1.0f, 1.0f, k_scales, v_scales, stream);
+}
+
+extern "C" fp8kv_status fp8kv_quant_append_e5m2(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                                int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
+                                                int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
+                                                float k_scale, float v_scale, void* stream) {
+    return append_impl(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, block_size, num_kv_heads,
+                       head_dim, k_scale, v_scale, nullptr, nullptr, stream, true);
 }

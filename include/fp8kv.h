@@ -187,6 +187,40 @@ fp8kv_status fp8kv_decode_step_per_head(const void* q, const void* k_new, const 
                                         int window, void* out, void* workspace, size_t workspace_bytes,
                                         void* stream);
 
+/*
+ * The E5M2 cache [G "What FP8 KV changes": the other FP8 format, 2 mantissa
+ * bits and a maximum of 57,344; E4M3 is the default].
+ *
+ * The same operations as fp8kv_quant_append, fp8kv_paged_decode and
+ * fp8kv_decode_step with E5M2 codes (S.EEEEE.MM, exponent bias 15,
+ * subnormals m * 2^-16): code = E5M2(fp32(x) / scale) with one IEEE fp32
+ * division and one round-to-nearest-even, saturating-finite conversion
+ * (|x| >= 57344 and infinities -> +-57344, NaN -> NaN).  A code stands for
+ * its exact value times the scale; E5M2 values are exact in f16, so the
+ * decode runs the same tensor-core path.  Arguments, layout, workspace and
+ * errors as the E4M3 calls.
+ */
+fp8kv_status fp8kv_quant_append_e5m2(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                     int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
+                                     int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
+                                     float k_scale, float v_scale, void* stream);
+
+fp8kv_status fp8kv_paged_decode_e5m2(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                     int64_t num_blocks, const int32_t* block_tables,
+                                     int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len,
+                                     int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                     int block_size, float k_scale, float v_scale, float sm_scale,
+                                     int window, void* out, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+fp8kv_status fp8kv_decode_step_e5m2(const void* q, const void* k_new, const void* v_new,
+                                    uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks,
+                                    const int32_t* block_tables, int max_blocks_per_seq,
+                                    const int32_t* seq_lens, int max_seq_len, int batch,
+                                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                    float k_scale, float v_scale, float sm_scale, int window, void* out,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* Which units perform the two contractions of the decode attention. */
 typedef enum {
     FP8KV_ENGINE_DEFAULT = 0,      /* the library's choice for the shape (the faster one measured) */
