@@ -577,6 +577,11 @@ def run_sweep(args, rank, ws):
         k8 = torch.zeros(cshape, dtype=torch.uint8, device=dev)
         v8 = torch.zeros_like(k8)
         fk.fp8kv_quant_append(w.k.to(dev), w.v.to(dev), sm, k8, v8, w.k_scale, w.v_scale)
+        k5 = torch.zeros(cshape, dtype=torch.uint8, device=dev)
+        v5 = torch.zeros_like(k5)
+        ks5 = float(np.float32(w.k.float().abs().max() / 57344.0))
+        vs5 = float(np.float32(w.v.float().abs().max() / 57344.0))
+        fk.fp8kv_quant_append_e5m2(w.k.to(dev), w.v.to(dev), sm, k5, v5, ks5, vs5)
         kb = torch.zeros(cshape, dtype=torch.bfloat16, device=dev)
         vb = torch.zeros_like(kb)
         kb[blk, :, off, :] = w.k.to(dev)
@@ -589,8 +594,12 @@ def run_sweep(args, rank, ws):
         calls = {
             "fp8": fk.prepare_paged_decode(q, k8, v8, bt, lens, L, w.k_scale, w.v_scale, w.sm_scale, 0, out, wsp),
             "bf16": fk.prepare_paged_decode_bf16(q, kb, vb, bt, lens, L, w.sm_scale, 0, out, wsp),
+            "e5m2": fk.PreparedCall("fp8kv_paged_decode_e5m2", fk.load().fp8kv_paged_decode_e5m2,
+                                    fk.prepare_paged_decode(q, k5, v5, bt, lens, L, ks5, vs5, w.sm_scale, 0, out,
+                                                            wsp).args),
         }
         read = {"fp8": accounting.decode_bytes([L], 32, 8, 128, 0),
+                "e5m2": accounting.decode_bytes([L], 32, 8, 128, 0),
                 "bf16": 2 * accounting.decode_bytes([L], 32, 8, 128, 0)}
         rec = {"context": L}
         for name, call in calls.items():
@@ -612,21 +621,22 @@ def run_sweep(args, rank, ws):
             rec[name + "_us"] = round(us, 3)
             rec[name + "_l2"] = "flushed" if flush.buf is not None else "larger than L2"
         points.append(rec)
-        del k8, v8, kb, vb
+        del k8, v8, k5, v5, kb, vb
         torch.cuda.empty_cache()
     fit = {}
-    for name in ("fp8", "bf16"):
+    for name in ("fp8", "e5m2", "bf16"):
         slope, icpt = _fit([p["context"] for p in points], [p[name + "_us"] for p in points])
         fit[name] = {"us_per_1k_tokens": round(slope * 1e3, 5), "intercept_us": round(icpt, 3)}
     ratio = fit["fp8"]["us_per_1k_tokens"] / fit["bf16"]["us_per_1k_tokens"]
     d_icpt = fit["fp8"]["intercept_us"] - fit["bf16"]["intercept_us"]
     d_slope = (fit["bf16"]["us_per_1k_tokens"] - fit["fp8"]["us_per_1k_tokens"]) / 1e3
     breakeven = round(d_icpt / d_slope) if d_icpt > 0 and d_slope > 0 else None  # None: fp8 never slower
-    return {"sweep": "paged decode time against context length, fp8 cache vs bf16 cache",
+    return {"sweep": "paged decode time against context length: E4M3 ('fp8') and E5M2 caches vs the bf16 cache",
             "config": {"workload": "llama31_8b_layer_b1", "num_q_heads": 32, "num_kv_heads": 8, "head_dim": 128,
                        "batch": 1, "block_size": 16, "window": 0, "timer": "CUDA events per call, median of %d"
                        % args.steps},
             "points": points, "fit": fit, "slope_ratio_fp8_over_bf16": round(ratio, 4),
+            "slope_ratio_e5m2_over_bf16": round(fit["e5m2"]["us_per_1k_tokens"] / fit["bf16"]["us_per_1k_tokens"], 4),
             "breakeven_context_tokens": breakeven, "n_gpus": ws}
 
 
