@@ -258,3 +258,47 @@ def decode_attention_e5m2(q_bits, k_codes, v_codes, seq_lens, k_scale, v_scale, 
     if rc != 0:
         raise ValueError("oracle_decode_attention_e5m2: bad arguments")
     return out
+
+
+# ---------------------------------------------------------------- prefill (chunked) attention
+
+def prefill_attention(q_bits, k_codes, v_codes, seq_lens, q_lens, k_scale, v_scale, sm_scale, window=0,
+                      nthreads=1) -> np.ndarray:
+    """fp64 causal attention of a chunk of new query tokens over an E4M3 cache.
+
+    q_bits   uint16 [sum(q_lens), Hq, d]: the queries of sequence b are its
+             last q_lens[b] tokens, positions seq_lens[b] - q_lens[b] ..
+             seq_lens[b] - 1, packed sequence after sequence
+    k_codes, v_codes  uint8 [sum(seq_lens), Hkv, d], sequences concatenated in
+             logical order (the chunk's own keys included)
+    Query token at position p attends keys [max(0, p + 1 - window), p]
+    (window <= 0: [0, p]); row by row this is the decode attention of a
+    sequence of length p + 1, which is how it is computed here.
+    """
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    kc = np.ascontiguousarray(k_codes, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_codes, dtype=np.uint8)
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    qls = np.asarray(q_lens, dtype=np.int64)
+    assert np.all(qls <= lens) and q.shape[0] == int(qls.sum())
+    R, Hq, d = q.shape
+    Hkv = kc.shape[1]
+    starts_seq = np.zeros(len(lens), dtype=np.int64)
+    if len(lens) > 1:
+        starts_seq[1:] = np.cumsum(lens)[:-1]
+    row_start = np.repeat(starts_seq, qls)
+    row_len = np.concatenate([np.arange(L - n + 1, L + 1) for L, n in zip(lens, qls)]).astype(np.int32) \
+        if R else np.zeros(0, np.int32)
+    max_len = int(max(1, row_len.max() if R else 1))
+    nthreads = max(1, int(nthreads))
+    scratch = np.empty(nthreads * (max_len + d), dtype=np.float64)
+    out = np.zeros((R, Hq, d), dtype=np.float64)
+    if R == 0:
+        return out
+    rc = _load().oracle_decode_attention(
+        _ptr(q.reshape(R, Hq, d)), _ptr(kc), _ptr(vc), _ptr(np.ascontiguousarray(row_start)),
+        _ptr(np.ascontiguousarray(row_len)), R, Hq, Hkv, d, float(k_scale), float(v_scale), float(sm_scale),
+        int(window), 0, nthreads, _ptr(scratch), max_len, _ptr(out))
+    if rc != 0:
+        raise ValueError("prefill_attention: bad arguments")
+    return out

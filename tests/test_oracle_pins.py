@@ -575,3 +575,56 @@ def test_e5m2_attention_matches_torch_fp64_softmax(window):
             ref[b, h] = (torch.softmax(0.25 * (K @ q[b, h].double()), dim=0) @ V).numpy()
         start += L
     assert np.allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------- prefill (chunked) attention
+
+@pytest.mark.parametrize("window", [0, 9])
+def test_prefill_matches_torch_causal_softmax(window):
+    lens, qlens, Hq, Hkv, d = [40, 17, 5], [12, 17, 1], 8, 2, 32
+    g = torch.Generator().manual_seed(51)
+    T = sum(lens)
+    k = torch.randn((T, Hkv, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((T, Hkv, d), generator=g).to(torch.bfloat16)
+    q = torch.randn((sum(qlens), Hq, d), generator=g).to(torch.bfloat16)
+    ks = float(np.float32(k.float().abs().max() / 448))
+    vs = float(np.float32(v.float().abs().max() / 448))
+    kc = oracle.quantize_bf16(_bits(k), ks)
+    vc = oracle.quantize_bf16(_bits(v), vs)
+    sm = float(np.float32(0.2))   # the oracle takes sm_scale as an fp32 value
+    got = oracle.prefill_attention(_bits(q), kc, vc, lens, qlens, ks, vs, sm, window)
+    kh = torch.from_numpy(oracle.e4m3_decode(kc)) * ks
+    vh = torch.from_numpy(oracle.e4m3_decode(vc)) * vs
+    G = Hq // Hkv
+    ref = np.zeros_like(got)
+    s0, r0 = 0, 0
+    for L, n in zip(lens, qlens):
+        pos = torch.arange(L)
+        for i in range(n):
+            p = L - n + i
+            mask = pos <= p
+            if window > 0:
+                mask &= pos > p - window
+            for h in range(Hq):
+                K = kh[s0:s0 + L, h // G]
+                V = vh[s0:s0 + L, h // G]
+                s = sm * (K @ q[r0 + i, h].double())
+                s = torch.where(mask, s, torch.tensor(float("-inf"), dtype=torch.float64))
+                ref[r0 + i, h] = (torch.softmax(s, dim=0) @ V).numpy()
+        s0 += L
+        r0 += n
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_prefill_last_row_is_the_decode_and_first_key_row_is_its_value():
+    lens, qlens = [30, 20], [30, 4]
+    q, qb, kc, vc, ks, vs = _rand_case(52, lens, 4, 2, 16)
+    # queries: one row per query token, taken from the decode case's random q
+    rng = np.random.default_rng(3)
+    qrows = rng.integers(0, 0x3F80, size=(sum(qlens), 4, 16)).astype(np.uint16)  # finite bf16 patterns
+    out = oracle.prefill_attention(qrows, kc, vc, lens, qlens, ks, vs, 0.3, 0)
+    dec = oracle.decode_attention(np.stack([qrows[qlens[0] - 1], qrows[-1]]), kc, vc, lens, ks, vs, 0.3, 0)
+    assert np.array_equal(out[qlens[0] - 1], dec[0]) and np.array_equal(out[-1], dec[1])
+    vh = oracle.e4m3_decode(vc) * vs
+    for h in range(4):   # the first token of sequence 0 attends only itself
+        assert np.array_equal(out[0, h], vh[0, h // 2])
