@@ -75,6 +75,8 @@ def load(build_if_missing: bool = False):
     lib.fp8kv_decode_step.argtypes = [P, P, P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
     lib.fp8kv_paged_decode_noalloc.restype = I
     lib.fp8kv_paged_decode_noalloc.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P]
+    lib.fp8kv_paged_prefill.restype = I
+    lib.fp8kv_paged_prefill.argtypes = [P, I64, P, P, I64, P, I, P, P, I, I, I, I, I, I, I, F, F, F, I, P, P, P]
     _lib = lib
     return lib
 
@@ -415,3 +417,37 @@ def fp8kv_decode_step_e5m2(q, k_new, v_new, k_cache, v_cache, block_tables, seq_
     _check("fp8kv_decode_step_e5m2", load().fp8kv_decode_step_e5m2(*_decode_step_args(
         q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale, v_scale, sm_scale,
         window, out, workspace, stream)))
+
+
+def prepare_paged_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_starts, max_q_len, max_seq_len, k_scale,
+                          v_scale, sm_scale, window, out, workspace=None, stream=None):
+    """q, out: bf16 [sum q_len, Hq, D] (the sequences' query rows packed in
+    order); caches uint8 [num_blocks, Hkv, bs, D]; block_tables int32
+    [B, max_blocks]; seq_lens int32 [B]; q_starts int32 [B + 1] (cumulative
+    q_len).  workspace: None, or a decode workspace whose error word then
+    records device-side argument errors."""
+    T, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    B = seq_lens.numel()
+    if d2 != d or tuple(out.shape) != (T, hq, d) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch between q, out and the caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or q_starts.numel() != B + 1:
+        raise ValueError("block_tables must be [B, max_blocks] and q_starts [B + 1]")
+    lib = load()
+    I = ctypes.c_int
+    ws = ctypes.c_void_p(None) if workspace is None else _dev(workspace, torch.uint8, "workspace")
+    args = (_dev(q, torch.bfloat16, "q"), ctypes.c_int64(T), _dev(k_cache, torch.uint8, "k_cache"),
+            _dev(v_cache, torch.uint8, "v_cache"), ctypes.c_int64(nb),
+            _dev(block_tables, torch.int32, "block_tables"), I(block_tables.shape[1]),
+            _dev(seq_lens, torch.int32, "seq_lens"), _dev(q_starts, torch.int32, "q_starts"), I(max_q_len),
+            I(max_seq_len), I(B), I(hq), I(hkv), I(d), I(bs), ctypes.c_float(k_scale), ctypes.c_float(v_scale),
+            ctypes.c_float(sm_scale), I(window), _dev(out, torch.bfloat16, "out"), ws, _stream(stream))
+    return PreparedCall("fp8kv_paged_prefill", lib.fp8kv_paged_prefill, args)
+
+
+def fp8kv_paged_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_starts, max_q_len, max_seq_len, k_scale,
+                        v_scale, sm_scale, window, out, workspace=None, stream=None):
+    """Causal (optionally windowed) attention of each sequence's newest
+    q_len tokens over its fp8 cache; see prepare_paged_prefill for shapes."""
+    prepare_paged_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_starts, max_q_len, max_seq_len, k_scale,
+                          v_scale, sm_scale, window, out, workspace, stream)()

@@ -191,3 +191,18 @@ def small_shape(base: str, batch: int, len_lo: int, len_hi: int, **kw) -> LayerS
     s = CONFIGS[base]
     return dataclasses.replace(s, name=f"{s.name}_small", batch=batch, len_lo=len_lo,
                                len_hi=len_hi, **kw)
+
+
+def prefill_queries(w: Workload, q_lens, seed: int = 0):
+    """Seeded queries for a prefill chunk: sequence b's last q_lens[b] tokens,
+    packed sequence after sequence, bf16 [sum q_lens, Hq, d] ~ N(0, 1), with
+    the int32 [B + 1] cumulative row offsets."""
+    q_lens = torch.as_tensor(q_lens, dtype=torch.int64).reshape(-1)
+    assert q_lens.numel() == w.seq_lens.numel() and bool((q_lens <= w.seq_lens.to(torch.int64)).all())
+    gen = torch.Generator(device="cpu").manual_seed(int(seed) + 7)
+    R = int(q_lens.sum())
+    q = torch.randn((R, w.shape.num_q_heads, w.shape.head_dim), generator=gen,
+                    dtype=torch.float32).to(torch.bfloat16)
+    starts = torch.zeros(q_lens.numel() + 1, dtype=torch.int32)
+    starts[1:] = torch.cumsum(q_lens, 0).to(torch.int32)
+    return q, starts

@@ -322,6 +322,55 @@ fp8kv_status fp8kv_paged_decode_noalloc(const void* q, const uint8_t* k_cache, c
                                         int block_size, float k_scale, float v_scale, float sm_scale,
                                         int window, void* out, void* stream);
 
+/*
+ * Chunked-prefill attention over the paged E4M3 cache [G "Attention backend
+ * interactions" (the prefill pass reads the same fp8 cache as decode);
+ * V "ACCURACY AT LONG CONTEXT" (P.V over the context in FP32)].
+ *
+ * Sequence b holds L = seq_lens[b] tokens in the cache, its n = q_len[b] =
+ * q_starts[b+1] - q_starts[b] newest ones included (append them first with
+ * fp8kv_quant_append).  Query row i < n of the sequence sits at position
+ * p = L - n + i and attends the keys t in [lo(p), p], lo(p) = (window > 0 &&
+ * p + 1 > window) ? p + 1 - window : 0 -- causal, optionally within a
+ * sliding window; row by row this is fp8kv_paged_decode of a sequence of
+ * length p + 1:
+ *     s_t = sm_scale * sum_i q[r][h][i] * decode(k code of t)[i] * k_scale
+ *     out[r][h][:] = sum_t exp(s_t - max s) decode(v code of t) * v_scale
+ *                    / sum_t exp(s_t - max s)
+ * with r = q_starts[b] + i.  Scores, the softmax and P.V accumulate in FP32;
+ * the result is rounded to bf16 (RNE).
+ *
+ *   q              bf16 [num_q_tokens][num_q_heads][head_dim], the query rows of
+ *                  all sequences packed in order, 16-byte aligned
+ *   num_q_tokens   rows of q and out (q_starts[batch])
+ *   k_cache,       uint8 E4M3 caches, layout as fp8kv_paged_decode
+ *   v_cache
+ *   block_tables   int32 [batch][max_blocks_per_seq]; only the pages a query
+ *                  attends are read
+ *   seq_lens       int32 [batch] on the device, 0 <= seq_lens[b] <= max_seq_len
+ *   q_starts       int32 [batch + 1] on the device, non-decreasing, q_starts[0] = 0,
+ *                  q_starts[b+1] - q_starts[b] <= min(seq_lens[b], max_q_len)
+ *   max_q_len      host-side upper bound of the q_len (sizes the grid)
+ *   window         <= 0: causal over the whole prefix; > 0: the last `window` keys
+ *   out            bf16 [num_q_tokens][num_q_heads][head_dim], 16-byte aligned
+ *   workspace      NULL, or a decode workspace (zero-filled, 4-byte aligned):
+ *                  its error word then records, for fp8kv_read_error, an
+ *                  out-of-range block id (block 0 is read instead) or a
+ *                  seq_lens / q_starts entry outside the bounds above (the
+ *                  sequence is clamped, or skipped if its rows would fall
+ *                  outside q / out)
+ * Supported: head_dim in {64, 128, 256}; block_size == 16; g in {1, 2, 4, 8};
+ *            num_blocks * num_kv_heads < 2^31.  batch == 0, max_q_len == 0 or
+ *            num_q_tokens == 0 is a no-op.
+ */
+fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens, const uint8_t* k_cache,
+                                 const uint8_t* v_cache, int64_t num_blocks, const int32_t* block_tables,
+                                 int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* q_starts,
+                                 int max_q_len, int max_seq_len, int batch, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size, float k_scale,
+                                 float v_scale, float sm_scale, int window, void* out, void* workspace,
+                                 void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,176 @@
+"""GPU parity of the chunked prefill over the E4M3 cache: every head layout
+with ragged lengths and chunk sizes (one token, a ragged tail of a tile, whole
+prompts), sliding windows, empty sequences, the full-size 8x20K serving batch
+and the 128K needle with sampled rows, and the device-side argument checks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_kv_cache_fp8kv_gb300 import binding as fk
+from fp8_kv_cache_fp8kv_gb300 import workload
+from tests._tol import BF16_HALF_ULP_REL, assert_attn_close_bf16_floor as assert_attn_close
+from tests.gpu_harness import Paged
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(p: Paged, q, q_starts, window, max_q_len=None, block_tables=None, seq_lens=None, ws=None):
+    w = p.w
+    out = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    qs = q_starts.cuda()
+    mq = int((q_starts[1:] - q_starts[:-1]).max()) if max_q_len is None else max_q_len
+    fk.fp8kv_paged_prefill(q.cuda(), p.k_cache, p.v_cache,
+                           p.block_tables if block_tables is None else block_tables,
+                           p.seq_lens if seq_lens is None else seq_lens, qs, mq, w.max_seq_len,
+                           w.k_scale, w.v_scale, w.sm_scale, window, out, ws)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy()
+
+
+def _oracle(p: Paged, q, q_lens, window):
+    kc, vc = p.gathered_codes()
+    w = p.w
+    return oracle.prefill_attention(workload.bf16_bits(q), kc, vc, w.seq_lens.numpy(), np.asarray(q_lens),
+                                    w.k_scale, w.v_scale, w.sm_scale, window, nthreads=oracle.max_threads())
+
+
+LAYOUTS = ["llama31_8b_b8_20k", "gptoss20b_b8_16k", "gemma4e2b_b16_8k32k", "llama33_70b_needle_128k"]
+
+
+@pytest.mark.parametrize("base", LAYOUTS)
+@pytest.mark.parametrize("window", [0, 40])
+def test_prefill_small_every_layout(base, window):
+    lens = [1, 17, 300, 95, 0, 64, 129]
+    q_lens = [1, 17, 37, 95, 0, 1, 64]          # whole prompts, one token, ragged tails of a tile
+    shape = workload.small_shape(base, len(lens), 1, 1, needle_margin=None)
+    w = workload.make_workload(shape, seed=3, lens=lens)
+    p = Paged(w, seed=3)
+    p.append_all()
+    q, qs = workload.prefill_queries(w, q_lens, seed=3)
+    got = _run(p, q, qs, window)
+    ref = _oracle(p, q, q_lens, window)
+    assert_attn_close(got, ref, f"{base} window={window}")
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_prefill_seeds_and_windows(seed):
+    shape = workload.small_shape("llama31_8b_b8_20k", 3, 200, 700)
+    w = workload.make_workload(shape, seed=seed)
+    p = Paged(w, seed=seed)
+    p.append_all()
+    L = w.seq_lens.tolist()
+    q_lens = [L[0], min(L[1], 130), 33]
+    q, qs = workload.prefill_queries(w, q_lens, seed=seed)
+    for window in (0, 16, 128, 5000):
+        got = _run(p, q, qs, window)
+        ref = _oracle(p, q, q_lens, window)
+        assert_attn_close(got, ref, f"seed={seed} window={window}")
+
+
+def test_prefill_window_one_is_value_of_own_token():
+    """window = 1: each row attends only its own key, so the output is that
+    token's decoded V times v_scale; the only error left is the rounding of
+    that value to bf16 (at most 2^-8 of it, plus the fp32 product's 2^-24)."""
+    shape = workload.small_shape("gptoss20b_b8_16k", 2, 50, 90)
+    w = workload.make_workload(shape, seed=4)
+    p = Paged(w, seed=4)
+    p.append_all()
+    q_lens = [20, 33]
+    q, qs = workload.prefill_queries(w, q_lens, seed=4)
+    got = _run(p, q, qs, 1).astype(np.float64)
+    ref = _oracle(p, q, q_lens, 1)
+    assert np.all(np.abs(got - ref) <= BF16_HALF_ULP_REL * (1 + 2.0 ** -16) * np.abs(ref))
+
+
+def test_prefill_max_q_len_larger_than_needed_and_zero_chunks():
+    """A grid sized for a longer chunk than any sequence has, and sequences
+    with no new tokens between others, leave no row unwritten and write no
+    row twice."""
+    lens = [40, 0, 33, 16]
+    q_lens = [40, 0, 0, 16]
+    shape = workload.small_shape("llama31_8b_b8_20k", len(lens), 1, 1)
+    w = workload.make_workload(shape, seed=6, lens=lens)
+    p = Paged(w, seed=6)
+    p.append_all()
+    q, qs = workload.prefill_queries(w, q_lens, seed=6)
+    got = _run(p, q, qs, 0, max_q_len=40)
+    ref = _oracle(p, q, q_lens, 0)
+    assert np.all(np.isfinite(got))
+    assert_attn_close(got, ref, "zero chunks")
+
+
+def _sampled_rows(p: Paged, q, q_lens, rows, window):
+    """Oracle rows one by one: row i of sequence b is the decode attention of
+    the sequence cut at position p + 1."""
+    w = p.w
+    kc, vc = p.gathered_codes()
+    starts = w.seq_starts.numpy()
+    L = w.seq_lens.numpy()
+    qs = np.concatenate([[0], np.cumsum(q_lens)])
+    out = []
+    for b, i in rows:
+        pos = int(L[b] - q_lens[b] + i)
+        s0 = int(starts[b])
+        r = oracle.prefill_attention(workload.bf16_bits(q[qs[b] + i:qs[b] + i + 1]), kc[s0:s0 + pos + 1],
+                                     vc[s0:s0 + pos + 1], [pos + 1], [1], w.k_scale, w.v_scale, w.sm_scale,
+                                     window, nthreads=oracle.max_threads())
+        out.append(r[0])
+    return np.stack(out)
+
+
+def test_prefill_full_size_serving_batch_sampled():
+    """8 sequences of ~20K tokens, the last 512 of each a prefill chunk."""
+    w = workload.make_workload("llama31_8b_b8_20k", seed=0)
+    p = Paged(w, seed=0)
+    p.append_all()
+    q_lens = [512] * 8
+    q, qs = workload.prefill_queries(w, q_lens, seed=0)
+    got = _run(p, q, qs, 0)
+    rng = np.random.default_rng(0)
+    rows = [(b, int(i)) for b in range(8) for i in [0, 511, *rng.integers(0, 512, 3)]]
+    ref = _sampled_rows(p, q, q_lens, rows, 0)
+    sel = np.stack([got[qs[b] + i] for b, i in rows])
+    assert_attn_close(sel, ref, "8x20K chunk 512")
+
+
+def test_prefill_needle_128k_sampled():
+    """The 131,072-token needle layout with a 256-token chunk at the end; the
+    chunk's last row carries the query the needle key was planted for, so
+    that row must retrieve the needle from among 128K keys."""
+    w = workload.make_workload("llama33_70b_needle_128k", seed=0)
+    p = Paged(w, seed=0)
+    p.append_all()
+    q_lens = [256]
+    q, qs = workload.prefill_queries(w, q_lens, seed=0)
+    q[255] = w.q[0]
+    got = _run(p, q, qs, 0)
+    rows = [(0, 0), (0, 97), (0, 255)]
+    ref = _sampled_rows(p, q, q_lens, rows, 0)
+    sel = np.stack([got[i] for _, i in rows])
+    assert_attn_close(sel, ref, "128K chunk 256")
+
+
+def test_prefill_reports_bad_block_id_and_lengths():
+    """Device-side checks: a block id outside the cache reads block 0 and is
+    reported; a chunk longer than its sequence is clamped and reported."""
+    shape = workload.small_shape("llama31_8b_b8_20k", 2, 60, 60)
+    w = workload.make_workload(shape, seed=8)
+    p = Paged(w, seed=8)
+    p.append_all()
+    q_lens = [20, 20]
+    q, qs = workload.prefill_queries(w, q_lens, seed=8)
+    ws = fk.alloc_workspace(2, 32, 8, 128, 64)
+    bt = p.block_tables.clone()
+    bt[1, 0] = p.num_blocks + 5
+    got = _run(p, q, qs, 0, block_tables=bt, ws=ws)
+    assert fk.fp8kv_read_error(ws) == 1
+    ref = _oracle(p, q, q_lens, 0)
+    assert_attn_close(got[:20], ref[:20], "sequence with valid pages")
+    assert np.all(np.isfinite(got))
+    short = p.seq_lens.clone()
+    short[0] = 10                                  # 20 query rows but only 10 tokens
+    _run(p, q, qs, 0, seq_lens=short, ws=ws)
+    assert fk.fp8kv_read_error(ws) == 1
+    _run(p, q, qs, 0, ws=ws)
+    assert fk.fp8kv_read_error(ws) == 0
