@@ -62,6 +62,9 @@ def parse_args(argv=None):
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--sweep", action="store_true",
                    help="instead of the step: decode time against context length, fp8 cache and bf16 cache")
+    p.add_argument("--prefill", type=str, default=None, metavar="CHUNKS",
+                   help="instead of the step: chunked prefill over the fp8 cache of --config, the last CHUNK "
+                        "tokens of every sequence as queries, for each comma-separated CHUNK")
     a = p.parse_args(argv)
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -115,6 +118,23 @@ def measured_peaks():
     except (OSError, ValueError):
         pass
     return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
+
+
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def measured_tensor_peak():
+    """Dense bf16 tensor TFLOP/s as a burst (the f16 MMA has the same nominal rate)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("bf16_tflops", "bf16_TFLOPs", "bf16"):
+            if key in d:
+                return float(d[key]), "measured (MEASURED_PEAKS.json)"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_BF16_TFLOPS, "fallback (no MEASURED_PEAKS.json)"
 
 
 class ClockSampler:
@@ -640,6 +660,75 @@ def run_sweep(args, rank, ws):
             "breakeven_context_tokens": breakeven, "n_gpus": ws}
 
 
+# ---------------------------------------------------------------- chunked prefill
+
+def run_prefill(args, rank, ws):
+    """fp8kv_paged_prefill on the workload's sequences with the last CHUNK
+    tokens of each as the query chunk (causal over the whole cached prefix,
+    the workload's window).  Algorithmic work: 4 * head_dim flops per (query
+    row, query head, attended key) -- the score and the P.V products -- and
+    the distinct cache pages the chunk attends plus q and out in bytes."""
+    from fp8_kv_cache_fp8kv_gb300 import binding as fk
+    fk.load(build_if_missing=True)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    window = workload.CONFIGS[args.config].windows[0] if args.window is None else args.window
+    w = workload.make_workload(args.config, seed=args.seed)
+    s = w.shape
+    cshape = (w.num_blocks, s.num_kv_heads, workload.BLOCK_SIZE, s.head_dim)
+    k8 = torch.zeros(cshape, dtype=torch.uint8, device=dev)
+    v8 = torch.zeros_like(k8)
+    fk.fp8kv_quant_append(w.k.to(dev), w.v.to(dev), w.slot_mapping.to(dev), k8, v8, w.k_scale, w.v_scale)
+    bt = w.block_tables.to(dev)
+    lens = w.seq_lens.to(dev)
+    L = w.seq_lens.to(torch.int64).numpy()
+    tflops_peak, peak_src = measured_tensor_peak()
+    points = []
+    for chunk in [int(c) for c in args.prefill.split(",")]:
+        q_lens = np.minimum(L, chunk)
+        q, qs = workload.prefill_queries(w, q_lens, seed=args.seed)
+        q = q.to(dev)
+        qs_d = qs.to(dev)
+        out = torch.empty_like(q)
+        wsp = fk.alloc_prefill_workspace(int(L.size), int(q_lens.max()), w.max_seq_len, s.num_q_heads,
+                                         s.num_kv_heads, s.head_dim, 16, window, device=dev)
+        call = fk.prepare_paged_prefill(q, k8, v8, bt, lens, qs_d, int(q_lens.max()), w.max_seq_len, w.k_scale,
+                                        w.v_scale, w.sm_scale, window, out, wsp)
+        pairs = 0
+        pages = 0
+        for Lb, n in zip(L.tolist(), q_lens.tolist()):
+            pos = np.arange(Lb - n, Lb, dtype=np.int64)
+            lo = np.maximum(0, pos + 1 - window) if window > 0 else np.zeros_like(pos)
+            pairs += int((pos + 1 - lo).sum())
+            if n:
+                pages += int(pos[-1] // 16 - lo[0] // 16 + 1)
+        flops = 4.0 * s.head_dim * s.num_q_heads * pairs
+        nbytes = 2 * pages * s.num_kv_heads * 16 * s.head_dim + 2 * 2 * q.numel()
+        flush = L2Policy(nbytes, dev)
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(args.steps):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        assert fk.fp8kv_read_error(wsp) == 0
+        us = reduce_max(statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3, ws)
+        points.append({"chunk": chunk, "workspace_bytes": int(wsp.numel()), "query_rows": int(q_lens.sum()), "us": round(us, 2),
+                       "tflops": round(flops / us / 1e6, 2), "frac_of_tensor_peak": round(flops / us / 1e6 / tflops_peak, 4),
+                       "gbs": round(nbytes / us / 1e3, 1), "flops": flops, "bytes": nbytes, "l2": flush.describe()})
+        del q, out, wsp
+    return {"prefill": "fp8kv_paged_prefill: chunked prefill over the E4M3 cache",
+            "config": {"workload": args.config, "window": window, "batch": int(L.size),
+                       "timer": "CUDA events per call, median of %d" % args.steps},
+            "tensor_peak_tflops": tflops_peak, "tensor_peak_source": peak_src, "points": points, "n_gpus": ws}
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -653,8 +742,8 @@ def main(argv=None):
     rank, ws = dist_setup(args)
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU for --impl fp8kv")
-    if args.sweep:
-        line = run_sweep(args, rank, ws)
+    if args.sweep or args.prefill:
+        line = run_sweep(args, rank, ws) if args.sweep else run_prefill(args, rank, ws)
         if rank == 0:
             print(json.dumps(line), flush=True)
         return 0

@@ -75,8 +75,10 @@ def load(build_if_missing: bool = False):
     lib.fp8kv_decode_step.argtypes = [P, P, P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
     lib.fp8kv_paged_decode_noalloc.restype = I
     lib.fp8kv_paged_decode_noalloc.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P]
+    lib.fp8kv_paged_prefill_workspace_size.restype = SZ
+    lib.fp8kv_paged_prefill_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
     lib.fp8kv_paged_prefill.restype = I
-    lib.fp8kv_paged_prefill.argtypes = [P, I64, P, P, I64, P, I, P, P, I, I, I, I, I, I, I, F, F, F, I, P, P, P]
+    lib.fp8kv_paged_prefill.argtypes = [P, I64, P, P, I64, P, I, P, P, I, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
     _lib = lib
     return lib
 
@@ -419,13 +421,31 @@ def fp8kv_decode_step_e5m2(q, k_new, v_new, k_cache, v_cache, block_tables, seq_
         window, out, workspace, stream)))
 
 
+def fp8kv_paged_prefill_workspace_size(batch, max_q_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,
+                                       block_size=16, window=0) -> int:
+    n = load().fp8kv_paged_prefill_workspace_size(int(batch), int(max_q_len), int(max_seq_len), int(num_q_heads),
+                                                  int(num_kv_heads), int(head_dim), int(block_size), int(window))
+    if n == 0:
+        raise Fp8kvError("fp8kv_paged_prefill_workspace_size", 1)
+    return int(n)
+
+
+def alloc_prefill_workspace(batch, max_q_len, max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size=16,
+                            window=0, device=None, stream=None):
+    """Allocates (through torch) and zero-fills a prefill workspace for these sizes."""
+    n = fp8kv_paged_prefill_workspace_size(batch, max_q_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,
+                                           block_size, window)
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    fp8kv_workspace_init(ws, stream)
+    return ws
+
+
 def prepare_paged_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_starts, max_q_len, max_seq_len, k_scale,
-                          v_scale, sm_scale, window, out, workspace=None, stream=None):
+                          v_scale, sm_scale, window, out, workspace, stream=None):
     """q, out: bf16 [sum q_len, Hq, D] (the sequences' query rows packed in
     order); caches uint8 [num_blocks, Hkv, bs, D]; block_tables int32
     [B, max_blocks]; seq_lens int32 [B]; q_starts int32 [B + 1] (cumulative
-    q_len).  workspace: None, or a decode workspace whose error word then
-    records device-side argument errors."""
+    q_len); workspace: uint8, fp8kv_paged_prefill_workspace_size bytes."""
     T, hq, d = q.shape
     nb, hkv, bs, d2 = k_cache.shape
     B = seq_lens.numel()
@@ -435,18 +455,18 @@ def prepare_paged_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_starts,
         raise ValueError("block_tables must be [B, max_blocks] and q_starts [B + 1]")
     lib = load()
     I = ctypes.c_int
-    ws = ctypes.c_void_p(None) if workspace is None else _dev(workspace, torch.uint8, "workspace")
     args = (_dev(q, torch.bfloat16, "q"), ctypes.c_int64(T), _dev(k_cache, torch.uint8, "k_cache"),
             _dev(v_cache, torch.uint8, "v_cache"), ctypes.c_int64(nb),
             _dev(block_tables, torch.int32, "block_tables"), I(block_tables.shape[1]),
             _dev(seq_lens, torch.int32, "seq_lens"), _dev(q_starts, torch.int32, "q_starts"), I(max_q_len),
             I(max_seq_len), I(B), I(hq), I(hkv), I(d), I(bs), ctypes.c_float(k_scale), ctypes.c_float(v_scale),
-            ctypes.c_float(sm_scale), I(window), _dev(out, torch.bfloat16, "out"), ws, _stream(stream))
+            ctypes.c_float(sm_scale), I(window), _dev(out, torch.bfloat16, "out"),
+            _dev(workspace, torch.uint8, "workspace"), ctypes.c_size_t(workspace.numel()), _stream(stream))
     return PreparedCall("fp8kv_paged_prefill", lib.fp8kv_paged_prefill, args)
 
 
 def fp8kv_paged_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_starts, max_q_len, max_seq_len, k_scale,
-                        v_scale, sm_scale, window, out, workspace=None, stream=None):
+                        v_scale, sm_scale, window, out, workspace, stream=None):
     """Causal (optionally windowed) attention of each sequence's newest
     q_len tokens over its fp8 cache; see prepare_paged_prefill for shapes."""
     prepare_paged_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_starts, max_q_len, max_seq_len, k_scale,

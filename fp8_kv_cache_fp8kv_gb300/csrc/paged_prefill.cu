@@ -10,19 +10,27 @@
 // the P.V contraction runs over the context, so partial sums live in real
 // FP32 registers).
 //
-// How: one CTA per (tile of 32 query rows, kv head, sequence).  A query row is
-// a (token, query head) pair of the kv head's group; each of the 4 warps owns
-// 8 rows, the n side of the m16n8k16 MMA, exactly as the decode kernel uses
-// its g heads.  The tile's key pages (from the first row's window start to
-// the last row's position) stream through a double-buffered shared-memory
-// page (cp.async, the 128-byte swizzle of a TMA box, so fragment loads are
-// conflict-free).  Per page and warp: S^T = K Q^T (keys on the m side), the
-// causal/window mask, an online softmax per row in log2 units, P rounded to
-// f16, the page's O^T = V^T P^T tile in fresh accumulators, then folded into
-// FP32 registers (O = O * alpha + tile).
-#include <cuda_bf16.h>
+// How: a unit is (tile of 64 query rows, kv head, sequence); a query row is a
+// (token, query head) pair of the kv head's group.  Each of the 4 warps owns
+// 16 rows, the M side of the m16n8k16 MMA:
+//   S  = Q K^T   A = Q (f16, pre-scaled per row by a power of two, staged in
+//                shared memory in fragment order), B = K (E4M3 -> f16 in
+//                registers; each thread reads contiguous key bytes and the
+//                Q fragments use the same permutation of the head dimension)
+//   O += P V     A = P straight from the score accumulators (rounded to f16),
+//                B = V (byte-permuted E4M3 -> f16; the output dimensions are
+//                permuted to match and put back at the store)
+// Keys stream through a 3-stage shared-memory ring of 2 pages (32 keys) per
+// stage (cp.async, the 128-byte swizzle of a TMA box, conflict-free fragment
+// loads).  Each stage's P.V tile is computed in fresh FP32 accumulators and
+// folded into the FP32 output registers (O = O * alpha + tile): the
+// two-level accumulation.  When the units are too few to fill the GPU, each
+// unit's key range is split over several CTAs whose FP32 partials (row
+// maximum, row sum, unnormalised output) a second kernel merges.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -30,31 +38,41 @@
 #include "ptx.cuh"
 
 namespace fp8kv {
+
+int device_sms(int* sms);  // SM count of the current device (paged_decode.cu)
+
 namespace prefill {
 
 constexpr int kBS = 16;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kRowsPerWarp = 8;
-constexpr int kRows = kWarps * kRowsPerWarp;  // query rows per CTA
+constexpr int kRows = kWarps * 16;      // query rows per unit
+constexpr int kStages = 3;              // ring depth
+constexpr int kMaxSplits = 64;
+constexpr int kMinSplitPages = 8;       // a split covers at least 128 keys
+constexpr size_t kHeader = 256;         // error word, then the partials
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Args {
-    const uint16_t* q;           // bf16 [sum q_len, Hq, D], packed by sequence
+    const uint16_t* q;           // bf16 [num_q_tokens, Hq, D], packed by sequence
     const uint8_t* k_cache;      // E4M3 [num_blocks, Hkv, 16, D]
     const uint8_t* v_cache;
     const int32_t* block_tables; // [B, max_blocks_per_seq]
     const int32_t* seq_lens;     // [B]
     const int32_t* q_starts;     // [B + 1] cumulative query-row offsets
-    uint16_t* out;               // bf16 [sum q_len, Hq, D]
-    uint32_t* err;               // error word (first word of a decode workspace), or null
+    uint16_t* out;               // bf16 [num_q_tokens, Hq, D]
+    uint32_t* err;               // error word
+    float* part_o;               // [units][splits][kRows][D] unnormalised FP32 outputs
+    float2* part_ml;             // [units][splits][kRows] (row maximum in log2 units, row sum)
     int64_t num_blocks;
-    int64_t num_q_tokens;        // rows of q and out
+    int64_t num_q_tokens;
     int max_blocks_per_seq;
     int max_seq_len;
     int max_q_len;
     int num_q_heads;
     int num_kv_heads;
+    int tiles;                   // query tiles per (sequence, kv head)
+    int splits;                  // CTAs per unit
     int window;
     float score_scale;           // sm_scale * k_scale * log2(e)
     float v_scale;
@@ -76,90 +94,121 @@ struct Geo {
     static constexpr int HALVES = D >= 128 ? D / 128 : 1;
     static constexpr int BOX = kBS * ROWB;
     static constexpr int PAGE = kBS * D;
+    static constexpr int PPS = D > 128 ? 1 : 2;      // pages per stage (register budget at D = 256)
+    static constexpr int STAGE = 2 * PPS * PAGE;     // K pages then V pages
     static constexpr int KS = D / 16;                // k-steps of the score MMA
-    static constexpr int MT = D / 16;                // m-tiles of the value MMA
     static constexpr int KW = ROWB / 4;              // K bytes a thread reads per row per box
     static constexpr int KSH = KW / 4;               // k-steps per box
     static constexpr int VW = ROWB / 8;              // V bytes a thread reads per key per box
-    static constexpr int MTH = VW / 2;               // m-tiles per box
+    static constexpr int NT = D / 8;                 // n-tiles of the value MMA (one per V byte column)
+    static constexpr size_t QSM = static_cast<size_t>(kWarps) * KS * 32 * 16;  // Q fragments
+    static constexpr size_t SMEM = static_cast<size_t>(kStages) * STAGE + QSM;
+    static_assert(KSH * HALVES == KS && VW * HALVES == NT, "boxes cover the head dimension");
 };
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
 
-__device__ __forceinline__ uint16_t f32_to_bf16(float x) {
-    __nv_bfloat16 h = __float2bfloat16_rn(x);
-    return *reinterpret_cast<uint16_t*>(&h);
-}
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-__device__ __forceinline__ void report(uint32_t* err, uint32_t code) {
-    if (err) atomicCAS(err, 0u, code);
+__device__ __forceinline__ void report(uint32_t* err, uint32_t code) { atomicCAS(err, 0u, code); }
+
+// Pages [pg, pg + np) of (block-table row bt, kv head hk) into one ring
+// stage: K page i at i * PAGE, V page i at (PPS + i) * PAGE.  A block id
+// outside [0, num_blocks) reads block 0 and is reported.
+template <int D>
+__device__ __forceinline__ void load_stage(const Args& a, const int32_t* bt, int hk, int pg, int np, uint32_t dst) {
+    using Gm = Geo<D>;
+    constexpr int kChunks = Gm::PAGE / 16;
+    for (int i = threadIdx.x; i < np * kChunks; i += kThreads) {
+        const int p = i / kChunks, ci = i % kChunks;
+        int id = __ldg(bt + pg + p);
+        if (id < 0 || id >= a.num_blocks) {
+            if (ci == 0) report(a.err, FP8KV_ERR_INVALID_ARG);
+            id = 0;
+        }
+        const int64_t base = (static_cast<int64_t>(id) * a.num_kv_heads + hk) * Gm::PAGE;
+        const int r = ci / (D / 16), c = ci % (D / 16);
+        const int h = (c * 16) / Gm::ROWB, o = (c * 16) % Gm::ROWB;
+        const uint32_t off = p * Gm::PAGE + h * Gm::BOX + swz<Gm::ROWB>(r, o);
+        cp_async16(dst + off, a.k_cache + base + r * D + c * 16);
+        cp_async16(dst + Gm::PPS * Gm::PAGE + off, a.v_cache + base + r * D + c * 16);
+    }
 }
 
-// Page `pg` of (sequence row `bt`, kv head hk) into the smem page (K and V).
-// A block id outside [0, num_blocks) reads block 0 and is reported.
-template <int D>
-__device__ __forceinline__ void load_page(const Args& a, const int32_t* bt, int hk, int pg, uint8_t* ks, uint8_t* vs) {
-    using Gm = Geo<D>;
-    int id = __ldg(bt + pg);
-    if (id < 0 || id >= a.num_blocks) {
-        if (threadIdx.x == 0) report(a.err, FP8KV_ERR_INVALID_ARG);
-        id = 0;
-    }
-    const int64_t base = (static_cast<int64_t>(id) * a.num_kv_heads + hk) * Gm::PAGE;
-    constexpr int kChunks = Gm::PAGE / 16;
-    for (int i = threadIdx.x; i < kChunks; i += kThreads) {
-        const int r = i / (D / 16), c = i % (D / 16);
-        const int h = (c * 16) / Gm::ROWB, o = (c * 16) % Gm::ROWB;
-        const uint32_t dst = h * Gm::BOX + swz<Gm::ROWB>(r, o);
-        cp_async16(ks + dst, a.k_cache + base + r * D + c * 16);
-        cp_async16(vs + dst, a.v_cache + base + r * D + c * 16);
-    }
+// What one (tile, kv head, sequence) covers: its query rows and the key
+// range the rows attend, from the device-side lengths (clamped; an entry
+// outside the documented bounds is reported when `report_errors`).
+struct Unit {
+    int q0;          // first packed query row of the sequence
+    int L;           // keys in the cache
+    int n;           // query tokens of the sequence
+    int rows;        // n * G
+    int R0;          // first row of the tile
+    int kmin, kmax;  // keys the tile attends (inclusive)
+};
+
+template <int G>
+__device__ __forceinline__ bool make_unit(const Args& a, int b, int tile, bool report_errors, Unit& u) {
+    u.q0 = __ldg(a.q_starts + b);
+    const int L_in = __ldg(a.seq_lens + b);
+    u.L = L_in < 0 ? 0 : min(L_in, a.max_seq_len);
+    const int n_in = __ldg(a.q_starts + b + 1) - u.q0;
+    int n = n_in < 0 ? 0 : min(n_in, min(u.L, a.max_q_len));
+    if (u.q0 < 0 || u.q0 + static_cast<int64_t>(n) > a.num_q_tokens) n = 0;  // never touch rows outside q / out
+    if (report_errors && (u.L != L_in || n != n_in)) report(a.err, FP8KV_ERR_INVALID_ARG);
+    u.n = n;
+    u.rows = n * G;
+    u.R0 = tile * kRows;
+    if (u.R0 >= u.rows) return false;
+    const int p_first = u.L - n + u.R0 / G;
+    u.kmax = u.L - n + (min(u.R0 + kRows, u.rows) - 1) / G;
+    u.kmin = (a.window > 0 && p_first + 1 > a.window) ? p_first + 1 - a.window : 0;
+    return true;
 }
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads) paged_prefill_kernel(const Args a) {
     using Gm = Geo<D>;
-    __shared__ __align__(1024) uint8_t sk[2][Gm::PAGE];
-    __shared__ __align__(1024) uint8_t sv[2][Gm::PAGE];
+    extern __shared__ __align__(1024) uint8_t smem[];
     griddep_wait();                // inputs may come from the previous grid on the stream
     griddep_launch_dependents();
     const int b = blockIdx.z, hk = blockIdx.y;
+    const int tile = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-    const int q0 = __ldg(a.q_starts + b);
-    const int L_in = __ldg(a.seq_lens + b);
-    const int L = L_in < 0 ? 0 : (L_in > a.max_seq_len ? a.max_seq_len : L_in);
-    const int n_in = __ldg(a.q_starts + b + 1) - q0;   // query tokens of this sequence
-    int n = n_in < 0 ? 0 : min(n_in, min(L, a.max_q_len));
-    if (q0 < 0 || q0 + static_cast<int64_t>(n) > a.num_q_tokens) n = 0;   // never touch rows outside q / out
-    if (L != L_in || n != n_in) {
-        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) report(a.err, FP8KV_ERR_INVALID_ARG);
-    }
-    const int rows = n * G;
-    const int R0 = blockIdx.x * kRows;
-    if (R0 >= rows) return;
-    const int p_first = L - n + R0 / G;                                  // position of the tile's first token
-    const int p_last = L - n + (min(R0 + kRows, rows) - 1) / G;
-    const int lo_first = (a.window > 0 && p_first + 1 > a.window) ? p_first + 1 - a.window : 0;
-    const int pg0 = lo_first / kBS, pg1 = p_last / kBS;
-    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
+    Unit u;
+    if (!make_unit<G>(a, b, tile, blockIdx.x == 0 && hk == 0 && threadIdx.x == 0, u)) return;
 
-    // ---- this warp's 8 query rows as f16 B fragments (power-of-two pre-scale
-    // per row so the f16 copy of the bf16 value is exact), as in decode
-    const int rw = R0 + warp * kRowsPerWarp;   // first row of the warp
-    uint32_t qf[Gm::KS][2];
+    // ---- this split's key pages
+    const int pg0 = u.kmin / kBS, np_all = u.kmax / kBS - pg0 + 1;
+    const int sp0 = pg0 + static_cast<int>(static_cast<int64_t>(split) * np_all / a.splits);
+    const int sp1 = pg0 + static_cast<int>(static_cast<int64_t>(split + 1) * np_all / a.splits);
+    const int nst = (sp1 - sp0 + Gm::PPS - 1) / Gm::PPS;
+    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
+    const uint32_t ring = smem_u32(smem);
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+        if (s < nst) load_stage<D>(a, bt, hk, sp0 + s * Gm::PPS, min(Gm::PPS, sp1 - sp0 - s * Gm::PPS), ring + s * Gm::STAGE);
+        cp_async_commit();
+    }
+
+    // ---- this warp's 16 query rows as f16 A fragments, each row pre-scaled by
+    // a power of two so the f16 copy of its bf16 values is exact; stored in
+    // shared memory in fragment order (each thread reads back only its own)
+    uint4* qsm = reinterpret_cast<uint4*>(smem + kStages * Gm::STAGE) + warp * Gm::KS * 32;
     float cs[2];
-    {
-        const int myrow = rw + gid;            // the row whose q this lane's B fragment column holds
-        const bool ok = myrow < rows;
-        const int tok = ok ? myrow / G : 0, hq = hk * G + (ok ? myrow % G : 0);
-        const uint16_t* qrow = a.q + (static_cast<int64_t>(q0 + tok) * a.num_q_heads + hq) * D;
+    int pq[2], lq[2];
+    bool rv[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {   // row gid + 8j: words 2e + j of each fragment
+        const int r = u.R0 + warp * 16 + gid + 8 * j;
+        rv[j] = r < u.rows;
+        const int tok = rv[j] ? r / G : 0, hq = hk * G + (rv[j] ? r % G : 0);
+        const uint16_t* qrow = a.q + (static_cast<int64_t>(u.q0 + tok) * a.num_q_heads + hq) * D;
         uint32_t qw[Gm::HALVES][Gm::KSH][2];
         float qmax = 0.f;
 #pragma unroll
@@ -167,7 +216,7 @@ __global__ void __launch_bounds__(kThreads) paged_prefill_kernel(const Args a) {
 #pragma unroll
             for (int c = 0; c < Gm::KW / 8; ++c) {
                 uint4 v = make_uint4(0, 0, 0, 0);
-                if (ok) v = __ldg(reinterpret_cast<const uint4*>(qrow + hh * 128 + tig * Gm::KW) + c);
+                if (rv[j]) v = __ldg(reinterpret_cast<const uint4*>(qrow + hh * 128 + tig * Gm::KW) + c);
                 const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -183,6 +232,7 @@ __global__ void __launch_bounds__(kThreads) paged_prefill_kernel(const Args a) {
             shift = max(-100, min(100, 14 - e));
         }
         const float up = __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
+        uint32_t* q32 = reinterpret_cast<uint32_t*>(qsm);
 #pragma unroll
         for (int hh = 0; hh < Gm::HALVES; ++hh)
 #pragma unroll
@@ -190,209 +240,424 @@ __global__ void __launch_bounds__(kThreads) paged_prefill_kernel(const Args a) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const uint32_t w = qw[hh][kk][e];
-                    qf[hh * Gm::KSH + kk][e] = pack_f16x2(bf16_to_f32(w & 0xFFFF) * up, bf16_to_f32(w >> 16) * up);
+                    q32[((hh * Gm::KSH + kk) * 32 + lane) * 4 + 2 * e + j] =
+                        pack_f16x2(bf16_to_f32(w & 0xFFFF) * up, bf16_to_f32(w >> 16) * up);
                 }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int sh = __shfl_sync(0xffffffffu, shift, (2 * tig + j) * 4);
-            cs[j] = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
-        }
-    }
-    // positions and window starts of this lane's two accumulator rows (2*tig, 2*tig+1)
-    int pq[2], lq[2];
-    bool rv[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int r = rw + 2 * tig + j;
-        rv[j] = r < rows;
-        pq[j] = L - n + (rv[j] ? r / G : 0);
+        cs[j] = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
+        pq[j] = u.L - u.n + (rv[j] ? r / G : 0);
         lq[j] = (a.window > 0 && pq[j] + 1 > a.window) ? pq[j] + 1 - a.window : 0;
     }
 
+    // the warp's first position and its last row's window start: a stage of
+    // keys in [wlo1, wpos0] is attended in full by every row of the warp
+    const int wr0 = u.R0 + warp * 16;
+    const bool warp_active = wr0 < u.rows;
+    const int wpos0 = u.L - u.n + wr0 / G;
+    const int wpos1 = u.L - u.n + (min(wr0 + 15, u.rows - 1)) / G;
+    const int wlo1 = (a.window > 0 && wpos1 + 1 > a.window) ? wpos1 + 1 - a.window : 0;
+
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-    float o[Gm::MT][4];
+    float o[Gm::NT][4];
 #pragma unroll
-    for (int mt = 0; mt < Gm::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    for (int nt = 0; nt < Gm::NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
-    load_page<D>(a, bt, hk, pg0, sk[0], sv[0]);
-    cp_async_commit();
-    for (int pg = pg0; pg <= pg1; ++pg) {
-        const int buf = (pg - pg0) & 1;
-        if (pg < pg1) load_page<D>(a, bt, hk, pg + 1, sk[buf ^ 1], sv[buf ^ 1]);
-        cp_async_commit();
-        cp_async_wait_1();             // this page has landed (the next may still be in flight)
-        __syncthreads();
-        const uint8_t* kst = sk[buf];
-        const uint8_t* vst = sv[buf];
-        const int t0 = pg * kBS;
+    for (int st = 0; st < nst; ++st) {
+        cp_async_wait<kStages - 2>();  // stage st has landed (later ones may be in flight)
+        __syncthreads();               // ... for every thread; and every warp is done with stage st - 1
+        {
+            const int s2 = st + kStages - 1;   // refill the slot stage st - 1 used
+            if (s2 < nst)
+                load_stage<D>(a, bt, hk, sp0 + s2 * Gm::PPS, min(Gm::PPS, sp1 - sp0 - s2 * Gm::PPS),
+                              ring + (s2 % kStages) * Gm::STAGE);
+            cp_async_commit();
+        }
+        if (!warp_active) continue;    // this warp's rows are past the chunk's end
+        const int pgs = sp0 + st * Gm::PPS;
+        const int np = min(Gm::PPS, sp1 - pgs);
+        const int t0 = pgs * kBS;
+        const uint8_t* kst = smem + (st % kStages) * Gm::STAGE;
+        const uint8_t* vst = kst + Gm::PPS * Gm::PAGE;
 
-        // ---- scores S^T[key][row] = K Q^T
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        // ---- scores S[row][key] = Q K^T; n-tile nt of page p holds keys p*16 + nt*8 + [0, 8)
+        float sc[Gm::PPS][2][4];
+#pragma unroll
+        for (int p = 0; p < Gm::PPS; ++p)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) sc[p][nt][0] = sc[p][nt][1] = sc[p][nt][2] = sc[p][nt][3] = 0.f;
 #pragma unroll
         for (int hh = 0; hh < Gm::HALVES; ++hh) {
-            const uint8_t* box = kst + hh * Gm::BOX;
-            uint32_t w0[Gm::KW / 4], w1[Gm::KW / 4];
+                uint32_t kw[Gm::PPS][2][Gm::KW / 4];
 #pragma unroll
-            for (int cc = 0; cc < Gm::KW / 16; ++cc) {
-                const uint4 x = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(gid, tig * Gm::KW + 16 * cc));
-                const uint4 y = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(gid + 8, tig * Gm::KW + 16 * cc));
-                w0[4 * cc + 0] = x.x; w0[4 * cc + 1] = x.y; w0[4 * cc + 2] = x.z; w0[4 * cc + 3] = x.w;
-                w1[4 * cc + 0] = y.x; w1[4 * cc + 1] = y.y; w1[4 * cc + 2] = y.z; w1[4 * cc + 3] = y.w;
-            }
+                for (int pp = 0; pp < Gm::PPS; ++pp)
 #pragma unroll
-            for (int kk = 0; kk < Gm::KSH; ++kk) {
-                uint32_t af[4];
-                e4m3x4_to_f16x2x2(w0[kk], af[0], af[2]);
-                e4m3x4_to_f16x2x2(w1[kk], af[1], af[3]);
-                mma_16816(sc, af, qf[hh * Gm::KSH + kk][0], qf[hh * Gm::KSH + kk][1], sc);
-            }
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int cc = 0; cc < Gm::KW / 16; ++cc) {
+                            uint4 x = make_uint4(0, 0, 0, 0);
+                            if (pp < np)
+                                x = *reinterpret_cast<const uint4*>(kst + pp * Gm::PAGE + hh * Gm::BOX +
+                                                                    swz<Gm::ROWB>(nt * 8 + gid, tig * Gm::KW + 16 * cc));
+                            kw[pp][nt][4 * cc + 0] = x.x;
+                            kw[pp][nt][4 * cc + 1] = x.y;
+                            kw[pp][nt][4 * cc + 2] = x.z;
+                            kw[pp][nt][4 * cc + 3] = x.w;
+                        }
+#pragma unroll
+                for (int kk = 0; kk < Gm::KSH; ++kk) {
+                    const uint4 qa = qsm[(hh * Gm::KSH + kk) * 32 + lane];
+                    const uint32_t af[4] = {qa.x, qa.y, qa.z, qa.w};
+#pragma unroll
+                    for (int pp = 0; pp < Gm::PPS; ++pp)
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            uint32_t b0, b1;
+                            e4m3x4_to_f16x2x2(kw[pp][nt][kk], b0, b1);
+                            mma_16816(sc[pp][nt], af, b0, b1, sc[pp][nt]);
+                        }
+                }
         }
 
-        // ---- causal / window mask, scale to log2 units, page maximum per row
+        // ---- causal / window mask (not needed where every key of the stage is
+        // attended by every row of the warp), log2 units, running maximum per row
+        const bool interior = np == Gm::PPS && t0 + Gm::PPS * kBS - 1 <= wpos0 && t0 >= wlo1;
         float mx[2] = {-INFINITY, -INFINITY};
+        if (interior) {
 #pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-            const int key = t0 + gid + 8 * e2;
+            for (int p = 0; p < Gm::PPS; ++p)
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const bool valid = rv[j] && key <= pq[j] && key >= lq[j];
-                const float t = valid ? sc[2 * e2 + j] * cs[j] : -INFINITY;
-                sc[2 * e2 + j] = t;
-                mx[j] = fmaxf(mx[j], t);
-            }
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        sc[p][nt][e] *= cs[e >> 1];
+                        mx[e >> 1] = fmaxf(mx[e >> 1], sc[p][nt][e]);
+                    }
+        } else {
+#pragma unroll
+            for (int p = 0; p < Gm::PPS; ++p)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = e >> 1;
+                        const int key = t0 + p * kBS + nt * 8 + 2 * tig + (e & 1);
+                        const bool valid = p < np && rv[j] && key >= lq[j] && key <= pq[j];
+                        const float t = valid ? sc[p][nt][e] * cs[j] : -INFINITY;
+                        sc[p][nt][e] = t;
+                        mx[j] = fmaxf(mx[j], t);
+                    }
         }
         float alpha[2], muse[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
-            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
-            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
+            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 1));
+            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 2));
             const float mn = fmaxf(m[j], mx[j]);
             muse[j] = mn == -INFINITY ? 0.f : mn;
             alpha[j] = fast_exp2(m[j] - muse[j]);
             m[j] = mn;
         }
-        const float p00 = fast_exp2(sc[0] - muse[0]), p01 = fast_exp2(sc[1] - muse[1]);
-        const float p10 = fast_exp2(sc[2] - muse[0]), p11 = fast_exp2(sc[3] - muse[1]);
-        l[0] = l[0] * alpha[0] + (p00 + p10);
-        l[1] = l[1] * alpha[1] + (p01 + p11);
-        const uint32_t pb0 = movmatrix_trans(pack_f16x2(p00, p01));
-        const uint32_t pb1 = movmatrix_trans(pack_f16x2(p10, p11));
 
-        // ---- P.V tile of this page: O^T[dim][row] = V^T P^T; keys that no row
-        // of the tile attends read as zero codes (stale NaN codes never meet p = 0)
-        const int kmin = lo_first, kmax = p_last;
-        float ot[Gm::MT][4];
+        // ---- probabilities: the score accumulators are already the A fragments of P V
+        uint32_t pa[Gm::PPS][4];
+        float ls[2] = {0.f, 0.f};
 #pragma unroll
-        for (int mt = 0; mt < Gm::MT; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
+        for (int p = 0; p < Gm::PPS; ++p) {
+            float pr[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    pr[nt][e] = fast_exp2(sc[p][nt][e] - muse[e >> 1]);
+                    ls[e >> 1] += pr[nt][e];
+                }
+            pa[p][0] = pack_f16x2(pr[0][0], pr[0][1]);
+            pa[p][1] = pack_f16x2(pr[0][2], pr[0][3]);
+            pa[p][2] = pack_f16x2(pr[1][0], pr[1][1]);
+            pa[p][3] = pack_f16x2(pr[1][2], pr[1][3]);
+        }
+        l[0] = l[0] * alpha[0] + ls[0];
+        l[1] = l[1] * alpha[1] + ls[1];
+
+        // ---- P V tile of this stage in fresh accumulators, folded into O.  The
+        // thread's V bytes: key rows 2tig, 2tig+1, 2tig+8, 2tig+9 of each page,
+        // VW bytes at column gid*VW of each box; keys outside the tile's range
+        // read as zero codes (stale NaN codes never meet a zero probability).
 #pragma unroll
         for (int hh = 0; hh < Gm::HALVES; ++hh) {
-            const uint8_t* box = vst + hh * Gm::BOX;
-            uint32_t v[4][Gm::VW / 4];
+                uint32_t v[Gm::PPS][4][Gm::VW / 4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int row = 2 * tig + (r & 1) + 8 * (r >> 1);
-                if constexpr (Gm::VW == 16) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(row, gid * 16));
-                    v[r][0] = x.x; v[r][1] = x.y; v[r][2] = x.z; v[r][3] = x.w;
-                } else {
-                    const uint2 x = *reinterpret_cast<const uint2*>(box + swz<Gm::ROWB>(row, gid * 8));
-                    v[r][0] = x.x; v[r][1] = x.y;
-                }
-                const int key = t0 + row;
-                if (key < kmin || key > kmax) {
+                for (int pp = 0; pp < Gm::PPS; ++pp)
 #pragma unroll
-                    for (int ww = 0; ww < Gm::VW / 4; ++ww) v[r][ww] = 0u;
-                }
+                    for (int r = 0; r < 4; ++r) {
+                        const int row = 2 * tig + (r & 1) + 8 * (r >> 1);
+                        const int key = t0 + pp * kBS + row;
+                        const bool ok = pp < np && (interior || (key >= u.kmin && key <= u.kmax));
+                        const uint8_t* src = vst + pp * Gm::PAGE + hh * Gm::BOX + swz<Gm::ROWB>(row, gid * Gm::VW);
+                        if constexpr (Gm::VW == 16) {
+                            uint4 x = make_uint4(0, 0, 0, 0);
+                            if (ok) x = *reinterpret_cast<const uint4*>(src);
+                            v[pp][r][0] = x.x; v[pp][r][1] = x.y; v[pp][r][2] = x.z; v[pp][r][3] = x.w;
+                        } else {
+                            uint2 x = make_uint2(0, 0);
+                            if (ok) x = *reinterpret_cast<const uint2*>(src);
+                            v[pp][r][0] = x.x; v[pp][r][1] = x.y;
+                        }
+                    }
+#pragma unroll
+                for (int w = 0; w < Gm::VW / 4; ++w)
+#pragma unroll
+                    for (int s = 0; s < 2; ++s) {
+                        const uint32_t sel = s ? 0x7362u : 0x5140u;
+                        float ot[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                        for (int pp = 0; pp < Gm::PPS; ++pp) {
+                            if (pp < np) {
+                                uint32_t b0[2], b1[2];
+                                e4m3x4_to_f16x2x2(byte_perm(v[pp][0][w], v[pp][1][w], sel), b0[0], b0[1]);
+                                e4m3x4_to_f16x2x2(byte_perm(v[pp][2][w], v[pp][3][w], sel), b1[0], b1[1]);
+                                mma_16816(ot[0], pa[pp], b0[0], b1[0], ot[0]);
+                                mma_16816(ot[1], pa[pp], b0[1], b1[1], ot[1]);
+                            }
+                        }
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const int nt = hh * Gm::VW + 4 * w + 2 * s + jj;
+                            o[nt][0] = fmaf(o[nt][0], alpha[0], ot[jj][0]);
+                            o[nt][1] = fmaf(o[nt][1], alpha[0], ot[jj][1]);
+                            o[nt][2] = fmaf(o[nt][2], alpha[1], ot[jj][2]);
+                            o[nt][3] = fmaf(o[nt][3], alpha[1], ot[jj][3]);
+                        }
+                    }
             }
-#pragma unroll
-            for (int mtl = 0; mtl < Gm::MTH; ++mtl) {
-                const uint32_t sel = (mtl & 1) ? 0x7362u : 0x5140u;
-                const uint32_t x01 = byte_perm(v[0][mtl >> 1], v[1][mtl >> 1], sel);
-                const uint32_t x23 = byte_perm(v[2][mtl >> 1], v[3][mtl >> 1], sel);
-                uint32_t af[4];
-                e4m3x4_to_f16x2x2(x01, af[0], af[1]);
-                e4m3x4_to_f16x2x2(x23, af[2], af[3]);
-                mma_16816(ot[hh * Gm::MTH + mtl], af, pb0, pb1, ot[hh * Gm::MTH + mtl]);
-            }
-        }
-#pragma unroll
-        for (int mt = 0; mt < Gm::MT; ++mt) {
-            o[mt][0] = fmaf(o[mt][0], alpha[0], ot[mt][0]);
-            o[mt][1] = fmaf(o[mt][1], alpha[1], ot[mt][1]);
-            o[mt][2] = fmaf(o[mt][2], alpha[0], ot[mt][2]);
-            o[mt][3] = fmaf(o[mt][3], alpha[1], ot[mt][3]);
-        }
-        __syncthreads();               // every warp is done with this buffer before it is refilled
     }
-    cp_async_wait_0();
+    cp_async_wait<0>();
 
-    // ---- normalise and write this lane's two rows
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-        l[j] += __shfl_xor_sync(0xffffffffu, l[j], 4);
-        l[j] += __shfl_xor_sync(0xffffffffu, l[j], 8);
-        l[j] += __shfl_xor_sync(0xffffffffu, l[j], 16);
+        l[j] += __shfl_xor_sync(0xffffffffu, l[j], 1);
+        l[j] += __shfl_xor_sync(0xffffffffu, l[j], 2);
     }
+
+    // ---- emit: n-tile nt = hh*VW + c, accumulator column n holds dimension
+    // hh*ROWB + n*VW + c, so this thread's two columns (2tig, 2tig+1) are two
+    // contiguous runs of VW dimensions per box
+    const int64_t unit = (static_cast<int64_t>(b) * a.num_kv_heads + hk) * a.tiles + tile;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-        const int r = rw + 2 * tig + j;
-        if (r >= rows) continue;
-        const float sc_out = l[j] > 0.f ? a.v_scale / l[j] : 0.f;
-        uint16_t* orow = a.out + (static_cast<int64_t>(q0 + r / G) * a.num_q_heads + hk * G + r % G) * D;
+        if (!rv[j]) continue;
+        const int rr = warp * 16 + gid + 8 * j;   // row within the tile
+        const int r = u.R0 + rr;
+        if (a.splits == 1) {
+            const float so = l[j] > 0.f ? a.v_scale / l[j] : 0.f;
+            uint16_t* orow = a.out + (static_cast<int64_t>(u.q0 + r / G) * a.num_q_heads + hk * G + r % G) * D;
 #pragma unroll
-        for (int mt = 0; mt < Gm::MT; ++mt)
+            for (int hh = 0; hh < Gm::HALVES; ++hh)
 #pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-                const int dim = (mt / Gm::MTH) * 128 + Gm::VW * gid + 2 * (mt % Gm::MTH) + e2;
-                orow[dim] = f32_to_bf16(o[mt][2 * e2 + j] * sc_out);
-            }
+                for (int cn = 0; cn < 2; ++cn) {
+                    uint32_t pk[Gm::VW / 2];
+#pragma unroll
+                    for (int c = 0; c < Gm::VW; c += 2)
+                        pk[c / 2] = pack_bf16x2(o[hh * Gm::VW + c][2 * j + cn] * so,
+                                                o[hh * Gm::VW + c + 1][2 * j + cn] * so);
+                    uint4* dst = reinterpret_cast<uint4*>(orow + hh * Gm::ROWB + (2 * tig + cn) * Gm::VW);
+#pragma unroll
+                    for (int i = 0; i < Gm::VW / 8; ++i)
+                        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+        } else {
+            const int64_t slot = (unit * a.splits + split) * kRows + rr;
+            float* po = a.part_o + slot * D;
+#pragma unroll
+            for (int hh = 0; hh < Gm::HALVES; ++hh)
+#pragma unroll
+                for (int cn = 0; cn < 2; ++cn) {
+                    float4* dst = reinterpret_cast<float4*>(po + hh * Gm::ROWB + (2 * tig + cn) * Gm::VW);
+#pragma unroll
+                    for (int i = 0; i < Gm::VW / 4; ++i)
+                        dst[i] = make_float4(o[hh * Gm::VW + 4 * i][2 * j + cn], o[hh * Gm::VW + 4 * i + 1][2 * j + cn],
+                                             o[hh * Gm::VW + 4 * i + 2][2 * j + cn],
+                                             o[hh * Gm::VW + 4 * i + 3][2 * j + cn]);
+                }
+            if (tig == 0) a.part_ml[slot] = make_float2(m[j], l[j]);
+        }
     }
 }
 
-template <int D>
-cudaError_t launch_g(int G, const Args& a, dim3 grid, cudaStream_t s) {
+// Combines a unit's split partials row by row in FP32: with M the largest
+// row maximum, weight_s = 2^(m_s - M), out = v_scale * sum_s weight_s o_s /
+// sum_s weight_s l_s, rounded to bf16.  One CTA per unit, a warp per row.
+template <int D, int G>
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
+    __shared__ float wsm[8][kMaxSplits];
+    const int b = blockIdx.z, hk = blockIdx.y, tile = blockIdx.x;
+    Unit u;
+    const bool ok = make_unit<G>(a, b, tile, false, u);  // only the lengths: read before the wait
+    griddep_wait();                                      // the partials are complete and visible
+    if (!ok) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t unit = (static_cast<int64_t>(b) * a.num_kv_heads + hk) * a.tiles + tile;
+    for (int rr = warp; rr < kRows && u.R0 + rr < u.rows; rr += 8) {
+        const int r = u.R0 + rr;
+        const int64_t slot0 = unit * a.splits * kRows + rr;     // split s at slot0 + s * kRows
+        float mmax = -INFINITY;
+        for (int s = lane; s < a.splits; s += 32) mmax = fmaxf(mmax, a.part_ml[slot0 + s * kRows].x);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, off));
+        float lsum = 0.f;
+        for (int s = lane; s < a.splits; s += 32) {
+            const float2 ml = a.part_ml[slot0 + s * kRows];
+            const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - mmax);
+            wsm[warp][s] = wgt;
+            lsum += wgt * ml.y;
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+        __syncwarp();
+        const float so = lsum > 0.f ? a.v_scale / lsum : 0.f;
+        const float* po = a.part_o + slot0 * D;
+        uint16_t* orow = a.out + (static_cast<int64_t>(u.q0 + r / G) * a.num_q_heads + hk * G + r % G) * D;
+        for (int d = 2 * lane; d < D; d += 64) {
+            float acc0 = 0.f, acc1 = 0.f;
+            for (int s = 0; s < a.splits; ++s) {
+                const float wgt = wsm[warp][s];
+                if (wgt != 0.f) {
+                    const float2 x = *reinterpret_cast<const float2*>(po + static_cast<int64_t>(s) * kRows * D + d);
+                    acc0 = fmaf(wgt, x.x, acc0);
+                    acc1 = fmaf(wgt, x.y, acc1);
+                }
+            }
+            *reinterpret_cast<uint32_t*>(orow + d) = pack_bf16x2(acc0 * so, acc1 * so);
+        }
+        __syncwarp();
+    }
+}
+
+// Split plan: the tiles a sequence's chunk may need, and how many CTAs share
+// each unit's key range so that the grid fills the GPU (at least 128 keys per
+// split, at most kMaxSplits).
+struct Plan {
+    int tiles = 0;
+    int splits = 1;
+    size_t ml = kHeader;   // offset of the (m, l) partials
+    size_t o = kHeader;    // offset of the output partials
+    size_t total = kHeader;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D, int window, int sms) {
+    Plan pl;
+    pl.tiles = static_cast<int>((static_cast<int64_t>(max_q_len) * G + kRows - 1) / kRows);
+    const int64_t units = static_cast<int64_t>(pl.tiles) * Hkv * batch;
+    int64_t pages = (static_cast<int64_t>(max_seq_len) + kBS - 1) / kBS;
+    if (window > 0) pages = std::min<int64_t>(pages, (static_cast<int64_t>(window) + kRows) / kBS + 2);
+    const int64_t target = 4LL * sms;
+    if (units > 0 && units < target) {
+        const int64_t want = (target + units - 1) / units;
+        pl.splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({want, pages / kMinSplitPages,
+                                                                              static_cast<int64_t>(kMaxSplits)})));
+    }
+    if (pl.splits > 1) {
+        const size_t slots = static_cast<size_t>(units) * pl.splits * kRows;
+        pl.ml = kHeader;
+        pl.o = pl.ml + align256(slots * sizeof(float2));
+        pl.total = pl.o + align256(slots * D * sizeof(float));
+    }
+    return pl;
+}
+
+template <int D, int G>
+cudaError_t launch(const Args& a, int batch, cudaStream_t s) {
+    static std::atomic<uint64_t> done_mask{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (bit == 0 || !(done_mask.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(paged_prefill_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(Geo<D>::SMEM));
+        if (e != cudaSuccess) return e;
+        done_mask.fetch_or(bit, std::memory_order_release);
+    }
+    // Both grids may start before the previous work on the stream ends; each
+    // waits (griddepcontrol.wait) before touching what that work wrote.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
+    cfg.gridDim = dim3(static_cast<unsigned>(a.tiles * a.splits), static_cast<unsigned>(a.num_kv_heads),
+                       static_cast<unsigned>(batch));
     cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Geo<D>::SMEM;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D, G>, a);
+    if (e != cudaSuccess || a.splits == 1) return e;
+    cfg.gridDim = dim3(static_cast<unsigned>(a.tiles), static_cast<unsigned>(a.num_kv_heads),
+                       static_cast<unsigned>(batch));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, prefill_merge_kernel<D, G>, a);
+}
+
+template <int D>
+cudaError_t launch_g(int G, const Args& a, int batch, cudaStream_t s) {
     switch (G) {
-        case 1: return cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D, 1>, a);
-        case 2: return cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D, 2>, a);
-        case 4: return cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D, 4>, a);
-        case 8: return cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D, 8>, a);
+        case 1: return launch<D, 1>(a, batch, s);
+        case 2: return launch<D, 2>(a, batch, s);
+        case 4: return launch<D, 4>(a, batch, s);
+        case 8: return launch<D, 8>(a, batch, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-}  // namespace prefill
-}  // namespace fp8kv
-
-extern "C" fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens, const uint8_t* k_cache, const uint8_t* v_cache,
-                                            int64_t num_blocks, const int32_t* block_tables, int max_blocks_per_seq,
-                                            const int32_t* seq_lens, const int32_t* q_starts, int max_q_len,
-                                            int max_seq_len, int batch, int num_q_heads, int num_kv_heads,
-                                            int head_dim, int block_size, float k_scale, float v_scale,
-                                            float sm_scale, int window, void* out, void* workspace,
-                                            void* stream) {
-    using namespace fp8kv::prefill;
-    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+// Shape checks shared by the size query and the call.
+fp8kv_status check_shape(int batch, int max_q_len, int max_seq_len, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size) {
     if (batch < 0 || batch > 65535 || num_kv_heads < 1 || num_kv_heads > 65535 || num_q_heads < 1 ||
-        num_q_heads % num_kv_heads != 0 || max_seq_len < 0 || max_q_len < 0 || max_q_len > max_seq_len ||
-        num_blocks < 1 || max_blocks_per_seq < 0 || num_q_tokens < 0)
-        return FP8KV_ERR_INVALID_ARG;
-    if (!std::isfinite(k_scale) || !(k_scale > 0) || !std::isfinite(v_scale) || !(v_scale > 0) ||
-        !std::isfinite(sm_scale))
+        num_q_heads % num_kv_heads != 0 || max_seq_len < 0 || max_q_len < 0 || max_q_len > max_seq_len)
         return FP8KV_ERR_INVALID_ARG;
     const int G = num_q_heads / num_kv_heads;
     if (!(head_dim == 64 || head_dim == 128 || head_dim == 256) || block_size != kBS ||
         !(G == 1 || G == 2 || G == 4 || G == 8))
         return FP8KV_ERR_UNSUPPORTED;
+    const int64_t tiles = (static_cast<int64_t>(max_q_len) * G + kRows - 1) / kRows;
+    if (tiles * kMaxSplits > INT32_MAX) return FP8KV_ERR_UNSUPPORTED;
+    return FP8KV_OK;
+}
+
+}  // namespace prefill
+}  // namespace fp8kv
+
+extern "C" size_t fp8kv_paged_prefill_workspace_size(int batch, int max_q_len, int max_seq_len, int num_q_heads,
+                                                     int num_kv_heads, int head_dim, int block_size, int window) {
+    using namespace fp8kv::prefill;
+    if (check_shape(batch, max_q_len, max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size) != FP8KV_OK)
+        return 0;
+    int sms = 0;
+    if (fp8kv::device_sms(&sms) != 0) return 0;
+    return make_plan(batch, max_q_len, max_seq_len, num_q_heads / num_kv_heads, num_kv_heads, head_dim,
+                     window > 0 ? window : 0, sms)
+        .total;
+}
+
+extern "C" fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens, const uint8_t* k_cache,
+                                            const uint8_t* v_cache, int64_t num_blocks, const int32_t* block_tables,
+                                            int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* q_starts,
+                                            int max_q_len, int max_seq_len, int batch, int num_q_heads,
+                                            int num_kv_heads, int head_dim, int block_size, float k_scale,
+                                            float v_scale, float sm_scale, int window, void* out, void* workspace,
+                                            size_t workspace_bytes, void* stream) {
+    using namespace fp8kv::prefill;
+    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const fp8kv_status sh = check_shape(batch, max_q_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,
+                                        block_size);
+    if (sh != FP8KV_OK) return sh;
+    if (num_blocks < 1 || max_blocks_per_seq < 0 || num_q_tokens < 0) return FP8KV_ERR_INVALID_ARG;
+    if (!std::isfinite(k_scale) || !(k_scale > 0) || !std::isfinite(v_scale) || !(v_scale > 0) ||
+        !std::isfinite(sm_scale))
+        return FP8KV_ERR_INVALID_ARG;
     if (num_blocks >= (INT64_C(1) << 31) || num_blocks * num_kv_heads >= (INT64_C(1) << 31))
         return FP8KV_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(max_blocks_per_seq) * block_size < max_seq_len) return FP8KV_ERR_INVALID_ARG;
@@ -400,10 +665,15 @@ extern "C" fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens,
     if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !q_starts || !out) return FP8KV_ERR_INVALID_ARG;
     if (!a16(q) || !a16(k_cache) || !a16(v_cache) || !a16(out)) return FP8KV_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
-        (reinterpret_cast<uintptr_t>(q_starts) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 3u))
+        (reinterpret_cast<uintptr_t>(q_starts) & 3u))
         return FP8KV_ERR_INVALID_ARG;
-    const int64_t tiles = (static_cast<int64_t>(max_q_len) * G + kRows - 1) / kRows;
-    if (tiles > INT32_MAX) return FP8KV_ERR_UNSUPPORTED;
+    int sms = 0;
+    if (fp8kv::device_sms(&sms) != 0) return FP8KV_ERR_CUDA;
+    const int G = num_q_heads / num_kv_heads;
+    const Plan pl = make_plan(batch, max_q_len, max_seq_len, G, num_kv_heads, head_dim, window > 0 ? window : 0, sms);
+    if (!workspace || workspace_bytes < pl.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return FP8KV_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
     Args a;
     a.q = static_cast<const uint16_t*>(q);
     a.k_cache = k_cache;
@@ -412,24 +682,27 @@ extern "C" fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens,
     a.seq_lens = seq_lens;
     a.q_starts = q_starts;
     a.out = static_cast<uint16_t*>(out);
+    a.err = reinterpret_cast<uint32_t*>(ws);
+    a.part_ml = reinterpret_cast<float2*>(ws + pl.ml);
+    a.part_o = reinterpret_cast<float*>(ws + pl.o);
     a.num_blocks = num_blocks;
     a.num_q_tokens = num_q_tokens;
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.max_seq_len = max_seq_len;
     a.max_q_len = max_q_len;
-    a.err = static_cast<uint32_t*>(workspace);
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = num_kv_heads;
+    a.tiles = pl.tiles;
+    a.splits = pl.splits;
     a.window = window > 0 ? window : 0;
     a.score_scale = sm_scale * k_scale * kLog2e;
     a.v_scale = v_scale;
-    const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(num_kv_heads), static_cast<unsigned>(batch));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (head_dim) {
-        case 64: e = launch_g<64>(G, a, grid, s); break;
-        case 128: e = launch_g<128>(G, a, grid, s); break;
-        default: e = launch_g<256>(G, a, grid, s); break;
+        case 64: e = launch_g<64>(G, a, batch, s); break;
+        case 128: e = launch_g<128>(G, a, batch, s); break;
+        default: e = launch_g<256>(G, a, batch, s); break;
     }
     return e == cudaSuccess ? FP8KV_OK : FP8KV_ERR_CUDA;
 }

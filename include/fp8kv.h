@@ -337,8 +337,9 @@ fp8kv_status fp8kv_paged_decode_noalloc(const void* q, const uint8_t* k_cache, c
  *     s_t = sm_scale * sum_i q[r][h][i] * decode(k code of t)[i] * k_scale
  *     out[r][h][:] = sum_t exp(s_t - max s) decode(v code of t) * v_scale
  *                    / sum_t exp(s_t - max s)
- * with r = q_starts[b] + i.  Scores, the softmax and P.V accumulate in FP32;
- * the result is rounded to bf16 (RNE).
+ * with r = q_starts[b] + i.  Scores, the softmax and P.V accumulate in FP32
+ * (key-range partials, when the call splits a long range over several CTAs,
+ * are merged in FP32); the result is rounded to bf16 (RNE).
  *
  *   q              bf16 [num_q_tokens][num_q_heads][head_dim], the query rows of
  *                  all sequences packed in order, 16-byte aligned
@@ -353,23 +354,28 @@ fp8kv_status fp8kv_paged_decode_noalloc(const void* q, const uint8_t* k_cache, c
  *   max_q_len      host-side upper bound of the q_len (sizes the grid)
  *   window         <= 0: causal over the whole prefix; > 0: the last `window` keys
  *   out            bf16 [num_q_tokens][num_q_heads][head_dim], 16-byte aligned
- *   workspace      NULL, or a decode workspace (zero-filled, 4-byte aligned):
- *                  its error word then records, for fp8kv_read_error, an
- *                  out-of-range block id (block 0 is read instead) or a
+ *   workspace      >= fp8kv_paged_prefill_workspace_size(...) bytes, 256-byte
+ *                  aligned, zero-filled before first use (fp8kv_workspace_init);
+ *                  its first word is the error word fp8kv_read_error reads: an
+ *                  out-of-range block id (block 0 is read instead), or a
  *                  seq_lens / q_starts entry outside the bounds above (the
  *                  sequence is clamped, or skipped if its rows would fall
- *                  outside q / out)
+ *                  outside q / out).  Calls that share a workspace must be
+ *                  ordered.  Missing or too small: FP8KV_ERR_WORKSPACE.
  * Supported: head_dim in {64, 128, 256}; block_size == 16; g in {1, 2, 4, 8};
  *            num_blocks * num_kv_heads < 2^31.  batch == 0, max_q_len == 0 or
  *            num_q_tokens == 0 is a no-op.
  */
+size_t fp8kv_paged_prefill_workspace_size(int batch, int max_q_len, int max_seq_len, int num_q_heads,
+                                          int num_kv_heads, int head_dim, int block_size, int window);
+
 fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens, const uint8_t* k_cache,
                                  const uint8_t* v_cache, int64_t num_blocks, const int32_t* block_tables,
                                  int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* q_starts,
                                  int max_q_len, int max_seq_len, int batch, int num_q_heads,
                                  int num_kv_heads, int head_dim, int block_size, float k_scale,
                                  float v_scale, float sm_scale, int window, void* out, void* workspace,
-                                 void* stream);
+                                 size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

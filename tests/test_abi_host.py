@@ -168,21 +168,29 @@ def test_workspace_calls_validate(lib):
 
 def _prefill(lib, **kw):
     a = dict(q=FAKE, T=64, k=FAKE, v=FAKE, nb=100, bt=FAKE, mb=8, sl=FAKE, qs=FAKE, mq=64, msl=128, B=2, hq=32,
-             hkv=8, d=128, bs=16, ks=0.01, vs=0.01, sm=0.088, win=0, out=FAKE, ws=None)
+             hkv=8, d=128, bs=16, ks=0.01, vs=0.01, sm=0.088, win=0, out=FAKE, ws=FAKE, wsb=1 << 30)
     a.update(kw)
     return lib.fp8kv_paged_prefill(a["q"], a["T"], a["k"], a["v"], a["nb"], a["bt"], a["mb"], a["sl"], a["qs"],
                                    a["mq"], a["msl"], a["B"], a["hq"], a["hkv"], a["d"], a["bs"], a["ks"], a["vs"],
-                                   a["sm"], a["win"], a["out"], a["ws"], None)
+                                   a["sm"], a["win"], a["out"], a["ws"], a["wsb"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(d=96), 2), (dict(d=512), 2), (dict(bs=32), 2), (dict(hq=128, hkv=8), 2),
     (dict(hq=30, hkv=8), 1), (dict(ks=0.0), 1), (dict(vs=float("nan")), 1), (dict(sm=float("inf")), 1),
     (dict(q=None), 1), (dict(out=None), 1), (dict(qs=None), 1), (dict(q=MISALIGNED), 1),
-    (dict(v=MISALIGNED), 1), (dict(ws=MISALIGNED), 1), (dict(mb=4, msl=128), 1), (dict(mq=200), 1),
+    (dict(v=MISALIGNED), 1), (dict(mb=4, msl=128), 1), (dict(mq=200), 1),
     (dict(mq=-1), 1), (dict(T=-1), 1), (dict(B=-1), 1), (dict(nb=0), 1), (dict(nb=1 << 31), 2),
     (dict(B=70000), 1),
     (dict(B=0, q=None, out=None), 0), (dict(mq=0, q=None), 0), (dict(T=0, out=None), 0),
 ])
 def test_prefill_validates(lib, kw, code):
     assert _prefill(lib, **kw) == code
+
+
+def test_prefill_workspace_size_rejects_bad_shapes(lib):
+    f = lib.fp8kv_paged_prefill_workspace_size
+    assert f(2, 64, 128, 32, 8, 96, 16, 0) == 0       # head_dim
+    assert f(2, 200, 128, 32, 8, 128, 16, 0) == 0     # max_q_len > max_seq_len
+    assert f(2, 64, 128, 30, 8, 128, 16, 0) == 0      # heads not a multiple
+    assert f(2, 64, 128, 32, 8, 128, 32, 0) == 0      # block size

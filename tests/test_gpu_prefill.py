@@ -15,16 +15,26 @@ from tests.gpu_harness import Paged
 pytestmark = pytest.mark.gpu
 
 
+def _ws(p: Paged, mq, window):
+    s = p.w.shape
+    return fk.alloc_prefill_workspace(p.q.shape[0], mq, p.w.max_seq_len, s.num_q_heads, s.num_kv_heads, s.head_dim,
+                                      16, window)
+
+
 def _run(p: Paged, q, q_starts, window, max_q_len=None, block_tables=None, seq_lens=None, ws=None):
     w = p.w
     out = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
     qs = q_starts.cuda()
     mq = int((q_starts[1:] - q_starts[:-1]).max()) if max_q_len is None else max_q_len
+    own_ws = ws is None
+    ws = _ws(p, mq, window) if own_ws else ws
     fk.fp8kv_paged_prefill(q.cuda(), p.k_cache, p.v_cache,
                            p.block_tables if block_tables is None else block_tables,
                            p.seq_lens if seq_lens is None else seq_lens, qs, mq, w.max_seq_len,
                            w.k_scale, w.v_scale, w.sm_scale, window, out, ws)
     torch.cuda.synchronize()
+    if own_ws:
+        assert fk.fp8kv_read_error(ws) == 0
     return out.float().cpu().numpy()
 
 
@@ -160,7 +170,7 @@ def test_prefill_reports_bad_block_id_and_lengths():
     p.append_all()
     q_lens = [20, 20]
     q, qs = workload.prefill_queries(w, q_lens, seed=8)
-    ws = fk.alloc_workspace(2, 32, 8, 128, 64)
+    ws = _ws(p, 20, 0)
     bt = p.block_tables.clone()
     bt[1, 0] = p.num_blocks + 5
     got = _run(p, q, qs, 0, block_tables=bt, ws=ws)
@@ -174,3 +184,23 @@ def test_prefill_reports_bad_block_id_and_lengths():
     assert fk.fp8kv_read_error(ws) == 1
     _run(p, q, qs, 0, ws=ws)
     assert fk.fp8kv_read_error(ws) == 0
+
+
+@pytest.mark.parametrize("base", ["llama31_8b_b8_20k", "gemma4e2b_b16_8k32k"])
+def test_prefill_short_chunk_long_context_splits_the_keys(base):
+    """Few query tiles over a long context: the key range of each tile is
+    split over many CTAs and their FP32 partials are merged."""
+    lens = [5000, 3100]
+    q_lens = [16, 3]
+    shape = workload.small_shape(base, len(lens), 1, 1)
+    w = workload.make_workload(shape, seed=9, lens=lens)
+    p = Paged(w, seed=9)
+    p.append_all()
+    s = w.shape
+    n_ws = fk.fp8kv_paged_prefill_workspace_size(2, 16, w.max_seq_len, s.num_q_heads, s.num_kv_heads, s.head_dim)
+    assert n_ws > 4096      # the plan splits: the workspace holds partials
+    q, qs = workload.prefill_queries(w, q_lens, seed=9)
+    for window in (0, 700):
+        got = _run(p, q, qs, window)
+        ref = _oracle(p, q, q_lens, window)
+        assert_attn_close(got, ref, f"{base} split window={window}")
