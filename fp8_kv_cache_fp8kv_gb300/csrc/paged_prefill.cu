@@ -36,6 +36,7 @@
 
 #include "fp8kv.h"
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 
 namespace fp8kv {
 
@@ -46,7 +47,8 @@ namespace prefill {
 constexpr int kBS = 16;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kRows = kWarps * 16;      // query rows per unit
+constexpr int kRows = kWarps * 16;      // query rows per unit of the mma.sync kernel
+constexpr int kRowsTC = 128;            // query rows per unit of the tcgen05 kernel (one per TMEM lane)
 constexpr int kStages = 3;              // ring depth
 constexpr int kMaxSplits = 64;
 constexpr int kMinSplitPages = 8;       // a split covers at least 128 keys
@@ -62,8 +64,8 @@ struct Args {
     const int32_t* q_starts;     // [B + 1] cumulative query-row offsets
     uint16_t* out;               // bf16 [num_q_tokens, Hq, D]
     uint32_t* err;               // error word
-    float* part_o;               // [units][splits][kRows][D] unnormalised FP32 outputs
-    float2* part_ml;             // [units][splits][kRows] (row maximum in log2 units, row sum)
+    float* part_o;               // [units][splits][rows][D] unnormalised FP32 outputs
+    float2* part_ml;             // [units][splits][rows] (row maximum in log2 units, row sum)
     int64_t num_blocks;
     int64_t num_q_tokens;
     int max_blocks_per_seq;
@@ -72,6 +74,7 @@ struct Args {
     int num_q_heads;
     int num_kv_heads;
     int tiles;                   // query tiles per (sequence, kv head)
+    int rows;                    // query rows per tile (kRows or kRowsTC)
     int splits;                  // CTAs per unit
     int window;
     float score_scale;           // sm_scale * k_scale * log2(e)
@@ -163,10 +166,10 @@ __device__ __forceinline__ bool make_unit(const Args& a, int b, int tile, bool r
     if (report_errors && (u.L != L_in || n != n_in)) report(a.err, FP8KV_ERR_INVALID_ARG);
     u.n = n;
     u.rows = n * G;
-    u.R0 = tile * kRows;
+    u.R0 = tile * a.rows;
     if (u.R0 >= u.rows) return false;
     const int p_first = u.L - n + u.R0 / G;
-    u.kmax = u.L - n + (min(u.R0 + kRows, u.rows) - 1) / G;
+    u.kmax = u.L - n + (min(u.R0 + a.rows, u.rows) - 1) / G;
     u.kmin = (a.window > 0 && p_first + 1 > a.window) ? p_first + 1 - a.window : 0;
     return true;
 }
@@ -465,7 +468,7 @@ __global__ void __launch_bounds__(kThreads) paged_prefill_kernel(const Args a) {
                         dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                 }
         } else {
-            const int64_t slot = (unit * a.splits + split) * kRows + rr;
+            const int64_t slot = (unit * a.splits + split) * a.rows + rr;
             float* po = a.part_o + slot * D;
 #pragma unroll
             for (int hh = 0; hh < Gm::HALVES; ++hh)
@@ -483,6 +486,329 @@ __global__ void __launch_bounds__(kThreads) paged_prefill_kernel(const Args a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// d = 128 on the 5th-generation tensor cores (tcgen05).
+//
+// A unit is 128 query rows; thread t of the 4 warps owns row t, which is
+// TMEM lane t of both accumulators.  Per stage of 64 keys (4 pages):
+//   1. the stage's fp8 K and V pages (cp.async into a 2-slot staging ring)
+//      are converted into f16 operand tiles, K as 64 keys x 128 dims and V
+//      transposed as 128 dims x 64 keys, both K-major with the 128-byte
+//      swizzle (the Q tile, 128 rows x 128 dims, is built once);
+//   2. one thread issues S = Q K^T (M = 128, N = 64: 8 MMAs of K = 16) into
+//      TMEM columns [0, 64) and commits it to an mbarrier;
+//   3. each thread loads its row of S, masks it, runs the online softmax in
+//      log2 units and writes its row of P (f16) over the K tile, which the
+//      finished score MMAs no longer need;
+//   4. one thread issues O_tile = P V (M = 128, N = 128: 4 MMAs) into TMEM
+//      columns [64, 192);
+//   5. each thread loads its row of O_tile and folds it into FP32 registers,
+//      O = O * alpha + O_tile: the two-level accumulation.
+namespace tcg {
+constexpr int kKeys = 64;                       // keys per stage
+constexpr int kPages = kKeys / kBS;             // 4 pages per stage
+constexpr int kQ = 0;                           // Q tile: 2 blocks x 128 rows x 128 B
+constexpr int kKT = kQ + 2 * 128 * 128;         // K tile: 2 blocks x 64 keys x 128 B (P tile aliases it)
+constexpr int kVT = kKT + 2 * kKeys * 128;      // V^T tile: 128 dims x 128 B
+constexpr int kStg = kVT + 128 * 128;           // staging: 2 slots x (K 8 KB, V 8 KB)
+constexpr int kStgSlot = 2 * kKeys * 128;
+constexpr int kSmem = kStg + 2 * kStgSlot;      // 96 KB (+ 1 KB for alignment)
+constexpr uint32_t kTmemCols = 256;             // S at [0, 64), O_tile at [64, 192)
+constexpr uint64_t kWaitNs = 500000000ull;      // bounded waits on the MMA barriers
+}  // namespace tcg
+
+// Pages [pg, pg + np) of (block-table row bt, kv head hk) into staging slot
+// `dst`: key k of the stage is row k (128 bytes).  K chunk c of row k sits at
+// c ^ (k & 7), V chunk c at c ^ ((k >> 3) & 7), so that both conversions
+// below read without bank conflicts.  A block id outside [0, num_blocks)
+// reads block 0 and is reported.
+__device__ __forceinline__ void load_stage_tc(const Args& a, const int32_t* bt, int hk, int pg, int np, uint32_t dst) {
+    for (int i = threadIdx.x; i < np * 128; i += 128) {
+        const int p = i >> 7, ci = i & 127;
+        int id = __ldg(bt + pg + p);
+        if (id < 0 || id >= a.num_blocks) {
+            if (ci == 0) report(a.err, FP8KV_ERR_INVALID_ARG);
+            id = 0;
+        }
+        const int64_t base = (static_cast<int64_t>(id) * a.num_kv_heads + hk) * (kBS * 128);
+        const int r = ci >> 3, c = ci & 7, k = p * kBS + r;
+        cp_async16(dst + k * 128 + ((c ^ (k & 7)) << 4), a.k_cache + base + r * 128 + c * 16);
+        cp_async16(dst + tcg::kKeys * 128 + k * 128 + ((c ^ ((k >> 3) & 7)) << 4), a.v_cache + base + r * 128 + c * 16);
+    }
+}
+
+template <int G>
+__global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
+    constexpr int D = 128;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t bars[2];
+    __shared__ uint32_t tmem_base;
+    uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t sb = smem_u32(sm);
+    const int t = threadIdx.x, warp = t >> 5;
+    if (t == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_barrier_init();
+    }
+    griddep_wait();                // inputs may come from the previous grid on the stream
+    griddep_launch_dependents();
+    const int b = blockIdx.z, hk = blockIdx.y;
+    const int tile = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
+    Unit u;
+    if (!make_unit<G>(a, b, tile, blockIdx.x == 0 && hk == 0 && t == 0, u)) return;
+
+    // ---- this split's key pages; the first stage's copies start now
+    const int pg0 = u.kmin / kBS, np_all = u.kmax / kBS - pg0 + 1;
+    const int sp0 = pg0 + static_cast<int>(static_cast<int64_t>(split) * np_all / a.splits);
+    const int sp1 = pg0 + static_cast<int>(static_cast<int64_t>(split + 1) * np_all / a.splits);
+    const int nst = (sp1 - sp0 + tcg::kPages - 1) / tcg::kPages;
+    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
+    if (nst > 0) load_stage_tc(a, bt, hk, sp0, min(tcg::kPages, sp1 - sp0), sb + tcg::kStg);
+    cp_async_commit();
+
+    // ---- this thread's query row into the Q tile as f16, pre-scaled by a
+    // power of two so that the copy of the bf16 values is exact
+    const int r = u.R0 + t;
+    const bool rv = r < u.rows;
+    float cs;
+    int pq, lq;
+    {
+        const int tok = rv ? r / G : 0, hq = hk * G + (rv ? r % G : 0);
+        const uint4* qrow = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(u.q0 + tok) * a.num_q_heads + hq) * D);
+        uint4 qv[16];
+        float qmax = 0.f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            qv[c] = rv ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
+            const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                qmax = fmaxf(qmax, fmaxf(fabsf(bf16_to_f32(w4[e] & 0xFFFF)), fabsf(bf16_to_f32(w4[e] >> 16))));
+        }
+        int shift = 0;
+        if (qmax > 0.f) {
+            const int e = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFF) - 127;
+            shift = max(-100, min(100, 14 - e));
+        }
+        const float up = __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+            uint32_t f[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                f[e] = pack_f16x2(bf16_to_f32(w4[e] & 0xFFFF) * up, bf16_to_f32(w4[e] >> 16) * up);
+            *reinterpret_cast<uint4*>(sm + tcg::kQ + (c >> 3) * 16384 + t * 128 + (((c & 7) ^ (t & 7)) << 4)) =
+                make_uint4(f[0], f[1], f[2], f[3]);
+        }
+        cs = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
+        pq = u.L - u.n + (rv ? r / G : 0);
+        lq = (a.window > 0 && pq + 1 > a.window) ? pq + 1 - a.window : 0;
+    }
+    // the warp's first position and its last valid row's window start: a
+    // stage of keys in [wlo1, wpos0] is attended in full by every row of the warp
+    const int wr0 = u.R0 + warp * 32;
+    const int wpos0 = u.L - u.n + wr0 / G;
+    const int wpos1 = u.L - u.n + max(0, min(wr0 + 31, u.rows - 1)) / G;
+    const int wlo1 = (a.window > 0 && wpos1 + 1 > a.window) ? wpos1 + 1 - a.window : 0;
+
+    if (warp == 0) tc::alloc(&tmem_base, tcg::kTmemCols);
+    tc::fence_proxy_async_smem();  // the Q tile is read by the tensor cores
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = tmem_base;
+    const uint32_t tm_row = tm + (static_cast<uint32_t>(warp * 32) << 16);   // this warp's 32 lanes
+
+    float m = -INFINITY, l = 0.f;
+    float o[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) o[d] = 0.f;
+    bool fail = false;
+    for (int st = 0; st < nst; ++st) {
+        cp_async_wait<0>();            // this stage's copies (this thread's) have landed
+        if (__syncthreads_or(fail)) {  // ... everyone's; the previous stage's tiles are free
+            fail = true;
+            break;
+        }
+        if (st + 1 < nst)
+            load_stage_tc(a, bt, hk, sp0 + (st + 1) * tcg::kPages, min(tcg::kPages, sp1 - sp0 - (st + 1) * tcg::kPages),
+                          sb + tcg::kStg + ((st + 1) & 1) * tcg::kStgSlot);
+        cp_async_commit();
+        const int pgs = sp0 + st * tcg::kPages;
+        const int np = min(tcg::kPages, sp1 - pgs);
+        const int t0 = pgs * kBS;
+        const uint8_t* stg = sm + tcg::kStg + (st & 1) * tcg::kStgSlot;
+
+        // ---- 1a. K: thread t converts dims [64h, 64h + 64) of key k
+        {
+            const int k = t & 63, h = t >> 6;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 x = *reinterpret_cast<const uint4*>(stg + k * 128 + (((4 * h + i) ^ (k & 7)) << 4));
+                uint32_t f[8];
+                e4m3x4_to_f16x2x2(x.x, f[0], f[1]);
+                e4m3x4_to_f16x2x2(x.y, f[2], f[3]);
+                e4m3x4_to_f16x2x2(x.z, f[4], f[5]);
+                e4m3x4_to_f16x2x2(x.w, f[6], f[7]);
+                uint8_t* dst = sm + tcg::kKT + h * (tcg::kKeys * 128) + k * 128;
+                *reinterpret_cast<uint4*>(dst + (((2 * i) ^ (k & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+                *reinterpret_cast<uint4*>(dst + (((2 * i + 1) ^ (k & 7)) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
+            }
+        }
+        // ---- 1b. V^T: thread t converts keys [8kb, 8kb + 8) x dims [8db, 8db + 8);
+        // keys outside the tile's range (or past the stage's pages) become zeros
+        {
+            const int kb = t & 7, db = t >> 3;
+            uint32_t w[8][2];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = 8 * kb + i, key = t0 + k;
+                uint2 x = make_uint2(0, 0);
+                if (k < np * kBS && key >= u.kmin && key <= u.kmax)
+                    x = *reinterpret_cast<const uint2*>(stg + tcg::kKeys * 128 + k * 128 + (((db >> 1) ^ kb) << 4) +
+                                                        8 * (db & 1));
+                w[i][0] = x.x;
+                w[i][1] = x.y;
+            }
+            uint32_t vt[8][4];   // [dim][key pair]
+#pragma unroll
+            for (int i2 = 0; i2 < 4; ++i2)
+#pragma unroll
+                for (int hw = 0; hw < 2; ++hw) {
+                    e4m3x4_to_f16x2x2(byte_perm(w[2 * i2][hw], w[2 * i2 + 1][hw], 0x5140u), vt[4 * hw + 0][i2],
+                                      vt[4 * hw + 1][i2]);
+                    e4m3x4_to_f16x2x2(byte_perm(w[2 * i2][hw], w[2 * i2 + 1][hw], 0x7362u), vt[4 * hw + 2][i2],
+                                      vt[4 * hw + 3][i2]);
+                }
+#pragma unroll
+            for (int dd = 0; dd < 8; ++dd)
+                *reinterpret_cast<uint4*>(sm + tcg::kVT + (8 * db + dd) * 128 + ((kb ^ dd) << 4)) =
+                    make_uint4(vt[dd][0], vt[dd][1], vt[dd][2], vt[dd][3]);
+        }
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+
+        // ---- 2. S = Q K^T
+        if (t == 0) {
+            tc::fence_after_sync();
+            constexpr uint32_t id_s = tc::idesc_f16_f32(128, tcg::kKeys);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (ks & 3) * 32;
+                tc::mma_f16(tm, tc::desc_k_sw128(sb + tcg::kQ + (ks >> 2) * 16384 + off),
+                            tc::desc_k_sw128(sb + tcg::kKT + (ks >> 2) * (tcg::kKeys * 128) + off), id_s, ks > 0);
+            }
+            tc::commit(&bars[0]);
+        }
+        const bool ok_s = mbar_wait_bounded(&bars[0], st & 1, tcg::kWaitNs);
+        tc::fence_after_sync();
+
+        // ---- 3. this row's scores -> online softmax -> its row of P
+        float sv[64];
+        {
+            float* lo = sv;
+            tc::ld32(tm_row, *reinterpret_cast<float(*)[32]>(lo));
+            tc::ld32(tm_row + 32, *reinterpret_cast<float(*)[32]>(lo + 32));
+            tc::wait_ld(*reinterpret_cast<float(*)[32]>(lo));
+            tc::wait_ld(*reinterpret_cast<float(*)[32]>(lo + 32));
+        }
+        const bool interior = np == tcg::kPages && t0 + tcg::kKeys - 1 <= wpos0 && t0 >= wlo1;
+        float mx = -INFINITY;
+        if (interior) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                sv[j] *= cs;
+                mx = fmaxf(mx, sv[j]);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const int key = t0 + j;
+                const bool valid = j < np * kBS && rv && key >= lq && key <= pq;
+                sv[j] = valid ? sv[j] * cs : -INFINITY;
+                mx = fmaxf(mx, sv[j]);
+            }
+        }
+        const float mn = fmaxf(m, mx);
+        const float muse = mn == -INFINITY ? 0.f : mn;
+        const float alpha = fast_exp2(m - muse);
+        m = mn;
+        float ls = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint32_t pw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float p0 = fast_exp2(sv[8 * c + 2 * e] - muse), p1 = fast_exp2(sv[8 * c + 2 * e + 1] - muse);
+                ls += p0 + p1;
+                pw[e] = pack_f16x2(p0, p1);
+            }
+            *reinterpret_cast<uint4*>(sm + tcg::kKT + t * 128 + ((c ^ (t & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        }
+        l = l * alpha + ls;
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        if (__syncthreads_or(!ok_s)) {
+            fail = true;
+            break;
+        }
+
+        // ---- 4. O_tile = P V
+        if (t == 0) {
+            tc::fence_after_sync();
+            constexpr uint32_t id_o = tc::idesc_f16_f32(128, D);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_f16(tm + 64, tc::desc_k_sw128(sb + tcg::kKT + ks * 32), tc::desc_k_sw128(sb + tcg::kVT + ks * 32),
+                            id_o, ks > 0);
+            tc::commit(&bars[1]);
+        }
+        fail = !mbar_wait_bounded(&bars[1], st & 1, tcg::kWaitNs);
+        tc::fence_after_sync();
+
+        // ---- 5. fold this row's tile into the FP32 output registers
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float x[32];
+            tc::ld32(tm_row + 64 + 32 * c, x);
+            tc::wait_ld(x);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[32 * c + j] = fmaf(o[32 * c + j], alpha, x[j]);
+        }
+        tc::fence_before_sync();
+    }
+    cp_async_wait<0>();
+    fail = __syncthreads_or(fail);
+    if (fail) {
+        if (t == 0) report(a.err, FP8KV_ERR_TIMEOUT);
+    } else if (rv) {
+        const int64_t unit = (static_cast<int64_t>(b) * a.num_kv_heads + hk) * a.tiles + tile;
+        if (a.splits == 1) {
+            const float so = l > 0.f ? a.v_scale / l : 0.f;
+            uint4* orow = reinterpret_cast<uint4*>(a.out + (static_cast<int64_t>(u.q0 + r / G) * a.num_q_heads + hk * G + r % G) * D);
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                orow[c] = make_uint4(pack_bf16x2(o[8 * c] * so, o[8 * c + 1] * so), pack_bf16x2(o[8 * c + 2] * so, o[8 * c + 3] * so),
+                                     pack_bf16x2(o[8 * c + 4] * so, o[8 * c + 5] * so), pack_bf16x2(o[8 * c + 6] * so, o[8 * c + 7] * so));
+        } else {
+            const int64_t slot = (unit * a.splits + split) * a.rows + t;
+            float4* po = reinterpret_cast<float4*>(a.part_o + slot * D);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) po[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+            a.part_ml[slot] = make_float2(m, l);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::dealloc(tm, tcg::kTmemCols);
+    }
+}
+
 // Combines a unit's split partials row by row in FP32: with M the largest
 // row maximum, weight_s = 2^(m_s - M), out = v_scale * sum_s weight_s o_s /
 // sum_s weight_s l_s, rounded to bf16.  One CTA per unit, a warp per row.
@@ -496,16 +822,16 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
     if (!ok) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t unit = (static_cast<int64_t>(b) * a.num_kv_heads + hk) * a.tiles + tile;
-    for (int rr = warp; rr < kRows && u.R0 + rr < u.rows; rr += 8) {
+    for (int rr = warp; rr < a.rows && u.R0 + rr < u.rows; rr += 8) {
         const int r = u.R0 + rr;
-        const int64_t slot0 = unit * a.splits * kRows + rr;     // split s at slot0 + s * kRows
+        const int64_t slot0 = unit * a.splits * a.rows + rr;     // split s at slot0 + s * rows
         float mmax = -INFINITY;
-        for (int s = lane; s < a.splits; s += 32) mmax = fmaxf(mmax, a.part_ml[slot0 + s * kRows].x);
+        for (int s = lane; s < a.splits; s += 32) mmax = fmaxf(mmax, a.part_ml[slot0 + s * a.rows].x);
 #pragma unroll
         for (int off = 16; off; off >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, off));
         float lsum = 0.f;
         for (int s = lane; s < a.splits; s += 32) {
-            const float2 ml = a.part_ml[slot0 + s * kRows];
+            const float2 ml = a.part_ml[slot0 + s * a.rows];
             const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - mmax);
             wsm[warp][s] = wgt;
             lsum += wgt * ml.y;
@@ -521,7 +847,7 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
             for (int s = 0; s < a.splits; ++s) {
                 const float wgt = wsm[warp][s];
                 if (wgt != 0.f) {
-                    const float2 x = *reinterpret_cast<const float2*>(po + static_cast<int64_t>(s) * kRows * D + d);
+                    const float2 x = *reinterpret_cast<const float2*>(po + static_cast<int64_t>(s) * a.rows * D + d);
                     acc0 = fmaf(wgt, x.x, acc0);
                     acc1 = fmaf(wgt, x.y, acc1);
                 }
@@ -545,12 +871,17 @@ struct Plan {
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Query rows per tile for a head dimension: the tcgen05 kernel at d = 128,
+// the mma.sync kernel otherwise.
+inline int rows_per_tile(int D) { return D == 128 ? kRowsTC : kRows; }
+
 Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D, int window, int sms) {
     Plan pl;
-    pl.tiles = static_cast<int>((static_cast<int64_t>(max_q_len) * G + kRows - 1) / kRows);
+    const int rows = rows_per_tile(D);
+    pl.tiles = static_cast<int>((static_cast<int64_t>(max_q_len) * G + rows - 1) / rows);
     const int64_t units = static_cast<int64_t>(pl.tiles) * Hkv * batch;
     int64_t pages = (static_cast<int64_t>(max_seq_len) + kBS - 1) / kBS;
-    if (window > 0) pages = std::min<int64_t>(pages, (static_cast<int64_t>(window) + kRows) / kBS + 2);
+    if (window > 0) pages = std::min<int64_t>(pages, (static_cast<int64_t>(window) + rows) / kBS + 2);
     const int64_t target = 4LL * sms;
     if (units > 0 && units < target) {
         const int64_t want = (target + units - 1) / units;
@@ -558,7 +889,7 @@ Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D,
                                                                               static_cast<int64_t>(kMaxSplits)})));
     }
     if (pl.splits > 1) {
-        const size_t slots = static_cast<size_t>(units) * pl.splits * kRows;
+        const size_t slots = static_cast<size_t>(units) * pl.splits * rows;
         pl.ml = kHeader;
         pl.o = pl.ml + align256(slots * sizeof(float2));
         pl.total = pl.o + align256(slots * D * sizeof(float));
@@ -568,14 +899,16 @@ Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D,
 
 template <int D, int G>
 cudaError_t launch(const Args& a, int batch, cudaStream_t s) {
+    // d = 128 runs on tcgen05, other head sizes on mma.sync
+    void (*kernel)(const Args) = D == 128 ? paged_prefill_tc_kernel<G> : paged_prefill_kernel<D, G>;
+    const size_t smem = D == 128 ? static_cast<size_t>(tcg::kSmem) + 1024 : Geo<D>::SMEM;
     static std::atomic<uint64_t> done_mask{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
     if (bit == 0 || !(done_mask.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(paged_prefill_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(Geo<D>::SMEM));
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         done_mask.fetch_or(bit, std::memory_order_release);
     }
@@ -588,11 +921,11 @@ cudaError_t launch(const Args& a, int batch, cudaStream_t s) {
     cfg.gridDim = dim3(static_cast<unsigned>(a.tiles * a.splits), static_cast<unsigned>(a.num_kv_heads),
                        static_cast<unsigned>(batch));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Geo<D>::SMEM;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D, G>, a);
+    e = cudaLaunchKernelEx(&cfg, kernel, a);
     if (e != cudaSuccess || a.splits == 1) return e;
     cfg.gridDim = dim3(static_cast<unsigned>(a.tiles), static_cast<unsigned>(a.num_kv_heads),
                        static_cast<unsigned>(batch));
@@ -622,7 +955,7 @@ fp8kv_status check_shape(int batch, int max_q_len, int max_seq_len, int num_q_he
     if (!(head_dim == 64 || head_dim == 128 || head_dim == 256) || block_size != kBS ||
         !(G == 1 || G == 2 || G == 4 || G == 8))
         return FP8KV_ERR_UNSUPPORTED;
-    const int64_t tiles = (static_cast<int64_t>(max_q_len) * G + kRows - 1) / kRows;
+    const int64_t tiles = (static_cast<int64_t>(max_q_len) * G + kRows - 1) / kRows;   // the larger count
     if (tiles * kMaxSplits > INT32_MAX) return FP8KV_ERR_UNSUPPORTED;
     return FP8KV_OK;
 }
@@ -693,6 +1026,7 @@ extern "C" fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens,
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = num_kv_heads;
     a.tiles = pl.tiles;
+    a.rows = rows_per_tile(head_dim);
     a.splits = pl.splits;
     a.window = window > 0 ? window : 0;
     a.score_scale = sm_scale * k_scale * kLog2e;

@@ -1,0 +1,110 @@
+// Inline-PTX building blocks for the 5th-generation tensor cores of sm_103a
+// (tcgen05): tensor-memory allocation, the shared-memory matrix and
+// instruction descriptors of kind::f16 MMAs, the MMA itself, its completion
+// on an mbarrier and the tensor-memory loads of the accumulator.
+//
+// Operand layout used throughout: K-major with the 128-byte swizzle.  An
+// operand of R rows and 64 f16 columns (128 bytes per row) is one "atom
+// column": row r's 16-byte chunk c sits at r * 128 + ((c ^ (r & 7)) * 16),
+// 8-row groups 1024 bytes apart, the block 1024-byte aligned.  Wider operands
+// are several such blocks side by side along K.  One MMA consumes K = 16
+// columns (32 bytes); the next K step starts 32 bytes further into the atom.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fp8kv {
+namespace tc {
+
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled operand
+// starting at shared address `saddr` (bits: start address >> 4 in [0,14),
+// leading-dimension offset in [16,30) (unused by swizzled K-major operands),
+// stride offset >> 4 in [32,46) = 1024 bytes between 8-row groups, version 1
+// in [46,48), base offset 0, layout type 2 = 128-byte swizzle in [61,64)).
+__device__ __forceinline__ uint64_t desc_k_sw128(uint32_t saddr) {
+    uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with f16 A and B, an FP32 accumulator
+// and both operands K-major (bits: D format 1 = F32 in [4,6), A and B
+// format 0 = F16 in [7,10) and [10,13), N >> 3 in [17,23), M >> 4 in [24,29)).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
+    return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// D[tmem] (+)= A * B^T for an M x K tile of A and an N x K tile of B (both
+// K-major in shared memory), K = 16; `accumulate` == 0 overwrites D.
+// Issued by one thread.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives (once) on `bar` when every tcgen05 operation this thread issued
+// before has completed.
+__device__ __forceinline__ void commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Whole warp: allocates `ncols` (a power of two >= 32) tensor-memory columns
+// and writes their base address to `dst` in shared memory.
+__device__ __forceinline__ void alloc(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+// Whole warp: frees what alloc() returned.
+__device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy reads of them (the MMA reading operands written with st.shared).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 32 consecutive FP32 columns starting at `taddr` of this thread's lane
+// (shape 32x32b: warp w of a 4-warp group reads lanes 32w .. 32w + 31).  The
+// values are valid only after wait_ld(), which takes them as operands so
+// that no use can be scheduled before it.
+__device__ __forceinline__ void ld32(uint32_t taddr, float (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7]),
+          "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]), "=f"(r[14]), "=f"(r[15]),
+          "=f"(r[16]), "=f"(r[17]), "=f"(r[18]), "=f"(r[19]), "=f"(r[20]), "=f"(r[21]), "=f"(r[22]), "=f"(r[23]),
+          "=f"(r[24]), "=f"(r[25]), "=f"(r[26]), "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]), "=f"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void wait_ld(float (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+f"(r[0]), "+f"(r[1]), "+f"(r[2]), "+f"(r[3]), "+f"(r[4]), "+f"(r[5]), "+f"(r[6]), "+f"(r[7]),
+                   "+f"(r[8]), "+f"(r[9]), "+f"(r[10]), "+f"(r[11]), "+f"(r[12]), "+f"(r[13]), "+f"(r[14]),
+                   "+f"(r[15]), "+f"(r[16]), "+f"(r[17]), "+f"(r[18]), "+f"(r[19]), "+f"(r[20]), "+f"(r[21]),
+                   "+f"(r[22]), "+f"(r[23]), "+f"(r[24]), "+f"(r[25]), "+f"(r[26]), "+f"(r[27]), "+f"(r[28]),
+                   "+f"(r[29]), "+f"(r[30]), "+f"(r[31])
+                 :
+                 : "memory");
+}
+
+}  // namespace tc
+}  // namespace fp8kv
