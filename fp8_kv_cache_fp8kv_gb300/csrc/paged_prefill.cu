@@ -811,56 +811,87 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
 
 // Combines a unit's split partials row by row in FP32: with M the largest
 // row maximum, weight_s = 2^(m_s - M), out = v_scale * sum_s weight_s o_s /
-// sum_s weight_s l_s, rounded to bf16.  One CTA per unit, a warp per row.
+// sum_s weight_s l_s, rounded to bf16.  A CTA covers 8 rows of a unit, a
+// warp one row; each lane owns D/32 dimensions and keeps 8 splits' loads in
+// flight.  Every split writes its partial (zeros and m = -inf when it has no
+// keys for the row), so all loads are of written values.
 template <int D, int G>
 __global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
+    constexpr int PER = D / 32;   // dimensions per lane: 2, 4 or 8
     __shared__ float wsm[8][kMaxSplits];
-    const int b = blockIdx.z, hk = blockIdx.y, tile = blockIdx.x;
+    const int b = blockIdx.z, hk = blockIdx.y;
+    const int groups = a.rows / 8;
+    const int tile = blockIdx.x / groups, grp = blockIdx.x % groups;
     Unit u;
     const bool ok = make_unit<G>(a, b, tile, false, u);  // only the lengths: read before the wait
     griddep_wait();                                      // the partials are complete and visible
     if (!ok) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rr = grp * 8 + warp;                       // row within the tile
+    const int r = u.R0 + rr;
+    if (r >= u.rows) return;                             // whole warp; no CTA-wide sync follows
     const int64_t unit = (static_cast<int64_t>(b) * a.num_kv_heads + hk) * a.tiles + tile;
-    for (int rr = warp; rr < a.rows && u.R0 + rr < u.rows; rr += 8) {
-        const int r = u.R0 + rr;
-        const int64_t slot0 = unit * a.splits * a.rows + rr;     // split s at slot0 + s * rows
-        float mmax = -INFINITY;
-        for (int s = lane; s < a.splits; s += 32) mmax = fmaxf(mmax, a.part_ml[slot0 + s * a.rows].x);
+    const int64_t slot0 = unit * a.splits * a.rows + rr;  // split s at slot0 + s * rows
+    float mmax = -INFINITY;
+    for (int sp = lane; sp < a.splits; sp += 32) mmax = fmaxf(mmax, a.part_ml[slot0 + sp * a.rows].x);
 #pragma unroll
-        for (int off = 16; off; off >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, off));
-        float lsum = 0.f;
-        for (int s = lane; s < a.splits; s += 32) {
-            const float2 ml = a.part_ml[slot0 + s * a.rows];
-            const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - mmax);
-            wsm[warp][s] = wgt;
-            lsum += wgt * ml.y;
-        }
-#pragma unroll
-        for (int off = 16; off; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-        __syncwarp();
-        const float so = lsum > 0.f ? a.v_scale / lsum : 0.f;
-        const float* po = a.part_o + slot0 * D;
-        uint16_t* orow = a.out + (static_cast<int64_t>(u.q0 + r / G) * a.num_q_heads + hk * G + r % G) * D;
-        for (int d = 2 * lane; d < D; d += 64) {
-            float acc0 = 0.f, acc1 = 0.f;
-            for (int s = 0; s < a.splits; ++s) {
-                const float wgt = wsm[warp][s];
-                if (wgt != 0.f) {
-                    const float2 x = *reinterpret_cast<const float2*>(po + static_cast<int64_t>(s) * a.rows * D + d);
-                    acc0 = fmaf(wgt, x.x, acc0);
-                    acc1 = fmaf(wgt, x.y, acc1);
-                }
-            }
-            *reinterpret_cast<uint32_t*>(orow + d) = pack_bf16x2(acc0 * so, acc1 * so);
-        }
-        __syncwarp();
+    for (int off = 16; off; off >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, off));
+    float lsum = 0.f;
+    for (int sp = lane; sp < a.splits; sp += 32) {
+        const float2 ml = a.part_ml[slot0 + sp * a.rows];
+        const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - mmax);
+        wsm[warp][sp] = wgt;
+        lsum += wgt * ml.y;
     }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    __syncwarp();
+    const float so = lsum > 0.f ? a.v_scale / lsum : 0.f;
+    const float* po = a.part_o + slot0 * D + lane * PER;
+    const int64_t stride = static_cast<int64_t>(a.rows) * D;
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    int sp = 0;
+    for (; sp + 8 <= a.splits; sp += 8) {
+        float v[8][PER];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int e = 0; e < PER; e += 2) {
+                const float2 x = *reinterpret_cast<const float2*>(po + (sp + i) * stride + e);
+                v[i][e] = x.x;
+                v[i][e + 1] = x.y;
+            }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float wgt = wsm[warp][sp + i];
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] = fmaf(wgt, v[i][e], acc[e]);
+        }
+    }
+    for (; sp < a.splits; ++sp) {
+        const float wgt = wsm[warp][sp];
+#pragma unroll
+        for (int e = 0; e < PER; e += 2) {
+            const float2 x = *reinterpret_cast<const float2*>(po + sp * stride + e);
+            acc[e] = fmaf(wgt, x.x, acc[e]);
+            acc[e + 1] = fmaf(wgt, x.y, acc[e + 1]);
+        }
+    }
+    uint16_t* orow = a.out + (static_cast<int64_t>(u.q0 + r / G) * a.num_q_heads + hk * G + r % G) * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; e += 2)
+        *reinterpret_cast<uint32_t*>(orow + e) = pack_bf16x2(acc[e] * so, acc[e + 1] * so);
 }
 
 // Split plan: the tiles a sequence's chunk may need, and how many CTAs share
-// each unit's key range so that the grid fills the GPU (at least 128 keys per
-// split, at most kMaxSplits).
+// each unit's key range.  Splitting pays only while the units do not fill
+// one wave of resident CTAs; the count is then chosen to minimise
+//     waves(units * splits) * (pages per split + kSplitCtaPages) (+ kMergePages if split)
+// where kSplitCtaPages stands for a CTA's fixed cost (query tile, first load
+// latency, partial write) and kMergePages for the merge kernel, both in
+// units of one page's work; at least 128 keys per split, at most kMaxSplits.
 struct Plan {
     int tiles = 0;
     int splits = 1;
@@ -869,25 +900,41 @@ struct Plan {
     size_t total = kHeader;
 };
 
+constexpr int64_t kSplitCtaPages = 8;
+constexpr int64_t kMergePages = 4;
+
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Query rows per tile for a head dimension: the tcgen05 kernel at d = 128,
 // the mma.sync kernel otherwise.
 inline int rows_per_tile(int D) { return D == 128 ? kRowsTC : kRows; }
 
-Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D, int window, int sms) {
+int choose_splits(int64_t units, int64_t pages, int64_t slots) {
+    if (units <= 0 || slots <= 0 || units >= slots) return 1;
+    auto cost = [&](int64_t sp) {
+        const int64_t waves = (units * sp + slots - 1) / slots;
+        return waves * ((pages + sp - 1) / sp + kSplitCtaPages) + (sp > 1 ? kMergePages : 0);
+    };
+    int best = 1;
+    int64_t best_cost = cost(1);
+    for (int sp = 2; sp <= kMaxSplits && static_cast<int64_t>(sp) * kMinSplitPages <= pages; ++sp) {
+        const int64_t c = cost(sp);
+        if (c < best_cost) {
+            best = sp;
+            best_cost = c;
+        }
+    }
+    return best;
+}
+
+Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D, int window, int sms, int per_sm) {
     Plan pl;
     const int rows = rows_per_tile(D);
     pl.tiles = static_cast<int>((static_cast<int64_t>(max_q_len) * G + rows - 1) / rows);
     const int64_t units = static_cast<int64_t>(pl.tiles) * Hkv * batch;
     int64_t pages = (static_cast<int64_t>(max_seq_len) + kBS - 1) / kBS;
     if (window > 0) pages = std::min<int64_t>(pages, (static_cast<int64_t>(window) + rows) / kBS + 2);
-    const int64_t target = 4LL * sms;
-    if (units > 0 && units < target) {
-        const int64_t want = (target + units - 1) / units;
-        pl.splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({want, pages / kMinSplitPages,
-                                                                              static_cast<int64_t>(kMaxSplits)})));
-    }
+    pl.splits = choose_splits(units, pages, static_cast<int64_t>(sms) * per_sm);
     if (pl.splits > 1) {
         const size_t slots = static_cast<size_t>(units) * pl.splits * rows;
         pl.ml = kHeader;
@@ -897,11 +944,61 @@ Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D,
     return pl;
 }
 
+// The prefill kernel for (D, G) and its dynamic shared memory.
+template <int D, int G>
+void kernel_of(void (**fn)(const Args), size_t* smem) {
+    if constexpr (D == 128) {
+        *fn = paged_prefill_tc_kernel<G>;
+        *smem = static_cast<size_t>(tcg::kSmem) + 1024;
+    } else {
+        *fn = paged_prefill_kernel<D, G>;
+        *smem = Geo<D>::SMEM;
+    }
+}
+
+template <int D>
+bool kernel_of_g(int G, void (**fn)(const Args), size_t* smem) {
+    switch (G) {
+        case 1: kernel_of<D, 1>(fn, smem); return true;
+        case 2: kernel_of<D, 2>(fn, smem); return true;
+        case 4: kernel_of<D, 4>(fn, smem); return true;
+        case 8: kernel_of<D, 8>(fn, smem); return true;
+        default: return false;
+    }
+}
+
+// Resident CTAs per SM of the prefill kernel for (D, G) on the current
+// device (the occupancy calculator, with the kernel's shared-memory opt-in
+// applied); 0 on failure.  Cached per device.
+int resident_per_sm(int D, int G) {
+    static std::atomic<int> cache[3][4][64] = {};
+    const int di = D == 64 ? 0 : (D == 128 ? 1 : 2);
+    const int gi = G == 1 ? 0 : (G == 2 ? 1 : (G == 4 ? 2 : 3));
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[di][gi][dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    void (*fn)(const Args) = nullptr;
+    size_t smem = 0;
+    const bool ok = D == 64 ? kernel_of_g<64>(G, &fn, &smem)
+                            : (D == 128 ? kernel_of_g<128>(G, &fn, &smem) : kernel_of_g<256>(G, &fn, &smem));
+    if (!ok) return 0;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem) != cudaSuccess || n < 1) return 0;
+    if (dev >= 0 && dev < 64) cache[di][gi][dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
 template <int D, int G>
 cudaError_t launch(const Args& a, int batch, cudaStream_t s) {
     // d = 128 runs on tcgen05, other head sizes on mma.sync
-    void (*kernel)(const Args) = D == 128 ? paged_prefill_tc_kernel<G> : paged_prefill_kernel<D, G>;
-    const size_t smem = D == 128 ? static_cast<size_t>(tcg::kSmem) + 1024 : Geo<D>::SMEM;
+    void (*kernel)(const Args) = nullptr;
+    size_t smem = 0;
+    kernel_of<D, G>(&kernel, &smem);
     static std::atomic<uint64_t> done_mask{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -927,7 +1024,7 @@ cudaError_t launch(const Args& a, int batch, cudaStream_t s) {
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kernel, a);
     if (e != cudaSuccess || a.splits == 1) return e;
-    cfg.gridDim = dim3(static_cast<unsigned>(a.tiles), static_cast<unsigned>(a.num_kv_heads),
+    cfg.gridDim = dim3(static_cast<unsigned>(a.tiles * (a.rows / 8)), static_cast<unsigned>(a.num_kv_heads),
                        static_cast<unsigned>(batch));
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
@@ -970,8 +1067,10 @@ extern "C" size_t fp8kv_paged_prefill_workspace_size(int batch, int max_q_len, i
         return 0;
     int sms = 0;
     if (fp8kv::device_sms(&sms) != 0) return 0;
-    return make_plan(batch, max_q_len, max_seq_len, num_q_heads / num_kv_heads, num_kv_heads, head_dim,
-                     window > 0 ? window : 0, sms)
+    const int G = num_q_heads / num_kv_heads;
+    const int per_sm = resident_per_sm(head_dim, G);
+    if (per_sm < 1) return 0;
+    return make_plan(batch, max_q_len, max_seq_len, G, num_kv_heads, head_dim, window > 0 ? window : 0, sms, per_sm)
         .total;
 }
 
@@ -1003,7 +1102,10 @@ extern "C" fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens,
     int sms = 0;
     if (fp8kv::device_sms(&sms) != 0) return FP8KV_ERR_CUDA;
     const int G = num_q_heads / num_kv_heads;
-    const Plan pl = make_plan(batch, max_q_len, max_seq_len, G, num_kv_heads, head_dim, window > 0 ? window : 0, sms);
+    const int per_sm = resident_per_sm(head_dim, G);
+    if (per_sm < 1) return FP8KV_ERR_CUDA;
+    const Plan pl = make_plan(batch, max_q_len, max_seq_len, G, num_kv_heads, head_dim, window > 0 ? window : 0, sms,
+                              per_sm);
     if (!workspace || workspace_bytes < pl.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return FP8KV_ERR_WORKSPACE;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
