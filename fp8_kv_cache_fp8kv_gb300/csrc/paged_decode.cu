@@ -92,7 +92,8 @@ struct DecodeArgs {
     int max_seq_len;
     int batch;
     int num_q_heads;
-    int num_kv_heads;
+    int num_kv_heads;           // units per sequence: the cache's kv heads << kv_shift
+    int kv_shift;               // 1 when g = 16 runs as two units of 8 query heads per cache head
     int window;
     float score_scale;          // sm_scale * k_scale * log2(e)
     float v_scale;
@@ -271,11 +272,11 @@ __device__ __forceinline__ void codes4_to_f16x2x2(uint32_t w, uint32_t& lo, uint
 // Score multiplier (sm_scale * k_scale * log2 e, multiplied in that order as
 // the host does for the per-tensor scale) and V scale of kv head hk.
 __device__ __forceinline__ float unit_score_scale(const DecodeArgs& a, int hk) {
-    return a.k_scales ? (a.sm_scale * __ldg(a.k_scales + hk)) * kLog2e : a.score_scale;
+    return a.k_scales ? (a.sm_scale * __ldg(a.k_scales + (hk >> a.kv_shift))) * kLog2e : a.score_scale;
 }
 
 __device__ __forceinline__ float unit_v_scale(const DecodeArgs& a, int hk) {
-    return a.v_scales ? __ldg(a.v_scales + hk) : a.v_scale;
+    return a.v_scales ? __ldg(a.v_scales + (hk >> a.kv_shift)) : a.v_scale;
 }
 
 template <int D, int G>
@@ -1003,7 +1004,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         int seg_b = w.b, seg_hk = w.hk;
         bool seg_last = appending && seg_reaches_end(w);
         NewRow<D> nrow;
-        if (seg_last) load_new_row<D>(nrow, new_rows + (static_cast<int64_t>(w.b) * Hkv + w.hk) * D, lane);
+        // the cache (and the new rows) have Hkv >> kv_shift heads; unit hk reads head hk >> kv_shift
+        const int kvs = a.kv_shift, Hc = Hkv >> kvs;
+        if (seg_last) load_new_row<D>(nrow, new_rows + (static_cast<int64_t>(w.b) * Hc + (w.hk >> kvs)) * D, lane);
         bool more = true;
         while (ok && more) {
             const int cur = nxt;
@@ -1026,7 +1029,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     seg_b = w.b;
                     seg_hk = w.hk;
                     seg_last = appending && seg_reaches_end(w);
-                    if (seg_last) load_new_row<D>(nrow, new_rows + (static_cast<int64_t>(w.b) * Hkv + w.hk) * D, lane);
+                    if (seg_last)
+                        load_new_row<D>(nrow, new_rows + (static_cast<int64_t>(w.b) * Hc + (w.hk >> kvs)) * D, lane);
                 }
             }
             nxt = more ? load_block_id(row + p0, lane, np_seg - p0, a.num_blocks, a.err) : 0;
@@ -1035,8 +1039,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const int id = my_ids[nb - 1];
                 if (id >= 0) {
                     const int L = lens[batch_b];
-                    uint8_t* dst_row = cache + ((static_cast<int64_t>(id) * Hkv + hk) * kBS + (L - 1) % kBS) * D;
-                    store_new_row<D, E5M2>(batch_row, dst_row, lane, head_scales ? __ldg(head_scales + hk) : scale_raw);
+                    // with two units per cache head both write the same bytes: identical values
+                    uint8_t* dst_row = cache + ((static_cast<int64_t>(id) * Hc + (hk >> kvs)) * kBS + (L - 1) % kBS) * D;
+                    store_new_row<D, E5M2>(batch_row, dst_row, lane,
+                                           head_scales ? __ldg(head_scales + (hk >> kvs)) : scale_raw);
                     fence_proxy_async_global();
                 }
                 __syncwarp();
@@ -1059,8 +1065,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         const int id = max(my_ids[q + p], 0);
 #pragma unroll
                         for (int h = 0; h < Gm::HALVES; ++h)
-                            tma_load_4d(dst + p * Gm::PAGE + h * Gm::BOX, tm, &full_bar[pw * S + slot], h * 128, 0, hk, id,
-                                        pol);
+                            tma_load_4d(dst + p * Gm::PAGE + h * Gm::BOX, tm, &full_bar[pw * S + slot], h * 128, 0,
+                                        hk >> kvs, id, pol);
                     }
                     ++st;
                 }
@@ -1663,7 +1669,22 @@ bool default_is_cuda_cores(int /*head_dim*/, int /*G*/) { return false; }
 
 bool supported(int head_dim, int block_size, int G) {
     return (head_dim == 64 || head_dim == 128 || head_dim == 256) && block_size == kBS &&
-           (G == 1 || G == 2 || G == 4 || G == 8);
+           (G == 1 || G == 2 || G == 4 || G == 8 || G == 16);
+}
+
+// How the kernels see the heads: g = 16 runs as two units of 8 query heads
+// per cache head (each reads the head's pages; the kernels are built for
+// g <= 8, whose heads fill the MMA's n side).
+struct HeadMap {
+    int units_per_seq;  // kv-head units per sequence
+    int g;              // query heads per unit
+    int shift;          // unit -> cache head: hk >> shift
+};
+
+HeadMap head_map(int num_q_heads, int num_kv_heads) {
+    const int G = num_q_heads / num_kv_heads;
+    if (G == 16) return {2 * num_kv_heads, 8, 1};
+    return {num_kv_heads, G, 0};
 }
 
 }  // namespace fp8kv
@@ -1677,8 +1698,9 @@ extern "C" size_t fp8kv_paged_decode_workspace_size(int batch, int num_q_heads, 
     if (!supported(head_dim, block_size, num_q_heads / num_kv_heads)) return 0;
     int sms = 0;
     if (device_sms(&sms) != 0) return 0;
-    const Plan p = make_plan(batch, num_kv_heads, head_dim, max_seq_len, window, sms);
-    return ws_layout(batch, num_q_heads, num_kv_heads, head_dim, p).total;
+    const HeadMap hm = head_map(num_q_heads, num_kv_heads);
+    const Plan p = make_plan(batch, hm.units_per_seq, head_dim, max_seq_len, window, sms);
+    return ws_layout(batch, num_q_heads, hm.units_per_seq, head_dim, p).total;
 }
 
 namespace {
@@ -1697,9 +1719,10 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
     if (!std::isfinite(k_scale) || !(k_scale > 0) || !std::isfinite(v_scale) || !(v_scale > 0) ||
         !std::isfinite(sm_scale))
         return FP8KV_ERR_INVALID_ARG;
-    const int G = num_q_heads / num_kv_heads;
-    if (!supported(head_dim, block_size, G)) return FP8KV_ERR_UNSUPPORTED;
+    if (!supported(head_dim, block_size, num_q_heads / num_kv_heads)) return FP8KV_ERR_UNSUPPORTED;
     if (es == 2 && head_dim == 256) return FP8KV_ERR_UNSUPPORTED;  // a bf16 page of 8 KB exceeds a stage
+    const HeadMap hm = head_map(num_q_heads, num_kv_heads);
+    const int G = hm.g;
     if (engine != FP8KV_ENGINE_DEFAULT && engine != FP8KV_ENGINE_TENSOR_CORES && engine != FP8KV_ENGINE_CUDA_CORES)
         return FP8KV_ERR_INVALID_ARG;
     const bool simt = engine == FP8KV_ENGINE_CUDA_CORES ||
@@ -1723,8 +1746,8 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         return FP8KV_ERR_INVALID_ARG;
     int sms = 0;
     if (device_sms(&sms) != 0) return FP8KV_ERR_CUDA;
-    const WsLayout w = ws_layout(batch, num_q_heads, num_kv_heads, head_dim,
-                                 make_plan(batch, num_kv_heads, head_dim, max_seq_len, window, sms));
+    const WsLayout w = ws_layout(batch, num_q_heads, hm.units_per_seq, head_dim,
+                                 make_plan(batch, hm.units_per_seq, head_dim, max_seq_len, window, sms));
     if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return FP8KV_ERR_WORKSPACE;
 
@@ -1739,7 +1762,7 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
     // stream, reusing the workspace.
     for (int b0 = 0; b0 < batch; b0 += kMaxBatch) {
         const int nb = std::min(kMaxBatch, batch - b0);
-        const Plan p = make_plan(nb, num_kv_heads, head_dim, max_seq_len, window, sms);
+        const Plan p = make_plan(nb, hm.units_per_seq, head_dim, max_seq_len, window, sms);
         DecodeArgs a;
         a.q = static_cast<const uint16_t*>(q) + static_cast<int64_t>(b0) * num_q_heads * head_dim;
         a.k_new = k_new ? static_cast<const uint16_t*>(k_new) + static_cast<int64_t>(b0) * num_kv_heads * head_dim
@@ -1765,7 +1788,8 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         a.max_seq_len = max_seq_len;
         a.batch = nb;
         a.num_q_heads = num_q_heads;
-        a.num_kv_heads = num_kv_heads;
+        a.num_kv_heads = hm.units_per_seq;
+        a.kv_shift = hm.shift;
         a.window = window > 0 ? window : 0;
         a.score_scale = sm_scale * k_scale * kLog2e;
         a.v_scale = v_scale;
@@ -1942,8 +1966,9 @@ extern "C" fp8kv_status fp8kv_paged_decode_noalloc(const void* q, const uint8_t*
     if (batch == 0) return FP8KV_OK;
     int sms = 0;
     if (device_sms(&sms) != 0) return FP8KV_ERR_CUDA;
-    const Plan p = make_plan(batch, num_kv_heads, head_dim, max_seq_len, window, sms);
-    const WsLayout w = ws_layout(batch, num_q_heads, num_kv_heads, head_dim, p);
+    const HeadMap hm = head_map(num_q_heads, num_kv_heads);
+    const Plan p = make_plan(batch, hm.units_per_seq, head_dim, max_seq_len, window, sms);
+    const WsLayout w = ws_layout(batch, num_q_heads, hm.units_per_seq, head_dim, p);
     if (w.total > kStaticScratchBytes) return FP8KV_ERR_WORKSPACE;  // problem too large for the fixed array
     void* scratch = static_scratch_address();
     if (scratch == nullptr) return FP8KV_ERR_CUDA;

@@ -963,6 +963,7 @@ bool kernel_of_g(int G, void (**fn)(const Args), size_t* smem) {
         case 2: kernel_of<D, 2>(fn, smem); return true;
         case 4: kernel_of<D, 4>(fn, smem); return true;
         case 8: kernel_of<D, 8>(fn, smem); return true;
+        case 16: kernel_of<D, 16>(fn, smem); return true;
         default: return false;
     }
 }
@@ -971,9 +972,9 @@ bool kernel_of_g(int G, void (**fn)(const Args), size_t* smem) {
 // device (the occupancy calculator, with the kernel's shared-memory opt-in
 // applied); 0 on failure.  Cached per device.
 int resident_per_sm(int D, int G) {
-    static std::atomic<int> cache[3][4][64] = {};
+    static std::atomic<int> cache[3][5][64] = {};
     const int di = D == 64 ? 0 : (D == 128 ? 1 : 2);
-    const int gi = G == 1 ? 0 : (G == 2 ? 1 : (G == 4 ? 2 : 3));
+    const int gi = G == 1 ? 0 : (G == 2 ? 1 : (G == 4 ? 2 : (G == 8 ? 3 : 4)));
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (dev >= 0 && dev < 64) {
@@ -1038,6 +1039,7 @@ cudaError_t launch_g(int G, const Args& a, int batch, cudaStream_t s) {
         case 2: return launch<D, 2>(a, batch, s);
         case 4: return launch<D, 4>(a, batch, s);
         case 8: return launch<D, 8>(a, batch, s);
+        case 16: return launch<D, 16>(a, batch, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -1050,7 +1052,7 @@ fp8kv_status check_shape(int batch, int max_q_len, int max_seq_len, int num_q_he
         return FP8KV_ERR_INVALID_ARG;
     const int G = num_q_heads / num_kv_heads;
     if (!(head_dim == 64 || head_dim == 128 || head_dim == 256) || block_size != kBS ||
-        !(G == 1 || G == 2 || G == 4 || G == 8))
+        !(G == 1 || G == 2 || G == 4 || G == 8 || G == 16))
         return FP8KV_ERR_UNSUPPORTED;
     const int64_t tiles = (static_cast<int64_t>(max_q_len) * G + kRows - 1) / kRows;   // the larger count
     if (tiles * kMaxSplits > INT32_MAX) return FP8KV_ERR_UNSUPPORTED;

@@ -137,7 +137,9 @@ fp8kv_status fp8kv_read_error(void* workspace, uint32_t* code, void* stream);
  *   workspace      >= fp8kv_paged_decode_workspace_size(...) bytes, 256-B
  *                  aligned, zero-filled before first use (fp8kv_workspace_init)
  * Supported: head_dim in {64, 128, 256}; block_size == 16;
- *            g in {1, 2, 4, 8}; num_blocks * num_kv_heads < 2^31.
+ *            g in {1, 2, 4, 8, 16}; num_blocks * num_kv_heads < 2^31.  At g = 16
+ *            each kv head runs as two units of 8 query heads, each reading the
+ *            head's pages (the kernels put a unit's heads on the MMA's n side).
  */
 fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
                                 int64_t num_blocks, const int32_t* block_tables,
@@ -259,7 +261,7 @@ fp8kv_status fp8kv_paged_decode_engine(const void* q, const uint8_t* k_cache, co
  *
  * Scores and P.V run on the tensor cores with bf16 operands (P rounded to
  * bf16) and FP32 accumulation, each stage's tile added into FP32 registers.
- * Supported: head_dim in {64, 128}; block_size == 16; g in {1, 2, 4, 8}.
+ * Supported: head_dim in {64, 128}; block_size == 16; g in {1, 2, 4, 8, 16}.
  */
 fp8kv_status fp8kv_paged_decode_bf16(const void* q, const void* k_cache, const void* v_cache,
                                      int64_t num_blocks, const int32_t* block_tables,
@@ -362,7 +364,7 @@ fp8kv_status fp8kv_paged_decode_noalloc(const void* q, const uint8_t* k_cache, c
  *                  sequence is clamped, or skipped if its rows would fall
  *                  outside q / out).  Calls that share a workspace must be
  *                  ordered.  Missing or too small: FP8KV_ERR_WORKSPACE.
- * Supported: head_dim in {64, 128, 256}; block_size == 16; g in {1, 2, 4, 8};
+ * Supported: head_dim in {64, 128, 256}; block_size == 16; g in {1, 2, 4, 8, 16};
  *            num_blocks * num_kv_heads < 2^31.  batch == 0, max_q_len == 0 or
  *            num_q_tokens == 0 is a no-op.
  */

@@ -43,7 +43,7 @@ def _decode(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(d=96), 2), (dict(d=512), 2), (dict(bs=32), 2), (dict(hq=128, hkv=8), 2),
+    (dict(d=96), 2), (dict(d=512), 2), (dict(bs=32), 2), (dict(hq=256, hkv=8), 2),
     (dict(hq=30, hkv=8), 1), (dict(ks=0.0), 1), (dict(vs=float("nan")), 1), (dict(sm=float("inf")), 1),
     (dict(q=None), 1), (dict(out=None), 1), (dict(bt=None), 1), (dict(q=MISALIGNED), 1),
     (dict(k=MISALIGNED), 1), (dict(mb=4, msl=128), 1), (dict(B=-1), 1), (dict(nb=0), 1),
@@ -84,7 +84,7 @@ def _bf16(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(d=256), 2), (dict(d=96), 2), (dict(bs=32), 2), (dict(hq=128, hkv=8), 2), (dict(hq=30, hkv=8), 1),
+    (dict(d=256), 2), (dict(d=96), 2), (dict(bs=32), 2), (dict(hq=256, hkv=8), 2), (dict(hq=30, hkv=8), 1),
     (dict(sm=float("nan")), 1), (dict(q=None), 1), (dict(k=MISALIGNED), 1), (dict(mb=4, msl=128), 1),
     (dict(B=0, q=None, out=None), 0),
 ])
@@ -176,7 +176,7 @@ def _prefill(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(d=96), 2), (dict(d=512), 2), (dict(bs=32), 2), (dict(hq=128, hkv=8), 2),
+    (dict(d=96), 2), (dict(d=512), 2), (dict(bs=32), 2), (dict(hq=256, hkv=8), 2),
     (dict(hq=30, hkv=8), 1), (dict(ks=0.0), 1), (dict(vs=float("nan")), 1), (dict(sm=float("inf")), 1),
     (dict(q=None), 1), (dict(out=None), 1), (dict(qs=None), 1), (dict(q=MISALIGNED), 1),
     (dict(v=MISALIGNED), 1), (dict(mb=4, msl=128), 1), (dict(mq=200), 1),

@@ -73,7 +73,7 @@ def test_bf16_small_cases_match_oracle(base, lens, windows):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("g", [1, 2, 4, 8])
+@pytest.mark.parametrize("g", [1, 2, 4, 8, 16])
 def test_bf16_every_supported_head_layout(d, g):
     hkv = 2
     shape = workload.LayerShape(f"b{d}_{g}", hkv * g, hkv, d, 3, 1, 1, (0,))

@@ -98,7 +98,7 @@ def test_decode_small_cases_match_oracle(base, lens, windows, engine):
 
 @pytest.mark.parametrize("engine", ENGINES)
 @pytest.mark.parametrize("d", [64, 128, 256])
-@pytest.mark.parametrize("g", [1, 2, 4, 8])
+@pytest.mark.parametrize("g", [1, 2, 4, 8, 16])
 def test_decode_every_supported_head_layout(d, g, engine):
     hkv = 2
     shape = workload.LayerShape(f"t{d}_{g}", hkv * g, hkv, d, 3, 1, 1, (0,))
