@@ -487,59 +487,86 @@ __global__ void __launch_bounds__(kThreads) paged_prefill_kernel(const Args a) {
 }
 
 // ---------------------------------------------------------------------------
-// d = 128 on the 5th-generation tensor cores (tcgen05).
+// d = 64 and d = 128 on the 5th-generation tensor cores (tcgen05).
 //
 // A unit is 128 query rows; thread t of the 4 warps owns row t, which is
 // TMEM lane t of both accumulators.  Per stage of 64 keys (4 pages):
 //   1. the stage's fp8 K and V pages (cp.async into a 2-slot staging ring)
-//      are converted into f16 operand tiles, K as 64 keys x 128 dims and V
-//      transposed as 128 dims x 64 keys, both K-major with the 128-byte
-//      swizzle (the Q tile, 128 rows x 128 dims, is built once);
-//   2. one thread issues S = Q K^T (M = 128, N = 64: 8 MMAs of K = 16) into
-//      TMEM columns [0, 64) and commits it to an mbarrier;
+//      are converted into f16 operand tiles, K as 64 keys x d and V
+//      transposed as d x 64 keys, both K-major with the 128-byte swizzle
+//      (the Q tile, 128 rows x d, is built once);
+//   2. one thread issues S = Q K^T (M = 128, N = 64: d/16 MMAs of K = 16)
+//      into TMEM columns [0, 64) and commits it to an mbarrier;
 //   3. each thread loads its row of S, masks it, runs the online softmax in
 //      log2 units and writes its row of P (f16) over the K tile, which the
 //      finished score MMAs no longer need;
-//   4. one thread issues O_tile = P V (M = 128, N = 128: 4 MMAs) into TMEM
-//      columns [64, 192);
+//   4. one thread issues O_tile = P V (M = 128, N = d: 4 MMAs) into TMEM
+//      columns [64, 64 + d);
 //   5. each thread loads its row of O_tile and folds it into FP32 registers,
 //      O = O * alpha + O_tile: the two-level accumulation.
 namespace tcg {
 constexpr int kKeys = 64;                       // keys per stage
 constexpr int kPages = kKeys / kBS;             // 4 pages per stage
-constexpr int kQ = 0;                           // Q tile: 2 blocks x 128 rows x 128 B
-constexpr int kKT = kQ + 2 * 128 * 128;         // K tile: 2 blocks x 64 keys x 128 B (P tile aliases it)
-constexpr int kVT = kKT + 2 * kKeys * 128;      // V^T tile: 128 dims x 128 B
-constexpr int kStg = kVT + 128 * 128;           // staging: 2 slots x (K 8 KB, V 8 KB)
-constexpr int kStgSlot = 2 * kKeys * 128;
-constexpr int kSmem = kStg + 2 * kStgSlot;      // 96 KB (+ 1 KB for alignment)
-constexpr uint32_t kTmemCols = 256;             // S at [0, 64), O_tile at [64, 192)
 constexpr uint64_t kWaitNs = 500000000ull;      // bounded waits on the MMA barriers
 }  // namespace tcg
 
+template <int D>
+struct TcGeo {
+    static constexpr int NB = D / 64;                             // 128-byte atom columns of a d-wide f16 row
+    static constexpr int QT = 0;                                  // Q tile: NB blocks x 128 rows x 128 B
+    static constexpr int KT = QT + NB * 128 * 128;                // K tile: NB blocks x 64 keys x 128 B; P aliases it
+    static constexpr int KP = NB * tcg::kKeys * 128 > 128 * 128 ? NB * tcg::kKeys * 128 : 128 * 128;
+    static constexpr int VT = KT + KP;                            // V^T tile: d rows x 128 B
+    static constexpr int STG = VT + D * 128;                      // staging: 2 slots x (K, V: 64 keys x d bytes)
+    static constexpr int SLOT = 2 * tcg::kKeys * D;
+    static constexpr int SMEM = STG + 2 * SLOT;                   // 96 KB at d = 128, 56 KB at d = 64
+    static constexpr uint32_t COLS = D == 128 ? 256 : 128;        // S at [0, 64), O_tile at [64, 64 + d)
+    static constexpr int CPR = D / 16;                            // 16-byte chunks per staged key row
+};
+
+// Staged key row k, 16-byte chunk c: the XOR keeps the conversions' reads free
+// of bank conflicts (8 consecutive keys per K read; 8 keys 8 apart per V read).
+template <int D>
+__device__ __forceinline__ uint32_t stg_k(int k, int c) {
+    if constexpr (D == 128) return k * 128 + ((c ^ (k & 7)) << 4);
+    else return k * 64 + ((c ^ ((k >> 1) & 3)) << 4);
+}
+template <int D>
+__device__ __forceinline__ uint32_t stg_v(int k, int c) {
+    if constexpr (D == 128) return k * 128 + ((c ^ ((k >> 3) & 7)) << 4);
+    else return k * 64 + ((c ^ ((k >> 3) & 3)) << 4);
+}
+// The same address for a key k = 8 kb + i of key block kb.
+template <int D>
+__device__ __forceinline__ uint32_t stg_v_kb(int k, int kb, int c) {
+    if constexpr (D == 128) return k * 128 + ((c ^ kb) << 4);
+    else return k * 64 + ((c ^ (kb & 3)) << 4);
+}
+
 // Pages [pg, pg + np) of (block-table row bt, kv head hk) into staging slot
-// `dst`: key k of the stage is row k (128 bytes).  K chunk c of row k sits at
-// c ^ (k & 7), V chunk c at c ^ ((k >> 3) & 7), so that both conversions
-// below read without bank conflicts.  A block id outside [0, num_blocks)
-// reads block 0 and is reported.
+// `dst` (K rows, then V rows).  A block id outside [0, num_blocks) reads
+// block 0 and is reported.
+template <int D>
 __device__ __forceinline__ void load_stage_tc(const Args& a, const int32_t* bt, int hk, int pg, int np, uint32_t dst) {
-    for (int i = threadIdx.x; i < np * 128; i += 128) {
-        const int p = i >> 7, ci = i & 127;
+    using Tg = TcGeo<D>;
+    constexpr int kChunks = kBS * Tg::CPR;      // 16-byte chunks per page
+    for (int i = threadIdx.x; i < np * kChunks; i += 128) {
+        const int p = i / kChunks, ci = i % kChunks;
         int id = __ldg(bt + pg + p);
         if (id < 0 || id >= a.num_blocks) {
             if (ci == 0) report(a.err, FP8KV_ERR_INVALID_ARG);
             id = 0;
         }
-        const int64_t base = (static_cast<int64_t>(id) * a.num_kv_heads + hk) * (kBS * 128);
-        const int r = ci >> 3, c = ci & 7, k = p * kBS + r;
-        cp_async16(dst + k * 128 + ((c ^ (k & 7)) << 4), a.k_cache + base + r * 128 + c * 16);
-        cp_async16(dst + tcg::kKeys * 128 + k * 128 + ((c ^ ((k >> 3) & 7)) << 4), a.v_cache + base + r * 128 + c * 16);
+        const int64_t base = (static_cast<int64_t>(id) * a.num_kv_heads + hk) * (kBS * D);
+        const int r = ci / Tg::CPR, c = ci % Tg::CPR, k = p * kBS + r;
+        cp_async16(dst + stg_k<D>(k, c), a.k_cache + base + r * D + c * 16);
+        cp_async16(dst + tcg::kKeys * D + stg_v<D>(k, c), a.v_cache + base + r * D + c * 16);
     }
 }
 
-template <int G>
+template <int D, int G>
 __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
-    constexpr int D = 128;
+    using Tg = TcGeo<D>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bars[2];
     __shared__ uint32_t tmem_base;
@@ -564,7 +591,7 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
     const int sp1 = pg0 + static_cast<int>(static_cast<int64_t>(split + 1) * np_all / a.splits);
     const int nst = (sp1 - sp0 + tcg::kPages - 1) / tcg::kPages;
     const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
-    if (nst > 0) load_stage_tc(a, bt, hk, sp0, min(tcg::kPages, sp1 - sp0), sb + tcg::kStg);
+    if (nst > 0) load_stage_tc<D>(a, bt, hk, sp0, min(tcg::kPages, sp1 - sp0), sb + Tg::STG);
     cp_async_commit();
 
     // ---- this thread's query row into the Q tile as f16, pre-scaled by a
@@ -574,12 +601,13 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
     float cs;
     int pq, lq;
     {
+        constexpr int NC = D / 8;  // 16-byte chunks of the bf16 row (8 values each)
         const int tok = rv ? r / G : 0, hq = hk * G + (rv ? r % G : 0);
         const uint4* qrow = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(u.q0 + tok) * a.num_q_heads + hq) * D);
-        uint4 qv[16];
+        uint4 qv[NC];
         float qmax = 0.f;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < NC; ++c) {
             qv[c] = rv ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
             const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
 #pragma unroll
@@ -593,13 +621,13 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
         }
         const float up = __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < NC; ++c) {
             const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
             uint32_t f[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 f[e] = pack_f16x2(bf16_to_f32(w4[e] & 0xFFFF) * up, bf16_to_f32(w4[e] >> 16) * up);
-            *reinterpret_cast<uint4*>(sm + tcg::kQ + (c >> 3) * 16384 + t * 128 + (((c & 7) ^ (t & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(sm + Tg::QT + (c >> 3) * 16384 + t * 128 + (((c & 7) ^ (t & 7)) << 4)) =
                 make_uint4(f[0], f[1], f[2], f[3]);
         }
         cs = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
@@ -613,7 +641,7 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
     const int wpos1 = u.L - u.n + max(0, min(wr0 + 31, u.rows - 1)) / G;
     const int wlo1 = (a.window > 0 && wpos1 + 1 > a.window) ? wpos1 + 1 - a.window : 0;
 
-    if (warp == 0) tc::alloc(&tmem_base, tcg::kTmemCols);
+    if (warp == 0) tc::alloc(&tmem_base, Tg::COLS);
     tc::fence_proxy_async_smem();  // the Q tile is read by the tensor cores
     tc::fence_before_sync();
     __syncthreads();
@@ -633,33 +661,37 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
             break;
         }
         if (st + 1 < nst)
-            load_stage_tc(a, bt, hk, sp0 + (st + 1) * tcg::kPages, min(tcg::kPages, sp1 - sp0 - (st + 1) * tcg::kPages),
-                          sb + tcg::kStg + ((st + 1) & 1) * tcg::kStgSlot);
+            load_stage_tc<D>(a, bt, hk, sp0 + (st + 1) * tcg::kPages,
+                             min(tcg::kPages, sp1 - sp0 - (st + 1) * tcg::kPages),
+                             sb + Tg::STG + ((st + 1) & 1) * Tg::SLOT);
         cp_async_commit();
         const int pgs = sp0 + st * tcg::kPages;
         const int np = min(tcg::kPages, sp1 - pgs);
         const int t0 = pgs * kBS;
-        const uint8_t* stg = sm + tcg::kStg + (st & 1) * tcg::kStgSlot;
+        const uint8_t* stg = sm + Tg::STG + (st & 1) * Tg::SLOT;
 
-        // ---- 1a. K: thread t converts dims [64h, 64h + 64) of key k
+        // ---- 1a. K: thread t converts CH staged chunks (16 dims each) of key t & 63
         {
-            const int k = t & 63, h = t >> 6;
+            constexpr int CH = D / 32;                        // 4 at d = 128, 2 at d = 64
+            const int k = t & 63, part = t >> 6;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint4 x = *reinterpret_cast<const uint4*>(stg + k * 128 + (((4 * h + i) ^ (k & 7)) << 4));
+            for (int i = 0; i < CH; ++i) {
+                const int c = part * CH + i;                   // staged chunk: dims 16c .. 16c + 15
+                const uint4 x = *reinterpret_cast<const uint4*>(stg + stg_k<D>(k, c));
                 uint32_t f[8];
                 e4m3x4_to_f16x2x2(x.x, f[0], f[1]);
                 e4m3x4_to_f16x2x2(x.y, f[2], f[3]);
                 e4m3x4_to_f16x2x2(x.z, f[4], f[5]);
                 e4m3x4_to_f16x2x2(x.w, f[6], f[7]);
-                uint8_t* dst = sm + tcg::kKT + h * (tcg::kKeys * 128) + k * 128;
-                *reinterpret_cast<uint4*>(dst + (((2 * i) ^ (k & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
-                *reinterpret_cast<uint4*>(dst + (((2 * i + 1) ^ (k & 7)) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
+                const int j = 2 * (c & 3);                     // f16 chunk within the 64-dim block c / 4
+                uint8_t* dst = sm + Tg::KT + (c >> 2) * (tcg::kKeys * 128) + k * 128;
+                *reinterpret_cast<uint4*>(dst + ((j ^ (k & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+                *reinterpret_cast<uint4*>(dst + (((j + 1) ^ (k & 7)) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
             }
         }
-        // ---- 1b. V^T: thread t converts keys [8kb, 8kb + 8) x dims [8db, 8db + 8);
+        // ---- 1b. V^T: thread t (t < d) converts keys [8kb, 8kb + 8) x dims [8db, 8db + 8);
         // keys outside the tile's range (or past the stage's pages) become zeros
-        {
+        if (D == 128 || t < D) {
             const int kb = t & 7, db = t >> 3;
             uint32_t w[8][2];
 #pragma unroll
@@ -667,7 +699,7 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
                 const int k = 8 * kb + i, key = t0 + k;
                 uint2 x = make_uint2(0, 0);
                 if (k < np * kBS && key >= u.kmin && key <= u.kmax)
-                    x = *reinterpret_cast<const uint2*>(stg + tcg::kKeys * 128 + k * 128 + (((db >> 1) ^ kb) << 4) +
+                    x = *reinterpret_cast<const uint2*>(stg + tcg::kKeys * D + stg_v_kb<D>(k, kb, db >> 1) +
                                                         8 * (db & 1));
                 w[i][0] = x.x;
                 w[i][1] = x.y;
@@ -684,7 +716,7 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
                 }
 #pragma unroll
             for (int dd = 0; dd < 8; ++dd)
-                *reinterpret_cast<uint4*>(sm + tcg::kVT + (8 * db + dd) * 128 + ((kb ^ dd) << 4)) =
+                *reinterpret_cast<uint4*>(sm + Tg::VT + (8 * db + dd) * 128 + ((kb ^ dd) << 4)) =
                     make_uint4(vt[dd][0], vt[dd][1], vt[dd][2], vt[dd][3]);
         }
         tc::fence_proxy_async_smem();
@@ -696,10 +728,10 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
             tc::fence_after_sync();
             constexpr uint32_t id_s = tc::idesc_f16_f32(128, tcg::kKeys);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
+            for (int ks = 0; ks < D / 16; ++ks) {
                 const uint32_t off = (ks & 3) * 32;
-                tc::mma_f16(tm, tc::desc_k_sw128(sb + tcg::kQ + (ks >> 2) * 16384 + off),
-                            tc::desc_k_sw128(sb + tcg::kKT + (ks >> 2) * (tcg::kKeys * 128) + off), id_s, ks > 0);
+                tc::mma_f16(tm, tc::desc_k_sw128(sb + Tg::QT + (ks >> 2) * 16384 + off),
+                            tc::desc_k_sw128(sb + Tg::KT + (ks >> 2) * (tcg::kKeys * 128) + off), id_s, ks > 0);
             }
             tc::commit(&bars[0]);
         }
@@ -708,13 +740,10 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
 
         // ---- 3. this row's scores -> online softmax -> its row of P
         float sv[64];
-        {
-            float* lo = sv;
-            tc::ld32(tm_row, *reinterpret_cast<float(*)[32]>(lo));
-            tc::ld32(tm_row + 32, *reinterpret_cast<float(*)[32]>(lo + 32));
-            tc::wait_ld(*reinterpret_cast<float(*)[32]>(lo));
-            tc::wait_ld(*reinterpret_cast<float(*)[32]>(lo + 32));
-        }
+        tc::ld32(tm_row, *reinterpret_cast<float(*)[32]>(sv));
+        tc::ld32(tm_row + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
+        tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv));
+        tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv + 32));
         const bool interior = np == tcg::kPages && t0 + tcg::kKeys - 1 <= wpos0 && t0 >= wlo1;
         float mx = -INFINITY;
         if (interior) {
@@ -746,7 +775,7 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
                 ls += p0 + p1;
                 pw[e] = pack_f16x2(p0, p1);
             }
-            *reinterpret_cast<uint4*>(sm + tcg::kKT + t * 128 + ((c ^ (t & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            *reinterpret_cast<uint4*>(sm + Tg::KT + t * 128 + ((c ^ (t & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
         }
         l = l * alpha + ls;
         tc::fence_proxy_async_smem();
@@ -762,7 +791,7 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
             constexpr uint32_t id_o = tc::idesc_f16_f32(128, D);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                tc::mma_f16(tm + 64, tc::desc_k_sw128(sb + tcg::kKT + ks * 32), tc::desc_k_sw128(sb + tcg::kVT + ks * 32),
+                tc::mma_f16(tm + 64, tc::desc_k_sw128(sb + Tg::KT + ks * 32), tc::desc_k_sw128(sb + Tg::VT + ks * 32),
                             id_o, ks > 0);
             tc::commit(&bars[1]);
         }
@@ -771,7 +800,7 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
 
         // ---- 5. fold this row's tile into the FP32 output registers
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
             float x[32];
             tc::ld32(tm_row + 64 + 32 * c, x);
             tc::wait_ld(x);
@@ -790,14 +819,14 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
             const float so = l > 0.f ? a.v_scale / l : 0.f;
             uint4* orow = reinterpret_cast<uint4*>(a.out + (static_cast<int64_t>(u.q0 + r / G) * a.num_q_heads + hk * G + r % G) * D);
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
+            for (int c = 0; c < D / 8; ++c)
                 orow[c] = make_uint4(pack_bf16x2(o[8 * c] * so, o[8 * c + 1] * so), pack_bf16x2(o[8 * c + 2] * so, o[8 * c + 3] * so),
                                      pack_bf16x2(o[8 * c + 4] * so, o[8 * c + 5] * so), pack_bf16x2(o[8 * c + 6] * so, o[8 * c + 7] * so));
         } else {
             const int64_t slot = (unit * a.splits + split) * a.rows + t;
             float4* po = reinterpret_cast<float4*>(a.part_o + slot * D);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) po[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+            for (int c = 0; c < D / 4; ++c) po[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
             a.part_ml[slot] = make_float2(m, l);
         }
     }
@@ -805,7 +834,7 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
     __syncthreads();
     if (warp == 0) {
         tc::fence_after_sync();
-        tc::dealloc(tm, tcg::kTmemCols);
+        tc::dealloc(tm, Tg::COLS);
     }
 }
 
@@ -905,9 +934,9 @@ constexpr int64_t kMergePages = 4;
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Query rows per tile for a head dimension: the tcgen05 kernel at d = 128,
-// the mma.sync kernel otherwise.
-inline int rows_per_tile(int D) { return D == 128 ? kRowsTC : kRows; }
+// Query rows per tile for a head dimension: the tcgen05 kernel at d = 64 and
+// 128, the mma.sync kernel at d = 256.
+inline int rows_per_tile(int D) { return D <= 128 ? kRowsTC : kRows; }
 
 int choose_splits(int64_t units, int64_t pages, int64_t slots) {
     if (units <= 0 || slots <= 0 || units >= slots) return 1;
@@ -947,9 +976,9 @@ Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D,
 // The prefill kernel for (D, G) and its dynamic shared memory.
 template <int D, int G>
 void kernel_of(void (**fn)(const Args), size_t* smem) {
-    if constexpr (D == 128) {
-        *fn = paged_prefill_tc_kernel<G>;
-        *smem = static_cast<size_t>(tcg::kSmem) + 1024;
+    if constexpr (D <= 128) {
+        *fn = paged_prefill_tc_kernel<D, G>;
+        *smem = static_cast<size_t>(TcGeo<D>::SMEM) + 1024;
     } else {
         *fn = paged_prefill_kernel<D, G>;
         *smem = Geo<D>::SMEM;
@@ -996,7 +1025,7 @@ int resident_per_sm(int D, int G) {
 
 template <int D, int G>
 cudaError_t launch(const Args& a, int batch, cudaStream_t s) {
-    // d = 128 runs on tcgen05, other head sizes on mma.sync
+    // d = 64 and 128 run on tcgen05, d = 256 on mma.sync
     void (*kernel)(const Args) = nullptr;
     size_t smem = 0;
     kernel_of<D, G>(&kernel, &smem);
