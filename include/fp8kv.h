@@ -1,6 +1,7 @@
 /*
- * libfp8kv -- fp8 (E4M3) paged KV cache: quantise-on-append and single-query
- * (decode) grouped-query attention, for NVIDIA GB300 (sm_103a).
+ * libfp8kv -- fp8 (E4M3) paged KV cache: quantise-on-append, single-query
+ * (decode) grouped-query attention and chunked-prefill attention over the
+ * cache, for NVIDIA GB300 (sm_103a).
  *
  * Sources the operations follow (the FP8 KV-cache web pages):
  *   [G] gpusmith.com, "FP8 KV Cache Quantization: Capacity Gains and Accuracy
