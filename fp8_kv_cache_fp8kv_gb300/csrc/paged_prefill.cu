@@ -37,6 +37,7 @@
 #include "fp8kv.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
+#include "prefill_plan.h"
 
 namespace fp8kv {
 
@@ -50,8 +51,6 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kRows = kWarps * 16;      // query rows per unit of the mma.sync kernel
 constexpr int kRowsTC = 128;            // query rows per unit of the tcgen05 kernel (one per TMEM lane)
 constexpr int kStages = 3;              // ring depth
-constexpr int kMaxSplits = 64;
-constexpr int kMinSplitPages = 8;       // a split covers at least 128 keys
 constexpr size_t kHeader = 256;         // error word, then the partials
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -914,13 +913,8 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
         *reinterpret_cast<uint32_t*>(orow + e) = pack_bf16x2(acc[e] * so, acc[e + 1] * so);
 }
 
-// Split plan: the tiles a sequence's chunk may need, and how many CTAs share
-// each unit's key range.  Splitting pays only while the units do not fill
-// one wave of resident CTAs; the count is then chosen to minimise
-//     waves(units * splits) * (pages per split + kSplitCtaPages) (+ kMergePages if split)
-// where kSplitCtaPages stands for a CTA's fixed cost (query tile, first load
-// latency, partial write) and kMergePages for the merge kernel, both in
-// units of one page's work; at least 128 keys per split, at most kMaxSplits.
+// Split plan: the tiles a sequence's chunk may need, how many CTAs share each
+// unit's key range (choose_splits in prefill_plan.h) and the workspace layout.
 struct Plan {
     int tiles = 0;
     int splits = 1;
@@ -929,32 +923,11 @@ struct Plan {
     size_t total = kHeader;
 };
 
-constexpr int64_t kSplitCtaPages = 8;
-constexpr int64_t kMergePages = 4;
-
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Query rows per tile for a head dimension: the tcgen05 kernel at d = 64 and
 // 128, the mma.sync kernel at d = 256.
 inline int rows_per_tile(int D) { return D <= 128 ? kRowsTC : kRows; }
-
-int choose_splits(int64_t units, int64_t pages, int64_t slots) {
-    if (units <= 0 || slots <= 0 || units >= slots) return 1;
-    auto cost = [&](int64_t sp) {
-        const int64_t waves = (units * sp + slots - 1) / slots;
-        return waves * ((pages + sp - 1) / sp + kSplitCtaPages) + (sp > 1 ? kMergePages : 0);
-    };
-    int best = 1;
-    int64_t best_cost = cost(1);
-    for (int sp = 2; sp <= kMaxSplits && static_cast<int64_t>(sp) * kMinSplitPages <= pages; ++sp) {
-        const int64_t c = cost(sp);
-        if (c < best_cost) {
-            best = sp;
-            best_cost = c;
-        }
-    }
-    return best;
-}
 
 Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D, int window, int sms, int per_sm) {
     Plan pl;
