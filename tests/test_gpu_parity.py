@@ -311,3 +311,22 @@ def test_inputs_written_by_the_previous_kernel_are_seen():
     gk, gv = pc.gathered_codes()
     assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
     assert_attn_close(_as_f64(out), oracle_out(w, kc, vc, 0), "fresh inputs")
+
+
+def test_long_contraction_with_nonzero_mean_values():
+    """131,072 keys, values ~ N(0.25, 0.125), near-flat attention: every key
+    contributes and a low-precision accumulator would swamp (the CPU test
+    test_tolerance_teeth shows the bar catches that).  The decode must meet
+    the bar against the fp64 oracle."""
+    shape = workload.LayerShape("flat_128k", 8, 1, 128, 1, 131072, 131072, (0,), kv_std=0.5)
+    w = workload.make_workload(shape, seed=5)
+    w.q = (w.q.float() * 0.05).to(torch.bfloat16)
+    w.v = (w.v.float() * 0.25 + 0.25).to(torch.bfloat16)
+    w.v_scale = workload.per_tensor_scale(w.v)
+    pc = Paged(w)
+    pc.append_all()
+    kc, vc = oracle_codes(w)
+    for engine in ENGINES:
+        out, err = pc.decode(window=0, engine=engine)
+        assert err == 0
+        assert_attn_close(_as_f64(out), oracle_out(w, kc, vc, 0), f"flat 128K engine={engine}")
