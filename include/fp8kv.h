@@ -369,6 +369,13 @@ fp8kv_status fp8kv_paged_decode_noalloc(const void* q, const uint8_t* k_cache, c
  *            num_blocks * num_kv_heads < 2^31.  batch == 0, max_q_len == 0 or
  *            num_q_tokens == 0 is a no-op.
  */
+/*
+ * Workspace bytes fp8kv_paged_prefill needs for this problem on the CURRENT
+ * device: the key-range split plan depends on its SM count and on how many
+ * prefill CTAs it holds at once.  At least 256 (the error word); larger
+ * when the call splits key ranges.  Returns 0 if the arguments are invalid
+ * or no device is available.
+ */
 size_t fp8kv_paged_prefill_workspace_size(int batch, int max_q_len, int max_seq_len, int num_q_heads,
                                           int num_kv_heads, int head_dim, int block_size, int window);
 
