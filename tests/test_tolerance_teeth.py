@@ -6,7 +6,8 @@ accumulator lost the needle; two-level accumulation fixed it) is a swamping
 failure: once the running sum is large, each new small term rounds away.
 Here a deliberately degraded accumulator, written only for this test on the
 CPU, sums p_t * v_t over 131,072 keys with its running value rounded to a few
-mantissa bits after every add.  Values ~ N(0.25, 0.125) under near-flat
+mantissa bits after every add; the row sum of p stays exact, so this isolates
+the P.V accumulator (the oracle's own acc_bits pin degrades both sums).  Values ~ N(0.25, 0.125) under near-flat
 attention make the output (about 0.25, where bf16 output rounding stays well
 inside the bar) depend on all keys.  At 10 or 14 bits the result misses the
 fp64 oracle by far more than the 8e-3 / 1e-3 bar; with a 23-bit (FP32-width)
