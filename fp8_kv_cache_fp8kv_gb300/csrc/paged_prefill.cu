@@ -10,23 +10,29 @@
 // the P.V contraction runs over the context, so partial sums live in real
 // FP32 registers).
 //
-// How: a unit is (tile of 64 query rows, kv head, sequence); a query row is a
-// (token, query head) pair of the kv head's group.  Each of the 4 warps owns
-// 16 rows, the M side of the m16n8k16 MMA:
-//   S  = Q K^T   A = Q (f16, pre-scaled per row by a power of two, staged in
-//                shared memory in fragment order), B = K (E4M3 -> f16 in
-//                registers; each thread reads contiguous key bytes and the
-//                Q fragments use the same permutation of the head dimension)
-//   O += P V     A = P straight from the score accumulators (rounded to f16),
-//                B = V (byte-permuted E4M3 -> f16; the output dimensions are
-//                permuted to match and put back at the store)
-// Keys stream through a 3-stage shared-memory ring of 2 pages (32 keys) per
-// stage (cp.async, the 128-byte swizzle of a TMA box, conflict-free fragment
-// loads).  Each stage's P.V tile is computed in fresh FP32 accumulators and
-// folded into the FP32 output registers (O = O * alpha + tile): the
-// two-level accumulation.  When the units are too few to fill the GPU, each
-// unit's key range is split over several CTAs whose FP32 partials (row
-// maximum, row sum, unnormalised output) a second kernel merges.
+// How: a unit is (tile of query rows, kv head, sequence); a query row is a
+// (token, query head) pair of the kv head's group.  Two kernels:
+//   - d = 64 and 128: paged_prefill_tc_kernel, 128 rows per unit on the
+//     5th-generation tensor cores (tcgen05.mma from swizzled f16 tiles in
+//     shared memory, S and O in tensor memory, one row per thread for the
+//     online softmax; see the comment above it);
+//   - d = 256: paged_prefill_kernel, 64 rows per unit, each of the 4 warps
+//     owning 16 rows on the M side of the m16n8k16 MMA:
+//       S  = Q K^T   A = Q (f16, pre-scaled per row by a power of two, staged
+//                    in shared memory in fragment order), B = K (E4M3 -> f16
+//                    in registers; each thread reads contiguous key bytes and
+//                    the Q fragments use the same permutation of the head
+//                    dimension)
+//       O += P V     A = P straight from the score accumulators (rounded to
+//                    f16), B = V (byte-permuted E4M3 -> f16; the output
+//                    dimensions are permuted to match and put back at the
+//                    store)
+//     with keys streaming through a 3-stage cp.async ring.
+// In both, each stage's P.V tile is computed in fresh FP32 accumulators and
+// folded into FP32 output registers (O = O * alpha + tile): the two-level
+// accumulation.  When the units are too few to fill the GPU, each unit's key
+// range is split over several CTAs whose FP32 partials (row maximum, row sum,
+// unnormalised output) a second kernel merges (split plan: prefill_plan.h).
 #include <cuda_runtime.h>
 
 #include <algorithm>
