@@ -19,23 +19,31 @@
 //    and cut into one equal contiguous range per CTA (2 CTAs per SM), so all
 //    CTAs finish together whatever the mix of sequence lengths.  A CTA walks
 //    the units its range overlaps ("segments").
-//  * Two producer warps stream the pages with TMA tensor copies (128-byte or
-//    64-byte swizzle, evict-first L2 policy), one the K pages and one the V
-//    pages, into a ring of shared-memory stages guarded by mbarriers, reading
-//    block ids 32 pages ahead.  Four consumer warps each own every fourth
-//    stage.  In a decode step (fp8kv_decode_step) the producer that owns a
-//    unit's last page first quantises and writes the sequence's newest K (V)
-//    row into it, orders that write before its own copies and then loads it.
+//  * Tensor-core engine (the default, stream_decode_kernel): no producer
+//    warps.  Each of the 4 warps of a CTA takes one contiguous share of every
+//    segment and streams it with 16-byte cp.async copies (evict-first L2
+//    policy) into a private ring of 3 stages (2 at d = 256), two stages
+//    ahead of the one it computes; its block ids are consecutive entries of
+//    one block-table row, read 32 at a time one window ahead.  Copies end by
+//    themselves, so there is no barrier handshake and no wait to bound.  In a
+//    decode step (fp8kv_decode_step) the warp whose share holds a unit's last
+//    page first quantises the sequence's newest K and V rows into it, fences,
+//    and only then copies it.  Many warps issuing small copies streamed the
+//    random 2 KB pages faster than two TMA-issuing producer warps per CTA.
+//  * CUDA-core engine (comparison only, paged_decode_kernel): two producer
+//    warps stream the pages with TMA tensor copies into a ring guarded by
+//    mbarriers (every wait bounded), four consumer warps own every fourth
+//    stage.
 //  * Per stage a consumer warp converts codes to f16 (exact) and runs the
 //    score contraction S^T = K Q^T and the value contraction O^T += V^T P^T on
 //    the tensor cores (mma m16n8k16, fp32 accumulators): the g <= 8 query
 //    heads form the n=8 side.  The stage's P.V tile is then added into
 //    separate FP32 registers (O = O*alpha + tile), so the long contraction is
-//    summed in IEEE FP32, not inside the MMA.  A CUDA-core engine (FP32 fma of
-//    exact f16 products, same pipeline) exists for comparison; it is slower at
-//    every supported g and is used only when asked for.
+//    summed in IEEE FP32, not inside the MMA.  The CUDA-core engine instead
+//    sums FP32 fma chains of exact f16 products; it is slower at every
+//    supported g and is used only when asked for.
 //  * The softmax max/sum use warp shuffles; P is rounded to f16 for the MMA.
-//  * At the end of a segment the four warps merge through shared memory; a
+//  * At the end of a segment the CTA's warps merge through shared memory; a
 //    unit split over several CTAs leaves FP32 partials that a small merge
 //    kernel combines.  It is launched as a programmatic dependent: it derives
 //    the split from the lengths while the decode grid finishes, then waits for
@@ -53,6 +61,7 @@
 #include "fp8kv.h"
 #include "partition.cuh"
 #include "ptx.cuh"
+#include "walk.cuh"
 
 namespace fp8kv {
 
@@ -150,6 +159,10 @@ __device__ __forceinline__ void report(uint32_t* err, uint32_t code) { atomicCAS
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kNCW * 32) : "memory"); }
 
+// Named barrier 1 over the first NW warps of the CTA.
+template <int NW>
+__device__ __forceinline__ void consumer_sync_n() { asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory"); }
+
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
 __device__ __forceinline__ uint16_t f32_to_bf16(float x) {
@@ -164,42 +177,6 @@ __device__ __forceinline__ int first_token(int L, int window) { return (window >
 __device__ __forceinline__ int attended_pages(int L, int window) {
     return L > 0 ? (L - 1) / kBS - first_token(L, window) / kBS + 1 : 0;
 }
-
-// Work of one launch: the attended pages of every (sequence, kv head) unit,
-// laid end to end (unit u = b*Hkv + hk holds pages [Hkv*pre[b] + hk*n_b,
-// ... + n_b)), split into equal contiguous ranges, one per CTA.  A CTA walks
-// the units its range overlaps; each overlap is one "segment".
-struct Walker {
-    int b, hk, n;       // sequence, kv head, pages per unit of this sequence
-    int64_t base;       // global index of the unit's first page
-    int64_t g;          // global index of the segment's first page
-};
-
-__device__ __forceinline__ void walk_start(Walker& w, const int32_t* pre, int B, int Hkv, int64_t s) {
-    int lo = 0, hi = B - 1;  // largest b with Hkv*pre[b] <= s (it has pages, since s < total)
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (static_cast<int64_t>(Hkv) * pre[mid] <= s) lo = mid; else hi = mid - 1;
-    }
-    w.b = lo;
-    w.n = pre[lo + 1] - pre[lo];
-    const int64_t off = s - static_cast<int64_t>(Hkv) * pre[lo];
-    w.hk = static_cast<int>(off / w.n);
-    w.base = static_cast<int64_t>(Hkv) * pre[lo] + static_cast<int64_t>(w.hk) * w.n;
-    w.g = s;
-}
-
-// Next unit (only called while the CTA's range continues past this unit).
-__device__ __forceinline__ void walk_next(Walker& w, const int32_t* pre, int Hkv) {
-    if (++w.hk == Hkv) {
-        w.hk = 0;
-        do { ++w.b; } while (pre[w.b + 1] == pre[w.b]);
-        w.n = pre[w.b + 1] - pre[w.b];
-    }
-    w.base = static_cast<int64_t>(Hkv) * pre[w.b] + static_cast<int64_t>(w.hk) * w.n;
-    w.g = w.base;
-}
-
 
 // Block id of page `lane` of a batch; an id outside [0, num_blocks) is
 // reported and returned as -1 (its page is then read from block 0 and never
@@ -1371,6 +1348,465 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 }
 
+// ---------------------------------------------------------------- streaming decode (per-warp rings)
+//
+// The same split-context flash-decoding step with a different copy pipeline:
+// there are no producer warps.  Every consumer warp streams its own pages
+// with 16-byte cp.async copies into a private ring of R stages in shared
+// memory, R-1 stages ahead of the stage it computes.  Each warp takes one
+// contiguous share of every segment of its CTA (the segment's pages cut into
+// NW equal runs), so its block ids are consecutive entries of one block-table
+// row; they are read 32 at a time, one window ahead.  Copies complete by
+// themselves (no barrier handshake, no bounded waits); the warps of a CTA
+// meet only at segment ends, to merge their partial softmax states.
+
+// One stage: the np (<= PPS) pages of K at kst and V at vst, holding tokens
+// [tok_base, tok_base + 16*np) of a sequence attended on [lo, L), folded into
+// the running state (m, l, o) of the warp (the g heads on the MMA's n side).
+template <int D, int G, int ES, bool E5M2>
+__device__ __forceinline__ void tc_stage(const uint8_t* kst, const uint8_t* vst, int np, int tok_base, int lo, int L,
+                                         int gid, int tig, const uint32_t (&qf)[Geo<D, ES>::KS][2],
+                                         const float (&cs)[2], float (&m)[2], float (&l)[2],
+                                         float (&o)[Geo<D, ES>::MT][4]) {
+    using Gm = Geo<D, ES>;
+    constexpr bool kEarlyV = Gm::MT == 8;
+    // ---- (d = 128) the stage's V fragments into registers first, so their
+    // shared-memory latency overlaps the score math
+    uint32_t vr[kEarlyV ? Gm::PPS : 1][kEarlyV ? Gm::HALVES : 1][4][Gm::VW / 4];
+    if constexpr (kEarlyV) {
+#pragma unroll
+        for (int p = 0; p < Gm::PPS; ++p)
+#pragma unroll
+            for (int hh = 0; hh < Gm::HALVES; ++hh)
+                load_v_box<D, ES>(vst + p * Gm::PAGE + hh * Gm::BOX, gid, tig, tok_base + p * kBS, lo, L, p < np,
+                                  vr[p][hh]);
+    }
+
+    // ---- scores S^T[token][head] = K Q^T, two accumulator chains per page
+    // (even and odd k-steps) to halve the dependent MMA latency
+    float sc[Gm::PPS][4];
+#pragma unroll
+    for (int p = 0; p < Gm::PPS; ++p) {
+        float s1[4] = {0.f, 0.f, 0.f, 0.f};
+        sc[p][0] = sc[p][1] = sc[p][2] = sc[p][3] = 0.f;
+        if (p < np) {
+#pragma unroll
+            for (int hh = 0; hh < Gm::HALVES; ++hh) {
+                const uint8_t* box = kst + p * Gm::PAGE + hh * Gm::BOX;
+                uint32_t w0[Gm::KW / 4], w1[Gm::KW / 4];
+#pragma unroll
+                for (int cc = 0; cc < Gm::KW / 16; ++cc) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(gid, tig * Gm::KW + 16 * cc));
+                    const uint4 y = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(gid + 8, tig * Gm::KW + 16 * cc));
+                    w0[4 * cc + 0] = x.x; w0[4 * cc + 1] = x.y; w0[4 * cc + 2] = x.z; w0[4 * cc + 3] = x.w;
+                    w1[4 * cc + 0] = y.x; w1[4 * cc + 1] = y.y; w1[4 * cc + 2] = y.z; w1[4 * cc + 3] = y.w;
+                }
+#pragma unroll
+                for (int kk = 0; kk < Gm::KSH; ++kk) {
+                    float(&acc)[4] = ((hh * Gm::KSH + kk) & 1) ? s1 : sc[p];
+                    uint32_t af[4];
+                    if constexpr (ES == 1) {
+                        codes4_to_f16x2x2<E5M2>(w0[kk], af[0], af[2]);
+                        codes4_to_f16x2x2<E5M2>(w1[kk], af[1], af[3]);
+                        mma_16816(acc, af, qf[hh * Gm::KSH + kk][0], qf[hh * Gm::KSH + kk][1], acc);
+                    } else {
+                        af[0] = w0[2 * kk];
+                        af[2] = w0[2 * kk + 1];
+                        af[1] = w1[2 * kk];
+                        af[3] = w1[2 * kk + 1];
+                        mma_16816_bf16(acc, af, qf[hh * Gm::KSH + kk][0], qf[hh * Gm::KSH + kk][1], acc);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) sc[p][r] += s1[r];
+    }
+
+    // ---- mask, scale to log2 units, stage maximum
+    float mx[2] = {-INFINITY, -INFINITY};
+    const bool interior = tok_base >= lo && tok_base + np * kBS <= L && np == Gm::PPS;
+#pragma unroll
+    for (int p = 0; p < Gm::PPS; ++p)
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+            const int tok = tok_base + p * kBS + gid + 8 * e2;
+            const bool valid = interior || ((p < np) && tok >= lo && tok < L);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float t = valid ? sc[p][2 * e2 + j] * cs[j] : -INFINITY;
+                sc[p][2 * e2 + j] = t;
+                mx[j] = fmaxf(mx[j], t);
+            }
+        }
+    float alpha[2], muse[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
+        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
+        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
+        const float mn = fmaxf(m[j], mx[j]);
+        muse[j] = mn == -INFINITY ? 0.f : mn;
+        alpha[j] = fast_exp2(m[j] - muse[j]);
+        m[j] = mn;
+    }
+
+    // ---- probabilities -> f16 (bf16 for the bf16 twin) B fragments of the value MMA
+    uint32_t pb[Gm::PPS][2];
+    float lsum[2] = {0.f, 0.f};
+#pragma unroll
+    for (int p = 0; p < Gm::PPS; ++p) {
+        const float p00 = fast_exp2(sc[p][0] - muse[0]);
+        const float p01 = fast_exp2(sc[p][1] - muse[1]);
+        const float p10 = fast_exp2(sc[p][2] - muse[0]);
+        const float p11 = fast_exp2(sc[p][3] - muse[1]);
+        lsum[0] += p00 + p10;
+        lsum[1] += p01 + p11;
+        if constexpr (ES == 1) {
+            pb[p][0] = movmatrix_trans(pack_f16x2(p00, p01));
+            pb[p][1] = movmatrix_trans(pack_f16x2(p10, p11));
+        } else {
+            pb[p][0] = movmatrix_trans(pack_bf16x2(p00, p01));
+            pb[p][1] = movmatrix_trans(pack_bf16x2(p10, p11));
+        }
+    }
+    l[0] = l[0] * alpha[0] + lsum[0];
+    l[1] = l[1] * alpha[1] + lsum[1];
+
+    // ---- P.V tile of this stage: O^T[dim][head] = V^T P^T
+    float ot[Gm::MT][4];
+#pragma unroll
+    for (int mt = 0; mt < Gm::MT; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
+#pragma unroll
+    for (int p = 0; p < Gm::PPS; ++p) {
+        if (p < np) {
+#pragma unroll
+            for (int hh = 0; hh < Gm::HALVES; ++hh) {
+                uint32_t v[4][Gm::VW / 4];
+                if constexpr (kEarlyV) {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int ww = 0; ww < Gm::VW / 4; ++ww) v[r][ww] = vr[p][hh][r][ww];
+                } else {
+                    load_v_box<D, ES>(vst + p * Gm::PAGE + hh * Gm::BOX, gid, tig, tok_base + p * kBS, lo, L, true, v);
+                }
+#pragma unroll
+                for (int mtl = 0; mtl < Gm::MTH; ++mtl) {
+                    uint32_t af[4];
+                    if constexpr (ES == 1) {
+                        const uint32_t sel = (mtl & 1) ? 0x7362u : 0x5140u;
+                        const uint32_t x01 = byte_perm(v[0][mtl >> 1], v[1][mtl >> 1], sel);
+                        const uint32_t x23 = byte_perm(v[2][mtl >> 1], v[3][mtl >> 1], sel);
+                        codes4_to_f16x2x2<E5M2>(x01, af[0], af[1]);
+                        codes4_to_f16x2x2<E5M2>(x23, af[2], af[3]);
+                        mma_16816(ot[hh * Gm::MTH + mtl], af, pb[p][0], pb[p][1], ot[hh * Gm::MTH + mtl]);
+                    } else {
+                        af[0] = byte_perm(v[0][mtl], v[1][mtl], 0x5410u);
+                        af[1] = byte_perm(v[0][mtl], v[1][mtl], 0x7632u);
+                        af[2] = byte_perm(v[2][mtl], v[3][mtl], 0x5410u);
+                        af[3] = byte_perm(v[2][mtl], v[3][mtl], 0x7632u);
+                        mma_16816_bf16(ot[hh * Gm::MTH + mtl], af, pb[p][0], pb[p][1], ot[hh * Gm::MTH + mtl]);
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- fold the tile into the FP32 accumulators
+#pragma unroll
+    for (int mt = 0; mt < Gm::MT; ++mt) {
+        o[mt][0] = fmaf(o[mt][0], alpha[0], ot[mt][0]);
+        o[mt][1] = fmaf(o[mt][1], alpha[1], ot[mt][1]);
+        o[mt][2] = fmaf(o[mt][2], alpha[0], ot[mt][2]);
+        o[mt][3] = fmaf(o[mt][3], alpha[1], ot[mt][3]);
+    }
+}
+
+// Warps and ring depth of the streaming kernel per head dimension.  Two CTAs
+// share an SM (228 KB of shared memory): at d = 256 the larger merge buffers
+// leave room for two ring stages per warp, elsewhere three.
+template <int D, int ES>
+struct StreamCfg {
+    static constexpr int NW = 4;                                // warps per CTA
+    static constexpr int R = Geo<D, ES>::XW > 40 ? 2 : 3;       // ring stages per warp
+    static constexpr int NBUF = NW / 2;                         // merge exchange buffers
+    static constexpr int CPP = Geo<D, ES>::PAGE / 512;          // 16-byte copies per lane per page (K or V)
+};
+
+template <int D, int ES>
+constexpr size_t stream_smem_bytes() {
+    using Sc = StreamCfg<D, ES>;
+    return 128 + static_cast<size_t>(Sc::NW) * Sc::R * kStageBytes + Sc::NBUF * Geo<D, ES>::XW * 32 * sizeof(float) +
+           (2 * kMaxBatch + 1 + 4) * sizeof(int32_t);
+}
+
+// Dynamic shared memory one of kCtasPerSm resident CTAs may take (228 KB per
+// SM, 1 KB of it reserved per CTA).
+constexpr size_t kSmemPerCta = (228u * 1024u) / kCtasPerSm - 1024u;
+
+template <int D, int G, int ES, bool E5M2>
+__global__ void __launch_bounds__(StreamCfg<D, ES>::NW * 32, kCtasPerSm)
+    stream_decode_kernel(const DecodeArgs a) {
+    using Gm = Geo<D, ES>;
+    using Sc = StreamCfg<D, ES>;
+    constexpr int NW = Sc::NW, R = Sc::R, CPP = Sc::CPP;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* rings = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    float* xbuf = reinterpret_cast<float*>(rings + NW * R * kStageBytes);            // [NBUF][XW][32]
+    int32_t* pre = reinterpret_cast<int32_t*>(xbuf + Sc::NBUF * Gm::XW * 32);         // [kMaxBatch + 1]
+    int32_t* lens = pre + kMaxBatch + 1;                                              // [kMaxBatch]
+    volatile int* flag = reinterpret_cast<volatile int*>(lens + kMaxBatch);            // [1] earlier timeout
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // This grid may have started before the previous one on the stream
+    // finished (programmatic launch): wait for it before reading any input.
+    griddep_wait();
+    // The merge kernel that follows may start now: it reads only the lengths
+    // before it waits for this grid's completion.
+    griddep_launch_dependents();
+    const int B = a.batch, Hkv = a.num_kv_heads, C = gridDim.x, c = blockIdx.x;
+
+    // ---- attended pages per sequence and their exclusive prefix; the error
+    // word is read alongside (a call that gave up a wait fails every later
+    // call on the workspace until it is re-initialised)
+    if (warp == 0) {
+        uint32_t prev_err = 0;
+        if (lane == 0) prev_err = *reinterpret_cast<volatile uint32_t*>(a.err);
+        int run = 0;
+        for (int b0 = 0; b0 < B; b0 += 32) {
+            const int b = b0 + lane;
+            int n = 0;
+            if (b < B) {
+                const int Lraw = __ldg(a.seq_lens + b);
+                if (Lraw < 0 || Lraw > a.max_seq_len) report(a.err, FP8KV_ERR_INVALID_ARG);
+                lens[b] = clamp_len(Lraw, a.max_seq_len);
+                n = attended_pages(lens[b], a.window);
+            }
+            int x = n;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += y;
+            }
+            if (b < B) pre[b] = run + x - n;
+            run += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) {
+            pre[B] = run;
+            flag[0] = prev_err == FP8KV_ERR_TIMEOUT;
+        }
+    }
+    __syncthreads();
+    if (flag[0]) return;
+
+    const int64_t P = static_cast<int64_t>(Hkv) * pre[B];
+    for (int b = c; b < B; b += C) {  // sequences with nothing to attend produce zeros
+        if (pre[b + 1] == pre[b]) {
+            uint16_t* ob = a.out + static_cast<int64_t>(b) * a.num_q_heads * D;
+            for (int i = tid; i < a.num_q_heads * D; i += NW * 32) ob[i] = 0;
+        }
+    }
+    const int Ce = static_cast<int>(P < C ? P : C);
+    if (c >= Ce) return;
+    const Partition part = make_partition(P, Ce);
+    const int64_t s = range_start(part, c);
+    const int64_t e = range_start(part, c + 1);
+
+    // ---- this warp's ring and its per-lane copy offsets: lane l copies the
+    // 16-byte chunks l, l+32, ... of a page, stored at their swizzled place
+    uint8_t* ring = rings + warp * R * kStageBytes;
+    const uint32_t ring_s = smem_u32(ring);
+    uint32_t soff[CPP];
+#pragma unroll
+    for (int i = 0; i < CPP; ++i) {
+        const int byte = (lane + 32 * i) * 16;
+        const int r = byte / Gm::RB, b = byte % Gm::RB;
+        soff[i] = (b / Gm::ROWB) * Gm::BOX + swz<Gm::ROWB>(r, b % Gm::ROWB);
+    }
+    const uint64_t pol = l2_policy_evict_first();
+    const bool appending = ES == 1 && a.k_new != nullptr;
+    const int kvs = a.kv_shift, Hc = Hkv >> kvs;
+
+    // ---- issue side: a cursor over this warp's pages in windows of up to 32
+    // pages that never straddle a segment (walk.cuh).  Lane l holds the block
+    // id of page start + l of the window; the window after the current one is
+    // read one window ahead, with the newest K/V rows when it holds a unit's
+    // last page and this is a decode step.
+    struct Win {
+        WinPos pos;
+        int id;     // lane-held block id
+        bool last;  // the window holds its unit's last page, which gets the new rows first
+        NewRow<D> krow, vrow;
+    };
+    auto load_win = [&](Win& x) {
+        x.id = 0;
+        x.last = false;
+        if (!x.pos.valid) return;
+        const int32_t* row = a.block_tables + static_cast<int64_t>(x.pos.w.b) * a.max_blocks_per_seq +
+                             first_token(lens[x.pos.w.b], a.window) / kBS + (x.pos.w.g - x.pos.w.base);
+        x.id = load_block_id(row + x.pos.start, lane, x.pos.n, a.num_blocks, a.err);
+        x.last = appending && window_holds_unit_end(x.pos, e);
+        if (x.last) {
+            const int64_t nr = static_cast<int64_t>(x.pos.w.b) * Hc + (x.pos.w.hk >> kvs);
+            load_new_row<D>(x.krow, a.k_new + nr * D, lane);
+            load_new_row<D>(x.vrow, a.v_new + nr * D, lane);
+        }
+    };
+    Win cur, nxt;
+    {
+        Walker w0;
+        walk_start(w0, pre, B, Hkv, s);
+        cur.pos = first_window_from(w0, true, pre, Hkv, e, warp, NW);
+        load_win(cur);
+        nxt.pos = next_window(cur.pos, pre, Hkv, e, warp, NW);
+        load_win(nxt);
+    }
+    int cpos = 0;   // pages of the current window already issued
+    int ist = 0;    // stages issued
+    // Issues this warp's next stage (up to PPS pages of K and V) into ring
+    // slot ist % R, or an empty copy group once its pages are exhausted.
+    auto issue_stage = [&]() {
+        if (cur.pos.valid) {
+            const int n = min(Gm::PPS, cur.pos.n - cpos);
+            const uint32_t slot = ring_s + (ist % R) * kStageBytes;
+            for (int p = 0; p < n; ++p) {
+                const int id = __shfl_sync(0xffffffffu, cur.id, cpos + p);
+                const int64_t page = static_cast<int64_t>(max(id, 0)) * Hc + (cur.pos.w.hk >> kvs);
+                const uint8_t* ksrc = a.k_cache + page * Gm::PAGE;
+                const uint8_t* vsrc = a.v_cache + page * Gm::PAGE;
+                if (cur.last && cur.pos.start + cpos + p == cur.pos.hi - 1 && id >= 0) {
+                    // the unit's last page: write the sequence's newest K and
+                    // V rows into it first (the same quantisation as the
+                    // append kernel), then copy it
+                    const int L = lens[cur.pos.w.b];
+                    const int64_t roff = static_cast<int64_t>((L - 1) % kBS) * D;
+                    const float ksc = a.k_scales ? __ldg(a.k_scales + (cur.pos.w.hk >> kvs)) : a.k_scale_raw;
+                    const float vsc = a.v_scales ? __ldg(a.v_scales + (cur.pos.w.hk >> kvs)) : a.v_scale_raw;
+                    store_new_row<D, E5M2>(cur.krow, a.k_cache + page * Gm::PAGE + roff, lane, ksc);
+                    store_new_row<D, E5M2>(cur.vrow, a.v_cache + page * Gm::PAGE + roff, lane, vsc);
+                    __threadfence();
+                    __syncwarp();
+                }
+#pragma unroll
+                for (int i = 0; i < CPP; ++i) {
+                    cp_async_16(slot + p * Gm::PAGE + soff[i], ksrc + (lane + 32 * i) * 16, pol);
+                    cp_async_16(slot + kStageHalf + p * Gm::PAGE + soff[i], vsrc + (lane + 32 * i) * 16, pol);
+                }
+            }
+            cpos += n;
+            if (cpos == cur.pos.n) {
+                cur = nxt;
+                cpos = 0;
+                nxt.pos = next_window(cur.pos, pre, Hkv, e, warp, NW);
+                load_win(nxt);
+            }
+        }
+        cp_async_commit();
+        ++ist;
+    };
+#pragma unroll
+    for (int i = 0; i < R - 1; ++i) issue_stage();
+
+    // ---- compute side: the segments of the CTA's range in order; in each,
+    // this warp's share stage by stage, then the CTA's warps merge
+    const int gid = lane >> 2, tig = lane & 3;
+    uint32_t qf[Gm::KS][2];
+    float cs[2];
+    float m[2], l[2];
+    float o[Gm::MT][4];
+    int kst = 0;  // stages computed
+    Walker w;
+    walk_start(w, pre, B, Hkv, s);
+    while (true) {
+        const int64_t seg_end = min(e, w.base + w.n);
+        const int lp0 = static_cast<int>(w.g - w.base);
+        int q0, q1;
+        warp_share(w, e, warp, NW, q0, q1);
+        const int L = lens[w.b];
+        const int lo = first_token(L, a.window);
+        const int pg_first = lo / kBS + lp0;
+        if constexpr (ES == 1)
+            load_query<D, G>(a, w.b, w.hk, gid, tig, qf, cs);
+        else
+            load_query_bf16<D, G>(a, w.b, w.hk, gid, tig, qf, cs);
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < Gm::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+        for (int p0 = q0; p0 < q1; p0 += Gm::PPS) {
+            issue_stage();
+            cp_async_wait<R - 1>();
+            __syncwarp();
+            const uint8_t* kst_p = ring + (kst % R) * kStageBytes;
+            tc_stage<D, G, ES, E5M2>(kst_p, kst_p + kStageHalf, min(Gm::PPS, q1 - p0), (pg_first + p0) * kBS, lo, L,
+                                     gid, tig, qf, cs, m, l, o);
+            __syncwarp();  // every lane is done with the slot before it is refilled
+            ++kst;
+        }
+
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 4);
+            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 8);
+            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 16);
+        }
+
+        // ---- merge the warps' states into warp 0 (tree through smem)
+#pragma unroll
+        for (int n = NW; n > 1; n -= n / 2) {
+            const int h = n / 2;
+            if (warp >= n - h && warp < n) publish<Gm::MT>(xbuf + (warp - (n - h)) * Gm::XW * 32, lane, m, l, o);
+            consumer_sync_n<NW>();
+            if (warp < h) absorb<Gm::MT>(xbuf + warp * Gm::XW * 32, lane, m, l, o);
+            consumer_sync_n<NW>();
+        }
+
+        // ---- emit: the whole unit in this CTA -> output; else a partial
+        const int u = w.b * Hkv + w.hk;
+        const int c_first = cta_of(part, w.base);
+        const int c_last = cta_of(part, w.base + w.n - 1);
+        if (warp == 0) {
+            if (c_first == c_last) {
+                uint16_t* out_u = a.out + (static_cast<int64_t>(w.b) * a.num_q_heads + w.hk * G) * D;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int h = 2 * tig + j;
+                    const float sc_out = l[j] > 0.f ? unit_v_scale(a, w.hk) / l[j] : 0.f;
+                    if (h < G) {
+#pragma unroll
+                        for (int mt = 0; mt < Gm::MT; ++mt)
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2) {
+                                const int dim = (mt / Gm::MTH) * Gm::DBOX + Gm::VWD * gid + 2 * (mt % Gm::MTH) + e2;
+                                out_u[h * D + dim] = f32_to_bf16(o[mt][2 * e2 + j] * sc_out);
+                            }
+                    }
+                }
+            } else {
+                const int64_t slot_idx = static_cast<int64_t>(u) + c;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int h = 2 * tig + j;
+                    if (h < G) {
+                        float* po = a.part_o + (slot_idx * G + h) * D;
+#pragma unroll
+                        for (int mt = 0; mt < Gm::MT; ++mt)
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2)
+                                po[(mt / Gm::MTH) * Gm::DBOX + Gm::VWD * gid + 2 * (mt % Gm::MTH) + e2] = o[mt][2 * e2 + j];
+                        if (gid == 0) a.part_ml[slot_idx * 8 + h] = make_float2(m[j], l[j]);
+                    }
+                }
+            }
+        }
+        if (seg_end >= e) break;
+        walk_next(w, pre, Hkv);
+    }
+    cp_async_wait<0>();
+}
+
 // Combines the partials of every (sequence, kv head) unit that was split over
 // several CTAs: one CTA per (unit, query head of the group).  Its threads split
 // the unit's partials into KS slices (8 loads in flight per thread, one online
@@ -1652,6 +2088,53 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     return cudaLaunchKernelEx(&mcfg, merge_kernel<D, G>, a);
 }
 
+template <int D, int G, int ES = 1, bool E5M2 = false>
+cudaError_t launch_stream(const DecodeArgs& a, int ctas, cudaStream_t stream) {
+    static_assert(stream_smem_bytes<D, ES>() <= kSmemPerCta, "two CTAs must fit on one SM");
+    static std::atomic<uint64_t> done_mask{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (bit == 0 || !(done_mask.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(stream_decode_kernel<D, G, ES, E5M2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(stream_smem_bytes<D, ES>()));
+        if (e != cudaSuccess) return e;
+        done_mask.fetch_or(bit, std::memory_order_release);
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(StreamCfg<D, ES>::NW * 32);
+    cfg.dynamicSmemBytes = stream_smem_bytes<D, ES>();
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, stream_decode_kernel<D, G, ES, E5M2>, a);
+    if (e != cudaSuccess || ctas == 1) return e;
+    cudaLaunchConfig_t mcfg = {};
+    mcfg.gridDim = dim3(a.batch * a.num_kv_heads, G);
+    mcfg.blockDim = dim3(kMergeThreads);
+    mcfg.dynamicSmemBytes = 0;
+    mcfg.stream = stream;
+    mcfg.attrs = attr;
+    mcfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&mcfg, merge_kernel<D, G>, a);
+}
+
+template <int D, int ES = 1, bool E5M2 = false>
+cudaError_t launch_stream_g(int G, const DecodeArgs& a, int ctas, cudaStream_t s) {
+    switch (G) {
+        case 1: return launch_stream<D, 1, ES, E5M2>(a, ctas, s);
+        case 2: return launch_stream<D, 2, ES, E5M2>(a, ctas, s);
+        case 4: return launch_stream<D, 4, ES, E5M2>(a, ctas, s);
+        case 8: return launch_stream<D, 8, ES, E5M2>(a, ctas, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 template <int D, bool SIMT, int ES = 1, bool E5M2 = false>
 cudaError_t launch_g(int G, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArgs& a, int ctas,
                      cudaStream_t s) {
@@ -1794,7 +2277,18 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         a.score_scale = sm_scale * k_scale * kLog2e;
         a.v_scale = v_scale;
         cudaError_t e;
-        if (es == 2) {
+        if (!simt) {
+            if (es == 2)
+                e = head_dim == 64 ? launch_stream_g<64, 2>(G, a, p.ctas, s) : launch_stream_g<128, 2>(G, a, p.ctas, s);
+            else if (e5m2)
+                e = head_dim == 64 ? launch_stream_g<64, 1, true>(G, a, p.ctas, s)
+                    : head_dim == 128 ? launch_stream_g<128, 1, true>(G, a, p.ctas, s)
+                                      : launch_stream_g<256, 1, true>(G, a, p.ctas, s);
+            else
+                e = head_dim == 64 ? launch_stream_g<64>(G, a, p.ctas, s)
+                    : head_dim == 128 ? launch_stream_g<128>(G, a, p.ctas, s)
+                                      : launch_stream_g<256>(G, a, p.ctas, s);
+        } else if (es == 2) {
             e = head_dim == 64 ? launch_g<64, false, 2>(G, mk, mv, a, p.ctas, s)
                                : launch_g<128, false, 2>(G, mk, mv, a, p.ctas, s);
         } else if (e5m2) {

@@ -86,6 +86,24 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const void* tmap, ui
         : "memory");
 }
 
+// 16-byte asynchronous global -> shared copy (L2 only, no L1 allocation) with
+// an L2 cache-policy hint.  Completion is tracked per thread by commit groups.
+__device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void* src, uint64_t cache_policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_dst), "l"(src),
+                 "l"(cache_policy)
+                 : "memory");
+}
+
+// Closes the calling thread's current group of cp.async copies.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until at most N of the calling thread's most recent copy groups are
+// still in flight.  Copies always complete: this wait ends by itself.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
