@@ -60,6 +60,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="time only --config (the default run also times the 128K needle workload as its own record)")
     p.add_argument("--sweep", action="store_true",
                    help="instead of the step: decode time against context length, fp8 cache and bf16 cache")
     p.add_argument("--prefill", type=str, default=None, metavar="CHUNKS",
@@ -327,11 +329,57 @@ class DecodeStep:
         self._step()
 
 
-def run_fp8kv(args, rank, ws):
+PER_CONFIG = ("llama33_70b_needle_128k",)   # also timed, as their own records, in a default run
+
+
+def time_steps(st, K, flush, stream):
+    """The timed region: K decode steps, returned as total milliseconds and a
+    description.  A workload that streams more than 1.5x the L2 size per step
+    runs its K steps back to back between one pair of CUDA events (inputs
+    larger than L2, nothing to flush); a smaller one gets an L2 flush before
+    every step, outside per-step events."""
+    if flush.buf is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            st.step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1), "one CUDA-event pair around the K back-to-back steps"
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush()
+        ev[i][0].record(stream)
+        st.step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)), "CUDA events around each step (L2 flushed before each)"
+
+
+def isolated_step_us(st, K, flush, stream):
+    """Median step time with CUDA events recorded around every single step
+    (an event between two steps keeps the next step from starting while the
+    previous one drains)."""
+    evs = []
+    for _ in range(K):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        st.step()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+
+
+def measure_config(args, rank, ws, config, window=None, extras=True):
+    """One workload's record: the decode step timed K times (see time_steps),
+    its roofline, SM clocks during the timed region and, unless disabled, the
+    end-to-end number through host buffers."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = workload.make_workload(args.config, seed=args.seed)
+    w = workload.make_workload(config, seed=args.seed)
     s = w.shape
-    window = s.windows[0] if args.window is None else args.window
+    window = s.windows[0] if window is None else window
     lens = w.seq_lens.tolist()
     B = len(lens)
     dec_bytes = accounting.decode_bytes(lens, s.num_q_heads, s.num_kv_heads, s.head_dim, window)
@@ -350,58 +398,53 @@ def run_fp8kv(args, rank, ws):
     assert st.fk.fp8kv_read_error(st.ws) == 0
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     barrier(ws)
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    for i in range(K):
-        flush()
-        ev[i][0].record(stream)
-        st.step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    total_ms, timing = time_steps(st, K, flush, stream)
     barrier(ws)
     t_wall1 = time.time()
-    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    total_ms = reduce_max(sum(step_ms), ws)
+    total_ms = reduce_max(total_ms, ws)
     clk = clocks.summary(t_wall0, t_wall1) if clocks else None
-    # for reference: the unfused pair (decode call alone, append call alone)
-    dec_ms, app_ms = [], []
-    for i in range(K):
-        flush()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        st.decode()
-        e1.record(stream)
-        dec_ms.append(e0)
-        dec_ms.append(e1)
-        flush()
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        st.append()
-        a1.record(stream)
-        app_ms.append(a0)
-        app_ms.append(a1)
-    torch.cuda.synchronize()
-    dec_ms = [dec_ms[2 * i].elapsed_time(dec_ms[2 * i + 1]) for i in range(K)]
-    app_ms = [app_ms[2 * i].elapsed_time(app_ms[2 * i + 1]) for i in range(K)]
-    dec_mean = reduce_max(statistics.fmean(dec_ms), ws)
-    # the two contraction engines of the decode call, back to back
-    eng_us = {}
-    for name, eng in (("tensor_cores", st.fk.ENGINE_TENSOR_CORES), ("cuda_cores", st.fk.ENGINE_CUDA_CORES)):
-        for _ in range(3):
-            st.decode_engine(eng)
-        evs = []
+    iso_us = reduce_max(isolated_step_us(st, K, flush, stream), ws)
+    assert st.fk.fp8kv_read_error(st.ws) == 0
+    rec = {}
+    if extras:
+        # for reference: the unfused pair (decode call alone, append call alone)
+        dec_ms, app_ms = [], []
         for i in range(K):
             flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            st.decode_engine(eng)
+            st.decode()
             e1.record(stream)
-            evs.append((e0, e1))
+            dec_ms.append((e0, e1))
+            flush()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            st.append()
+            a1.record(stream)
+            app_ms.append((a0, a1))
         torch.cuda.synchronize()
-        assert st.fk.fp8kv_read_error(st.ws) == 0
-        eng_us[name + "_us"] = round(reduce_max(statistics.fmean(a.elapsed_time(b) for a, b in evs), ws) * 1e3, 3)
+        rec["paged_decode_us"] = round(reduce_max(statistics.fmean(a.elapsed_time(b) for a, b in dec_ms), ws) * 1e3, 3)
+        rec["quant_append_us"] = round(statistics.fmean(a.elapsed_time(b) for a, b in app_ms) * 1e3, 3)
+        # the two contraction engines of the decode call, each call timed alone
+        eng_us = {}
+        for name, eng in (("tensor_cores", st.fk.ENGINE_TENSOR_CORES), ("cuda_cores", st.fk.ENGINE_CUDA_CORES)):
+            for _ in range(3):
+                st.decode_engine(eng)
+            evs = []
+            for i in range(K):
+                flush()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                st.decode_engine(eng)
+                e1.record(stream)
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+            assert st.fk.fp8kv_read_error(st.ws) == 0
+            eng_us[name + "_us"] = round(reduce_max(statistics.fmean(a.elapsed_time(b) for a, b in evs), ws) * 1e3, 3)
+        rec["paged_decode_engines"] = eng_us
     if clocks:
         clocks.stop()
 
@@ -410,20 +453,17 @@ def run_fp8kv(args, rank, ws):
         e2e = measure_e2e(st, args, ws, step_bytes, flush)
 
     ms_per_step = total_ms / K
-    value = ws * step_bytes / (ms_per_step * 1e-3) / 1e9
     peak, peak_src = measured_peaks()
     # roofline of the step call itself (decode kernel with the fused append,
-    # then the split merge), timed per step inside the timed region above
+    # then the split merge), timed inside the timed region above
     achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
-    key = "decode_step/%s/w%d" % (args.config, window)
+    key = "decode_step/%s/w%d" % (config, window)
     traffic = traffic_for(key)
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
-        "us_per_step": round(ms_per_step * 1e3, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded N(0,1) bf16, per-tensor amax/448 E4M3 scales, shuffled 16-token pages)",
-        "config": {"workload": args.config, "batch": B, "num_q_heads": s.num_q_heads,
+    out = {
+        "value": round(ws * achieved, 2), "unit": "GB/s", "ms_per_step": round(ms_per_step, 6),
+        "us_per_step": round(ms_per_step * 1e3, 3), "us_per_step_isolated": round(iso_us, 3),
+        "timing": timing,
+        "config": {"workload": config, "batch": B, "num_q_heads": s.num_q_heads,
                    "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": 16,
                    "seq_lens": "uniform %d..%d" % (s.len_lo, s.len_hi), "total_tokens": int(sum(lens)),
                    "window": window, "kv_cache": "e4m3, per-tensor k/v scales",
@@ -431,61 +471,79 @@ def run_fp8kv(args, rank, ws):
                    "l2": flush.describe(),
                    "parallelism": "replicas" if ws > 1 else "1 gpu",
                    "input_sha256": w.digest()[:16]},
-        "step_bytes": step_bytes, "paged_decode_us": round(dec_mean * 1e3, 3),
-        "quant_append_us": round(statistics.fmean(app_ms) * 1e3, 3),
-        "paged_decode_engines": eng_us,
-        "roofline": {"kernel": "fp8kv_decode_step call: flattened split-context decode kernel with the "
-                               "append fused in + split-merge kernel",
+        "step_bytes": step_bytes,
+        "roofline": {"kernel": "fp8kv_decode_step call: split-context decode kernel (per-warp cp.async "
+                               "streaming, append fused in) + split-merge kernel",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": step_bytes},
         "gpu_launches": 2 * K,  # decode kernel + split-merge kernel per step
         "clocks": clk,
     }
+    out.update(rec)
     if e2e is not None:
-        line["e2e"] = e2e
+        out["e2e"] = e2e
+    out["_w"] = (w, window, dec_bytes + app_bytes)
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_fp8kv(args, rank, ws):
+    main = measure_config(args, rank, ws, args.config, args.window)
+    w, window, step_bytes = main.pop("_w")
+    line = {"metric": METRIC, "value": main.pop("value"), "unit": main.pop("unit"), "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup}
+    line.update(main)
+    line.update({"higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                 "data": "synthetic (seeded N(0,1) bf16, per-tensor amax/448 E4M3 scales, shuffled 16-token pages)"})
+    if args.config == "llama31_8b_b8_20k" and args.window is None and not args.no_per_config:
+        line["per_config"] = {}
+        for cfg in PER_CONFIG:
+            rec = measure_config(args, rank, ws, cfg, None, extras=False)
+            rec.pop("_w")
+            line["per_config"][cfg] = rec
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, window, dec_bytes + app_bytes)
+        line["cpu_baseline"] = cpu_baseline(w, window, step_bytes)
     return line
 
 
 def measure_e2e(st, args, ws, step_bytes, flush):
-    """Same step through the public API from pinned host buffers: one H2D copy
-    of the step's packed inputs (q, the new K/V rows, the sequence lengths),
-    the step call, the D2H copy of out."""
+    """The same step through the C ABI from host buffers: fp8kv_decode_step_host
+    copies the step's packed inputs (q, the new K/V rows, the sequence
+    lengths) from pinned host memory to the device, runs the step and copies
+    out back to pinned host memory; the host then waits for the stream.  Each
+    step is timed with the host clock from the call to the end of the wait."""
     h_in = st.h_inputs.pin_memory()
     h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
     stream = torch.cuda.current_stream()
     h2d = h_in.numel() * h_in.element_size()
     d2h = h_out.numel() * h_out.element_size()
-
-    def one():
-        st.inputs.copy_(h_in, non_blocking=True)
-        st.step()
-        h_out.copy_(st.out, non_blocking=True)
-
+    w = st.w
+    call = st.fk.prepare_decode_step_host(h_in, st.inputs, h_out, st.q, st.k_new, st.v_new, st.k_cache, st.v_cache,
+                                          st.block_tables, st.seq_lens, w.max_seq_len, w.k_scale, w.v_scale,
+                                          w.sm_scale, st.window, st.out, st.ws)
     for _ in range(args.warmup):
-        one()
-    torch.cuda.synchronize()
+        call()
+        stream.synchronize()
     K = args.steps
     times = []
     barrier(ws)
     for _ in range(K):
         flush()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
+        stream.synchronize()
         t0 = time.perf_counter()
-        e0.record(stream)
-        one()
-        e1.record(stream)
-        e1.synchronize()
+        call()
+        stream.synchronize()
         times.append(time.perf_counter() - t0)
     barrier(ws)
+    assert torch.equal(h_out, st.out.cpu())
     mean_s = reduce_max(statistics.fmean(times), ws)
     return {"value": round(ws * step_bytes / mean_s / 1e9, 2), "unit": "GB/s",
-            "us_per_step": round(mean_s * 1e6, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "timer": "host wall clock per step incl. H2D, kernels, D2H and the stream sync"}
+            "us_per_step": round(mean_s * 1e6, 3), "us_per_step_median": round(statistics.median(times) * 1e6, 3),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "call": "fp8kv_decode_step_host (one H2D copy of the packed inputs, the step, one D2H copy of out)",
+            "timer": "host wall clock per step: the C call through the stream synchronisation"}
 
 
 # ---------------------------------------------------------------- the CPU oracle

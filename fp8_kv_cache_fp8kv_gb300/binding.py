@@ -73,6 +73,9 @@ def load(build_if_missing: bool = False):
     lib.fp8kv_decode_step_e5m2.argtypes = [P, P, P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
     lib.fp8kv_decode_step.restype = I
     lib.fp8kv_decode_step.argtypes = [P, P, P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P]
+    lib.fp8kv_decode_step_host.restype = I
+    lib.fp8kv_decode_step_host.argtypes = [P, P, SZ, P] + [P, P, P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I,
+                                                           P, P, SZ, P]
     lib.fp8kv_paged_decode_noalloc.restype = I
     lib.fp8kv_paged_decode_noalloc.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P]
     lib.fp8kv_paged_prefill_workspace_size.restype = SZ
@@ -305,6 +308,33 @@ def prepare_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, seq_len
     args = _decode_step_args(q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale,
                              v_scale, sm_scale, window, out, workspace, stream)
     return PreparedCall("fp8kv_decode_step", load().fp8kv_decode_step, args)
+
+
+def _host(t, name):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError("%s must be a host tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def prepare_decode_step_host(h_in, d_in, h_out, q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens,
+                             max_seq_len, k_scale, v_scale, sm_scale, window, out, workspace, stream=None):
+    """fp8kv_decode_step_host, marshalled once: h_in (host, pinned) is copied to
+    d_in (device, same byte size) before the step; q, k_new, v_new and
+    seq_lens are device views the caller placed inside d_in; out is copied to
+    h_out (host, pinned, same shape as out) after it."""
+    if h_in.numel() * h_in.element_size() != d_in.numel() * d_in.element_size():
+        raise ValueError("h_in and d_in must have the same size in bytes")
+    if tuple(h_out.shape) != tuple(out.shape) or h_out.dtype != out.dtype:
+        raise ValueError("h_out must match out")
+    if not d_in.is_cuda:
+        raise TypeError("d_in must be a CUDA tensor")
+    args = (_host(h_in, "h_in"), ctypes.c_void_p(d_in.data_ptr()), ctypes.c_size_t(d_in.numel() * d_in.element_size()),
+            _host(h_out, "h_out")) + _decode_step_args(q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens,
+                                                       max_seq_len, k_scale, v_scale, sm_scale, window, out,
+                                                       workspace, stream)
+    return PreparedCall("fp8kv_decode_step_host", load().fp8kv_decode_step_host, args)
 
 
 def _decode_bf16_args(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, sm_scale, window, out,

@@ -2188,13 +2188,23 @@ extern "C" size_t fp8kv_paged_decode_workspace_size(int batch, int num_q_heads, 
 
 namespace {
 
+// Host-side staging around a decode call: the inputs copied in before it, the
+// output copied out after it (fp8kv_decode_step_host).
+struct HostStage {
+    const void* h_in;
+    void* d_in;
+    size_t in_bytes;
+    void* h_out;
+};
+
 fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, const uint8_t* k_cache,
                          const uint8_t* v_cache, int64_t num_blocks, const int32_t* block_tables,
                          int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len, int batch,
                          int num_q_heads, int num_kv_heads, int head_dim, int block_size, float k_scale,
                          float v_scale, float sm_scale, int window, void* out, void* workspace,
                          size_t workspace_bytes, void* stream, int engine, int es = 1,
-                         const float* k_scales = nullptr, const float* v_scales = nullptr, bool e5m2 = false) {
+                         const float* k_scales = nullptr, const float* v_scales = nullptr, bool e5m2 = false,
+                         const HostStage* hs = nullptr) {
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (batch < 0 || batch > 65535 || num_kv_heads < 1 || num_kv_heads > 65535 || num_q_heads < 1 ||
         num_q_heads % num_kv_heads != 0 || max_seq_len < 0 || num_blocks < 1 || max_blocks_per_seq < 0)
@@ -2241,6 +2251,9 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (hs && hs->in_bytes > 0 &&
+        cudaMemcpyAsync(hs->d_in, hs->h_in, hs->in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return FP8KV_ERR_CUDA;
     // Batches above kMaxBatch sequences run as consecutive launches on the
     // stream, reusing the workspace.
     for (int b0 = 0; b0 < batch; b0 += kMaxBatch) {
@@ -2305,6 +2318,9 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         }
         if (e != cudaSuccess) return FP8KV_ERR_CUDA;
     }
+    if (hs && cudaMemcpyAsync(hs->h_out, out, static_cast<size_t>(batch) * num_q_heads * head_dim * 2,
+                              cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return FP8KV_ERR_CUDA;
     return FP8KV_OK;
 }
 
@@ -2410,6 +2426,29 @@ extern "C" fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, cons
     return decode_impl(q, k_new, v_new, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                        max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale, v_scale,
                        sm_scale, window, out, workspace, workspace_bytes, stream, FP8KV_ENGINE_DEFAULT);
+}
+
+extern "C" fp8kv_status fp8kv_decode_step_host(const void* h_in, void* d_in, size_t in_bytes, void* h_out,
+                                               const void* q, const void* k_new, const void* v_new,
+                                               uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks,
+                                               const int32_t* block_tables, int max_blocks_per_seq,
+                                               const int32_t* seq_lens, int max_seq_len, int batch,
+                                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                               float k_scale, float v_scale, float sm_scale, int window, void* out,
+                                               void* workspace, size_t workspace_bytes, void* stream) {
+    if (batch > 0 && (!k_new || !v_new)) return FP8KV_ERR_INVALID_ARG;
+    if ((in_bytes > 0 && (!h_in || !d_in)) || (batch > 0 && !h_out)) return FP8KV_ERR_INVALID_ARG;
+    if (batch == 0) {  // nothing to attend: only the inputs move
+        if (in_bytes > 0 && cudaMemcpyAsync(d_in, h_in, in_bytes, cudaMemcpyHostToDevice,
+                                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return FP8KV_ERR_CUDA;
+        return FP8KV_OK;
+    }
+    const HostStage hs{h_in, d_in, in_bytes, h_out};
+    return decode_impl(q, k_new, v_new, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
+                       max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale, v_scale,
+                       sm_scale, window, out, workspace, workspace_bytes, stream, FP8KV_ENGINE_DEFAULT, 1, nullptr,
+                       nullptr, false, &hs);
 }
 
 // ---------------------------------------------------------------- allocation-free variant

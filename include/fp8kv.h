@@ -295,6 +295,35 @@ fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, const void* v_n
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fp8kv_decode_step for a caller whose per-step inputs and result live in
+ * host memory (an engine that computes q and the new K/V rows on the host, or
+ * a test harness).  No counterpart on the pages: it only moves the step's
+ * inputs and output across the host link around the step above.
+ *
+ * On `stream`, in order: one copy of in_bytes bytes from h_in to d_in, the
+ * decode step, one copy of the step's output (batch*num_q_heads*head_dim bf16)
+ * from `out` to h_out.  It returns once the three are enqueued; h_out is valid
+ * after the caller synchronises the stream.
+ *
+ *   h_in    host buffer (page-locked for an asynchronous copy) holding the
+ *           step's inputs exactly as they must appear at d_in
+ *   d_in    device buffer of in_bytes bytes; q, k_new, v_new and seq_lens are
+ *           device pointers, usually into d_in (the caller chooses the layout)
+ *   h_out   host buffer for the output (page-locked for an asynchronous copy)
+ *   all other arguments as for fp8kv_decode_step.
+ * Errors: those of fp8kv_decode_step (checked before anything is enqueued);
+ * null h_in, d_in or h_out with in_bytes > 0 is FP8KV_ERR_INVALID_ARG; a
+ * failed copy is FP8KV_ERR_CUDA.
+ */
+fp8kv_status fp8kv_decode_step_host(const void* h_in, void* d_in, size_t in_bytes, void* h_out,
+                                    const void* q, const void* k_new, const void* v_new, uint8_t* k_cache,
+                                    uint8_t* v_cache, int64_t num_blocks, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len,
+                                    int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                    int block_size, float k_scale, float v_scale, float sm_scale, int window,
+                                    void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Allocation-free paged decode.  This entry point has no counterpart on the
  * pages: it exists for callers that cannot allocate device memory when they
  * decode -- e.g. a serving engine that reserved nearly all HBM for its own
