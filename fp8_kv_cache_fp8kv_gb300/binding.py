@@ -78,6 +78,13 @@ def load(build_if_missing: bool = False):
                                                            P, P, SZ, P]
     lib.fp8kv_paged_decode_noalloc.restype = I
     lib.fp8kv_paged_decode_noalloc.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P]
+    U64 = ctypes.c_uint64
+    lib.fp8kv_debug_paged_decode_stall.restype = I
+    lib.fp8kv_debug_paged_decode_stall.argtypes = [P, P, P, I64, P, I, P, I, I, I, I, I, I, F, F, F, I, P, P, SZ, P,
+                                                   I, U64]
+    lib.fp8kv_debug_paged_prefill_stall.restype = I
+    lib.fp8kv_debug_paged_prefill_stall.argtypes = [P, I64, P, P, I64, P, I, P, P, I, I, I, I, I, I, I, F, F, F, I, P,
+                                                    P, SZ, P, I, U64]
     lib.fp8kv_paged_prefill_workspace_size.restype = SZ
     lib.fp8kv_paged_prefill_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
     lib.fp8kv_paged_prefill.restype = I
@@ -501,3 +508,27 @@ def fp8kv_paged_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_starts, m
     q_len tokens over its fp8 cache; see prepare_paged_prefill for shapes."""
     prepare_paged_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_starts, max_q_len, max_seq_len, k_scale,
                           v_scale, sm_scale, window, out, workspace, stream)()
+
+
+# ---------------------------------------------------------------- failure-path test hooks
+
+def debug_paged_decode_stall(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale, v_scale, sm_scale,
+                             window, out, workspace, stall_stage, wait_limit_ns, stream=None) -> int:
+    """fp8kv_debug_paged_decode_stall: the CUDA-core decode with stage
+    `stall_stage` of CTA 0 never issued and every ring wait limited to
+    wait_limit_ns.  Returns the launch status (the timeout itself is reported
+    through the workspace error word)."""
+    args = prepare_paged_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, k_scale, v_scale,
+                                sm_scale, window, out, workspace, stream).args
+    return load().fp8kv_debug_paged_decode_stall(*args, ctypes.c_int(stall_stage), ctypes.c_uint64(wait_limit_ns))
+
+
+def debug_paged_prefill_stall(q, k_cache, v_cache, block_tables, seq_lens, q_starts, max_q_len, max_seq_len, k_scale,
+                              v_scale, sm_scale, window, out, workspace, stall_stage, wait_limit_ns,
+                              stream=None) -> int:
+    """fp8kv_debug_paged_prefill_stall: the prefill with the score MMAs of
+    stage `stall_stage` of CTA (0, 0, 0) never issued and the MMA waits
+    limited to wait_limit_ns.  Returns the launch status."""
+    args = prepare_paged_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_starts, max_q_len, max_seq_len,
+                                 k_scale, v_scale, sm_scale, window, out, workspace, stream).args
+    return load().fp8kv_debug_paged_prefill_stall(*args, ctypes.c_int(stall_stage), ctypes.c_uint64(wait_limit_ns))

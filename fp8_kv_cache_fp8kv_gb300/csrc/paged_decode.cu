@@ -106,6 +106,11 @@ struct DecodeArgs {
     int window;
     float score_scale;          // sm_scale * k_scale * log2(e)
     float v_scale;
+    // Failure-path test hook of the CUDA-core engine (fp8kv_debug_paged_decode_stall):
+    // the K producer of CTA 0 never issues stage stall_stage (-1: none), and
+    // the ring waits give up after wait_ns (normally kWaitLimitNs).
+    uint64_t wait_ns;
+    int stall_stage;
 };
 
 // Geometry of one head dimension D with ES-byte elements (1: E4M3 codes,
@@ -137,11 +142,11 @@ struct Geo {
 
 // The CUDA-core consumers also keep the segment's f16 queries ([G][D]) and
 // their shifts ([8]) in shared memory.
-template <int D, int G, bool SIMT, int ES = 1>
+template <int D, int G>
 constexpr size_t smem_bytes() {
-    return 1024 + Geo<D, ES>::STAGES * kStageBytes + 2 * Geo<D, ES>::XW * 32 * sizeof(float) +
-           4 * Geo<D, ES>::STAGES * sizeof(uint64_t) + (2 * kMaxBatch + 1 + 4 + 32 * kNPW) * sizeof(int32_t) +
-           (SIMT ? 16 + G * D * sizeof(uint16_t) + 8 * sizeof(int) : 0);
+    return 1024 + Geo<D>::STAGES * kStageBytes + 2 * Geo<D>::XW * 32 * sizeof(float) +
+           4 * Geo<D>::STAGES * sizeof(uint64_t) + (2 * kMaxBatch + 1 + 4 + 32 * kNPW) * sizeof(int32_t) + 16 +
+           G * D * sizeof(uint16_t) + 8 * sizeof(int);
 }
 
 // Byte offset of (row r, byte o) inside one TMA box written with the 128-byte
@@ -638,7 +643,7 @@ __device__ __forceinline__ void simt_consumers(const DecodeArgs& a, const CtaVie
             const int st = st_base + i;
             const int slot = st % S;
             if (v.flag[1]) break;
-            if (!mbar_wait_bounded(&v.full_bar[slot], (st / S) & 1, kWaitLimitNs)) {
+            if (!mbar_wait_bounded(&v.full_bar[slot], (st / S) & 1, a.wait_ns)) {
                 report(a.err, FP8KV_ERR_TIMEOUT);
                 v.flag[1] = 1;
                 break;
@@ -749,7 +754,7 @@ __device__ __forceinline__ void simt_consumers(const DecodeArgs& a, const CtaVie
             __syncwarp();
 
             // ---- P.V: o[j][d] += sum_t P[t][j] V[t][d] over the stage's valid tokens
-            if (!mbar_wait_bounded(&v.full_bar[S + slot], (st / S) & 1, kWaitLimitNs)) {
+            if (!mbar_wait_bounded(&v.full_bar[S + slot], (st / S) & 1, a.wait_ns)) {
                 report(a.err, FP8KV_ERR_TIMEOUT);
                 v.flag[1] = 1;
                 break;
@@ -839,17 +844,13 @@ __device__ __forceinline__ void simt_consumers(const DecodeArgs& a, const CtaVie
     }
 }
 
-template <int D, int G, bool SIMT, int ES = 1, bool E5M2 = false>
+// The CUDA-core engine: TMA producers, an mbarrier-guarded ring, CUDA-core
+// consumers (simt_consumers).  E4M3 cache, per-tensor or per-head scales.
+template <int D, int G>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeArgs a) {
-    static_assert(ES == 1 || !SIMT, "the bf16 twin runs on the tensor cores only");
-    static_assert(!E5M2 || (ES == 1 && !SIMT), "the E5M2 cache runs on the tensor cores only");
-    using Gm = Geo<D, ES>;
-    // At d = 128 the V fragments move to registers as soon as they land (a
-    // measured gain); the accumulators of d = 256 leave no room, and at d = 64
-    // it measured slower.
-    constexpr bool kEarlyV = Gm::MT == 8;
+    using Gm = Geo<D>;
     constexpr int S = Gm::STAGES;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned ring (the swizzle pattern is a function of address
@@ -961,7 +962,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // unit's last page first writes that sequence's newest K (or V) row
         // into the page, orders the write before its own copies
         // (fence.proxy.async), and only then issues the page.
-        const bool appending = ES == 1 && a.k_new != nullptr;
+        const bool appending = a.k_new != nullptr;
         const uint16_t* new_rows = pw == 0 ? a.k_new : a.v_new;
         uint8_t* cache = pw == 0 ? a.k_cache : a.v_cache;
         const float scale_raw = pw == 0 ? a.k_scale_raw : a.v_scale_raw;  // per-tensor; per head below
@@ -1018,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     const int L = lens[batch_b];
                     // with two units per cache head both write the same bytes: identical values
                     uint8_t* dst_row = cache + ((static_cast<int64_t>(id) * Hc + (hk >> kvs)) * kBS + (L - 1) % kBS) * D;
-                    store_new_row<D, E5M2>(batch_row, dst_row, lane,
+                    store_new_row<D>(batch_row, dst_row, lane,
                                            head_scales ? __ldg(head_scales + (hk >> kvs)) : scale_raw);
                     fence_proxy_async_global();
                 }
@@ -1029,11 +1030,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     const int np = min(Gm::PPS, nb - q);
                     const int slot = st % S;
                     if (flag[1] || (st >= S && !mbar_wait_bounded(&empty_bar[pw * S + slot], ((st / S) & 1) ^ 1,
-                                                                   kWaitLimitNs))) {
+                                                                   a.wait_ns))) {
                         report(a.err, FP8KV_ERR_TIMEOUT);
                         flag[1] = 1;
                         ok = false;
                         break;
+                    }
+                    if (c == 0 && pw == 0 && st == a.stall_stage) {  // test hook: this stage never arrives
+                        ++st;
+                        continue;
                     }
                     // this producer's half of the stage (K or V)
                     mbar_arrive_expect_tx(&full_bar[pw * S + slot], static_cast<uint32_t>(np * Gm::PAGE));
@@ -1050,302 +1055,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-        // Only after a failed wait can copies still be in flight while the
-        // consumers have stopped waiting: drain them (bounded) before exit.
-        if (!ok && lane == 0) {
+        // The CTA must not exit with copies in flight, and consumers that gave
+        // up a wait no longer wait for them: before leaving, the producer waits
+        // (with the normal limit) for the last ring's worth of stages it
+        // issued.  Normally those have landed or are about to.
+        if (lane == 0) {
             for (int t = st > S ? st - S : 0; t < st; ++t)
-                mbar_wait_bounded(&full_bar[pw * S + t % S], (t / S) & 1, kWaitLimitNs);
+                if (!(c == 0 && pw == 0 && t == a.stall_stage))  // a stage the test hook skipped has no copies
+                    mbar_wait_bounded(&full_bar[pw * S + t % S], (t / S) & 1, kWaitLimitNs);
         }
         return;
     }
 
     // ---------------------------------------------------------------- consumers
-    if constexpr (SIMT) {
-        const CtaView v{ring, xbuf, full_bar, empty_bar, pre, lens, flag, qsm, qsh, s, e, part, c};
-        simt_consumers<D, G>(a, v, warp, lane);
-        return;
-    }
-    const int gid = lane >> 2, tig = lane & 3;
-    uint32_t qf[Gm::KS][2];
-    float cs[2];
-    float m[2], l[2];
-    float o[Gm::MT][4];
-    int st_base = 0;
-    Walker w;
-    walk_start(w, pre, B, Hkv, s);
-    while (true) {
-        const int64_t seg_end = min(e, w.base + w.n);
-        const int lp0 = static_cast<int>(w.g - w.base);
-        const int np_seg = static_cast<int>(seg_end - w.g);
-        const int nst = (np_seg + Gm::PPS - 1) / Gm::PPS;
-        const int L = lens[w.b];
-        const int lo = first_token(L, a.window);
-        const int pg_first = lo / kBS + lp0;  // page index (in the sequence) of the segment's first page
-        if constexpr (ES == 1)
-            load_query<D, G>(a, w.b, w.hk, gid, tig, qf, cs);
-        else
-            load_query_bf16<D, G>(a, w.b, w.hk, gid, tig, qf, cs);
-        if (seg_end < e && gid < G) {  // warm L2 with the next segment's queries
-            Walker nw = w;
-            walk_next(nw, pre, Hkv);
-#pragma unroll
-            for (int hh = 0; hh < Gm::HALVES; ++hh)
-                prefetch_l2(a.q + (static_cast<int64_t>(nw.b) * a.num_q_heads + nw.hk * G + gid) * D +
-                            hh * Gm::DBOX + tig * (Gm::KW / ES));
-        }
-        m[0] = m[1] = -INFINITY;
-        l[0] = l[1] = 0.f;
-#pragma unroll
-        for (int mt = 0; mt < Gm::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-
-        for (int i = (warp - st_base % kNCW + kNCW) % kNCW; i < nst; i += kNCW) {
-            const int st = st_base + i;
-            const int slot = st % S;
-            if (flag[1]) break;
-            if (!mbar_wait_bounded(&full_bar[slot], (st / S) & 1, kWaitLimitNs)) {
-                report(a.err, FP8KV_ERR_TIMEOUT);
-                flag[1] = 1;
-                break;
-            }
-            const int p0 = i * Gm::PPS;
-            const int np = min(Gm::PPS, np_seg - p0);
-            const uint8_t* kst = ring + slot * kStageBytes;
-            const uint8_t* vst = kst + kStageHalf;
-            const int tok_base = (pg_first + p0) * kBS;
-
-            // ---- (d = 128) the stage's V fragments into registers first, and
-            // the V half back to its producer: it is not held through the
-            // scores and the softmax (a held half is one copy fewer in flight)
-            uint32_t vr[kEarlyV ? Gm::PPS : 1][kEarlyV ? Gm::HALVES : 1][4][Gm::VW / 4];
-            if constexpr (kEarlyV) {
-                if (!mbar_wait_bounded(&full_bar[S + slot], (st / S) & 1, kWaitLimitNs)) {
-                    report(a.err, FP8KV_ERR_TIMEOUT);
-                    flag[1] = 1;
-                    break;
-                }
-#pragma unroll
-                for (int p = 0; p < Gm::PPS; ++p)
-#pragma unroll
-                    for (int hh = 0; hh < Gm::HALVES; ++hh)
-                        load_v_box<D, ES>(vst + p * Gm::PAGE + hh * Gm::BOX, gid, tig, tok_base + p * kBS, lo, L,
-                                          p < np, vr[p][hh]);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty_bar[S + slot]);
-            }
-
-            // ---- scores S^T[token][head] = K Q^T
-            float sc[Gm::PPS][4];
-#pragma unroll
-            for (int p = 0; p < Gm::PPS; ++p) {
-                sc[p][0] = sc[p][1] = sc[p][2] = sc[p][3] = 0.f;
-                if (p < np) {
-#pragma unroll
-                    for (int hh = 0; hh < Gm::HALVES; ++hh) {
-                        const uint8_t* box = kst + p * Gm::PAGE + hh * Gm::BOX;
-                        uint32_t w0[Gm::KW / 4], w1[Gm::KW / 4];
-#pragma unroll
-                        for (int cc = 0; cc < Gm::KW / 16; ++cc) {
-                            const uint4 x = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(gid, tig * Gm::KW + 16 * cc));
-                            const uint4 y = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(gid + 8, tig * Gm::KW + 16 * cc));
-                            w0[4 * cc + 0] = x.x; w0[4 * cc + 1] = x.y; w0[4 * cc + 2] = x.z; w0[4 * cc + 3] = x.w;
-                            w1[4 * cc + 0] = y.x; w1[4 * cc + 1] = y.y; w1[4 * cc + 2] = y.z; w1[4 * cc + 3] = y.w;
-                        }
-#pragma unroll
-                        for (int kk = 0; kk < Gm::KSH; ++kk) {
-                            uint32_t af[4];
-                            if constexpr (ES == 1) {
-                                codes4_to_f16x2x2<E5M2>(w0[kk], af[0], af[2]);
-                                codes4_to_f16x2x2<E5M2>(w1[kk], af[1], af[3]);
-                                mma_16816(sc[p], af, qf[hh * Gm::KSH + kk][0], qf[hh * Gm::KSH + kk][1], sc[p]);
-                            } else {
-                                af[0] = w0[2 * kk];
-                                af[2] = w0[2 * kk + 1];
-                                af[1] = w1[2 * kk];
-                                af[3] = w1[2 * kk + 1];
-                                mma_16816_bf16(sc[p], af, qf[hh * Gm::KSH + kk][0], qf[hh * Gm::KSH + kk][1], sc[p]);
-                            }
-                        }
-                    }
-                }
-            }
-
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[slot]);  // the K half is free again
-
-            // ---- mask, scale to log2 units, stage maximum
-            float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-            for (int p = 0; p < Gm::PPS; ++p)
-#pragma unroll
-                for (int e2 = 0; e2 < 2; ++e2) {
-                    const int tok = tok_base + p * kBS + gid + 8 * e2;
-                    const bool valid = (p < np) && tok >= lo && tok < L;
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const float t = valid ? sc[p][2 * e2 + j] * cs[j] : -INFINITY;
-                        sc[p][2 * e2 + j] = t;
-                        mx[j] = fmaxf(mx[j], t);
-                    }
-                }
-            float alpha[2], muse[2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
-                mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
-                mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
-                const float mn = fmaxf(m[j], mx[j]);
-                muse[j] = mn == -INFINITY ? 0.f : mn;
-                alpha[j] = fast_exp2(m[j] - muse[j]);
-                m[j] = mn;
-            }
-
-            // ---- probabilities -> f16 B fragments of the value MMA
-            uint32_t pb[Gm::PPS][2];
-            float lsum[2] = {0.f, 0.f};
-#pragma unroll
-            for (int p = 0; p < Gm::PPS; ++p) {
-                const float p00 = fast_exp2(sc[p][0] - muse[0]);
-                const float p01 = fast_exp2(sc[p][1] - muse[1]);
-                const float p10 = fast_exp2(sc[p][2] - muse[0]);
-                const float p11 = fast_exp2(sc[p][3] - muse[1]);
-                lsum[0] += p00 + p10;
-                lsum[1] += p01 + p11;
-                if constexpr (ES == 1) {
-                    pb[p][0] = movmatrix_trans(pack_f16x2(p00, p01));
-                    pb[p][1] = movmatrix_trans(pack_f16x2(p10, p11));
-                } else {
-                    pb[p][0] = movmatrix_trans(pack_bf16x2(p00, p01));
-                    pb[p][1] = movmatrix_trans(pack_bf16x2(p10, p11));
-                }
-            }
-            l[0] = l[0] * alpha[0] + lsum[0];
-            l[1] = l[1] * alpha[1] + lsum[1];
-
-            // ---- P.V tile of this stage: O^T[dim][head] = V^T P^T
-            if constexpr (!kEarlyV) {
-                if (!mbar_wait_bounded(&full_bar[S + slot], (st / S) & 1, kWaitLimitNs)) {
-                    report(a.err, FP8KV_ERR_TIMEOUT);
-                    flag[1] = 1;
-                    break;
-                }
-            }
-            float ot[Gm::MT][4];
-#pragma unroll
-            for (int mt = 0; mt < Gm::MT; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
-#pragma unroll
-            for (int p = 0; p < Gm::PPS; ++p) {
-                if (p < np) {
-#pragma unroll
-                    for (int hh = 0; hh < Gm::HALVES; ++hh) {
-                        uint32_t v[4][Gm::VW / 4];
-                        if constexpr (kEarlyV) {
-#pragma unroll
-                            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                                for (int ww = 0; ww < Gm::VW / 4; ++ww) v[r][ww] = vr[p][hh][r][ww];
-                        } else {
-                            load_v_box<D, ES>(vst + p * Gm::PAGE + hh * Gm::BOX, gid, tig, tok_base + p * kBS, lo, L,
-                                              true, v);
-                        }
-#pragma unroll
-                        for (int mtl = 0; mtl < Gm::MTH; ++mtl) {
-                            uint32_t af[4];
-                            if constexpr (ES == 1) {
-                                const uint32_t sel = (mtl & 1) ? 0x7362u : 0x5140u;
-                                const uint32_t x01 = byte_perm(v[0][mtl >> 1], v[1][mtl >> 1], sel);
-                                const uint32_t x23 = byte_perm(v[2][mtl >> 1], v[3][mtl >> 1], sel);
-                                codes4_to_f16x2x2<E5M2>(x01, af[0], af[1]);
-                                codes4_to_f16x2x2<E5M2>(x23, af[2], af[3]);
-                                mma_16816(ot[hh * Gm::MTH + mtl], af, pb[p][0], pb[p][1], ot[hh * Gm::MTH + mtl]);
-                            } else {
-                                // element pair 2*mtl of the thread's 8: tokens (2tig, 2tig+1) and (2tig+8, 2tig+9)
-                                af[0] = byte_perm(v[0][mtl], v[1][mtl], 0x5410u);
-                                af[1] = byte_perm(v[0][mtl], v[1][mtl], 0x7632u);
-                                af[2] = byte_perm(v[2][mtl], v[3][mtl], 0x5410u);
-                                af[3] = byte_perm(v[2][mtl], v[3][mtl], 0x7632u);
-                                mma_16816_bf16(ot[hh * Gm::MTH + mtl], af, pb[p][0], pb[p][1], ot[hh * Gm::MTH + mtl]);
-                            }
-                        }
-                    }
-                }
-            }
-            if constexpr (!kEarlyV) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty_bar[S + slot]);
-            }
-
-            // ---- fold the tile into the FP32 accumulators
-#pragma unroll
-            for (int mt = 0; mt < Gm::MT; ++mt) {
-                o[mt][0] = fmaf(o[mt][0], alpha[0], ot[mt][0]);
-                o[mt][1] = fmaf(o[mt][1], alpha[1], ot[mt][1]);
-                o[mt][2] = fmaf(o[mt][2], alpha[0], ot[mt][2]);
-                o[mt][3] = fmaf(o[mt][3], alpha[1], ot[mt][3]);
-            }
-        }
-        st_base += nst;
-
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 4);
-            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 8);
-            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 16);
-        }
-
-        // ---- merge the four warps' states into warp 0 (tree through smem)
-        if (warp >= 2) publish<Gm::MT>(xbuf + (warp - 2) * Gm::XW * 32, lane, m, l, o);
-        consumer_sync();
-        if (warp < 2) absorb<Gm::MT>(xbuf + warp * Gm::XW * 32, lane, m, l, o);
-        consumer_sync();
-        if (warp == 1) publish<Gm::MT>(xbuf, lane, m, l, o);
-        consumer_sync();
-        if (warp == 0) absorb<Gm::MT>(xbuf, lane, m, l, o);
-
-        // ---- emit: the whole unit in this CTA -> output; else a partial
-        // that the merge kernel combines.  The CTA holding the unit's first
-        // page records where the unit's partials are.
-        const int u = w.b * Hkv + w.hk;
-        const int c_first = cta_of(part, w.base);
-        const int c_last = cta_of(part, w.base + w.n - 1);
-        const int k_u = c_last - c_first + 1;
-        if (warp == 0) {
-            if (k_u == 1) {
-                uint16_t* out_u = a.out + (static_cast<int64_t>(w.b) * a.num_q_heads + w.hk * G) * D;
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int h = 2 * tig + j;
-                    const float sc_out = l[j] > 0.f ? unit_v_scale(a, w.hk) / l[j] : 0.f;
-                    if (h < G) {
-#pragma unroll
-                        for (int mt = 0; mt < Gm::MT; ++mt)
-#pragma unroll
-                            for (int e2 = 0; e2 < 2; ++e2) {
-                                const int dim = (mt / Gm::MTH) * Gm::DBOX + Gm::VWD * gid + 2 * (mt % Gm::MTH) + e2;
-                                out_u[h * D + dim] = f32_to_bf16(o[mt][2 * e2 + j] * sc_out);
-                            }
-                    }
-                }
-            } else {
-                const int64_t slot_idx = static_cast<int64_t>(u) + c;
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int h = 2 * tig + j;
-                    if (h < G) {
-                        float* po = a.part_o + (slot_idx * G + h) * D;
-#pragma unroll
-                        for (int mt = 0; mt < Gm::MT; ++mt)
-#pragma unroll
-                            for (int e2 = 0; e2 < 2; ++e2)
-                                po[(mt / Gm::MTH) * Gm::DBOX + Gm::VWD * gid + 2 * (mt % Gm::MTH) + e2] = o[mt][2 * e2 + j];
-                        if (gid == 0) a.part_ml[slot_idx * 8 + h] = make_float2(m[j], l[j]);
-                    }
-                }
-            }
-        }
-        consumer_sync();  // warp 0 is done with the exchange buffer
-        if (seg_end >= e) break;
-        walk_next(w, pre, Hkv);
-    }
+    const CtaView v{ring, xbuf, full_bar, empty_bar, pre, lens, flag, qsm, qsh, s, e, part, c};
+    simt_consumers<D, G>(a, v, warp, lane);
 }
 
 // ---------------------------------------------------------------- streaming decode (per-warp rings)
@@ -1865,6 +1589,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a
     // grid has.
     griddep_wait();
     if (k_u <= 1) return;  // empty (zeros), or written directly by its only CTA
+    // a decode CTA gave up a wait (in this call or an earlier one on this
+    // workspace): the partials are incomplete, and the error word says so
+    if (*reinterpret_cast<volatile uint32_t*>(a.err) == FP8KV_ERR_TIMEOUT) return;
     const int64_t s0 = static_cast<int64_t>(u) + c_first;
     float M = -INFINITY, Lh = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -2049,7 +1776,7 @@ bool make_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int Hk
     return true;
 }
 
-template <int D, int G, bool SIMT, int ES = 1, bool E5M2 = false>
+template <int D, int G>
 cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArgs& a, int ctas,
                    cudaStream_t stream) {
     // The shared-memory opt-in is per device; remember which devices have it.
@@ -2059,8 +1786,8 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
     if (bit == 0 || !(done_mask.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(paged_decode_kernel<D, G, SIMT, ES, E5M2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem_bytes<D, G, SIMT, ES>()));
+        e = cudaFuncSetAttribute(paged_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem_bytes<D, G>()));
         if (e != cudaSuccess) return e;
         done_mask.fetch_or(bit, std::memory_order_release);
     }
@@ -2072,11 +1799,11 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes<D, G, SIMT, ES>();
+    cfg.dynamicSmemBytes = smem_bytes<D, G>();
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G, SIMT, ES, E5M2>, mk, mv, a);
+    e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G>, mk, mv, a);
     if (e != cudaSuccess || ctas == 1) return e;  // one CTA: every unit is written directly
     cudaLaunchConfig_t mcfg = {};
     mcfg.gridDim = dim3(a.batch * a.num_kv_heads, G);
@@ -2135,14 +1862,14 @@ cudaError_t launch_stream_g(int G, const DecodeArgs& a, int ctas, cudaStream_t s
     }
 }
 
-template <int D, bool SIMT, int ES = 1, bool E5M2 = false>
+template <int D>
 cudaError_t launch_g(int G, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArgs& a, int ctas,
                      cudaStream_t s) {
     switch (G) {
-        case 1: return launch<D, 1, SIMT, ES, E5M2>(mk, mv, a, ctas, s);
-        case 2: return launch<D, 2, SIMT, ES, E5M2>(mk, mv, a, ctas, s);
-        case 4: return launch<D, 4, SIMT, ES, E5M2>(mk, mv, a, ctas, s);
-        case 8: return launch<D, 8, SIMT, ES, E5M2>(mk, mv, a, ctas, s);
+        case 1: return launch<D, 1>(mk, mv, a, ctas, s);
+        case 2: return launch<D, 2>(mk, mv, a, ctas, s);
+        case 4: return launch<D, 4>(mk, mv, a, ctas, s);
+        case 8: return launch<D, 8>(mk, mv, a, ctas, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -2197,6 +1924,12 @@ struct HostStage {
     void* h_out;
 };
 
+// The failure-path test hook's settings (fp8kv_debug_paged_decode_stall).
+struct StallHook {
+    int stall_stage;
+    uint64_t wait_ns;
+};
+
 fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, const uint8_t* k_cache,
                          const uint8_t* v_cache, int64_t num_blocks, const int32_t* block_tables,
                          int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len, int batch,
@@ -2204,7 +1937,7 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
                          float v_scale, float sm_scale, int window, void* out, void* workspace,
                          size_t workspace_bytes, void* stream, int engine, int es = 1,
                          const float* k_scales = nullptr, const float* v_scales = nullptr, bool e5m2 = false,
-                         const HostStage* hs = nullptr) {
+                         const HostStage* hs = nullptr, const StallHook* dbg = nullptr) {
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (batch < 0 || batch > 65535 || num_kv_heads < 1 || num_kv_heads > 65535 || num_q_heads < 1 ||
         num_q_heads % num_kv_heads != 0 || max_seq_len < 0 || num_blocks < 1 || max_blocks_per_seq < 0)
@@ -2244,9 +1977,9 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
     if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return FP8KV_ERR_WORKSPACE;
 
-    CUtensorMap mk, mv;  // the caches as bytes: rows of head_dim * es bytes
-    if (!make_cache_map(&mk, k_cache, num_blocks, num_kv_heads, head_dim * es) ||
-        !make_cache_map(&mv, v_cache, num_blocks, num_kv_heads, head_dim * es))
+    CUtensorMap mk, mv;  // the CUDA-core engine's TMA view of the caches (rows of head_dim bytes)
+    if (simt && (!make_cache_map(&mk, k_cache, num_blocks, num_kv_heads, head_dim) ||
+                 !make_cache_map(&mv, v_cache, num_blocks, num_kv_heads, head_dim)))
         return FP8KV_ERR_CUDA;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -2289,6 +2022,8 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         a.window = window > 0 ? window : 0;
         a.score_scale = sm_scale * k_scale * kLog2e;
         a.v_scale = v_scale;
+        a.wait_ns = dbg ? dbg->wait_ns : kWaitLimitNs;
+        a.stall_stage = dbg ? dbg->stall_stage : -1;
         cudaError_t e;
         if (!simt) {
             if (es == 2)
@@ -2301,20 +2036,10 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
                 e = head_dim == 64 ? launch_stream_g<64>(G, a, p.ctas, s)
                     : head_dim == 128 ? launch_stream_g<128>(G, a, p.ctas, s)
                                       : launch_stream_g<256>(G, a, p.ctas, s);
-        } else if (es == 2) {
-            e = head_dim == 64 ? launch_g<64, false, 2>(G, mk, mv, a, p.ctas, s)
-                               : launch_g<128, false, 2>(G, mk, mv, a, p.ctas, s);
-        } else if (e5m2) {
-            e = head_dim == 64 ? launch_g<64, false, 1, true>(G, mk, mv, a, p.ctas, s)
-                : head_dim == 128 ? launch_g<128, false, 1, true>(G, mk, mv, a, p.ctas, s)
-                                  : launch_g<256, false, 1, true>(G, mk, mv, a, p.ctas, s);
-        } else switch (head_dim * 2 + (simt ? 1 : 0)) {
-            case 128: e = launch_g<64, false>(G, mk, mv, a, p.ctas, s); break;
-            case 129: e = launch_g<64, true>(G, mk, mv, a, p.ctas, s); break;
-            case 256: e = launch_g<128, false>(G, mk, mv, a, p.ctas, s); break;
-            case 257: e = launch_g<128, true>(G, mk, mv, a, p.ctas, s); break;
-            case 512: e = launch_g<256, false>(G, mk, mv, a, p.ctas, s); break;
-            default: e = launch_g<256, true>(G, mk, mv, a, p.ctas, s); break;
+        } else {
+            e = head_dim == 64 ? launch_g<64>(G, mk, mv, a, p.ctas, s)
+                : head_dim == 128 ? launch_g<128>(G, mk, mv, a, p.ctas, s)
+                                  : launch_g<256>(G, mk, mv, a, p.ctas, s);
         }
         if (e != cudaSuccess) return FP8KV_ERR_CUDA;
     }
@@ -2451,6 +2176,23 @@ extern "C" fp8kv_status fp8kv_decode_step_host(const void* h_in, void* d_in, siz
                        nullptr, false, &hs);
 }
 
+extern "C" fp8kv_status fp8kv_debug_paged_decode_stall(const void* q, const uint8_t* k_cache,
+                                                       const uint8_t* v_cache, int64_t num_blocks,
+                                                       const int32_t* block_tables, int max_blocks_per_seq,
+                                                       const int32_t* seq_lens, int max_seq_len, int batch,
+                                                       int num_q_heads, int num_kv_heads, int head_dim,
+                                                       int block_size, float k_scale, float v_scale, float sm_scale,
+                                                       int window, void* out, void* workspace,
+                                                       size_t workspace_bytes, void* stream, int stall_stage,
+                                                       uint64_t wait_limit_ns) {
+    if (stall_stage < 0 || wait_limit_ns == 0 || wait_limit_ns > kWaitLimitNs) return FP8KV_ERR_INVALID_ARG;
+    const StallHook dbg{stall_stage, wait_limit_ns};
+    return decode_impl(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
+                       max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale, v_scale,
+                       sm_scale, window, out, workspace, workspace_bytes, stream, FP8KV_ENGINE_CUDA_CORES, 1, nullptr,
+                       nullptr, false, nullptr, &dbg);
+}
+
 // ---------------------------------------------------------------- allocation-free variant
 //
 // Some callers cannot allocate device memory at the point where they decode:
@@ -2463,9 +2205,11 @@ extern "C" fp8kv_status fp8kv_decode_step_host(const void* h_in, void* d_in, siz
 
 namespace fp8kv {
 
-// 8 MiB covers every workload shape exercised here (the largest, 16 x 32K
-// tokens at head_dim 256, needs about 5 MiB).  Every device that loads the
-// library holds this array until the process exits.
+// 8 MiB covers every workload shape exercised here: the largest, 16
+// sequences of up to 32K tokens at head_dim 256 with 8 query heads per kv
+// head, needs (16 units + 304 CTAs) x 8 heads x 256 dims x 4 B = 2.6 MB of
+// partials.  Every device that loads the library holds this array until the
+// process exits.
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 

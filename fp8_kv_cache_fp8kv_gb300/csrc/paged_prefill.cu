@@ -84,6 +84,11 @@ struct Args {
     int window;
     float score_scale;           // sm_scale * k_scale * log2(e)
     float v_scale;
+    // Failure-path test hook of the tcgen05 kernel (fp8kv_debug_paged_prefill_stall):
+    // CTA (0, 0, 0) never issues the score MMAs of stage stall_stage (-1: none),
+    // and the MMA waits give up after wait_ns (normally 0.5 s).
+    uint64_t wait_ns;
+    int stall_stage;
 };
 
 // Byte offset of (row r, byte o) inside a 16-row box with rows of ROWB bytes,
@@ -729,7 +734,8 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
         __syncthreads();
 
         // ---- 2. S = Q K^T
-        if (t == 0) {
+        const bool stalled = st == a.stall_stage && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+        if (t == 0 && !stalled) {
             tc::fence_after_sync();
             constexpr uint32_t id_s = tc::idesc_f16_f32(128, tcg::kKeys);
 #pragma unroll
@@ -740,7 +746,7 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
             }
             tc::commit(&bars[0]);
         }
-        const bool ok_s = mbar_wait_bounded(&bars[0], st & 1, tcg::kWaitNs);
+        const bool ok_s = mbar_wait_bounded(&bars[0], st & 1, a.wait_ns);
         tc::fence_after_sync();
 
         // ---- 3. this row's scores -> online softmax -> its row of P
@@ -800,7 +806,7 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
                             id_o, ks > 0);
             tc::commit(&bars[1]);
         }
-        fail = !mbar_wait_bounded(&bars[1], st & 1, tcg::kWaitNs);
+        fail = !mbar_wait_bounded(&bars[1], st & 1, a.wait_ns);
         tc::fence_after_sync();
 
         // ---- 5. fold this row's tile into the FP32 output registers
@@ -860,6 +866,9 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
     const bool ok = make_unit<G>(a, b, tile, false, u);  // only the lengths: read before the wait
     griddep_wait();                                      // the partials are complete and visible
     if (!ok) return;
+    // a CTA of this call gave up a wait: its partials are missing, and the
+    // error word says so
+    if (*reinterpret_cast<volatile uint32_t*>(a.err) == FP8KV_ERR_TIMEOUT) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rr = grp * 8 + warp;                       // row within the tile
     const int r = u.R0 + rr;
@@ -1084,13 +1093,14 @@ extern "C" size_t fp8kv_paged_prefill_workspace_size(int batch, int max_q_len, i
         .total;
 }
 
-extern "C" fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens, const uint8_t* k_cache,
-                                            const uint8_t* v_cache, int64_t num_blocks, const int32_t* block_tables,
-                                            int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* q_starts,
-                                            int max_q_len, int max_seq_len, int batch, int num_q_heads,
-                                            int num_kv_heads, int head_dim, int block_size, float k_scale,
-                                            float v_scale, float sm_scale, int window, void* out, void* workspace,
-                                            size_t workspace_bytes, void* stream) {
+namespace {
+
+fp8kv_status prefill_impl(const void* q, int64_t num_q_tokens, const uint8_t* k_cache, const uint8_t* v_cache,
+                          int64_t num_blocks, const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* seq_lens, const int32_t* q_starts, int max_q_len, int max_seq_len, int batch,
+                          int num_q_heads, int num_kv_heads, int head_dim, int block_size, float k_scale,
+                          float v_scale, float sm_scale, int window, void* out, void* workspace,
+                          size_t workspace_bytes, void* stream, int stall_stage, uint64_t wait_ns) {
     using namespace fp8kv::prefill;
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     const fp8kv_status sh = check_shape(batch, max_q_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,
@@ -1143,6 +1153,8 @@ extern "C" fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens,
     a.window = window > 0 ? window : 0;
     a.score_scale = sm_scale * k_scale * kLog2e;
     a.v_scale = v_scale;
+    a.wait_ns = wait_ns;
+    a.stall_stage = stall_stage;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (head_dim) {
@@ -1151,4 +1163,34 @@ extern "C" fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens,
         default: e = launch_g<256>(G, a, batch, s); break;
     }
     return e == cudaSuccess ? FP8KV_OK : FP8KV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens, const uint8_t* k_cache,
+                                            const uint8_t* v_cache, int64_t num_blocks, const int32_t* block_tables,
+                                            int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* q_starts,
+                                            int max_q_len, int max_seq_len, int batch, int num_q_heads,
+                                            int num_kv_heads, int head_dim, int block_size, float k_scale,
+                                            float v_scale, float sm_scale, int window, void* out, void* workspace,
+                                            size_t workspace_bytes, void* stream) {
+    return prefill_impl(q, num_q_tokens, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
+                        q_starts, max_q_len, max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                        k_scale, v_scale, sm_scale, window, out, workspace, workspace_bytes, stream, -1,
+                        fp8kv::prefill::tcg::kWaitNs);
+}
+
+extern "C" fp8kv_status fp8kv_debug_paged_prefill_stall(
+    const void* q, int64_t num_q_tokens, const uint8_t* k_cache, const uint8_t* v_cache, int64_t num_blocks,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* q_starts,
+    int max_q_len, int max_seq_len, int batch, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+    float k_scale, float v_scale, float sm_scale, int window, void* out, void* workspace, size_t workspace_bytes,
+    void* stream, int stall_stage, uint64_t wait_limit_ns) {
+    if (stall_stage < 0 || wait_limit_ns == 0 || wait_limit_ns > fp8kv::prefill::tcg::kWaitNs)
+        return FP8KV_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return FP8KV_ERR_UNSUPPORTED;  // only the tcgen05 kernel waits
+    return prefill_impl(q, num_q_tokens, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
+                        q_starts, max_q_len, max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                        k_scale, v_scale, sm_scale, window, out, workspace, workspace_bytes, stream, stall_stage,
+                        wait_limit_ns);
 }

@@ -334,13 +334,17 @@ fp8kv_status fp8kv_decode_step_host(const void* h_in, void* d_in, size_t in_byte
  *
  * Scratch: a fixed 8 MiB array compiled into the library (every device that
  * loads the library keeps it until the process exits).  The call allocates
- * nothing and calls no allocating routine; it clears the array's error word
- * and split counters (cudaMemsetAsync on `stream`) and then runs the decode.
+ * nothing and calls no allocating routine; it zeroes the array's 256-byte
+ * header, which holds the error word (cudaMemsetAsync on `stream`), and then
+ * runs the decode.  The split partials need no clearing: every call writes
+ * the ones it reads.
  *   - A problem whose split-merge scratch would exceed 8 MiB is rejected with
  *     FP8KV_ERR_WORKSPACE before anything is launched.
  *   - The first call on each device looks up the array's device address with
  *     that device current (cudaGetSymbolAddress); make that first call before
- *     any stream capture.
+ *     any stream capture.  The address is kept for the life of the process:
+ *     after a device reset (cudaDeviceReset) the array moves, so do not call
+ *     this entry point on a device that was reset.
  *   - All calls share the one array: calls that overlap on the GPU (different
  *     streams without ordering, or different host threads) race and corrupt
  *     each other's results.  Order them.
@@ -415,6 +419,47 @@ fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens, const uint
                                  int num_kv_heads, int head_dim, int block_size, float k_scale,
                                  float v_scale, float sm_scale, int window, void* out, void* workspace,
                                  size_t workspace_bytes, void* stream);
+
+/*
+ * Failure-path test hooks.  No counterpart on the pages: the pages' failure
+ * mode is silent (a wrong answer, no error), and these make the library's
+ * answer to a stall observable.  A kernel wait that runs out writes
+ * FP8KV_ERR_TIMEOUT into the workspace error word, waits (with the normal
+ * limit) for the copies it has in flight, frees what it holds and returns.
+ * Later calls on that workspace skip their work until it is zero-filled again
+ * (fp8kv_workspace_init).  Nothing faults and nothing hangs: every wait is
+ * bounded.
+ *
+ * fp8kv_debug_paged_decode_stall: fp8kv_paged_decode_engine with
+ * FP8KV_ENGINE_CUDA_CORES (the engine whose copies run through barriers),
+ * except that the K producer of CTA 0 never issues stage `stall_stage` and
+ * every ring wait gives up after wait_limit_ns nanoseconds.
+ *
+ * fp8kv_debug_paged_prefill_stall: fp8kv_paged_prefill, except that CTA
+ * (0, 0, 0) never issues the score MMAs of stage `stall_stage` and the MMA
+ * waits give up after wait_limit_ns nanoseconds.  head_dim 64 or 128 only (the
+ * tcgen05 kernel); FP8KV_ERR_UNSUPPORTED otherwise.
+ *
+ * Both: stall_stage >= 0 and 0 < wait_limit_ns <= 500,000,000, else
+ * FP8KV_ERR_INVALID_ARG; all other arguments and errors as the wrapped call.
+ */
+fp8kv_status fp8kv_debug_paged_decode_stall(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                            int64_t num_blocks, const int32_t* block_tables,
+                                            int max_blocks_per_seq, const int32_t* seq_lens, int max_seq_len,
+                                            int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                            int block_size, float k_scale, float v_scale, float sm_scale,
+                                            int window, void* out, void* workspace, size_t workspace_bytes,
+                                            void* stream, int stall_stage, uint64_t wait_limit_ns);
+
+fp8kv_status fp8kv_debug_paged_prefill_stall(const void* q, int64_t num_q_tokens, const uint8_t* k_cache,
+                                             const uint8_t* v_cache, int64_t num_blocks,
+                                             const int32_t* block_tables, int max_blocks_per_seq,
+                                             const int32_t* seq_lens, const int32_t* q_starts, int max_q_len,
+                                             int max_seq_len, int batch, int num_q_heads, int num_kv_heads,
+                                             int head_dim, int block_size, float k_scale, float v_scale,
+                                             float sm_scale, int window, void* out, void* workspace,
+                                             size_t workspace_bytes, void* stream, int stall_stage,
+                                             uint64_t wait_limit_ns);
 
 #ifdef __cplusplus
 }

@@ -110,44 +110,56 @@ def test_prefill_max_q_len_larger_than_needed_and_zero_chunks():
     assert_attn_close(got, ref, "zero chunks")
 
 
-def _sampled_rows(p: Paged, q, q_lens, rows, window):
-    """Oracle rows one by one: row i of sequence b is the decode attention of
-    the sequence cut at position p + 1."""
+def _oracle_rows(p: Paged, codes, q, q_lens, b, i0, i1, window):
+    """Oracle for chunk rows [i0, i1) of sequence b: they are the last i1 - i0
+    query tokens of the sequence cut just after row i1 - 1's position."""
     w = p.w
-    kc, vc = p.gathered_codes()
-    starts = w.seq_starts.numpy()
-    L = w.seq_lens.numpy()
+    kc, vc = codes
+    s0 = int(w.seq_starts.numpy()[b])
+    L = int(w.seq_lens.numpy()[b])
     qs = np.concatenate([[0], np.cumsum(q_lens)])
-    out = []
-    for b, i in rows:
-        pos = int(L[b] - q_lens[b] + i)
-        s0 = int(starts[b])
-        r = oracle.prefill_attention(workload.bf16_bits(q[qs[b] + i:qs[b] + i + 1]), kc[s0:s0 + pos + 1],
-                                     vc[s0:s0 + pos + 1], [pos + 1], [1], w.k_scale, w.v_scale, w.sm_scale,
-                                     window, nthreads=oracle.max_threads())
-        out.append(r[0])
-    return np.stack(out)
+    end = L - q_lens[b] + i1                    # tokens the cut sequence holds
+    return oracle.prefill_attention(workload.bf16_bits(q[qs[b] + i0:qs[b] + i1]), kc[s0:s0 + end],
+                                    vc[s0:s0 + end], [end], [i1 - i0], w.k_scale, w.v_scale, w.sm_scale, window,
+                                    nthreads=oracle.max_threads())
 
 
-def test_prefill_full_size_serving_batch_sampled():
-    """8 sequences of ~20K tokens, the last 512 of each a prefill chunk."""
+def _tile_blocks(q_len, tile_tokens, whole_tiles):
+    """Row blocks to check: the whole tiles listed, and the two rows on both
+    sides of every tile boundary of the chunk."""
+    blocks = [(t * tile_tokens, min(q_len, (t + 1) * tile_tokens)) for t in whole_tiles]
+    for bnd in range(tile_tokens, q_len, tile_tokens):
+        blocks.append((bnd - 2, bnd + 2))
+    blocks.append((q_len - 1, q_len))
+    return blocks
+
+
+def test_prefill_full_size_serving_batch_tiles_and_boundaries():
+    """8 sequences of ~20K tokens, the last 512 of each a prefill chunk.  A
+    tile holds 128 (token, head) rows = 32 tokens at g = 4: the first and the
+    last tile of two sequences are compared whole, and every tile boundary of
+    every sequence on both sides."""
     w = workload.make_workload("llama31_8b_b8_20k", seed=0)
     p = Paged(w, seed=0)
     p.append_all()
     q_lens = [512] * 8
     q, qs = workload.prefill_queries(w, q_lens, seed=0)
     got = _run(p, q, qs, 0)
-    rng = np.random.default_rng(0)
-    rows = [(b, int(i)) for b in range(8) for i in [0, 511, *rng.integers(0, 512, 3)]]
-    ref = _sampled_rows(p, q, q_lens, rows, 0)
-    sel = np.stack([got[qs[b] + i] for b, i in rows])
-    assert_attn_close(sel, ref, "8x20K chunk 512")
+    codes = p.gathered_codes()
+    tile_tokens = 128 // (w.shape.num_q_heads // w.shape.num_kv_heads)
+    for b in range(8):
+        whole = [0, 512 // tile_tokens - 1] if b in (0, 7) else []
+        for i0, i1 in _tile_blocks(512, tile_tokens, whole):
+            ref = _oracle_rows(p, codes, q, q_lens, b, i0, i1, 0)
+            assert_attn_close(got[qs[b] + i0:qs[b] + i1], ref, "8x20K chunk 512, seq %d rows %d..%d" % (b, i0, i1))
 
 
-def test_prefill_needle_128k_sampled():
+def test_prefill_needle_128k_tiles_and_boundaries():
     """The 131,072-token needle layout with a 256-token chunk at the end; the
     chunk's last row carries the query the needle key was planted for, so
-    that row must retrieve the needle from among 128K keys."""
+    that row must retrieve the needle from among 128K keys.  A tile holds 16
+    tokens at g = 8: the first and the last tile are compared whole, with
+    both sides of every tile boundary."""
     w = workload.make_workload("llama33_70b_needle_128k", seed=0)
     p = Paged(w, seed=0)
     p.append_all()
@@ -155,10 +167,11 @@ def test_prefill_needle_128k_sampled():
     q, qs = workload.prefill_queries(w, q_lens, seed=0)
     q[255] = w.q[0]
     got = _run(p, q, qs, 0)
-    rows = [(0, 0), (0, 97), (0, 255)]
-    ref = _sampled_rows(p, q, q_lens, rows, 0)
-    sel = np.stack([got[i] for _, i in rows])
-    assert_attn_close(sel, ref, "128K chunk 256")
+    codes = p.gathered_codes()
+    tile_tokens = 128 // (w.shape.num_q_heads // w.shape.num_kv_heads)
+    for i0, i1 in _tile_blocks(256, tile_tokens, [0, 256 // tile_tokens - 1]):
+        ref = _oracle_rows(p, codes, q, q_lens, 0, i0, i1, 0)
+        assert_attn_close(got[i0:i1], ref, "128K chunk 256 rows %d..%d" % (i0, i1))
 
 
 def test_prefill_reports_bad_block_id_and_lengths():
