@@ -10,29 +10,18 @@
 // the P.V contraction runs over the context, so partial sums live in real
 // FP32 registers).
 //
-// How: a unit is (tile of query rows, kv head, sequence); a query row is a
-// (token, query head) pair of the kv head's group.  Two kernels:
-//   - d = 64 and 128: paged_prefill_tc_kernel, 128 rows per unit on the
-//     5th-generation tensor cores (tcgen05.mma from swizzled f16 tiles in
-//     shared memory, S and O in tensor memory, one row per thread for the
-//     online softmax; see the comment above it);
-//   - d = 256: paged_prefill_kernel, 64 rows per unit, each of the 4 warps
-//     owning 16 rows on the M side of the m16n8k16 MMA:
-//       S  = Q K^T   A = Q (f16, pre-scaled per row by a power of two, staged
-//                    in shared memory in fragment order), B = K (E4M3 -> f16
-//                    in registers; each thread reads contiguous key bytes and
-//                    the Q fragments use the same permutation of the head
-//                    dimension)
-//       O += P V     A = P straight from the score accumulators (rounded to
-//                    f16), B = V (byte-permuted E4M3 -> f16; the output
-//                    dimensions are permuted to match and put back at the
-//                    store)
-//     with keys streaming through a 3-stage cp.async ring.
-// In both, each stage's P.V tile is computed in fresh FP32 accumulators and
-// folded into FP32 output registers (O = O * alpha + tile): the two-level
-// accumulation.  When the units are too few to fill the GPU, each unit's key
-// range is split over several CTAs whose FP32 partials (row maximum, row sum,
-// unnormalised output) a second kernel merges (split plan: prefill_plan.h).
+// How: a unit is (tile of 128 query rows, kv head, sequence); a query row is
+// a (token, query head) pair of the kv head's group.  One kernel,
+// paged_prefill_tc_kernel, for d = 64, 128 and 256, on the 5th-generation
+// tensor cores: tcgen05.mma from swizzled f16 tiles in shared memory, S and
+// the P.V tile in tensor memory, one row per thread (TMEM lane) for the
+// online softmax; see the comment above it.  Each stage's P.V tile is
+// computed in fresh FP32 accumulators and folded into an FP32 output
+// accumulator (O = O * alpha + tile, IEEE FMA): registers at d <= 128, tensor
+// memory at d = 256.  That is the two-level accumulation.  When the units are
+// too few to fill the GPU, each unit's key range is split over several CTAs
+// whose FP32 partials (row maximum, row sum, unnormalised output) a second
+// kernel merges (split plan: prefill_plan.h).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -54,9 +43,7 @@ namespace prefill {
 constexpr int kBS = 16;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kRows = kWarps * 16;      // query rows per unit of the mma.sync kernel
 constexpr int kRowsTC = 128;            // query rows per unit of the tcgen05 kernel (one per TMEM lane)
-constexpr int kStages = 3;              // ring depth
 constexpr size_t kHeader = 256;         // error word, then the partials
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -79,7 +66,7 @@ struct Args {
     int num_q_heads;
     int num_kv_heads;
     int tiles;                   // query tiles per (sequence, kv head)
-    int rows;                    // query rows per tile (kRows or kRowsTC)
+    int rows;                    // query rows per tile (kRowsTC)
     int splits;                  // CTAs per unit
     int window;
     float score_scale;           // sm_scale * k_scale * log2(e)
@@ -89,34 +76,6 @@ struct Args {
     // and the MMA waits give up after wait_ns (normally 0.5 s).
     uint64_t wait_ns;
     int stall_stage;
-};
-
-// Byte offset of (row r, byte o) inside a 16-row box with rows of ROWB bytes,
-// 128-byte (or 64-byte) swizzle: the layout a TMA box lands in.
-template <int ROWB>
-__device__ __forceinline__ uint32_t swz(int r, int o) {
-    if constexpr (ROWB == 128)
-        return r * 128 + ((((o >> 4) ^ (r & 7)) << 4) | (o & 15));
-    else
-        return r * 64 + ((((o >> 4) ^ ((r >> 1) & 3)) << 4) | (o & 15));
-}
-
-template <int D>
-struct Geo {
-    static constexpr int ROWB = D >= 128 ? 128 : D;  // bytes per box row
-    static constexpr int HALVES = D >= 128 ? D / 128 : 1;
-    static constexpr int BOX = kBS * ROWB;
-    static constexpr int PAGE = kBS * D;
-    static constexpr int PPS = D > 128 ? 1 : 2;      // pages per stage (register budget at D = 256)
-    static constexpr int STAGE = 2 * PPS * PAGE;     // K pages then V pages
-    static constexpr int KS = D / 16;                // k-steps of the score MMA
-    static constexpr int KW = ROWB / 4;              // K bytes a thread reads per row per box
-    static constexpr int KSH = KW / 4;               // k-steps per box
-    static constexpr int VW = ROWB / 8;              // V bytes a thread reads per key per box
-    static constexpr int NT = D / 8;                 // n-tiles of the value MMA (one per V byte column)
-    static constexpr size_t QSM = static_cast<size_t>(kWarps) * KS * 32 * 16;  // Q fragments
-    static constexpr size_t SMEM = static_cast<size_t>(kStages) * STAGE + QSM;
-    static_assert(KSH * HALVES == KS && VW * HALVES == NT, "boxes cover the head dimension");
 };
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
@@ -129,29 +88,6 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ void report(uint32_t* err, uint32_t code) { atomicCAS(err, 0u, code); }
-
-// Pages [pg, pg + np) of (block-table row bt, kv head hk) into one ring
-// stage: K page i at i * PAGE, V page i at (PPS + i) * PAGE.  A block id
-// outside [0, num_blocks) reads block 0 and is reported.
-template <int D>
-__device__ __forceinline__ void load_stage(const Args& a, const int32_t* bt, int hk, int pg, int np, uint32_t dst) {
-    using Gm = Geo<D>;
-    constexpr int kChunks = Gm::PAGE / 16;
-    for (int i = threadIdx.x; i < np * kChunks; i += kThreads) {
-        const int p = i / kChunks, ci = i % kChunks;
-        int id = __ldg(bt + pg + p);
-        if (id < 0 || id >= a.num_blocks) {
-            if (ci == 0) report(a.err, FP8KV_ERR_INVALID_ARG);
-            id = 0;
-        }
-        const int64_t base = (static_cast<int64_t>(id) * a.num_kv_heads + hk) * Gm::PAGE;
-        const int r = ci / (D / 16), c = ci % (D / 16);
-        const int h = (c * 16) / Gm::ROWB, o = (c * 16) % Gm::ROWB;
-        const uint32_t off = p * Gm::PAGE + h * Gm::BOX + swz<Gm::ROWB>(r, o);
-        cp_async16(dst + off, a.k_cache + base + r * D + c * 16);
-        cp_async16(dst + Gm::PPS * Gm::PAGE + off, a.v_cache + base + r * D + c * 16);
-    }
-}
 
 // What one (tile, kv head, sequence) covers: its query rows and the key
 // range the rows attend, from the device-side lengths (clamped; an entry
@@ -184,320 +120,8 @@ __device__ __forceinline__ bool make_unit(const Args& a, int b, int tile, bool r
     return true;
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(kThreads) paged_prefill_kernel(const Args a) {
-    using Gm = Geo<D>;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    griddep_wait();                // inputs may come from the previous grid on the stream
-    griddep_launch_dependents();
-    const int b = blockIdx.z, hk = blockIdx.y;
-    const int tile = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-    Unit u;
-    if (!make_unit<G>(a, b, tile, blockIdx.x == 0 && hk == 0 && threadIdx.x == 0, u)) return;
-
-    // ---- this split's key pages
-    const int pg0 = u.kmin / kBS, np_all = u.kmax / kBS - pg0 + 1;
-    const int sp0 = pg0 + static_cast<int>(static_cast<int64_t>(split) * np_all / a.splits);
-    const int sp1 = pg0 + static_cast<int>(static_cast<int64_t>(split + 1) * np_all / a.splits);
-    const int nst = (sp1 - sp0 + Gm::PPS - 1) / Gm::PPS;
-    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
-    const uint32_t ring = smem_u32(smem);
-#pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-        if (s < nst) load_stage<D>(a, bt, hk, sp0 + s * Gm::PPS, min(Gm::PPS, sp1 - sp0 - s * Gm::PPS), ring + s * Gm::STAGE);
-        cp_async_commit();
-    }
-
-    // ---- this warp's 16 query rows as f16 A fragments, each row pre-scaled by
-    // a power of two so the f16 copy of its bf16 values is exact; stored in
-    // shared memory in fragment order (each thread reads back only its own)
-    uint4* qsm = reinterpret_cast<uint4*>(smem + kStages * Gm::STAGE) + warp * Gm::KS * 32;
-    float cs[2];
-    int pq[2], lq[2];
-    bool rv[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {   // row gid + 8j: words 2e + j of each fragment
-        const int r = u.R0 + warp * 16 + gid + 8 * j;
-        rv[j] = r < u.rows;
-        const int tok = rv[j] ? r / G : 0, hq = hk * G + (rv[j] ? r % G : 0);
-        const uint16_t* qrow = a.q + (static_cast<int64_t>(u.q0 + tok) * a.num_q_heads + hq) * D;
-        uint32_t qw[Gm::HALVES][Gm::KSH][2];
-        float qmax = 0.f;
-#pragma unroll
-        for (int hh = 0; hh < Gm::HALVES; ++hh)
-#pragma unroll
-            for (int c = 0; c < Gm::KW / 8; ++c) {
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (rv[j]) v = __ldg(reinterpret_cast<const uint4*>(qrow + hh * 128 + tig * Gm::KW) + c);
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    qw[hh][c * 2 + e / 2][e % 2] = w4[e];
-                    qmax = fmaxf(qmax, fmaxf(fabsf(bf16_to_f32(w4[e] & 0xFFFF)), fabsf(bf16_to_f32(w4[e] >> 16))));
-                }
-            }
-        qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
-        qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
-        int shift = 0;
-        if (qmax > 0.f) {
-            const int e = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFF) - 127;
-            shift = max(-100, min(100, 14 - e));
-        }
-        const float up = __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
-        uint32_t* q32 = reinterpret_cast<uint32_t*>(qsm);
-#pragma unroll
-        for (int hh = 0; hh < Gm::HALVES; ++hh)
-#pragma unroll
-            for (int kk = 0; kk < Gm::KSH; ++kk)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const uint32_t w = qw[hh][kk][e];
-                    q32[((hh * Gm::KSH + kk) * 32 + lane) * 4 + 2 * e + j] =
-                        pack_f16x2(bf16_to_f32(w & 0xFFFF) * up, bf16_to_f32(w >> 16) * up);
-                }
-        cs[j] = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
-        pq[j] = u.L - u.n + (rv[j] ? r / G : 0);
-        lq[j] = (a.window > 0 && pq[j] + 1 > a.window) ? pq[j] + 1 - a.window : 0;
-    }
-
-    // the warp's first position and its last row's window start: a stage of
-    // keys in [wlo1, wpos0] is attended in full by every row of the warp
-    const int wr0 = u.R0 + warp * 16;
-    const bool warp_active = wr0 < u.rows;
-    const int wpos0 = u.L - u.n + wr0 / G;
-    const int wpos1 = u.L - u.n + (min(wr0 + 15, u.rows - 1)) / G;
-    const int wlo1 = (a.window > 0 && wpos1 + 1 > a.window) ? wpos1 + 1 - a.window : 0;
-
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-    float o[Gm::NT][4];
-#pragma unroll
-    for (int nt = 0; nt < Gm::NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-
-    for (int st = 0; st < nst; ++st) {
-        cp_async_wait<kStages - 2>();  // stage st has landed (later ones may be in flight)
-        __syncthreads();               // ... for every thread; and every warp is done with stage st - 1
-        {
-            const int s2 = st + kStages - 1;   // refill the slot stage st - 1 used
-            if (s2 < nst)
-                load_stage<D>(a, bt, hk, sp0 + s2 * Gm::PPS, min(Gm::PPS, sp1 - sp0 - s2 * Gm::PPS),
-                              ring + (s2 % kStages) * Gm::STAGE);
-            cp_async_commit();
-        }
-        if (!warp_active) continue;    // this warp's rows are past the chunk's end
-        const int pgs = sp0 + st * Gm::PPS;
-        const int np = min(Gm::PPS, sp1 - pgs);
-        const int t0 = pgs * kBS;
-        const uint8_t* kst = smem + (st % kStages) * Gm::STAGE;
-        const uint8_t* vst = kst + Gm::PPS * Gm::PAGE;
-
-        // ---- scores S[row][key] = Q K^T; n-tile nt of page p holds keys p*16 + nt*8 + [0, 8)
-        float sc[Gm::PPS][2][4];
-#pragma unroll
-        for (int p = 0; p < Gm::PPS; ++p)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) sc[p][nt][0] = sc[p][nt][1] = sc[p][nt][2] = sc[p][nt][3] = 0.f;
-#pragma unroll
-        for (int hh = 0; hh < Gm::HALVES; ++hh) {
-                uint32_t kw[Gm::PPS][2][Gm::KW / 4];
-#pragma unroll
-                for (int pp = 0; pp < Gm::PPS; ++pp)
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int cc = 0; cc < Gm::KW / 16; ++cc) {
-                            uint4 x = make_uint4(0, 0, 0, 0);
-                            if (pp < np)
-                                x = *reinterpret_cast<const uint4*>(kst + pp * Gm::PAGE + hh * Gm::BOX +
-                                                                    swz<Gm::ROWB>(nt * 8 + gid, tig * Gm::KW + 16 * cc));
-                            kw[pp][nt][4 * cc + 0] = x.x;
-                            kw[pp][nt][4 * cc + 1] = x.y;
-                            kw[pp][nt][4 * cc + 2] = x.z;
-                            kw[pp][nt][4 * cc + 3] = x.w;
-                        }
-#pragma unroll
-                for (int kk = 0; kk < Gm::KSH; ++kk) {
-                    const uint4 qa = qsm[(hh * Gm::KSH + kk) * 32 + lane];
-                    const uint32_t af[4] = {qa.x, qa.y, qa.z, qa.w};
-#pragma unroll
-                    for (int pp = 0; pp < Gm::PPS; ++pp)
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            uint32_t b0, b1;
-                            e4m3x4_to_f16x2x2(kw[pp][nt][kk], b0, b1);
-                            mma_16816(sc[pp][nt], af, b0, b1, sc[pp][nt]);
-                        }
-                }
-        }
-
-        // ---- causal / window mask (not needed where every key of the stage is
-        // attended by every row of the warp), log2 units, running maximum per row
-        const bool interior = np == Gm::PPS && t0 + Gm::PPS * kBS - 1 <= wpos0 && t0 >= wlo1;
-        float mx[2] = {-INFINITY, -INFINITY};
-        if (interior) {
-#pragma unroll
-            for (int p = 0; p < Gm::PPS; ++p)
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        sc[p][nt][e] *= cs[e >> 1];
-                        mx[e >> 1] = fmaxf(mx[e >> 1], sc[p][nt][e]);
-                    }
-        } else {
-#pragma unroll
-            for (int p = 0; p < Gm::PPS; ++p)
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = e >> 1;
-                        const int key = t0 + p * kBS + nt * 8 + 2 * tig + (e & 1);
-                        const bool valid = p < np && rv[j] && key >= lq[j] && key <= pq[j];
-                        const float t = valid ? sc[p][nt][e] * cs[j] : -INFINITY;
-                        sc[p][nt][e] = t;
-                        mx[j] = fmaxf(mx[j], t);
-                    }
-        }
-        float alpha[2], muse[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 1));
-            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 2));
-            const float mn = fmaxf(m[j], mx[j]);
-            muse[j] = mn == -INFINITY ? 0.f : mn;
-            alpha[j] = fast_exp2(m[j] - muse[j]);
-            m[j] = mn;
-        }
-
-        // ---- probabilities: the score accumulators are already the A fragments of P V
-        uint32_t pa[Gm::PPS][4];
-        float ls[2] = {0.f, 0.f};
-#pragma unroll
-        for (int p = 0; p < Gm::PPS; ++p) {
-            float pr[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    pr[nt][e] = fast_exp2(sc[p][nt][e] - muse[e >> 1]);
-                    ls[e >> 1] += pr[nt][e];
-                }
-            pa[p][0] = pack_f16x2(pr[0][0], pr[0][1]);
-            pa[p][1] = pack_f16x2(pr[0][2], pr[0][3]);
-            pa[p][2] = pack_f16x2(pr[1][0], pr[1][1]);
-            pa[p][3] = pack_f16x2(pr[1][2], pr[1][3]);
-        }
-        l[0] = l[0] * alpha[0] + ls[0];
-        l[1] = l[1] * alpha[1] + ls[1];
-
-        // ---- P V tile of this stage in fresh accumulators, folded into O.  The
-        // thread's V bytes: key rows 2tig, 2tig+1, 2tig+8, 2tig+9 of each page,
-        // VW bytes at column gid*VW of each box; keys outside the tile's range
-        // read as zero codes (stale NaN codes never meet a zero probability).
-#pragma unroll
-        for (int hh = 0; hh < Gm::HALVES; ++hh) {
-                uint32_t v[Gm::PPS][4][Gm::VW / 4];
-#pragma unroll
-                for (int pp = 0; pp < Gm::PPS; ++pp)
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int row = 2 * tig + (r & 1) + 8 * (r >> 1);
-                        const int key = t0 + pp * kBS + row;
-                        const bool ok = pp < np && (interior || (key >= u.kmin && key <= u.kmax));
-                        const uint8_t* src = vst + pp * Gm::PAGE + hh * Gm::BOX + swz<Gm::ROWB>(row, gid * Gm::VW);
-                        if constexpr (Gm::VW == 16) {
-                            uint4 x = make_uint4(0, 0, 0, 0);
-                            if (ok) x = *reinterpret_cast<const uint4*>(src);
-                            v[pp][r][0] = x.x; v[pp][r][1] = x.y; v[pp][r][2] = x.z; v[pp][r][3] = x.w;
-                        } else {
-                            uint2 x = make_uint2(0, 0);
-                            if (ok) x = *reinterpret_cast<const uint2*>(src);
-                            v[pp][r][0] = x.x; v[pp][r][1] = x.y;
-                        }
-                    }
-#pragma unroll
-                for (int w = 0; w < Gm::VW / 4; ++w)
-#pragma unroll
-                    for (int s = 0; s < 2; ++s) {
-                        const uint32_t sel = s ? 0x7362u : 0x5140u;
-                        float ot[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                        for (int pp = 0; pp < Gm::PPS; ++pp) {
-                            if (pp < np) {
-                                uint32_t b0[2], b1[2];
-                                e4m3x4_to_f16x2x2(byte_perm(v[pp][0][w], v[pp][1][w], sel), b0[0], b0[1]);
-                                e4m3x4_to_f16x2x2(byte_perm(v[pp][2][w], v[pp][3][w], sel), b1[0], b1[1]);
-                                mma_16816(ot[0], pa[pp], b0[0], b1[0], ot[0]);
-                                mma_16816(ot[1], pa[pp], b0[1], b1[1], ot[1]);
-                            }
-                        }
-#pragma unroll
-                        for (int jj = 0; jj < 2; ++jj) {
-                            const int nt = hh * Gm::VW + 4 * w + 2 * s + jj;
-                            o[nt][0] = fmaf(o[nt][0], alpha[0], ot[jj][0]);
-                            o[nt][1] = fmaf(o[nt][1], alpha[0], ot[jj][1]);
-                            o[nt][2] = fmaf(o[nt][2], alpha[1], ot[jj][2]);
-                            o[nt][3] = fmaf(o[nt][3], alpha[1], ot[jj][3]);
-                        }
-                    }
-            }
-    }
-    cp_async_wait<0>();
-
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        l[j] += __shfl_xor_sync(0xffffffffu, l[j], 1);
-        l[j] += __shfl_xor_sync(0xffffffffu, l[j], 2);
-    }
-
-    // ---- emit: n-tile nt = hh*VW + c, accumulator column n holds dimension
-    // hh*ROWB + n*VW + c, so this thread's two columns (2tig, 2tig+1) are two
-    // contiguous runs of VW dimensions per box
-    const int64_t unit = (static_cast<int64_t>(b) * a.num_kv_heads + hk) * a.tiles + tile;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        if (!rv[j]) continue;
-        const int rr = warp * 16 + gid + 8 * j;   // row within the tile
-        const int r = u.R0 + rr;
-        if (a.splits == 1) {
-            const float so = l[j] > 0.f ? a.v_scale / l[j] : 0.f;
-            uint16_t* orow = a.out + (static_cast<int64_t>(u.q0 + r / G) * a.num_q_heads + hk * G + r % G) * D;
-#pragma unroll
-            for (int hh = 0; hh < Gm::HALVES; ++hh)
-#pragma unroll
-                for (int cn = 0; cn < 2; ++cn) {
-                    uint32_t pk[Gm::VW / 2];
-#pragma unroll
-                    for (int c = 0; c < Gm::VW; c += 2)
-                        pk[c / 2] = pack_bf16x2(o[hh * Gm::VW + c][2 * j + cn] * so,
-                                                o[hh * Gm::VW + c + 1][2 * j + cn] * so);
-                    uint4* dst = reinterpret_cast<uint4*>(orow + hh * Gm::ROWB + (2 * tig + cn) * Gm::VW);
-#pragma unroll
-                    for (int i = 0; i < Gm::VW / 8; ++i)
-                        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
-        } else {
-            const int64_t slot = (unit * a.splits + split) * a.rows + rr;
-            float* po = a.part_o + slot * D;
-#pragma unroll
-            for (int hh = 0; hh < Gm::HALVES; ++hh)
-#pragma unroll
-                for (int cn = 0; cn < 2; ++cn) {
-                    float4* dst = reinterpret_cast<float4*>(po + hh * Gm::ROWB + (2 * tig + cn) * Gm::VW);
-#pragma unroll
-                    for (int i = 0; i < Gm::VW / 4; ++i)
-                        dst[i] = make_float4(o[hh * Gm::VW + 4 * i][2 * j + cn], o[hh * Gm::VW + 4 * i + 1][2 * j + cn],
-                                             o[hh * Gm::VW + 4 * i + 2][2 * j + cn],
-                                             o[hh * Gm::VW + 4 * i + 3][2 * j + cn]);
-                }
-            if (tig == 0) a.part_ml[slot] = make_float2(m[j], l[j]);
-        }
-    }
-}
-
 // ---------------------------------------------------------------------------
-// d = 64 and d = 128 on the 5th-generation tensor cores (tcgen05).
+// The prefill kernel, on the 5th-generation tensor cores (tcgen05).
 //
 // A unit is 128 query rows; thread t of the 4 warps owns row t, which is
 // TMEM lane t of both accumulators.  Per stage of 64 keys (4 pages):
@@ -514,6 +138,14 @@ __global__ void __launch_bounds__(kThreads) paged_prefill_kernel(const Args a) {
 //      columns [64, 64 + d);
 //   5. each thread loads its row of O_tile and folds it into FP32 registers,
 //      O = O * alpha + O_tile: the two-level accumulation.
+// At d = 256 a row's 256 FP32 outputs do not fit in registers beside its
+// scores: the accumulator lives in TMEM columns [256, 512) (zeroed at the
+// start), and steps 4-5 run twice per stage, for output dimensions [0, 128)
+// and [128, 256), through the same 128 O_tile columns.  The fold is then a
+// tcgen05.ld of the tile and of the accumulator, the FMA, and a tcgen05.st
+// back.  The operand tiles take 192 KB of shared memory: one CTA per SM.
+// Every tcgen05.ld/st is warp-collective: all threads execute them, also
+// those whose row lies past the tile's last.
 namespace tcg {
 constexpr int kKeys = 64;                       // keys per stage
 constexpr int kPages = kKeys / kBS;             // 4 pages per stage
@@ -529,27 +161,34 @@ struct TcGeo {
     static constexpr int VT = KT + KP;                            // V^T tile: d rows x 128 B
     static constexpr int STG = VT + D * 128;                      // staging: 2 slots x (K, V: 64 keys x d bytes)
     static constexpr int SLOT = 2 * tcg::kKeys * D;
-    static constexpr int SMEM = STG + 2 * SLOT;                   // 96 KB at d = 128, 56 KB at d = 64
-    static constexpr uint32_t COLS = D == 128 ? 256 : 128;        // S at [0, 64), O_tile at [64, 64 + d)
+    static constexpr int SMEM = STG + 2 * SLOT;                   // 192 KB at d = 256, 96 KB at 128, 56 KB at 64
+    // TMEM: S at [0, 64), O_tile at [64, 64 + min(d, 128)); at d = 256 the
+    // FP32 output accumulator (d columns) at [256, 512)
+    static constexpr uint32_t COLS = D == 256 ? 512 : (D == 128 ? 256 : 128);
+    static constexpr int ON = D == 256 ? 128 : D;                 // N of one P.V MMA group
+    static constexpr uint32_t OACC = 256;                         // d = 256: accumulator columns
     static constexpr int CPR = D / 16;                            // 16-byte chunks per staged key row
+    static constexpr int VPASS = D == 256 ? 2 : 1;                // passes of the V^T conversion
 };
 
 // Staged key row k, 16-byte chunk c: the XOR keeps the conversions' reads free
 // of bank conflicts (8 consecutive keys per K read; 8 keys 8 apart per V read).
+// (At d = 256 a key row is 256 bytes: the XOR of the low 3 chunk bits keeps
+// each 128-byte half's chunks apart in the same way.)
 template <int D>
 __device__ __forceinline__ uint32_t stg_k(int k, int c) {
-    if constexpr (D == 128) return k * 128 + ((c ^ (k & 7)) << 4);
+    if constexpr (D >= 128) return k * D + ((c ^ (k & 7)) << 4);
     else return k * 64 + ((c ^ ((k >> 1) & 3)) << 4);
 }
 template <int D>
 __device__ __forceinline__ uint32_t stg_v(int k, int c) {
-    if constexpr (D == 128) return k * 128 + ((c ^ ((k >> 3) & 7)) << 4);
+    if constexpr (D >= 128) return k * D + ((c ^ ((k >> 3) & 7)) << 4);
     else return k * 64 + ((c ^ ((k >> 3) & 3)) << 4);
 }
 // The same address for a key k = 8 kb + i of key block kb.
 template <int D>
 __device__ __forceinline__ uint32_t stg_v_kb(int k, int kb, int c) {
-    if constexpr (D == 128) return k * 128 + ((c ^ kb) << 4);
+    if constexpr (D >= 128) return k * D + ((c ^ kb) << 4);
     else return k * 64 + ((c ^ (kb & 3)) << 4);
 }
 
@@ -611,19 +250,23 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
     float cs;
     int pq, lq;
     {
-        constexpr int NC = D / 8;  // 16-byte chunks of the bf16 row (8 values each)
+        // 16-byte chunks of the bf16 row (8 values each), in passes of at
+        // most 16 chunks (d = 256 reads its row twice: maximum, then copy)
+        constexpr int NC = D / 8, PC = NC > 16 ? 16 : NC, NP = NC / PC;
         const int tok = rv ? r / G : 0, hq = hk * G + (rv ? r % G : 0);
         const uint4* qrow = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(u.q0 + tok) * a.num_q_heads + hq) * D);
-        uint4 qv[NC];
+        uint4 qv[PC];
         float qmax = 0.f;
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            qv[c] = rv ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
-            const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+        for (int ps = 0; ps < NP; ++ps)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                qmax = fmaxf(qmax, fmaxf(fabsf(bf16_to_f32(w4[e] & 0xFFFF)), fabsf(bf16_to_f32(w4[e] >> 16))));
-        }
+            for (int c = 0; c < PC; ++c) {
+                qv[c] = rv ? __ldg(qrow + ps * PC + c) : make_uint4(0, 0, 0, 0);
+                const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    qmax = fmaxf(qmax, fmaxf(fabsf(bf16_to_f32(w4[e] & 0xFFFF)), fabsf(bf16_to_f32(w4[e] >> 16))));
+            }
         int shift = 0;
         if (qmax > 0.f) {
             const int e = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFF) - 127;
@@ -631,15 +274,19 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
         }
         const float up = __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
-            uint32_t f[4];
+        for (int ps = 0; ps < NP; ++ps)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                f[e] = pack_f16x2(bf16_to_f32(w4[e] & 0xFFFF) * up, bf16_to_f32(w4[e] >> 16) * up);
-            *reinterpret_cast<uint4*>(sm + Tg::QT + (c >> 3) * 16384 + t * 128 + (((c & 7) ^ (t & 7)) << 4)) =
-                make_uint4(f[0], f[1], f[2], f[3]);
-        }
+            for (int cc = 0; cc < PC; ++cc) {
+                const int c = ps * PC + cc;
+                if (NP > 1) qv[cc] = rv ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
+                const uint32_t w4[4] = {qv[cc].x, qv[cc].y, qv[cc].z, qv[cc].w};
+                uint32_t f[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    f[e] = pack_f16x2(bf16_to_f32(w4[e] & 0xFFFF) * up, bf16_to_f32(w4[e] >> 16) * up);
+                *reinterpret_cast<uint4*>(sm + Tg::QT + (c >> 3) * 16384 + t * 128 + (((c & 7) ^ (t & 7)) << 4)) =
+                    make_uint4(f[0], f[1], f[2], f[3]);
+            }
         cs = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
         pq = u.L - u.n + (rv ? r / G : 0);
         lq = (a.window > 0 && pq + 1 > a.window) ? pq + 1 - a.window : 0;
@@ -660,9 +307,18 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
     const uint32_t tm_row = tm + (static_cast<uint32_t>(warp * 32) << 16);   // this warp's 32 lanes
 
     float m = -INFINITY, l = 0.f;
-    float o[D];
+    // FP32 output accumulator: registers at d <= 128, TMEM columns at d = 256
+    float o[D <= 128 ? D : 1];
 #pragma unroll
-    for (int d = 0; d < D; ++d) o[d] = 0.f;
+    for (int d = 0; d < (D <= 128 ? D : 1); ++d) o[d] = 0.f;
+    if constexpr (D == 256) {
+        float z[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = 0.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tc::st32(tm_row + Tg::OACC + 32 * c, z);
+        tc::wait_st();
+    }
     bool fail = false;
     for (int st = 0; st < nst; ++st) {
         cp_async_wait<0>();            // this stage's copies (this thread's) have landed
@@ -701,8 +357,10 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
         }
         // ---- 1b. V^T: thread t (t < d) converts keys [8kb, 8kb + 8) x dims [8db, 8db + 8);
         // keys outside the tile's range (or past the stage's pages) become zeros
-        if (D == 128 || t < D) {
-            const int kb = t & 7, db = t >> 3;
+#pragma unroll
+        for (int vp = 0; vp < Tg::VPASS; ++vp)
+        if (D >= 128 || t < D) {
+            const int kb = t & 7, db = (t >> 3) + 16 * vp;
             uint32_t w[8][2];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -796,35 +454,93 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
             break;
         }
 
-        // ---- 4. O_tile = P V
-        if (t == 0) {
+        // ---- 4. O_tile = P V (d = 256: two halves of 128 output dimensions,
+        // one after the other through the same O_tile columns)
+#pragma unroll
+        for (int oh = 0; oh < D / Tg::ON; ++oh) {
+            if (oh > 0) {  // every row's load of the previous half is done before the MMA overwrites it
+                tc::fence_before_sync();
+                if (__syncthreads_or(fail)) {
+                    fail = true;
+                    break;
+                }
+            }
+            if (t == 0) {
+                tc::fence_after_sync();
+                constexpr uint32_t id_o = tc::idesc_f16_f32(128, Tg::ON);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_f16(tm + 64, tc::desc_k_sw128(sb + Tg::KT + ks * 32),
+                                tc::desc_k_sw128(sb + Tg::VT + oh * Tg::ON * 128 + ks * 32), id_o, ks > 0);
+                tc::commit(&bars[1]);
+            }
+            // bars[1] completes D / ON times per stage
+            fail = !mbar_wait_bounded(&bars[1], (st * (D / Tg::ON) + oh) & 1, a.wait_ns);
             tc::fence_after_sync();
-            constexpr uint32_t id_o = tc::idesc_f16_f32(128, D);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_f16(tm + 64, tc::desc_k_sw128(sb + Tg::KT + ks * 32), tc::desc_k_sw128(sb + Tg::VT + ks * 32),
-                            id_o, ks > 0);
-            tc::commit(&bars[1]);
-        }
-        fail = !mbar_wait_bounded(&bars[1], st & 1, a.wait_ns);
-        tc::fence_after_sync();
 
-        // ---- 5. fold this row's tile into the FP32 output registers
+            // ---- 5. fold this row's tile into the FP32 accumulator,
+            // O = O * alpha + O_tile (IEEE FMA, FP32): the two-level accumulation
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            float x[32];
-            tc::ld32(tm_row + 64 + 32 * c, x);
-            tc::wait_ld(x);
+            for (int c = 0; c < Tg::ON / 32; ++c) {
+                float x[32];
+                tc::ld32(tm_row + 64 + 32 * c, x);
+                if constexpr (D <= 128) {
+                    tc::wait_ld(x);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[32 * c + j] = fmaf(o[32 * c + j], alpha, x[j]);
+                    for (int j = 0; j < 32; ++j) o[32 * c + j] = fmaf(o[32 * c + j], alpha, x[j]);
+                } else {
+                    float y[32];
+                    const uint32_t acc = tm_row + Tg::OACC + oh * Tg::ON + 32 * c;
+                    tc::ld32(acc, y);
+                    tc::wait_ld(x);
+                    tc::wait_ld(y);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) y[j] = fmaf(y[j], alpha, x[j]);
+                    tc::st32(acc, y);
+                }
+            }
+            if constexpr (D == 256) tc::wait_st();
         }
+        // a failed wait (possibly in some threads only) ends the loop at the
+        // next stage's __syncthreads_or, where every thread agrees
         tc::fence_before_sync();
     }
     cp_async_wait<0>();
     fail = __syncthreads_or(fail);
     if (fail) {
         if (t == 0) report(a.err, FP8KV_ERR_TIMEOUT);
-    } else if (rv) {
+    } else if (D == 256 || rv) {
+        if constexpr (D == 256) {
+            // The accumulator moves from TMEM to registers, 32 columns at a
+            // time.  tcgen05.ld is warp-collective (.sync.aligned): every
+            // thread loads, including those whose row is past the tile's
+            // last, and only valid rows store.
+            const int64_t unit = (static_cast<int64_t>(b) * a.num_kv_heads + hk) * a.tiles + tile;
+            const float so = l > 0.f ? a.v_scale / l : 0.f;
+            uint4* orow = reinterpret_cast<uint4*>(a.out + (static_cast<int64_t>(u.q0 + r / G) * a.num_q_heads + hk * G + r % G) * D);
+            const int64_t slot = (unit * a.splits + split) * a.rows + t;
+            float4* po = reinterpret_cast<float4*>(a.part_o + slot * D);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                float x[32];
+                tc::ld32(tm_row + Tg::OACC + 32 * c, x);
+                tc::wait_ld(x);
+                if (!rv) continue;
+                if (a.splits == 1) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        orow[4 * c + i] = make_uint4(pack_bf16x2(x[8 * i] * so, x[8 * i + 1] * so),
+                                                     pack_bf16x2(x[8 * i + 2] * so, x[8 * i + 3] * so),
+                                                     pack_bf16x2(x[8 * i + 4] * so, x[8 * i + 5] * so),
+                                                     pack_bf16x2(x[8 * i + 6] * so, x[8 * i + 7] * so));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        po[8 * c + i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+                }
+            }
+            if (rv && a.splits > 1) a.part_ml[slot] = make_float2(m, l);
+        } else {
         const int64_t unit = (static_cast<int64_t>(b) * a.num_kv_heads + hk) * a.tiles + tile;
         if (a.splits == 1) {
             const float so = l > 0.f ? a.v_scale / l : 0.f;
@@ -839,6 +555,7 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
 #pragma unroll
             for (int c = 0; c < D / 4; ++c) po[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
             a.part_ml[slot] = make_float2(m, l);
+        }
         }
     }
     tc::fence_before_sync();
@@ -942,7 +659,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 // Query rows per tile for a head dimension: the tcgen05 kernel at d = 64 and
 // 128, the mma.sync kernel at d = 256.
-inline int rows_per_tile(int D) { return D <= 128 ? kRowsTC : kRows; }
+inline int rows_per_tile(int) { return kRowsTC; }
 
 Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D, int window, int sms, int per_sm) {
     Plan pl;
@@ -964,13 +681,8 @@ Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D,
 // The prefill kernel for (D, G) and its dynamic shared memory.
 template <int D, int G>
 void kernel_of(void (**fn)(const Args), size_t* smem) {
-    if constexpr (D <= 128) {
-        *fn = paged_prefill_tc_kernel<D, G>;
-        *smem = static_cast<size_t>(TcGeo<D>::SMEM) + 1024;
-    } else {
-        *fn = paged_prefill_kernel<D, G>;
-        *smem = Geo<D>::SMEM;
-    }
+    *fn = paged_prefill_tc_kernel<D, G>;
+    *smem = static_cast<size_t>(TcGeo<D>::SMEM) + 1024;
 }
 
 template <int D>
@@ -1013,7 +725,6 @@ int resident_per_sm(int D, int G) {
 
 template <int D, int G>
 cudaError_t launch(const Args& a, int batch, cudaStream_t s) {
-    // d = 64 and 128 run on tcgen05, d = 256 on mma.sync
     void (*kernel)(const Args) = nullptr;
     size_t smem = 0;
     kernel_of<D, G>(&kernel, &smem);
@@ -1071,7 +782,7 @@ fp8kv_status check_shape(int batch, int max_q_len, int max_seq_len, int num_q_he
     if (!(head_dim == 64 || head_dim == 128 || head_dim == 256) || block_size != kBS ||
         !(G == 1 || G == 2 || G == 4 || G == 8 || G == 16))
         return FP8KV_ERR_UNSUPPORTED;
-    const int64_t tiles = (static_cast<int64_t>(max_q_len) * G + kRows - 1) / kRows;   // the larger count
+    const int64_t tiles = (static_cast<int64_t>(max_q_len) * G + kRowsTC - 1) / kRowsTC;
     if (tiles * kMaxSplits > INT32_MAX) return FP8KV_ERR_UNSUPPORTED;
     return FP8KV_OK;
 }
@@ -1188,7 +899,6 @@ extern "C" fp8kv_status fp8kv_debug_paged_prefill_stall(
     void* stream, int stall_stage, uint64_t wait_limit_ns) {
     if (stall_stage < 0 || wait_limit_ns == 0 || wait_limit_ns > fp8kv::prefill::tcg::kWaitNs)
         return FP8KV_ERR_INVALID_ARG;
-    if (head_dim != 64 && head_dim != 128) return FP8KV_ERR_UNSUPPORTED;  // only the tcgen05 kernel waits
     return prefill_impl(q, num_q_tokens, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                         q_starts, max_q_len, max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size,
                         k_scale, v_scale, sm_scale, window, out, workspace, workspace_bytes, stream, stall_stage,

@@ -437,8 +437,7 @@ fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens, const uint
  *
  * fp8kv_debug_paged_prefill_stall: fp8kv_paged_prefill, except that CTA
  * (0, 0, 0) never issues the score MMAs of stage `stall_stage` and the MMA
- * waits give up after wait_limit_ns nanoseconds.  head_dim 64 or 128 only (the
- * tcgen05 kernel); FP8KV_ERR_UNSUPPORTED otherwise.
+ * waits give up after wait_limit_ns nanoseconds.
  *
  * Both: stall_stage >= 0 and 0 < wait_limit_ns <= 500,000,000, else
  * FP8KV_ERR_INVALID_ARG; all other arguments and errors as the wrapped call.

@@ -92,7 +92,7 @@ def test_decode_stall_hook_rejects_bad_arguments():
                                            w.k_scale, w.v_scale, w.sm_scale, 0, out, ws, stage, ns) == 1
 
 
-@pytest.mark.parametrize("head_dim_base", ["llama31_8b_b8_20k", "gptoss20b_b8_16k"])
+@pytest.mark.parametrize("head_dim_base", ["llama31_8b_b8_20k", "gptoss20b_b8_16k", "gemma4e2b_b16_8k32k"])
 def test_prefill_wait_runs_out_reports_timeout(head_dim_base):
     lens = [700, 300, 129]
     q_lens = [200, 64, 129]
@@ -123,18 +123,3 @@ def test_prefill_wait_runs_out_reports_timeout(head_dim_base):
     ref = oracle.prefill_attention(workload.bf16_bits(q), kc, vc, w.seq_lens.numpy(), np.asarray(q_lens), w.k_scale,
                                    w.v_scale, w.sm_scale, 0, nthreads=oracle.max_threads())
     assert_attn_close_bf16_floor(out2.float().cpu().numpy(), ref, "prefill after a timeout")
-
-
-def test_prefill_stall_hook_is_unsupported_on_the_mma_sync_kernel():
-    lens = [300]
-    shape = workload.small_shape("gemma4e2b_b16_8k32k", 1, 1, 1, needle_margin=None)
-    w = workload.make_workload(shape, seed=5, lens=lens)
-    p = Paged(w, seed=5)
-    p.append_all()
-    q, qs = workload.prefill_queries(w, [16], seed=5)
-    s = w.shape
-    ws = fk.alloc_prefill_workspace(1, 16, w.max_seq_len, s.num_q_heads, s.num_kv_heads, s.head_dim, 16, 0)
-    out = torch.zeros(q.shape, dtype=torch.bfloat16, device="cuda")
-    assert fk.debug_paged_prefill_stall(q.cuda(), p.k_cache, p.v_cache, p.block_tables, p.seq_lens, qs.cuda(), 16,
-                                        w.max_seq_len, w.k_scale, w.v_scale, w.sm_scale, 0, out, ws, 0,
-                                        LIMIT_NS) == 2
