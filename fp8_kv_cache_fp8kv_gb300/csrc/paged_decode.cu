@@ -59,6 +59,7 @@
 #include <mutex>
 
 #include "fp8kv.h"
+#include "trace.cuh"
 #include "partition.cuh"
 #include "ptx.cuh"
 #include "walk.cuh"
@@ -75,6 +76,7 @@ constexpr int kCtasPerSm = 2;
 constexpr int kMaxBatch = 512;             // sequences per launch; larger batches run in chunks
 constexpr int kMaxMergeSplits = 1024;      // CTAs per launch are capped at this (the merge keeps one weight each)
 constexpr int kMinPagesPerCta = 16;
+constexpr int kMaxG = 16;                  // query heads per kv head at most (partial (max, sum) entries per slot)
 constexpr uint64_t kWaitLimitNs = 500000000ull;  // 0.5 s: far beyond any legitimate wait
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -94,7 +96,7 @@ struct DecodeArgs {
     uint16_t* out;              // bf16 [B, Hq, D]
     uint32_t* err;              // workspace error word
     int decode_ctas;            // grid size of the decode kernel (the merge recomputes its split)
-    float2* part_ml;            // [B*Hkv + ctas][8]     (max, sum) in log2 units
+    float2* part_ml;            // [B*Hkv + ctas][kMaxG] (max, sum) in log2 units
     float* part_o;              // [B*Hkv + ctas][G][D]  unnormalised partial outputs
     int64_t num_blocks;
     int max_blocks_per_seq;
@@ -263,7 +265,7 @@ __device__ __forceinline__ float unit_v_scale(const DecodeArgs& a, int hk) {
 
 template <int D, int G>
 __device__ __forceinline__ void load_query(const DecodeArgs& a, int b, int hk, int gid, int tig,
-                                           uint32_t (&qf)[Geo<D>::KS][2], float (&cs)[2]) {
+                                           uint32_t (&qf)[Geo<D>::KS][2], float (&cs)[2], int h0 = 0) {
     using Gm = Geo<D>;
     uint32_t qw[Gm::HALVES][Gm::KSH][2];
     float qmax = 0.f;
@@ -272,8 +274,8 @@ __device__ __forceinline__ void load_query(const DecodeArgs& a, int b, int hk, i
 #pragma unroll
         for (int c = 0; c < Gm::KW / 8; ++c) {
             uint4 v = make_uint4(0, 0, 0, 0);
-            if (gid < G)
-                v = __ldg(reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.num_q_heads + hk * G + gid) * D +
+            if (h0 + gid < G)
+                v = __ldg(reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.num_q_heads + hk * G + h0 + gid) * D +
                                                          hh * 128 + tig * Gm::KW) + c);
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -313,14 +315,14 @@ __device__ __forceinline__ void load_query(const DecodeArgs& a, int b, int hk, i
 // of box hh are elements hh*64 + tig*16 + 4*kk + e and ... + 2 + e.
 template <int D, int G>
 __device__ __forceinline__ void load_query_bf16(const DecodeArgs& a, int b, int hk, int gid, int tig,
-                                                uint32_t (&qf)[Geo<D, 2>::KS][2], float (&cs)[2]) {
+                                                uint32_t (&qf)[Geo<D, 2>::KS][2], float (&cs)[2], int h0 = 0) {
     using Gm = Geo<D, 2>;
 #pragma unroll
     for (int hh = 0; hh < Gm::HALVES; ++hh) {
         uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
-        if (gid < G) {
+        if (h0 + gid < G) {
             const uint4* src = reinterpret_cast<const uint4*>(
-                a.q + (static_cast<int64_t>(b) * a.num_q_heads + hk * G + gid) * D + hh * Gm::DBOX + tig * 16);
+                a.q + (static_cast<int64_t>(b) * a.num_q_heads + hk * G + h0 + gid) * D + hh * Gm::DBOX + tig * 16);
             v0 = __ldg(src);
             v1 = __ldg(src + 1);
         }
@@ -834,7 +836,7 @@ __device__ __forceinline__ void simt_consumers(const DecodeArgs& a, const CtaVie
                     float* po = a.part_o + (slot_idx * G + j) * D + lane * DPL;
 #pragma unroll
                     for (int d = 0; d < DPL; d += 2) *reinterpret_cast<float2*>(po + d) = make_float2(o[j][d], o[j][d + 1]);
-                    if (lane == 0) a.part_ml[slot_idx * 8 + j] = make_float2(m[j], l[j]);
+                    if (lane == 0) a.part_ml[slot_idx * kMaxG + j] = make_float2(m[j], l[j]);
                 }
             }
         }
@@ -1086,14 +1088,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
 // One stage: the np (<= PPS) pages of K at kst and V at vst, holding tokens
 // [tok_base, tok_base + 16*np) of a sequence attended on [lo, L), folded into
-// the running state (m, l, o) of the warp (the g heads on the MMA's n side).
-template <int D, int G, int ES, bool E5M2>
+// the running state (m, l, o) of the warp.  The query heads sit on the MMA's
+// n side, 8 per n-tile: NT = 2 n-tiles carry g = 16 heads, and the converted
+// K and V fragments feed both tiles' MMAs, so each page is read once.
+template <int D, int ES, bool E5M2, int NT>
 __device__ __forceinline__ void tc_stage(const uint8_t* kst, const uint8_t* vst, int np, int tok_base, int lo, int L,
-                                         int gid, int tig, const uint32_t (&qf)[Geo<D, ES>::KS][2],
-                                         const float (&cs)[2], float (&m)[2], float (&l)[2],
-                                         float (&o)[Geo<D, ES>::MT][4]) {
+                                         int gid, int tig, const uint32_t (&qf)[NT][Geo<D, ES>::KS][2],
+                                         const float (&cs)[NT][2], float (&m)[NT][2], float (&l)[NT][2],
+                                         float (&o)[NT][Geo<D, ES>::MT][4]) {
     using Gm = Geo<D, ES>;
-    constexpr bool kEarlyV = Gm::MT == 8;
+    constexpr bool kEarlyV = Gm::MT == 8 && NT == 1;
     // ---- (d = 128) the stage's V fragments into registers first, so their
     // shared-memory latency overlaps the score math
     uint32_t vr[kEarlyV ? Gm::PPS : 1][kEarlyV ? Gm::HALVES : 1][4][Gm::VW / 4];
@@ -1107,12 +1111,15 @@ __device__ __forceinline__ void tc_stage(const uint8_t* kst, const uint8_t* vst,
     }
 
     // ---- scores S^T[token][head] = K Q^T, two accumulator chains per page
-    // (even and odd k-steps) to halve the dependent MMA latency
-    float sc[Gm::PPS][4];
+    // and n-tile (even and odd k-steps) to halve the dependent MMA latency
+    float sc[Gm::PPS][NT][4];
 #pragma unroll
     for (int p = 0; p < Gm::PPS; ++p) {
-        float s1[4] = {0.f, 0.f, 0.f, 0.f};
-        sc[p][0] = sc[p][1] = sc[p][2] = sc[p][3] = 0.f;
+        float s1[NT][4];
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) sc[p][t][r] = s1[t][r] = 0.f;
         if (p < np) {
 #pragma unroll
             for (int hh = 0; hh < Gm::HALVES; ++hh) {
@@ -1127,80 +1134,99 @@ __device__ __forceinline__ void tc_stage(const uint8_t* kst, const uint8_t* vst,
                 }
 #pragma unroll
                 for (int kk = 0; kk < Gm::KSH; ++kk) {
-                    float(&acc)[4] = ((hh * Gm::KSH + kk) & 1) ? s1 : sc[p];
+                    const int ks = hh * Gm::KSH + kk;
                     uint32_t af[4];
                     if constexpr (ES == 1) {
                         codes4_to_f16x2x2<E5M2>(w0[kk], af[0], af[2]);
                         codes4_to_f16x2x2<E5M2>(w1[kk], af[1], af[3]);
-                        mma_16816(acc, af, qf[hh * Gm::KSH + kk][0], qf[hh * Gm::KSH + kk][1], acc);
                     } else {
                         af[0] = w0[2 * kk];
                         af[2] = w0[2 * kk + 1];
                         af[1] = w1[2 * kk];
                         af[3] = w1[2 * kk + 1];
-                        mma_16816_bf16(acc, af, qf[hh * Gm::KSH + kk][0], qf[hh * Gm::KSH + kk][1], acc);
+                    }
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        float(&acc)[4] = (ks & 1) ? s1[t] : sc[p][t];
+                        if constexpr (ES == 1)
+                            mma_16816(acc, af, qf[t][ks][0], qf[t][ks][1], acc);
+                        else
+                            mma_16816_bf16(acc, af, qf[t][ks][0], qf[t][ks][1], acc);
                     }
                 }
             }
         }
 #pragma unroll
-        for (int r = 0; r < 4; ++r) sc[p][r] += s1[r];
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) sc[p][t][r] += s1[t][r];
     }
 
     // ---- mask, scale to log2 units, stage maximum
-    float mx[2] = {-INFINITY, -INFINITY};
+    float mx[NT][2];
     const bool interior = tok_base >= lo && tok_base + np * kBS <= L && np == Gm::PPS;
 #pragma unroll
-    for (int p = 0; p < Gm::PPS; ++p)
+    for (int t = 0; t < NT; ++t) {
+        mx[t][0] = mx[t][1] = -INFINITY;
 #pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-            const int tok = tok_base + p * kBS + gid + 8 * e2;
-            const bool valid = interior || ((p < np) && tok >= lo && tok < L);
+        for (int p = 0; p < Gm::PPS; ++p)
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float t = valid ? sc[p][2 * e2 + j] * cs[j] : -INFINITY;
-                sc[p][2 * e2 + j] = t;
-                mx[j] = fmaxf(mx[j], t);
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int tok = tok_base + p * kBS + gid + 8 * e2;
+                const bool valid = interior || ((p < np) && tok >= lo && tok < L);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float x = valid ? sc[p][t][2 * e2 + j] * cs[t][j] : -INFINITY;
+                    sc[p][t][2 * e2 + j] = x;
+                    mx[t][j] = fmaxf(mx[t][j], x);
+                }
             }
-        }
-    float alpha[2], muse[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
-        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
-        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
-        const float mn = fmaxf(m[j], mx[j]);
-        muse[j] = mn == -INFINITY ? 0.f : mn;
-        alpha[j] = fast_exp2(m[j] - muse[j]);
-        m[j] = mn;
     }
+    float alpha[NT][2], muse[NT][2];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            mx[t][j] = fmaxf(mx[t][j], __shfl_xor_sync(0xffffffffu, mx[t][j], 4));
+            mx[t][j] = fmaxf(mx[t][j], __shfl_xor_sync(0xffffffffu, mx[t][j], 8));
+            mx[t][j] = fmaxf(mx[t][j], __shfl_xor_sync(0xffffffffu, mx[t][j], 16));
+            const float mn = fmaxf(m[t][j], mx[t][j]);
+            muse[t][j] = mn == -INFINITY ? 0.f : mn;
+            alpha[t][j] = fast_exp2(m[t][j] - muse[t][j]);
+            m[t][j] = mn;
+        }
 
     // ---- probabilities -> f16 (bf16 for the bf16 twin) B fragments of the value MMA
-    uint32_t pb[Gm::PPS][2];
-    float lsum[2] = {0.f, 0.f};
+    uint32_t pb[Gm::PPS][NT][2];
 #pragma unroll
-    for (int p = 0; p < Gm::PPS; ++p) {
-        const float p00 = fast_exp2(sc[p][0] - muse[0]);
-        const float p01 = fast_exp2(sc[p][1] - muse[1]);
-        const float p10 = fast_exp2(sc[p][2] - muse[0]);
-        const float p11 = fast_exp2(sc[p][3] - muse[1]);
-        lsum[0] += p00 + p10;
-        lsum[1] += p01 + p11;
-        if constexpr (ES == 1) {
-            pb[p][0] = movmatrix_trans(pack_f16x2(p00, p01));
-            pb[p][1] = movmatrix_trans(pack_f16x2(p10, p11));
-        } else {
-            pb[p][0] = movmatrix_trans(pack_bf16x2(p00, p01));
-            pb[p][1] = movmatrix_trans(pack_bf16x2(p10, p11));
+    for (int t = 0; t < NT; ++t) {
+        float lsum[2] = {0.f, 0.f};
+#pragma unroll
+        for (int p = 0; p < Gm::PPS; ++p) {
+            const float p00 = fast_exp2(sc[p][t][0] - muse[t][0]);
+            const float p01 = fast_exp2(sc[p][t][1] - muse[t][1]);
+            const float p10 = fast_exp2(sc[p][t][2] - muse[t][0]);
+            const float p11 = fast_exp2(sc[p][t][3] - muse[t][1]);
+            lsum[0] += p00 + p10;
+            lsum[1] += p01 + p11;
+            if constexpr (ES == 1) {
+                pb[p][t][0] = movmatrix_trans(pack_f16x2(p00, p01));
+                pb[p][t][1] = movmatrix_trans(pack_f16x2(p10, p11));
+            } else {
+                pb[p][t][0] = movmatrix_trans(pack_bf16x2(p00, p01));
+                pb[p][t][1] = movmatrix_trans(pack_bf16x2(p10, p11));
+            }
         }
+        l[t][0] = l[t][0] * alpha[t][0] + lsum[0];
+        l[t][1] = l[t][1] * alpha[t][1] + lsum[1];
     }
-    l[0] = l[0] * alpha[0] + lsum[0];
-    l[1] = l[1] * alpha[1] + lsum[1];
 
     // ---- P.V tile of this stage: O^T[dim][head] = V^T P^T
-    float ot[Gm::MT][4];
+    float ot[NT][Gm::MT][4];
 #pragma unroll
-    for (int mt = 0; mt < Gm::MT; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int mt = 0; mt < Gm::MT; ++mt) ot[t][mt][0] = ot[t][mt][1] = ot[t][mt][2] = ot[t][mt][3] = 0.f;
 #pragma unroll
     for (int p = 0; p < Gm::PPS; ++p) {
         if (p < np) {
@@ -1224,13 +1250,19 @@ __device__ __forceinline__ void tc_stage(const uint8_t* kst, const uint8_t* vst,
                         const uint32_t x23 = byte_perm(v[2][mtl >> 1], v[3][mtl >> 1], sel);
                         codes4_to_f16x2x2<E5M2>(x01, af[0], af[1]);
                         codes4_to_f16x2x2<E5M2>(x23, af[2], af[3]);
-                        mma_16816(ot[hh * Gm::MTH + mtl], af, pb[p][0], pb[p][1], ot[hh * Gm::MTH + mtl]);
                     } else {
                         af[0] = byte_perm(v[0][mtl], v[1][mtl], 0x5410u);
                         af[1] = byte_perm(v[0][mtl], v[1][mtl], 0x7632u);
                         af[2] = byte_perm(v[2][mtl], v[3][mtl], 0x5410u);
                         af[3] = byte_perm(v[2][mtl], v[3][mtl], 0x7632u);
-                        mma_16816_bf16(ot[hh * Gm::MTH + mtl], af, pb[p][0], pb[p][1], ot[hh * Gm::MTH + mtl]);
+                    }
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        float(&acc)[4] = ot[t][hh * Gm::MTH + mtl];
+                        if constexpr (ES == 1)
+                            mma_16816(acc, af, pb[p][t][0], pb[p][t][1], acc);
+                        else
+                            mma_16816_bf16(acc, af, pb[p][t][0], pb[p][t][1], acc);
                     }
                 }
             }
@@ -1239,12 +1271,14 @@ __device__ __forceinline__ void tc_stage(const uint8_t* kst, const uint8_t* vst,
 
     // ---- fold the tile into the FP32 accumulators
 #pragma unroll
-    for (int mt = 0; mt < Gm::MT; ++mt) {
-        o[mt][0] = fmaf(o[mt][0], alpha[0], ot[mt][0]);
-        o[mt][1] = fmaf(o[mt][1], alpha[1], ot[mt][1]);
-        o[mt][2] = fmaf(o[mt][2], alpha[0], ot[mt][2]);
-        o[mt][3] = fmaf(o[mt][3], alpha[1], ot[mt][3]);
-    }
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int mt = 0; mt < Gm::MT; ++mt) {
+            o[t][mt][0] = fmaf(o[t][mt][0], alpha[t][0], ot[t][mt][0]);
+            o[t][mt][1] = fmaf(o[t][mt][1], alpha[t][1], ot[t][mt][1]);
+            o[t][mt][2] = fmaf(o[t][mt][2], alpha[t][0], ot[t][mt][2]);
+            o[t][mt][3] = fmaf(o[t][mt][3], alpha[t][1], ot[t][mt][3]);
+        }
 }
 
 // Warps and ring depth of the streaming kernel per head dimension.  Two CTAs
@@ -1435,10 +1469,11 @@ __global__ void __launch_bounds__(StreamCfg<D, ES>::NW * 32, kCtasPerSm)
     // ---- compute side: the segments of the CTA's range in order; in each,
     // this warp's share stage by stage, then the CTA's warps merge
     const int gid = lane >> 2, tig = lane & 3;
-    uint32_t qf[Gm::KS][2];
-    float cs[2];
-    float m[2], l[2];
-    float o[Gm::MT][4];
+    constexpr int NT = G > 8 ? 2 : 1;  // n-tiles of 8 query heads
+    uint32_t qf[NT][Gm::KS][2];
+    float cs[NT][2];
+    float m[NT][2], l[NT][2];
+    float o[NT][Gm::MT][4];
     int kst = 0;  // stages computed
     Walker w;
     walk_start(w, pre, B, Hkv, s);
@@ -1450,77 +1485,89 @@ __global__ void __launch_bounds__(StreamCfg<D, ES>::NW * 32, kCtasPerSm)
         const int L = lens[w.b];
         const int lo = first_token(L, a.window);
         const int pg_first = lo / kBS + lp0;
-        if constexpr (ES == 1)
-            load_query<D, G>(a, w.b, w.hk, gid, tig, qf, cs);
-        else
-            load_query_bf16<D, G>(a, w.b, w.hk, gid, tig, qf, cs);
-        m[0] = m[1] = -INFINITY;
-        l[0] = l[1] = 0.f;
 #pragma unroll
-        for (int mt = 0; mt < Gm::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        for (int t = 0; t < NT; ++t) {
+            if constexpr (ES == 1)
+                load_query<D, G>(a, w.b, w.hk, gid, tig, qf[t], cs[t], 8 * t);
+            else
+                load_query_bf16<D, G>(a, w.b, w.hk, gid, tig, qf[t], cs[t], 8 * t);
+            m[t][0] = m[t][1] = -INFINITY;
+            l[t][0] = l[t][1] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < Gm::MT; ++mt) o[t][mt][0] = o[t][mt][1] = o[t][mt][2] = o[t][mt][3] = 0.f;
+        }
 
         for (int p0 = q0; p0 < q1; p0 += Gm::PPS) {
             issue_stage();
             cp_async_wait<R - 1>();
             __syncwarp();
             const uint8_t* kst_p = ring + (kst % R) * kStageBytes;
-            tc_stage<D, G, ES, E5M2>(kst_p, kst_p + kStageHalf, min(Gm::PPS, q1 - p0), (pg_first + p0) * kBS, lo, L,
-                                     gid, tig, qf, cs, m, l, o);
+            tc_stage<D, ES, E5M2, NT>(kst_p, kst_p + kStageHalf, min(Gm::PPS, q1 - p0), (pg_first + p0) * kBS, lo, L,
+                                      gid, tig, qf, cs, m, l, o);
             __syncwarp();  // every lane is done with the slot before it is refilled
             ++kst;
         }
 
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 4);
-            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 8);
-            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 16);
-        }
-
-        // ---- merge the warps' states into warp 0 (tree through smem)
+        for (int t = 0; t < NT; ++t)
 #pragma unroll
-        for (int n = NW; n > 1; n -= n / 2) {
-            const int h = n / 2;
-            if (warp >= n - h && warp < n) publish<Gm::MT>(xbuf + (warp - (n - h)) * Gm::XW * 32, lane, m, l, o);
-            consumer_sync_n<NW>();
-            if (warp < h) absorb<Gm::MT>(xbuf + warp * Gm::XW * 32, lane, m, l, o);
-            consumer_sync_n<NW>();
-        }
+            for (int j = 0; j < 2; ++j) {
+                l[t][j] += __shfl_xor_sync(0xffffffffu, l[t][j], 4);
+                l[t][j] += __shfl_xor_sync(0xffffffffu, l[t][j], 8);
+                l[t][j] += __shfl_xor_sync(0xffffffffu, l[t][j], 16);
+            }
+
+        // ---- merge the warps' states into warp 0 (tree through smem), one
+        // n-tile after the other through the same buffers
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int n = NW; n > 1; n -= n / 2) {
+                const int h = n / 2;
+                if (warp >= n - h && warp < n)
+                    publish<Gm::MT>(xbuf + (warp - (n - h)) * Gm::XW * 32, lane, m[t], l[t], o[t]);
+                consumer_sync_n<NW>();
+                if (warp < h) absorb<Gm::MT>(xbuf + warp * Gm::XW * 32, lane, m[t], l[t], o[t]);
+                consumer_sync_n<NW>();
+            }
 
         // ---- emit: the whole unit in this CTA -> output; else a partial
         const int u = w.b * Hkv + w.hk;
         const int c_first = cta_of(part, w.base);
         const int c_last = cta_of(part, w.base + w.n - 1);
         if (warp == 0) {
-            if (c_first == c_last) {
-                uint16_t* out_u = a.out + (static_cast<int64_t>(w.b) * a.num_q_heads + w.hk * G) * D;
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int h = 2 * tig + j;
-                    const float sc_out = l[j] > 0.f ? unit_v_scale(a, w.hk) / l[j] : 0.f;
-                    if (h < G) {
+            for (int t = 0; t < NT; ++t) {
+                if (c_first == c_last) {
+                    uint16_t* out_u = a.out + (static_cast<int64_t>(w.b) * a.num_q_heads + w.hk * G) * D;
 #pragma unroll
-                        for (int mt = 0; mt < Gm::MT; ++mt)
+                    for (int j = 0; j < 2; ++j) {
+                        const int h = 8 * t + 2 * tig + j;
+                        const float sc_out = l[t][j] > 0.f ? unit_v_scale(a, w.hk) / l[t][j] : 0.f;
+                        if (h < G) {
 #pragma unroll
-                            for (int e2 = 0; e2 < 2; ++e2) {
-                                const int dim = (mt / Gm::MTH) * Gm::DBOX + Gm::VWD * gid + 2 * (mt % Gm::MTH) + e2;
-                                out_u[h * D + dim] = f32_to_bf16(o[mt][2 * e2 + j] * sc_out);
-                            }
+                            for (int mt = 0; mt < Gm::MT; ++mt)
+#pragma unroll
+                                for (int e2 = 0; e2 < 2; ++e2) {
+                                    const int dim = (mt / Gm::MTH) * Gm::DBOX + Gm::VWD * gid + 2 * (mt % Gm::MTH) + e2;
+                                    out_u[h * D + dim] = f32_to_bf16(o[t][mt][2 * e2 + j] * sc_out);
+                                }
+                        }
                     }
-                }
-            } else {
-                const int64_t slot_idx = static_cast<int64_t>(u) + c;
+                } else {
+                    const int64_t slot_idx = static_cast<int64_t>(u) + c;
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int h = 2 * tig + j;
-                    if (h < G) {
-                        float* po = a.part_o + (slot_idx * G + h) * D;
+                    for (int j = 0; j < 2; ++j) {
+                        const int h = 8 * t + 2 * tig + j;
+                        if (h < G) {
+                            float* po = a.part_o + (slot_idx * G + h) * D;
 #pragma unroll
-                        for (int mt = 0; mt < Gm::MT; ++mt)
+                            for (int mt = 0; mt < Gm::MT; ++mt)
 #pragma unroll
-                            for (int e2 = 0; e2 < 2; ++e2)
-                                po[(mt / Gm::MTH) * Gm::DBOX + Gm::VWD * gid + 2 * (mt % Gm::MTH) + e2] = o[mt][2 * e2 + j];
-                        if (gid == 0) a.part_ml[slot_idx * 8 + h] = make_float2(m[j], l[j]);
+                                for (int e2 = 0; e2 < 2; ++e2)
+                                    po[(mt / Gm::MTH) * Gm::DBOX + Gm::VWD * gid + 2 * (mt % Gm::MTH) + e2] = o[t][mt][2 * e2 + j];
+                            if (gid == 0) a.part_ml[slot_idx * kMaxG + h] = make_float2(m[t][j], l[t][j]);
+                        }
                     }
                 }
             }
@@ -1602,7 +1649,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a
         for (int j = 0; j < 8; ++j) {
             const int k = k0 + j * KS;
             if (k < k_u) {
-                ml[j] = a.part_ml[(s0 + k) * 8 + h];
+                ml[j] = a.part_ml[(s0 + k) * kMaxG + h];
                 v[j] = *(reinterpret_cast<const float4*>(a.part_o + ((s0 + k) * G + h) * D) + g4);
             } else {
                 ml[j] = make_float2(-INFINITY, 0.f);
@@ -1682,7 +1729,7 @@ WsLayout ws_layout(int batch, int num_q_heads, int num_kv_heads, int D, const Pl
     const int G = num_q_heads / num_kv_heads;
     WsLayout w;
     w.ml = 256;  // after the header (the error word)
-    w.o = w.ml + align256(slots * 8 * sizeof(float2));
+    w.o = w.ml + align256(slots * kMaxG * sizeof(float2));
     w.total = w.o + align256(slots * G * D * sizeof(float));
     return w;
 }
@@ -1858,6 +1905,9 @@ cudaError_t launch_stream_g(int G, const DecodeArgs& a, int ctas, cudaStream_t s
         case 2: return launch_stream<D, 2, ES, E5M2>(a, ctas, s);
         case 4: return launch_stream<D, 4, ES, E5M2>(a, ctas, s);
         case 8: return launch_stream<D, 8, ES, E5M2>(a, ctas, s);
+        case 16:
+            if constexpr (D <= 128) return launch_stream<D, 16, ES, E5M2>(a, ctas, s);
+            else return cudaErrorInvalidValue;  // g = 16 at d = 256 runs as two units of 8 (head_map)
         default: return cudaErrorInvalidValue;
     }
 }
@@ -1882,18 +1932,20 @@ bool supported(int head_dim, int block_size, int G) {
            (G == 1 || G == 2 || G == 4 || G == 8 || G == 16);
 }
 
-// How the kernels see the heads: g = 16 runs as two units of 8 query heads
-// per cache head (each reads the head's pages; the kernels are built for
-// g <= 8, whose heads fill the MMA's n side).
+// How the kernels see the heads.  The streaming kernel at d <= 128 carries
+// g = 16 natively (two MMA n-tiles of 8 heads on the same K and V fragments:
+// each page is read once).  At d = 256, and on the CUDA-core engine, g = 16
+// runs as two units of 8 query heads per cache head (each reads the head's
+// pages): two n-tiles' accumulators do not fit beside the rest there.
 struct HeadMap {
     int units_per_seq;  // kv-head units per sequence
     int g;              // query heads per unit
     int shift;          // unit -> cache head: hk >> shift
 };
 
-HeadMap head_map(int num_q_heads, int num_kv_heads) {
+HeadMap head_map(int num_q_heads, int num_kv_heads, int head_dim, bool simt) {
     const int G = num_q_heads / num_kv_heads;
-    if (G == 16) return {2 * num_kv_heads, 8, 1};
+    if (G == 16 && (simt || head_dim > 128)) return {2 * num_kv_heads, 8, 1};
     return {num_kv_heads, G, 0};
 }
 
@@ -1908,9 +1960,14 @@ extern "C" size_t fp8kv_paged_decode_workspace_size(int batch, int num_q_heads, 
     if (!supported(head_dim, block_size, num_q_heads / num_kv_heads)) return 0;
     int sms = 0;
     if (device_sms(&sms) != 0) return 0;
-    const HeadMap hm = head_map(num_q_heads, num_kv_heads);
-    const Plan p = make_plan(batch, hm.units_per_seq, head_dim, max_seq_len, window, sms);
-    return ws_layout(batch, num_q_heads, hm.units_per_seq, head_dim, p).total;
+    // enough for either engine (their head mappings differ at g = 16)
+    size_t total = 0;
+    for (const bool simt : {false, true}) {
+        const HeadMap hm = head_map(num_q_heads, num_kv_heads, head_dim, simt);
+        const Plan p = make_plan(batch, hm.units_per_seq, head_dim, max_seq_len, window, sms);
+        total = std::max(total, ws_layout(batch, hm.units_per_seq * hm.g, hm.units_per_seq, head_dim, p).total);
+    }
+    return total;
 }
 
 namespace {
@@ -1947,12 +2004,12 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         return FP8KV_ERR_INVALID_ARG;
     if (!supported(head_dim, block_size, num_q_heads / num_kv_heads)) return FP8KV_ERR_UNSUPPORTED;
     if (es == 2 && head_dim == 256) return FP8KV_ERR_UNSUPPORTED;  // a bf16 page of 8 KB exceeds a stage
-    const HeadMap hm = head_map(num_q_heads, num_kv_heads);
-    const int G = hm.g;
     if (engine != FP8KV_ENGINE_DEFAULT && engine != FP8KV_ENGINE_TENSOR_CORES && engine != FP8KV_ENGINE_CUDA_CORES)
         return FP8KV_ERR_INVALID_ARG;
     const bool simt = engine == FP8KV_ENGINE_CUDA_CORES ||
-                      (engine == FP8KV_ENGINE_DEFAULT && default_is_cuda_cores(head_dim, G));
+                      (engine == FP8KV_ENGINE_DEFAULT && default_is_cuda_cores(head_dim, num_q_heads / num_kv_heads));
+    const HeadMap hm = head_map(num_q_heads, num_kv_heads, head_dim, simt);
+    const int G = hm.g;
     if (num_blocks >= (INT64_C(1) << 31) || num_blocks * num_kv_heads >= (INT64_C(1) << 31))
         return FP8KV_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(max_blocks_per_seq) * block_size < max_seq_len) return FP8KV_ERR_INVALID_ARG;
@@ -2057,6 +2114,7 @@ extern "C" fp8kv_status fp8kv_paged_decode(const void* q, const uint8_t* k_cache
                                            int num_kv_heads, int head_dim, int block_size, float k_scale,
                                            float v_scale, float sm_scale, int window, void* out, void* workspace,
                                            size_t workspace_bytes, void* stream) {
+    FP8KV_TRACE("fp8kv_paged_decode");
     return decode_impl(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
                        seq_lens, max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale,
                        v_scale, sm_scale, window, out, workspace, workspace_bytes, stream, FP8KV_ENGINE_DEFAULT);
@@ -2069,6 +2127,7 @@ extern "C" fp8kv_status fp8kv_paged_decode_engine(const void* q, const uint8_t* 
                                                   int block_size, float k_scale, float v_scale, float sm_scale,
                                                   int window, void* out, void* workspace, size_t workspace_bytes,
                                                   void* stream, int engine) {
+    FP8KV_TRACE("fp8kv_paged_decode_engine");
     return decode_impl(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
                        seq_lens, max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale,
                        v_scale, sm_scale, window, out, workspace, workspace_bytes, stream, engine);
@@ -2080,6 +2139,7 @@ extern "C" fp8kv_status fp8kv_paged_decode_bf16(const void* q, const void* k_cac
                                                 int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                                 int block_size, float sm_scale, int window, void* out,
                                                 void* workspace, size_t workspace_bytes, void* stream) {
+    FP8KV_TRACE("fp8kv_paged_decode_bf16");
     return decode_impl(q, nullptr, nullptr, static_cast<const uint8_t*>(k_cache), static_cast<const uint8_t*>(v_cache),
                        num_blocks, block_tables, max_blocks_per_seq, seq_lens, max_seq_len, batch, num_q_heads,
                        num_kv_heads, head_dim, block_size, 1.0f, 1.0f, sm_scale, window, out, workspace,
@@ -2093,6 +2153,7 @@ extern "C" fp8kv_status fp8kv_paged_decode_per_head(const void* q, const uint8_t
                                                     int head_dim, int block_size, const float* k_scales,
                                                     const float* v_scales, float sm_scale, int window, void* out,
                                                     void* workspace, size_t workspace_bytes, void* stream) {
+    FP8KV_TRACE("fp8kv_paged_decode_per_head");
     if (batch > 0 && (!k_scales || !v_scales)) return FP8KV_ERR_INVALID_ARG;
     return decode_impl(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
                        seq_lens, max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, 1.0f, 1.0f,
@@ -2108,6 +2169,7 @@ extern "C" fp8kv_status fp8kv_decode_step_per_head(const void* q, const void* k_
                                                    const float* k_scales, const float* v_scales, float sm_scale,
                                                    int window, void* out, void* workspace, size_t workspace_bytes,
                                                    void* stream) {
+    FP8KV_TRACE("fp8kv_decode_step_per_head");
     if (batch > 0 && (!k_new || !v_new || !k_scales || !v_scales)) return FP8KV_ERR_INVALID_ARG;
     return decode_impl(q, k_new, v_new, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                        max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, 1.0f, 1.0f, sm_scale,
@@ -2121,6 +2183,7 @@ extern "C" fp8kv_status fp8kv_paged_decode_e5m2(const void* q, const uint8_t* k_
                                                 int block_size, float k_scale, float v_scale, float sm_scale,
                                                 int window, void* out, void* workspace, size_t workspace_bytes,
                                                 void* stream) {
+    FP8KV_TRACE("fp8kv_paged_decode_e5m2");
     return decode_impl(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
                        seq_lens, max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale,
                        v_scale, sm_scale, window, out, workspace, workspace_bytes, stream, FP8KV_ENGINE_TENSOR_CORES,
@@ -2134,6 +2197,7 @@ extern "C" fp8kv_status fp8kv_decode_step_e5m2(const void* q, const void* k_new,
                                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                                float k_scale, float v_scale, float sm_scale, int window, void* out,
                                                void* workspace, size_t workspace_bytes, void* stream) {
+    FP8KV_TRACE("fp8kv_decode_step_e5m2");
     if (batch > 0 && (!k_new || !v_new)) return FP8KV_ERR_INVALID_ARG;
     return decode_impl(q, k_new, v_new, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                        max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale, v_scale,
@@ -2147,6 +2211,7 @@ extern "C" fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, cons
                                           int batch, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                           float k_scale, float v_scale, float sm_scale, int window, void* out,
                                           void* workspace, size_t workspace_bytes, void* stream) {
+    FP8KV_TRACE("fp8kv_decode_step");
     if (batch > 0 && (!k_new || !v_new)) return FP8KV_ERR_INVALID_ARG;
     return decode_impl(q, k_new, v_new, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                        max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale, v_scale,
@@ -2161,6 +2226,7 @@ extern "C" fp8kv_status fp8kv_decode_step_host(const void* h_in, void* d_in, siz
                                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                                float k_scale, float v_scale, float sm_scale, int window, void* out,
                                                void* workspace, size_t workspace_bytes, void* stream) {
+    FP8KV_TRACE("fp8kv_decode_step_host");
     if (batch > 0 && (!k_new || !v_new)) return FP8KV_ERR_INVALID_ARG;
     if ((in_bytes > 0 && (!h_in || !d_in)) || (batch > 0 && !h_out)) return FP8KV_ERR_INVALID_ARG;
     if (batch == 0) {  // nothing to attend: only the inputs move
@@ -2185,6 +2251,7 @@ extern "C" fp8kv_status fp8kv_debug_paged_decode_stall(const void* q, const uint
                                                        int window, void* out, void* workspace,
                                                        size_t workspace_bytes, void* stream, int stall_stage,
                                                        uint64_t wait_limit_ns) {
+    FP8KV_TRACE("fp8kv_debug_paged_decode_stall");
     if (stall_stage < 0 || wait_limit_ns == 0 || wait_limit_ns > kWaitLimitNs) return FP8KV_ERR_INVALID_ARG;
     const StallHook dbg{stall_stage, wait_limit_ns};
     return decode_impl(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
@@ -2237,13 +2304,14 @@ extern "C" fp8kv_status fp8kv_paged_decode_noalloc(const void* q, const uint8_t*
                                                    int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                                    int block_size, float k_scale, float v_scale, float sm_scale,
                                                    int window, void* out, void* stream) {
+    FP8KV_TRACE("fp8kv_paged_decode_noalloc");
     if (batch < 0 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads != 0 || max_seq_len < 0)
         return FP8KV_ERR_INVALID_ARG;
     if (!supported(head_dim, block_size, num_q_heads / num_kv_heads)) return FP8KV_ERR_UNSUPPORTED;
     if (batch == 0) return FP8KV_OK;
     int sms = 0;
     if (device_sms(&sms) != 0) return FP8KV_ERR_CUDA;
-    const HeadMap hm = head_map(num_q_heads, num_kv_heads);
+    const HeadMap hm = head_map(num_q_heads, num_kv_heads, head_dim, false);  // the default engine's
     const Plan p = make_plan(batch, hm.units_per_seq, head_dim, max_seq_len, window, sms);
     const WsLayout w = ws_layout(batch, num_q_heads, hm.units_per_seq, head_dim, p);
     if (w.total > kStaticScratchBytes) return FP8KV_ERR_WORKSPACE;  // problem too large for the fixed array
@@ -2258,6 +2326,7 @@ extern "C" fp8kv_status fp8kv_paged_decode_noalloc(const void* q, const uint8_t*
 }
 
 extern "C" fp8kv_status fp8kv_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+    FP8KV_TRACE("fp8kv_workspace_init");
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FP8KV_ERR_INVALID_ARG;
     return cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? FP8KV_OK
@@ -2265,6 +2334,7 @@ extern "C" fp8kv_status fp8kv_workspace_init(void* workspace, size_t workspace_b
 }
 
 extern "C" fp8kv_status fp8kv_read_error(void* workspace, uint32_t* code, void* stream) {
+    FP8KV_TRACE("fp8kv_read_error");
     if (!workspace || !code) return FP8KV_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t zero = 0;

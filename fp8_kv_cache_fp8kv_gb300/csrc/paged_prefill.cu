@@ -30,6 +30,7 @@
 #include <cstdint>
 
 #include "fp8kv.h"
+#include "trace.cuh"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
 #include "prefill_plan.h"
@@ -885,6 +886,7 @@ extern "C" fp8kv_status fp8kv_paged_prefill(const void* q, int64_t num_q_tokens,
                                             int num_kv_heads, int head_dim, int block_size, float k_scale,
                                             float v_scale, float sm_scale, int window, void* out, void* workspace,
                                             size_t workspace_bytes, void* stream) {
+    FP8KV_TRACE("fp8kv_paged_prefill");
     return prefill_impl(q, num_q_tokens, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                         q_starts, max_q_len, max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size,
                         k_scale, v_scale, sm_scale, window, out, workspace, workspace_bytes, stream, -1,
@@ -897,6 +899,7 @@ extern "C" fp8kv_status fp8kv_debug_paged_prefill_stall(
     int max_q_len, int max_seq_len, int batch, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
     float k_scale, float v_scale, float sm_scale, int window, void* out, void* workspace, size_t workspace_bytes,
     void* stream, int stall_stage, uint64_t wait_limit_ns) {
+    FP8KV_TRACE("fp8kv_debug_paged_prefill_stall");
     if (stall_stage < 0 || wait_limit_ns == 0 || wait_limit_ns > fp8kv::prefill::tcg::kWaitNs)
         return FP8KV_ERR_INVALID_ARG;
     return prefill_impl(q, num_q_tokens, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,

@@ -22,6 +22,7 @@
 #include <cstdint>
 
 #include "fp8kv.h"
+#include "trace.cuh"
 #include "ptx.cuh"
 
 namespace fp8kv {
@@ -145,6 +146,7 @@ extern "C" fp8kv_status fp8kv_quant_append(const void* k_new, const void* v_new,
                                            int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
                                            int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
                                            float k_scale, float v_scale, void* stream) {
+    FP8KV_TRACE("fp8kv_quant_append");
     return append_impl(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, block_size, num_kv_heads,
                        head_dim, k_scale, v_scale, nullptr, nullptr, stream);
 }
@@ -154,6 +156,7 @@ extern "C" fp8kv_status fp8kv_quant_append_per_head(const void* k_new, const voi
                                                     uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks,
                                                     int block_size, int num_kv_heads, int head_dim,
                                                     const float* k_scales, const float* v_scales, void* stream) {
+    FP8KV_TRACE("fp8kv_quant_append_per_head");
     if (num_tokens > 0 && (!k_scales || !v_scales)) return FP8KV_ERR_INVALID_ARG;
     return append_impl(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, block_size, num_kv_heads,
                        head_dim, 1.0f, 1.0f, k_scales, v_scales, stream);
@@ -163,6 +166,7 @@ extern "C" fp8kv_status fp8kv_quant_append_e5m2(const void* k_new, const void* v
                                                 int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
                                                 int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
                                                 float k_scale, float v_scale, void* stream) {
+    FP8KV_TRACE("fp8kv_quant_append_e5m2");
     return append_impl(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, block_size, num_kv_heads,
                        head_dim, k_scale, v_scale, nullptr, nullptr, stream, true);
 }

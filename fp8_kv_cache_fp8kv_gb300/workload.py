@@ -45,8 +45,9 @@ class LayerShape:
         return self.num_q_heads // self.num_kv_heads
 
 
-# The five decode workloads.  "~16K" for the gpt-oss-like layer is read as
-# uniform in [14000, 18000], the same +-2000 spread as the ~20K serving batch.
+# The five decode workloads (and one g = 16 layer).  "~16K" for the
+# gpt-oss-like layer is read as uniform in [14000, 18000], the same +-2000
+# spread as the ~20K serving batch.
 CONFIGS = {
     "llama31_8b_b1_4k": LayerShape("llama31_8b_b1_4k", 32, 8, 128, 1, 4096, 4096, (0,)),
     "llama31_8b_b8_20k": LayerShape("llama31_8b_b8_20k", 32, 8, 128, 8, 18000, 22000, (0,)),
@@ -54,6 +55,9 @@ CONFIGS = {
     "gemma4e2b_b16_8k32k": LayerShape("gemma4e2b_b16_8k32k", 8, 1, 256, 16, 8192, 32768, (0, 512)),
     "llama33_70b_needle_128k": LayerShape("llama33_70b_needle_128k", 64, 8, 128, 1, 131072, 131072,
                                           (0,), kv_std=0.5, needle_margin=12.0),
+    # not one of the five: 16 query heads per kv head, to measure that each
+    # page is read once at g = 16
+    "g16_b4_32k": LayerShape("g16_b4_32k", 64, 4, 128, 4, 28000, 36000, (0,)),
 }
 
 

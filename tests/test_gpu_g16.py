@@ -1,9 +1,11 @@
-"""GPU parity at 16 query heads per kv head (each kv head runs as two units of
-8 query heads over the same pages): the fused step bit-identical to
-append-then-decode, per-head scales against the per-head oracle, the
-allocation-free call bit-identical to the workspace call, and the prefill at
-d = 128 (tcgen05) and d = 64 (mma.sync).  The decode itself, both engines,
-and the bf16 twin are covered with every other head layout."""
+"""GPU parity at 16 query heads per kv head.  The default decode carries the 16
+heads as two MMA n-tiles of one unit per kv head at d <= 128 (each page read
+once); at d = 256 and on the CUDA-core engine each kv head runs as two units
+of 8 query heads over the same pages.  Checked: the fused step bit-identical
+to append-then-decode, per-head scales against the per-head oracle, the
+allocation-free call bit-identical to the workspace call, and the prefill.
+The decode itself, both engines, and the bf16 twin are covered with every
+other head layout, and at full size by the g16_b4_32k workload."""
 import numpy as np
 import pytest
 import torch
