@@ -64,6 +64,9 @@ def parse_args(argv=None):
                    help="time only --config (the default run also times the 128K needle workload as its own record)")
     p.add_argument("--sweep", action="store_true",
                    help="instead of the step: decode time against context length, fp8 cache and bf16 cache")
+    p.add_argument("--copy-probe", action="store_true",
+                   help="instead of the step: build and run the copy-pipeline probe (csrc/probe/copy_probe.cu), "
+                        "the page-streaming rates the decode kernel's design rests on")
     p.add_argument("--prefill", type=str, default=None, metavar="CHUNKS",
                    help="instead of the step: chunked prefill over the fp8 cache of --config, the last CHUNK "
                         "tokens of every sequence as queries, for each comma-separated CHUNK")
@@ -819,6 +822,26 @@ def run_prefill(args, rank, ws):
             "tensor_peak_tflops": tflops_peak, "tensor_peak_source": peak_src, "points": points, "n_gpus": ws}
 
 
+def run_copy_probe(args, rank, ws):
+    """Builds csrc/probe/copy_probe.cu with nvcc and runs it: the 8x20K step's
+    2 KB pages streamed into shared memory by TMA boxes from 2, 4 or 8
+    producer warps per CTA, by per-warp cp.async rings, and by plain loads."""
+    import re
+    src = os.path.join(ROOT, "fp8_kv_cache_fp8kv_gb300", "csrc", "probe", "copy_probe.cu")
+    exe = os.path.join(ROOT, "fp8_kv_cache_fp8kv_gb300", "_build", "copy_probe")
+    os.makedirs(os.path.dirname(exe), exist_ok=True)
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", src, "-o", exe],
+                   check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, check=True)
+    rates = {}
+    for line in r.stdout.splitlines():
+        m = re.match(r"(.+?): ([0-9.]+) us ([0-9.]+) GB/s", line)
+        if m:
+            rates[m.group(1)] = {"us": float(m.group(2)), "gbs": float(m.group(3))}
+    return {"copy_probe": "page streaming into shared memory, no attention math (8x20K step's pages)",
+            "header": r.stdout.splitlines()[0], "rates": rates, "n_gpus": ws}
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -832,8 +855,9 @@ def main(argv=None):
     rank, ws = dist_setup(args)
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU for --impl fp8kv")
-    if args.sweep or args.prefill:
-        line = run_sweep(args, rank, ws) if args.sweep else run_prefill(args, rank, ws)
+    if args.sweep or args.prefill or args.copy_probe:
+        line = (run_sweep(args, rank, ws) if args.sweep else
+                run_prefill(args, rank, ws) if args.prefill else run_copy_probe(args, rank, ws))
         if rank == 0:
             print(json.dumps(line), flush=True)
         return 0
