@@ -13,12 +13,16 @@ roofline of the decode call against the measured HBM peak, an end-to-end
 number through host (pinned) buffers, SM clocks sampled during the timed
 region, and the CPU oracle timed on the host cores.
 
-Timing: W warm-up steps, then K timed steps; workloads that stream more than
-1.5x the L2 size per step run back to back (inputs larger than L2), smaller
-ones get an L2 flush (a device write larger than L2) before every timed step,
-outside the events; CUDA events on the stream
-the library launches on; barrier + synchronize around the region; max over
-ranks.  With --gpus N > 1 (torchrun) every rank runs an independent replica
+Timing: W warm-up steps, then K timed steps back to back between one pair of
+CUDA events on the stream the library launches on; barrier + synchronize
+around the region; max over ranks.  The inputs are larger than L2: a workload
+that streams less than 1.5x the L2 size per step gets several copies of its
+cache ("layers", as the attention layers of one model have), and step i reads
+layer i mod n, so that a layer's pages have left L2 before it comes round
+again.  Where the copies would not fit in 8 GB (the windowed workloads, which
+read a small part of a large cache) every step is timed alone after an L2
+flush (a device write larger than L2, then a read of another buffer larger
+than L2, so that L2 holds no dirty lines), outside the events.  With --gpus N > 1 (torchrun) every rank runs an independent replica
 (the path does not exchange data between GPUs).
 
 --impl reference times the CPU oracle (the only other implementation of this
@@ -233,45 +237,91 @@ def kernel_source_hash():
 
 
 class L2Policy:
-    """Between timed steps: when the step streams more than 1.5x the L2 size
-    there is nothing to flush (inputs larger than L2); otherwise a device
-    buffer larger than L2 is written before every step, outside the events."""
+    """An L2 flush between timed calls when a call streams less than 1.5x the
+    L2 size (else nothing to flush: inputs larger than L2): a device buffer
+    larger than L2 is written, then another one read, so that the next call
+    starts with none of its inputs in L2 and no dirty lines to write back."""
 
     def __init__(self, step_read_bytes, device):
         self.l2 = int(torch.cuda.get_device_properties(device).L2_cache_size)
         self.read = int(step_read_bytes)
-        self.buf = None
+        self.buf = self.rbuf = None
         if self.read <= 3 * self.l2 // 2:
-            self.buf = torch.empty(max(FLUSH_BYTES, 2 * self.l2), dtype=torch.uint8, device=device)
+            n = max(FLUSH_BYTES, 2 * self.l2)
+            self.buf = torch.empty(n, dtype=torch.uint8, device=device)
+            self.rbuf = torch.ones(n, dtype=torch.uint8, device=device)
 
     def __call__(self):
         if self.buf is not None:
             self.buf.zero_()
+            self.rbuf.sum(dtype=torch.int64)
 
     def describe(self):
         if self.buf is None:
             return ("inputs larger than L2: %.0f MB read per step vs %.0f MB L2, no flush"
                     % (self.read / 1e6, self.l2 / 1e6))
-        return ("flushed before every timed step (%.0f MiB device write vs %.0f MB L2, outside the events)"
-                % (self.buf.numel() / 2 ** 20, self.l2 / 1e6))
+        return ("flushed before every timed step (%.0f MiB device write, then a %.0f MiB read, vs %.0f MB L2; "
+                "outside the events)" % (self.buf.numel() / 2 ** 20, self.rbuf.numel() / 2 ** 20, self.l2 / 1e6))
+
+
+class NoFlush:
+    buf = None
+
+    def __call__(self):
+        pass
+
+
+LAYER_BUDGET_BYTES = 8 << 30   # device memory the extra layer caches may take
+
+
+def layer_plan(read_bytes, cache_bytes, device):
+    """How a decode workload keeps its inputs out of L2 between timed steps:
+    (layers, flush).  More than 1.5x L2 read per step: one layer, no flush.
+    Otherwise n = ceil(3 x L2 / read) copies of the cache, read in turn (the
+    other n - 1 layers stream at least 2x L2 between two visits of a layer),
+    when they fit in LAYER_BUDGET_BYTES; else one layer and an L2 flush before
+    every timed step."""
+    l2 = int(torch.cuda.get_device_properties(device).L2_cache_size)
+    if read_bytes > 3 * l2 // 2:
+        return 1, NoFlush()
+    n = -(-3 * l2 // max(1, int(read_bytes)))
+    if n * cache_bytes <= LAYER_BUDGET_BYTES:
+        return n, NoFlush()
+    return 1, L2Policy(read_bytes, device)
+
+
+def describe_layers(layers, flush, read_bytes, cache_bytes, device):
+    l2 = int(torch.cuda.get_device_properties(device).L2_cache_size)
+    if flush.buf is not None:
+        return flush.describe()
+    if layers == 1:
+        return "inputs larger than L2: %.0f MB read per step vs %.0f MB L2, no flush" % (read_bytes / 1e6, l2 / 1e6)
+    return ("inputs larger than L2: %d copies of the %.0f MB cache (layers), step i reads layer i mod %d; "
+            "%.0f MB read per step, %.0f MB by the other layers between two visits of one, vs %.0f MB L2"
+            % (layers, cache_bytes / 1e6, layers, read_bytes / 1e6, (layers - 1) * read_bytes / 1e6, l2 / 1e6))
 
 
 # ---------------------------------------------------------------- the CUDA path
 
 class DecodeStep:
-    """Device state of one workload and one decode step through the C ABI."""
+    """Device state of one workload and one decode step through the C ABI.
+    With layers > 1 the cache is copied that many times (the KV caches of
+    consecutive attention layers) and each call goes to the next layer."""
 
-    def __init__(self, w, window, device):
+    def __init__(self, w, window, device, layers=1):
         from fp8_kv_cache_fp8kv_gb300 import binding as fk
         self.fk = fk
         fk.load(build_if_missing=True)
         s = w.shape
         self.w, self.window, self.dev = w, window, device
         shape = (w.num_blocks, s.num_kv_heads, workload.BLOCK_SIZE, s.head_dim)
-        self.k_cache = torch.zeros(shape, dtype=torch.uint8, device=device)
-        self.v_cache = torch.zeros(shape, dtype=torch.uint8, device=device)
+        k_cache = torch.zeros(shape, dtype=torch.uint8, device=device)
+        v_cache = torch.zeros(shape, dtype=torch.uint8, device=device)
         fk.fp8kv_quant_append(w.k.to(device), w.v.to(device), w.slot_mapping.to(device),
-                              self.k_cache, self.v_cache, w.k_scale, w.v_scale)
+                              k_cache, v_cache, w.k_scale, w.v_scale)
+        self.caches = [(k_cache, v_cache)] + [(k_cache.clone(), v_cache.clone()) for _ in range(layers - 1)]
+        self.k_cache, self.v_cache = k_cache, v_cache
+        self.cache_bytes = 2 * k_cache.numel()
         rows = w.new_token_rows()
         self.h_q = w.q.contiguous()
         self.h_k_new = w.k[rows].contiguous()
@@ -304,32 +354,44 @@ class DecodeStep:
                                      w.max_seq_len, 16, window, device=device)
         torch.cuda.synchronize()
 
-        self._append = fk.prepare_quant_append(self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache,
-                                               w.k_scale, w.v_scale)
-        self._decode = fk.prepare_paged_decode(self.q, self.k_cache, self.v_cache, self.block_tables,
-                                               self.seq_lens, w.max_seq_len, w.k_scale, w.v_scale,
-                                               w.sm_scale, window, self.out, self.ws)
-        self._decode_engine = {
-            e: fk.prepare_paged_decode(self.q, self.k_cache, self.v_cache, self.block_tables, self.seq_lens,
-                                       w.max_seq_len, w.k_scale, w.v_scale, w.sm_scale, window, self.out,
-                                       self.ws, engine=e)
-            for e in (fk.ENGINE_TENSOR_CORES, fk.ENGINE_CUDA_CORES)}
-        self._step = fk.prepare_decode_step(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
-                                            self.block_tables, self.seq_lens, w.max_seq_len, w.k_scale,
-                                            w.v_scale, w.sm_scale, window, self.out, self.ws)
+        self._append, self._decode, self._step = [], [], []
+        self._decode_engine = {fk.ENGINE_TENSOR_CORES: [], fk.ENGINE_CUDA_CORES: []}
+        for kc, vc in self.caches:
+            self._append.append(fk.prepare_quant_append(self.k_new, self.v_new, self.slots, kc, vc,
+                                                        w.k_scale, w.v_scale))
+            self._decode.append(fk.prepare_paged_decode(self.q, kc, vc, self.block_tables, self.seq_lens,
+                                                        w.max_seq_len, w.k_scale, w.v_scale, w.sm_scale, window,
+                                                        self.out, self.ws))
+            for e in self._decode_engine:
+                self._decode_engine[e].append(
+                    fk.prepare_paged_decode(self.q, kc, vc, self.block_tables, self.seq_lens, w.max_seq_len,
+                                            w.k_scale, w.v_scale, w.sm_scale, window, self.out, self.ws, engine=e))
+            self._step.append(fk.prepare_decode_step(self.q, self.k_new, self.v_new, kc, vc, self.block_tables,
+                                                     self.seq_lens, w.max_seq_len, w.k_scale, w.v_scale,
+                                                     w.sm_scale, window, self.out, self.ws))
+        self.layer = 0
+
+    @property
+    def layers(self):
+        return len(self.caches)
+
+    def _next(self):
+        i = self.layer
+        self.layer = (i + 1) % len(self.caches)
+        return i
 
     def append(self):
-        self._append()
+        self._append[self._next()]()
 
     def decode(self):
-        self._decode()
+        self._decode[self._next()]()
 
     def decode_engine(self, engine):
-        self._decode_engine[engine]()
+        self._decode_engine[engine][self._next()]()
 
     def step(self):
         """The decode step: every sequence's newest row appended, then attended."""
-        self._step()
+        self._step[self._next()]()
 
 
 PER_CONFIG = ("llama33_70b_needle_128k",)   # also timed, as their own records, in a default run
@@ -337,10 +399,10 @@ PER_CONFIG = ("llama33_70b_needle_128k",)   # also timed, as their own records, 
 
 def time_steps(st, K, flush, stream):
     """The timed region: K decode steps, returned as total milliseconds and a
-    description.  A workload that streams more than 1.5x the L2 size per step
-    runs its K steps back to back between one pair of CUDA events (inputs
-    larger than L2, nothing to flush); a smaller one gets an L2 flush before
-    every step, outside per-step events."""
+    description.  Inputs larger than L2 (directly, or through the rotation
+    over layer caches): the K steps run back to back between one pair of CUDA
+    events.  Otherwise an L2 flush before every step, outside per-step
+    events."""
     if flush.buf is None:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -388,14 +450,15 @@ def measure_config(args, rank, ws, config, window=None, extras=True):
     dec_bytes = accounting.decode_bytes(lens, s.num_q_heads, s.num_kv_heads, s.head_dim, window)
     app_bytes = accounting.append_bytes(B, s.num_kv_heads, s.head_dim)
     step_bytes = dec_bytes + app_bytes
-    st = DecodeStep(w, window, dev)
+    cache_bytes = 2 * w.num_blocks * s.num_kv_heads * workload.BLOCK_SIZE * s.head_dim
+    layers, flush = layer_plan(dec_bytes, cache_bytes, dev)
+    st = DecodeStep(w, window, dev, layers=layers)
     stream = torch.cuda.current_stream()
-    flush = L2Policy(dec_bytes, dev)
 
     clocks = ClockSampler(torch.cuda.current_device()) if not args.no_clocks else None
     if clocks:
         clocks.start()
-    for _ in range(args.warmup):
+    for _ in range(max(args.warmup, st.layers)):
         st.step()
     torch.cuda.synchronize()
     assert st.fk.fp8kv_read_error(st.ws) == 0
@@ -471,7 +534,7 @@ def measure_config(args, rank, ws, config, window=None, extras=True):
                    "seq_lens": "uniform %d..%d" % (s.len_lo, s.len_hi), "total_tokens": int(sum(lens)),
                    "window": window, "kv_cache": "e4m3, per-tensor k/v scales",
                    "step": "fp8kv_decode_step: append B new tokens + paged decode, one call",
-                   "l2": flush.describe(),
+                   "l2": describe_layers(layers, flush, dec_bytes, cache_bytes, dev),
                    "parallelism": "replicas" if ws > 1 else "1 gpu",
                    "input_sha256": w.digest()[:16]},
         "step_bytes": step_bytes,
@@ -529,25 +592,36 @@ def measure_e2e(st, args, ws, step_bytes, flush):
     w = st.w
     side = torch.cuda.Stream()
 
-    def prepared(stream):
-        return st.fk.prepare_decode_step_host(h_in, st.inputs, h_out, st.q, st.k_new, st.v_new, st.k_cache,
-                                              st.v_cache, st.block_tables, st.seq_lens, w.max_seq_len, w.k_scale,
+    def prepared(stream, layer):
+        kc, vc = st.caches[layer]
+        return st.fk.prepare_decode_step_host(h_in, st.inputs, h_out, st.q, st.k_new, st.v_new, kc, vc,
+                                              st.block_tables, st.seq_lens, w.max_seq_len, w.k_scale,
                                               w.v_scale, w.sm_scale, st.window, st.out, st.ws, stream=stream)
 
-    direct = prepared(side)
-    for _ in range(args.warmup):
-        direct()
+    n = st.layers
+    calls = [prepared(side, i) for i in range(n)]
+    for i in range(max(args.warmup, n)):
+        calls[i % n]()
         side.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=side):
-        prepared(side)()
+    graphs = []
+    for i in range(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            prepared(side, i)()
+        graphs.append(g)
     torch.cuda.synchronize()
+    nxt = [0]
+
+    def direct():
+        calls[nxt[0]]()
+        nxt[0] = (nxt[0] + 1) % n
 
     def run_graph():
-        graph.replay()
+        graphs[nxt[0]].replay()
+        nxt[0] = (nxt[0] + 1) % n
 
     def timed(one, stream):
-        for _ in range(args.warmup):
+        for _ in range(max(args.warmup, n)):
             one()
             stream.synchronize()
         times = []
@@ -573,7 +647,7 @@ def measure_e2e(st, args, ws, step_bytes, flush):
             "us_per_step": round(mean_g * 1e6, 3), "us_per_step_median": round(statistics.median(t_graph) * 1e6, 3),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "call": "fp8kv_decode_step_host (one H2D copy of the packed inputs, the step, one D2H copy of out), "
-                    "captured once in a CUDA graph and replayed every step",
+                    "captured once per layer cache in a CUDA graph and replayed every step",
             "direct_call": {"value": round(ws * step_bytes / mean_d / 1e9, 2), "unit": "GB/s",
                             "us_per_step": round(mean_d * 1e6, 3),
                             "us_per_step_median": round(statistics.median(t_direct) * 1e6, 3),

@@ -45,10 +45,14 @@
 //    supported g and is used only when asked for.
 //  * The softmax max/sum use warp shuffles; P is rounded to f16 for the MMA.
 //  * At the end of a segment the CTA's warps merge through shared memory; a
-//    unit split over several CTAs leaves FP32 partials that a small merge
-//    kernel combines.  It is launched as a programmatic dependent: it derives
-//    the split from the lengths while the decode grid finishes, then waits for
-//    that grid and reads the partials.
+//    unit split over several CTAs leaves FP32 partials.  When the plan gives
+//    units few partials, each such CTA of the tensor-core engine counts its
+//    partial on a per-unit counter in the workspace, and the CTA whose partial
+//    completes the count combines the unit's partials at the end of its range
+//    (one launch per call).  Otherwise, and always in the CUDA-core engine, a
+//    small merge kernel combines them, launched as a programmatic dependent:
+//    it derives the split from the lengths while the decode grid finishes,
+//    then waits for that grid and reads the partials.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -99,6 +103,9 @@ struct DecodeArgs {
     int decode_ctas;            // grid size of the decode kernel (the merge recomputes its split)
     float2* part_ml;            // [B*Hkv + ctas][kMaxG] (max, sum) in log2 units
     float* part_o;              // [B*Hkv + ctas][G][D]  unnormalised partial outputs
+    int32_t* split_cnt;         // [B*Hkv] partials written so far per split unit (tensor-core engine);
+                                // zero between calls: the CTA that completes a unit resets it
+    int inline_merge;           // 1: the CTA that completes a split unit merges it; 0: the merge kernel does
     int64_t num_blocks;
     int max_blocks_per_seq;
     int max_seq_len;
@@ -1282,6 +1289,88 @@ __device__ __forceinline__ void tc_stage(const uint8_t* kst, const uint8_t* vst,
         }
 }
 
+// Combines the k_u partials of unit u (slots u + c_first ...) into its output
+// rows, with all NTHR threads of the CTA.  The partials come from other CTAs
+// of the grid, so they are read through L2: the unit's slots are contiguous,
+// and chunks of them are copied into `stage` (shared memory the streaming no
+// longer needs) by 16-byte cp.async copies issued all at once; thread i then
+// folds (query head, 4 dims) items i, i + NTHR, ... over the chunk (max, then
+// rescale and accumulate).
+template <int D, int G, int NTHR, int STAGE_BYTES>
+__device__ __forceinline__ void merge_unit(const DecodeArgs& a, int u, int c_first, int k_u, int tid,
+                                           uint8_t* stage) {
+    constexpr int NG = D / 4;                      // float4 groups per head
+    constexpr int ITEMS = G * NG;
+    constexpr int IT = (ITEMS + NTHR - 1) / NTHR;  // items per thread
+    constexpr int OB = G * D * 4;                  // bytes of one partial's outputs
+    constexpr int MB = kMaxG * 8;                  // bytes of one partial's (max, sum) entries
+    constexpr int cap = STAGE_BYTES / (OB + MB);   // partials per chunk
+    static_assert(cap >= 1, "the staging area holds at least one partial");
+    const int Hkv = a.num_kv_heads, b = u / Hkv, hk = u - b * Hkv;
+    const int64_t s0 = static_cast<int64_t>(u) + c_first;
+    const float4* so = reinterpret_cast<const float4*>(stage);             // [cap][G][NG]
+    const float2* sml = reinterpret_cast<const float2*>(stage + cap * OB);  // [cap][kMaxG]
+    const uint32_t so_s = smem_u32(stage), sml_s = smem_u32(stage + cap * OB);
+    float M[IT], Lh[IT];
+    float4 acc[IT];
+#pragma unroll
+    for (int j = 0; j < IT; ++j) {
+        M[j] = -INFINITY;
+        Lh[j] = 0.f;
+        acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int k0 = 0; k0 < k_u; k0 += cap) {
+        const int kc = min(cap, k_u - k0);
+        const uint8_t* go = reinterpret_cast<const uint8_t*>(a.part_o + (s0 + k0) * G * D);
+        const uint8_t* gml = reinterpret_cast<const uint8_t*>(a.part_ml + (s0 + k0) * kMaxG);
+        for (int i = tid; i < kc * (OB / 16); i += NTHR) cp_async_16(so_s + i * 16, go + i * 16);
+        for (int i = tid; i < kc * (MB / 16); i += NTHR) cp_async_16(sml_s + i * 16, gml + i * 16);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < IT; ++j) {
+            const int it = tid + j * NTHR;
+            if (it < ITEMS) {
+                const int h = it / NG, g4 = it - (it / NG) * NG;
+                float Mb = M[j];
+                for (int k = 0; k < kc; ++k) Mb = fmaxf(Mb, sml[k * kMaxG + h].x);
+                const float Mbu = Mb == -INFINITY ? 0.f : Mb;
+                const float r = fast_exp2(M[j] - Mbu);
+                float4 x = acc[j];
+                float lx = Lh[j] * r;
+                x.x *= r; x.y *= r; x.z *= r; x.w *= r;
+                for (int k = 0; k < kc; ++k) {
+                    const float2 ml = sml[k * kMaxG + h];
+                    const float f = fast_exp2(ml.x - Mbu);
+                    const float4 v = so[(k * G + h) * NG + g4];
+                    x.x += f * v.x; x.y += f * v.y; x.z += f * v.z; x.w += f * v.w;
+                    lx += f * ml.y;
+                }
+                acc[j] = x;
+                Lh[j] = lx;
+                M[j] = Mb;
+            }
+        }
+        __syncthreads();  // the chunk is consumed before the next one lands
+    }
+    const float vsc = unit_v_scale(a, hk);
+#pragma unroll
+    for (int j = 0; j < IT; ++j) {
+        const int it = tid + j * NTHR;
+        if (it < ITEMS) {
+            const int h = it / NG, g4 = it - (it / NG) * NG;
+            const float sc_out = Lh[j] > 0.f ? vsc / Lh[j] : 0.f;
+            uint16_t* out = a.out + (static_cast<int64_t>(b) * a.num_q_heads + hk * G + h) * D;
+            const uint32_t lo2 =
+                f32_to_bf16(acc[j].x * sc_out) | (static_cast<uint32_t>(f32_to_bf16(acc[j].y * sc_out)) << 16);
+            const uint32_t hi2 =
+                f32_to_bf16(acc[j].z * sc_out) | (static_cast<uint32_t>(f32_to_bf16(acc[j].w * sc_out)) << 16);
+            *reinterpret_cast<uint2*>(out + g4 * 4) = make_uint2(lo2, hi2);
+        }
+    }
+}
+
 // Warps and ring depth of the streaming kernel.  Two CTAs share an SM
 // (228 KB of shared memory, 64K registers).  At d = 256 the larger merge
 // buffers leave room for two ring stages per warp, elsewhere three.  At
@@ -1300,7 +1389,7 @@ template <int D, int ES, int G>
 constexpr size_t stream_smem_bytes() {
     using Sc = StreamCfg<D, ES, G>;
     return 128 + static_cast<size_t>(Sc::NW) * Sc::R * kStageBytes + Sc::NBUF * Geo<D, ES>::XW * 32 * sizeof(float) +
-           (2 * kMaxBatch + 1 + 4) * sizeof(int32_t);
+           (2 * kMaxBatch + 1 + 8) * sizeof(int32_t);
 }
 
 // Dynamic shared memory one of kCtasPerSm resident CTAs may take (228 KB per
@@ -1319,13 +1408,14 @@ __global__ void __launch_bounds__(StreamCfg<D, ES, G>::NW * 32, kCtasPerSm)
     int32_t* pre = reinterpret_cast<int32_t*>(xbuf + Sc::NBUF * Gm::XW * 32);         // [kMaxBatch + 1]
     int32_t* lens = pre + kMaxBatch + 1;                                              // [kMaxBatch]
     volatile int* flag = reinterpret_cast<volatile int*>(lens + kMaxBatch);            // [1] earlier timeout
+    int32_t* mlist = lens + kMaxBatch + 1;  // [0]: units this CTA completes; then (u, c_first, k_u) each
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // This grid may have started before the previous one on the stream
     // finished (programmatic launch): wait for it before reading any input.
     griddep_wait();
-    // The merge kernel that follows may start now: it reads only the lengths
-    // before it waits for this grid's completion.
+    // The next grid on the stream may start its set-up now; it waits for
+    // this grid's completion before it reads anything this grid writes.
     griddep_launch_dependents();
     const int B = a.batch, Hkv = a.num_kv_heads, C = gridDim.x, c = blockIdx.x;
 
@@ -1357,6 +1447,7 @@ __global__ void __launch_bounds__(StreamCfg<D, ES, G>::NW * 32, kCtasPerSm)
         if (lane == 0) {
             pre[B] = run;
             flag[0] = prev_err == FP8KV_ERR_TIMEOUT;
+            mlist[0] = 0;
         }
     }
     __syncthreads();
@@ -1575,15 +1666,44 @@ __global__ void __launch_bounds__(StreamCfg<D, ES, G>::NW * 32, kCtasPerSm)
                     }
                 }
             }
+            if (c_first != c_last && a.inline_merge) {
+                // Publish the partial, then count it.  The CTA that brings the
+                // count to k_u merges the unit once its own range is done (a
+                // range holds at most two split units: its first and its last
+                // segment).
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) {
+                    const int k_u = c_last - c_first + 1;
+                    if (atomicAdd(a.split_cnt + u, 1) == k_u - 1) {
+                        a.split_cnt[u] = 0;  // every partial is in: ready for the next call
+                        __threadfence();
+                        const int i = mlist[0];
+                        mlist[1 + 3 * i] = u;
+                        mlist[2 + 3 * i] = c_first;
+                        mlist[3 + 3 * i] = k_u;
+                        mlist[0] = i + 1;
+                    }
+                }
+            }
         }
         if (seg_end >= e) break;
         walk_next(w, pre, Hkv);
     }
     cp_async_wait<0>();
+
+    // ---- the units this CTA completed: combine their partials into the output
+    // (the rings and the exchange buffers, contiguous, stage the partials)
+    __syncthreads();
+    const int nm = mlist[0];
+    for (int i = 0; i < nm; ++i)
+        merge_unit<D, G, NW * 32, NW * R * kStageBytes + Sc::NBUF * Gm::XW * 32 * static_cast<int>(sizeof(float))>(
+            a, mlist[1 + 3 * i], mlist[2 + 3 * i], mlist[3 + 3 * i], tid, rings);
 }
 
 // Combines the partials of every (sequence, kv head) unit that was split over
-// several CTAs: one CTA per (unit, query head of the group).  Its threads split
+// several CTAs, when the decode grid does not (see merge_inline): one CTA per
+// (unit, query head of the group).  Its threads split
 // the unit's partials into KS slices (8 loads in flight per thread, one online
 // softmax-merge pass), then combine the slices in shared memory.  It starts as
 // a programmatic dependent of the decode grid and waits for that grid's
@@ -1720,8 +1840,28 @@ Plan make_plan(int batch, int num_kv_heads, int D, int max_seq_len, int window, 
     return p;
 }
 
+// Who merges the split units of a tensor-core launch.  The CTA that completes
+// a unit merges it when the unit's partials are few (one SM reads them all
+// through L2: about 25 GB/s measured); otherwise the merge kernel, whose CTAs
+// (one per unit and query head) spread the reading over many SMs.  The
+// partials per unit are estimated from the plan with every sequence at
+// max_seq_len: a unit of n pages meets at most ceil(n / pages per CTA) + 1
+// CTAs.  Shorter sequences only change the speed of the chosen merge.
+constexpr int64_t kInlineMergeBytes = 32 << 10;
+
+bool merge_inline(const Plan& p, int batch, int units_per_seq, int G, int D, int max_seq_len, int window) {
+    if (p.ctas <= 1 || max_seq_len <= 0) return true;
+    const int64_t all_pages = (max_seq_len + kBS - 1) / kBS;
+    int64_t n = all_pages;
+    if (window > 0 && window < max_seq_len) n = std::min<int64_t>(all_pages, (window + kBS - 1) / kBS + 1);
+    const int64_t total = static_cast<int64_t>(batch) * units_per_seq * n;
+    const int64_t per_cta = std::max<int64_t>(1, total / p.ctas);
+    const int64_t k_est = std::min<int64_t>(p.ctas, (n + per_cta - 1) / per_cta + 1);
+    return k_est * G * D * static_cast<int64_t>(sizeof(float)) <= kInlineMergeBytes;
+}
+
 struct WsLayout {
-    size_t ml, o, total;
+    size_t cnt, ml, o, total;  // byte offsets of the split counters, the partial (max, sum), the partial outputs
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -1732,7 +1872,8 @@ WsLayout ws_layout(int batch, int num_q_heads, int num_kv_heads, int D, const Pl
     const size_t slots = units + p.ctas;
     const int G = num_q_heads / num_kv_heads;
     WsLayout w;
-    w.ml = 256;  // after the header (the error word)
+    w.cnt = 256;  // after the header (the error word)
+    w.ml = w.cnt + align256(units * sizeof(int32_t));
     w.o = w.ml + align256(slots * kMaxG * sizeof(float2));
     w.total = w.o + align256(slots * G * D * sizeof(float));
     return w;
@@ -1891,7 +2032,7 @@ cudaError_t launch_stream(const DecodeArgs& a, int ctas, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, stream_decode_kernel<D, G, ES, E5M2>, a);
-    if (e != cudaSuccess || ctas == 1) return e;
+    if (e != cudaSuccess || ctas == 1 || a.inline_merge) return e;  // merged inside the decode grid
     cudaLaunchConfig_t mcfg = {};
     mcfg.gridDim = dim3(a.batch * a.num_kv_heads, G);
     mcfg.blockDim = dim3(kMergeThreads);
@@ -2073,6 +2214,8 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         a.decode_ctas = p.ctas;
         a.part_ml = reinterpret_cast<float2*>(ws + w.ml);
         a.part_o = reinterpret_cast<float*>(ws + w.o);
+        a.split_cnt = reinterpret_cast<int32_t*>(ws + w.cnt);
+        a.inline_merge = !simt && merge_inline(p, nb, hm.units_per_seq, G, head_dim, max_seq_len, window);
         a.num_blocks = num_blocks;
         a.max_blocks_per_seq = max_blocks_per_seq;
         a.max_seq_len = max_seq_len;
@@ -2321,8 +2464,8 @@ extern "C" fp8kv_status fp8kv_paged_decode_noalloc(const void* q, const uint8_t*
     if (w.total > kStaticScratchBytes) return FP8KV_ERR_WORKSPACE;  // problem too large for the fixed array
     void* scratch = static_scratch_address();
     if (scratch == nullptr) return FP8KV_ERR_CUDA;
-    // The array keeps the previous call's contents: the error word must start
-    // at zero.
+    // The array keeps the previous call's contents: the error word and the
+    // split counters must start at zero.
     if (cudaMemsetAsync(scratch, 0, w.ml, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8KV_ERR_CUDA;
     return fp8kv_paged_decode(q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                               max_seq_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, k_scale, v_scale,

@@ -94,6 +94,11 @@ __device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void* src, 
                  : "memory");
 }
 
+// The same copy with the default L2 policy.
+__device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(src) : "memory");
+}
+
 // Closes the calling thread's current group of cp.async copies.
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 

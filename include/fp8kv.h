@@ -95,7 +95,8 @@ size_t fp8kv_paged_decode_workspace_size(int batch, int num_q_heads, int num_kv_
 /*
  * Zero-fills a workspace (asynchronously on `stream`).  A workspace must be
  * zero-filled once before its first fp8kv_paged_decode call; every call that
- * completes leaves it ready for the next one.  After a call that failed with
+ * completes leaves it ready for the next one (its per-unit split counters
+ * back at zero).  After a call that failed with
  * FP8KV_ERR_TIMEOUT the workspace must be zero-filled again.  Calls that share one workspace must be ordered (same
  * stream or explicit dependencies).
  */
@@ -276,7 +277,7 @@ fp8kv_status fp8kv_paged_decode_bf16(const void* q, const void* k_cache, const v
  * G "Attention backend interactions"; V "ACCURACY AT LONG CONTEXT"].
  *
  * Equivalent to fp8kv_quant_append of each sequence's newest row followed by
- * fp8kv_paged_decode, in one launch (plus the split merge): for every b with
+ * fp8kv_paged_decode, in one launch: for every b with
  * L = seq_lens[b] > 0 the row k_new[b] (v_new[b]) is quantised exactly as
  * fp8kv_quant_append does and written at token L-1 of the sequence, i.e. at
  * page block_tables[b][(L-1)/block_size], offset (L-1) % block_size; then the
@@ -334,10 +335,10 @@ fp8kv_status fp8kv_decode_step_host(const void* h_in, void* d_in, size_t in_byte
  *
  * Scratch: a fixed 8 MiB array compiled into the library (every device that
  * loads the library keeps it until the process exits).  The call allocates
- * nothing and calls no allocating routine; it zeroes the array's 256-byte
- * header, which holds the error word (cudaMemsetAsync on `stream`), and then
- * runs the decode.  The split partials need no clearing: every call writes
- * the ones it reads.
+ * nothing and calls no allocating routine; it zeroes the array's header
+ * (the error word) and its per-unit split counters (one cudaMemsetAsync on
+ * `stream`), and then runs the decode.  The split partials need no clearing:
+ * every call writes the ones it reads.
  *   - A problem whose split-merge scratch would exceed 8 MiB is rejected with
  *     FP8KV_ERR_WORKSPACE before anything is launched.
  *   - The first call on each device looks up the array's device address with
