@@ -66,6 +66,8 @@ def parse_args(argv=None):
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-per-config", action="store_true",
                    help="time only --config (the default run also times the 128K needle workload as its own record)")
+    p.add_argument("--sweep-layout", choices=list(SWEEP_LAYOUTS), default="llama",
+                   help="head layout of the --sweep layer")
     p.add_argument("--sweep", action="store_true",
                    help="instead of the step: decode time against context length, fp8 cache and bf16 cache")
     p.add_argument("--copy-probe", action="store_true",
@@ -734,6 +736,8 @@ def run_reference(args, rank, ws):
 # ---------------------------------------------------------------- context sweep
 
 SWEEP_LENS = (1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072)
+# one attention layer, batch 1: (name, q heads, kv heads, head_dim)
+SWEEP_LAYOUTS = {"llama": ("llama31_8b_layer_b1", 32, 8, 128), "gemma": ("gemma4e2b_layer_b1", 8, 1, 256)}
 
 
 def _fit(xs, ys):
@@ -744,18 +748,20 @@ def _fit(xs, ys):
 
 
 def run_sweep(args, rank, ws):
-    """Decode time of one Llama-3.1-8B attention layer (32 q / 8 kv heads,
-    d = 128, batch 1) against context length, for the fp8 cache
-    (fp8kv_paged_decode) and the bf16 cache (fp8kv_paged_decode_bf16): the
-    per-token cost of each and their ratio, the GB300 counterpart of the
-    fitted ITL slopes the pages compare."""
+    """Decode time of one attention layer at batch 1 against context length,
+    for the fp8 cache (fp8kv_paged_decode) and the bf16 cache
+    (fp8kv_paged_decode_bf16): the per-token cost of each and their ratio,
+    the GB300 counterpart of the fitted ITL slopes the pages compare.  Layouts
+    (--sweep-layout): Llama-3.1-8B (32 q / 8 kv heads, d = 128) and
+    gemma-4-E2B-like (8 q / 1 kv head, d = 256)."""
     from fp8_kv_cache_fp8kv_gb300 import binding as fk
     fk.load(build_if_missing=True)
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
     points = []
     for L in SWEEP_LENS:
-        shape = workload.LayerShape("llama31_8b_layer_b1", 32, 8, 128, 1, L, L, (0,))
+        name, hq, hkv, hd = SWEEP_LAYOUTS[args.sweep_layout]
+        shape = workload.LayerShape(name, hq, hkv, hd, 1, L, L, (0,))
         w = workload.make_workload(shape, seed=args.seed, lens=[L])
         s = w.shape
         cshape = (w.num_blocks, s.num_kv_heads, workload.BLOCK_SIZE, s.head_dim)
@@ -785,9 +791,9 @@ def run_sweep(args, rank, ws):
                                     fk.prepare_paged_decode(q, k5, v5, bt, lens, L, ks5, vs5, w.sm_scale, 0, out,
                                                             wsp).args),
         }
-        read = {"fp8": accounting.decode_bytes([L], 32, 8, 128, 0),
-                "e5m2": accounting.decode_bytes([L], 32, 8, 128, 0),
-                "bf16": 2 * accounting.decode_bytes([L], 32, 8, 128, 0)}
+        read = {"fp8": accounting.decode_bytes([L], hq, hkv, hd, 0),
+                "e5m2": accounting.decode_bytes([L], hq, hkv, hd, 0),
+                "bf16": 2 * accounting.decode_bytes([L], hq, hkv, hd, 0)}
         rec = {"context": L}
         for name, call in calls.items():
             flush = L2Policy(read[name], dev)
@@ -819,7 +825,8 @@ def run_sweep(args, rank, ws):
     d_slope = (fit["bf16"]["us_per_1k_tokens"] - fit["fp8"]["us_per_1k_tokens"]) / 1e3
     breakeven = round(d_icpt / d_slope) if d_icpt > 0 and d_slope > 0 else None  # None: fp8 never slower
     return {"sweep": "paged decode time against context length: E4M3 ('fp8') and E5M2 caches vs the bf16 cache",
-            "config": {"workload": "llama31_8b_layer_b1", "num_q_heads": 32, "num_kv_heads": 8, "head_dim": 128,
+            "config": {"workload": SWEEP_LAYOUTS[args.sweep_layout][0], "num_q_heads": SWEEP_LAYOUTS[args.sweep_layout][1],
+                       "num_kv_heads": SWEEP_LAYOUTS[args.sweep_layout][2], "head_dim": SWEEP_LAYOUTS[args.sweep_layout][3],
                        "batch": 1, "block_size": 16, "window": 0, "timer": "CUDA events per call, median of %d"
                        % args.steps},
             "points": points, "fit": fit, "slope_ratio_fp8_over_bf16": round(ratio, 4),
@@ -875,6 +882,10 @@ def run_prefill(args, rank, ws):
         for _ in range(args.warmup):
             call()
         torch.cuda.synchronize()
+        clocks = ClockSampler(torch.cuda.current_device()) if not args.no_clocks else None
+        if clocks:
+            clocks.start()
+        t_wall0 = time.time()
         evs = []
         for _ in range(args.steps):
             flush()
@@ -884,11 +895,16 @@ def run_prefill(args, rank, ws):
             e1.record(stream)
             evs.append((e0, e1))
         torch.cuda.synchronize()
+        t_wall1 = time.time()
+        clk = clocks.summary(t_wall0, t_wall1) if clocks else None
+        if clocks:
+            clocks.stop()
         assert fk.fp8kv_read_error(wsp) == 0
         us = reduce_max(statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3, ws)
         points.append({"chunk": chunk, "workspace_bytes": int(wsp.numel()), "query_rows": int(q_lens.sum()), "us": round(us, 2),
                        "tflops": round(flops / us / 1e6, 2), "frac_of_tensor_peak": round(flops / us / 1e6 / tflops_peak, 4),
-                       "gbs": round(nbytes / us / 1e3, 1), "flops": flops, "bytes": nbytes, "l2": flush.describe()})
+                       "gbs": round(nbytes / us / 1e3, 1), "flops": flops, "bytes": nbytes, "l2": flush.describe(),
+                       "clocks": clk})
         del q, out, wsp
     return {"prefill": "fp8kv_paged_prefill: chunked prefill over the E4M3 cache",
             "config": {"workload": args.config, "window": window, "batch": int(L.size),

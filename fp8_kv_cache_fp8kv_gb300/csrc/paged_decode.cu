@@ -130,7 +130,9 @@ template <int D, int ES = 1>
 struct Geo {
     static constexpr int RB = D * ES;                   // bytes of one token row of one head
     static constexpr int PAGE = kBS * RB;               // bytes of one K (or V) page
-    static constexpr int PPS = kStageHalf / PAGE;       // pages per stage: 4, 2, 1
+    static constexpr int SH = PAGE > kStageHalf ? PAGE : kStageHalf;  // K bytes (and V bytes) per stage
+    static constexpr int SB = 2 * SH;                   // bytes per stage
+    static constexpr int PPS = SH / PAGE;               // pages per stage: 4, 2, 1
     static constexpr int HALVES = RB >= 128 ? RB / 128 : 1;
     static constexpr int ROWB = RB >= 128 ? 128 : RB;   // bytes per smem row of one TMA box
     static constexpr int BOX = kBS * ROWB;              // bytes of one TMA box
@@ -144,7 +146,7 @@ struct Geo {
     static constexpr int MTH = VWD / 2;                 // m-tiles per box
     static constexpr int XW = MT * 4 + 4;               // per-lane words exchanged in the warp merge
     static constexpr int STAGES = XW > 40 ? 8 : 12;     // ring slots (a multiple of kNCW)
-    static_assert(PPS >= 1 && PPS * PAGE == kStageHalf, "stage must hold whole pages");
+    static_assert(PPS >= 1 && PPS * PAGE == SH, "stage must hold whole pages");
     static_assert(STAGES % kNCW == 0, "every consumer warp owns whole ring slots");
     static_assert(32 % PPS == 0, "a 32-page block-id batch holds whole stages");
     static_assert(KSH * HALVES == KS && MTH * HALVES == MT, "boxes cover the head dimension");
@@ -1376,10 +1378,13 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int u, int c_fir
 // buffers leave room for two ring stages per warp, elsewhere three.  At
 // d = 64 (g <= 8, whose registers allow it) 6 warps with two stages each
 // measured 7% faster than 4 warps with three: more warps issuing copies.
+// The bf16 cache at d = 256 has 8 KB pages: a stage is one page of K and one
+// of V (16 KB), and three warps with two stages each fit.
 template <int D, int ES, int G>
 struct StreamCfg {
     static constexpr bool kWide = D == 64 && ES == 1 && G <= 8;
-    static constexpr int NW = kWide ? 6 : 4;                                 // warps per CTA
+    static constexpr bool kBigPage = Geo<D, ES>::SH > kStageHalf;            // bf16 at d = 256: 8 KB pages
+    static constexpr int NW = kWide ? 6 : kBigPage ? 3 : 4;                  // warps per CTA
     static constexpr int R = (Geo<D, ES>::XW > 40 || kWide) ? 2 : 3;         // ring stages per warp
     static constexpr int NBUF = NW / 2;                                      // merge exchange buffers
     static constexpr int CPP = Geo<D, ES>::PAGE / 512;                       // 16-byte copies per lane per page
@@ -1388,7 +1393,7 @@ struct StreamCfg {
 template <int D, int ES, int G>
 constexpr size_t stream_smem_bytes() {
     using Sc = StreamCfg<D, ES, G>;
-    return 128 + static_cast<size_t>(Sc::NW) * Sc::R * kStageBytes + Sc::NBUF * Geo<D, ES>::XW * 32 * sizeof(float) +
+    return 128 + static_cast<size_t>(Sc::NW) * Sc::R * Geo<D, ES>::SB + Sc::NBUF * Geo<D, ES>::XW * 32 * sizeof(float) +
            (2 * kMaxBatch + 1 + 8) * sizeof(int32_t);
 }
 
@@ -1404,7 +1409,7 @@ __global__ void __launch_bounds__(StreamCfg<D, ES, G>::NW * 32, kCtasPerSm)
     constexpr int NW = Sc::NW, R = Sc::R, CPP = Sc::CPP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* rings = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
-    float* xbuf = reinterpret_cast<float*>(rings + NW * R * kStageBytes);            // [NBUF][XW][32]
+    float* xbuf = reinterpret_cast<float*>(rings + NW * R * Gm::SB);                 // [NBUF][XW][32]
     int32_t* pre = reinterpret_cast<int32_t*>(xbuf + Sc::NBUF * Gm::XW * 32);         // [kMaxBatch + 1]
     int32_t* lens = pre + kMaxBatch + 1;                                              // [kMaxBatch]
     volatile int* flag = reinterpret_cast<volatile int*>(lens + kMaxBatch);            // [1] earlier timeout
@@ -1468,7 +1473,7 @@ __global__ void __launch_bounds__(StreamCfg<D, ES, G>::NW * 32, kCtasPerSm)
 
     // ---- this warp's ring and its per-lane copy offsets: lane l copies the
     // 16-byte chunks l, l+32, ... of a page, stored at their swizzled place
-    uint8_t* ring = rings + warp * R * kStageBytes;
+    uint8_t* ring = rings + warp * R * Gm::SB;
     const uint32_t ring_s = smem_u32(ring);
     uint32_t soff[CPP];
 #pragma unroll
@@ -1522,7 +1527,7 @@ __global__ void __launch_bounds__(StreamCfg<D, ES, G>::NW * 32, kCtasPerSm)
     auto issue_stage = [&]() {
         if (cur.pos.valid) {
             const int n = min(Gm::PPS, cur.pos.n - cpos);
-            const uint32_t slot = ring_s + (ist % R) * kStageBytes;
+            const uint32_t slot = ring_s + (ist % R) * Gm::SB;
             for (int p = 0; p < n; ++p) {
                 const int id = __shfl_sync(0xffffffffu, cur.id, cpos + p);
                 const int64_t page = static_cast<int64_t>(max(id, 0)) * Hc + (cur.pos.w.hk >> kvs);
@@ -1544,7 +1549,7 @@ __global__ void __launch_bounds__(StreamCfg<D, ES, G>::NW * 32, kCtasPerSm)
 #pragma unroll
                 for (int i = 0; i < CPP; ++i) {
                     cp_async_16(slot + p * Gm::PAGE + soff[i], ksrc + (lane + 32 * i) * 16, pol);
-                    cp_async_16(slot + kStageHalf + p * Gm::PAGE + soff[i], vsrc + (lane + 32 * i) * 16, pol);
+                    cp_async_16(slot + Gm::SH + p * Gm::PAGE + soff[i], vsrc + (lane + 32 * i) * 16, pol);
                 }
             }
             cpos += n;
@@ -1596,8 +1601,8 @@ __global__ void __launch_bounds__(StreamCfg<D, ES, G>::NW * 32, kCtasPerSm)
             issue_stage();
             cp_async_wait<R - 1>();
             __syncwarp();
-            const uint8_t* kst_p = ring + (kst % R) * kStageBytes;
-            tc_stage<D, ES, E5M2, NT>(kst_p, kst_p + kStageHalf, min(Gm::PPS, q1 - p0), (pg_first + p0) * kBS, lo, L,
+            const uint8_t* kst_p = ring + (kst % R) * Gm::SB;
+            tc_stage<D, ES, E5M2, NT>(kst_p, kst_p + Gm::SH, min(Gm::PPS, q1 - p0), (pg_first + p0) * kBS, lo, L,
                                       gid, tig, qf, cs, m, l, o);
             __syncwarp();  // every lane is done with the slot before it is refilled
             ++kst;
@@ -1697,23 +1702,25 @@ __global__ void __launch_bounds__(StreamCfg<D, ES, G>::NW * 32, kCtasPerSm)
     __syncthreads();
     const int nm = mlist[0];
     for (int i = 0; i < nm; ++i)
-        merge_unit<D, G, NW * 32, NW * R * kStageBytes + Sc::NBUF * Gm::XW * 32 * static_cast<int>(sizeof(float))>(
+        merge_unit<D, G, NW * 32, NW * R * Gm::SB + Sc::NBUF * Gm::XW * 32 * static_cast<int>(sizeof(float))>(
             a, mlist[1 + 3 * i], mlist[2 + 3 * i], mlist[3 + 3 * i], tid, rings);
 }
 
 // Combines the partials of every (sequence, kv head) unit that was split over
 // several CTAs, when the decode grid does not (see merge_inline): one CTA per
-// (unit, query head of the group).  Its threads split
-// the unit's partials into KS slices (8 loads in flight per thread, one online
+// (unit, query head of the group).  Its 4 * D threads split the unit's
+// partials into 16 slices (8 loads in flight per thread, one online
 // softmax-merge pass), then combine the slices in shared memory.  It starts as
 // a programmatic dependent of the decode grid and waits for that grid's
 // completion before reading.
-constexpr int kMergeThreads = 256;
+template <int D>
+__host__ __device__ constexpr int merge_threads() { return 4 * D; }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(merge_threads<D>()) merge_kernel(const DecodeArgs a) {
+    constexpr int kMergeThreads = merge_threads<D>();
     constexpr int NG = D / 4;                // float4 groups per head: 16, 32, 64
-    constexpr int KS = kMergeThreads / NG;   // slices of the partial list: 16, 8, 4
+    constexpr int KS = kMergeThreads / NG;   // slices of the partial list: 16
     __shared__ float sm_m[KS][NG], sm_l[KS][NG];
     __shared__ float4 sm_o[KS][NG];
     griddep_launch_dependents();  // the next call's set-up may overlap this merge
@@ -1999,7 +2006,7 @@ cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeArg
     if (e != cudaSuccess || ctas == 1) return e;  // one CTA: every unit is written directly
     cudaLaunchConfig_t mcfg = {};
     mcfg.gridDim = dim3(a.batch * a.num_kv_heads, G);
-    mcfg.blockDim = dim3(kMergeThreads);
+    mcfg.blockDim = dim3(merge_threads<D>());
     mcfg.dynamicSmemBytes = 0;
     mcfg.stream = stream;
     mcfg.attrs = attr;
@@ -2035,7 +2042,7 @@ cudaError_t launch_stream(const DecodeArgs& a, int ctas, cudaStream_t stream) {
     if (e != cudaSuccess || ctas == 1 || a.inline_merge) return e;  // merged inside the decode grid
     cudaLaunchConfig_t mcfg = {};
     mcfg.gridDim = dim3(a.batch * a.num_kv_heads, G);
-    mcfg.blockDim = dim3(kMergeThreads);
+    mcfg.blockDim = dim3(merge_threads<D>());
     mcfg.dynamicSmemBytes = 0;
     mcfg.stream = stream;
     mcfg.attrs = attr;
@@ -2148,7 +2155,6 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         !std::isfinite(sm_scale))
         return FP8KV_ERR_INVALID_ARG;
     if (!supported(head_dim, block_size, num_q_heads / num_kv_heads)) return FP8KV_ERR_UNSUPPORTED;
-    if (es == 2 && head_dim == 256) return FP8KV_ERR_UNSUPPORTED;  // a bf16 page of 8 KB exceeds a stage
     if (engine != FP8KV_ENGINE_DEFAULT && engine != FP8KV_ENGINE_TENSOR_CORES && engine != FP8KV_ENGINE_CUDA_CORES)
         return FP8KV_ERR_INVALID_ARG;
     const bool simt = engine == FP8KV_ENGINE_CUDA_CORES ||
@@ -2231,7 +2237,9 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         cudaError_t e;
         if (!simt) {
             if (es == 2)
-                e = head_dim == 64 ? launch_stream_g<64, 2>(G, a, p.ctas, s) : launch_stream_g<128, 2>(G, a, p.ctas, s);
+                e = head_dim == 64 ? launch_stream_g<64, 2>(G, a, p.ctas, s)
+                    : head_dim == 128 ? launch_stream_g<128, 2>(G, a, p.ctas, s)
+                                      : launch_stream_g<256, 2>(G, a, p.ctas, s);
             else if (e5m2)
                 e = head_dim == 64 ? launch_stream_g<64, 1, true>(G, a, p.ctas, s)
                     : head_dim == 128 ? launch_stream_g<128, 1, true>(G, a, p.ctas, s)

@@ -11,14 +11,19 @@
 // FP32 registers).
 //
 // How: a unit is (tile of 128 query rows, kv head, sequence); a query row is
-// a (token, query head) pair of the kv head's group.  One kernel,
-// paged_prefill_tc_kernel, for d = 64, 128 and 256, on the 5th-generation
-// tensor cores: tcgen05.mma from swizzled f16 tiles in shared memory, S and
-// the P.V tile in tensor memory, one row per thread (TMEM lane) for the
-// online softmax; see the comment above it.  Each stage's P.V tile is
-// computed in fresh FP32 accumulators and folded into an FP32 output
-// accumulator (O = O * alpha + tile, IEEE FMA): registers at d <= 128, tensor
-// memory at d = 256.  That is the two-level accumulation.  When the units are
+// a (token, query head) pair of the kv head's group.  Two kernels on the
+// 5th-generation tensor cores (tcgen05.mma from swizzled f16 tiles in shared
+// memory, S and the P.V tile in tensor memory, one row per thread (TMEM lane)
+// for the online softmax):
+//  * paged_prefill_ws_kernel (d = 128, chunks of two or more tiles): two
+//    tiles per CTA and warp roles -- converter warps, one MMA-issuing thread,
+//    a softmax-and-fold warpgroup per tile -- that overlap through mbarriers;
+//  * paged_prefill_tc_kernel (d = 64 and 256, and single-tile chunks): one
+//    tile per CTA, its four warps taking each stage's steps in turn.
+// See the comments above them.  Each stage's P.V tile is computed in fresh
+// FP32 accumulators and folded into an FP32 output accumulator (O = O * alpha
+// + tile, IEEE FMA): registers at d <= 128 in the one-tile kernel, tensor
+// memory otherwise.  That is the two-level accumulation.  When the units are
 // too few to fill the GPU, each unit's key range is split over several CTAs
 // whose FP32 partials (row maximum, row sum, unnormalised output) a second
 // kernel merges (split plan: prefill_plan.h).
@@ -197,10 +202,11 @@ __device__ __forceinline__ uint32_t stg_v_kb(int k, int kb, int c) {
 // `dst` (K rows, then V rows).  A block id outside [0, num_blocks) reads
 // block 0 and is reported.
 template <int D>
-__device__ __forceinline__ void load_stage_tc(const Args& a, const int32_t* bt, int hk, int pg, int np, uint32_t dst) {
+__device__ __forceinline__ void load_stage_tc(const Args& a, const int32_t* bt, int hk, int pg, int np, uint32_t dst,
+                                              int tid = threadIdx.x) {
     using Tg = TcGeo<D>;
     constexpr int kChunks = kBS * Tg::CPR;      // 16-byte chunks per page
-    for (int i = threadIdx.x; i < np * kChunks; i += 128) {
+    for (int i = tid; i < np * kChunks; i += 128) {
         const int p = i / kChunks, ci = i % kChunks;
         int id = __ldg(bt + pg + p);
         if (id < 0 || id >= a.num_blocks) {
@@ -212,6 +218,67 @@ __device__ __forceinline__ void load_stage_tc(const Args& a, const int32_t* bt, 
         cp_async16(dst + stg_k<D>(k, c), a.k_cache + base + r * D + c * 16);
         cp_async16(dst + tcg::kKeys * D + stg_v<D>(k, c), a.v_cache + base + r * D + c * 16);
     }
+}
+
+// One stage's operand tiles, by 128 threads (thread index ct): the staged
+// fp8 K rows of the stage's 64 keys into the f16 K tile at kt (64 keys x d,
+// K-major, 128-byte swizzle) and the staged V rows, transposed, into the f16
+// V^T tile at vt (d rows x 64 keys).  Keys outside [kmin, kmax] or past the
+// stage's np pages become zeros in V^T (their scores are masked).
+template <int D>
+__device__ __forceinline__ void convert_stage(const uint8_t* stg, uint8_t* kt, uint8_t* vt, int ct, int t0, int np,
+                                              int kmin, int kmax) {
+    using Tg = TcGeo<D>;
+    // K: thread ct converts CH staged chunks (16 dims each) of key ct & 63
+    {
+        constexpr int CH = D / 32;                        // 8 at d = 256, 4 at 128, 2 at 64
+        const int k = ct & 63, part = ct >> 6;
+#pragma unroll
+        for (int i = 0; i < CH; ++i) {
+            const int c = part * CH + i;                   // staged chunk: dims 16c .. 16c + 15
+            const uint4 x = *reinterpret_cast<const uint4*>(stg + stg_k<D>(k, c));
+            uint32_t f[8];
+            e4m3x4_to_f16x2x2(x.x, f[0], f[1]);
+            e4m3x4_to_f16x2x2(x.y, f[2], f[3]);
+            e4m3x4_to_f16x2x2(x.z, f[4], f[5]);
+            e4m3x4_to_f16x2x2(x.w, f[6], f[7]);
+            const int j = 2 * (c & 3);                     // f16 chunk within the 64-dim block c / 4
+            uint8_t* dst = kt + (c >> 2) * (tcg::kKeys * 128) + k * 128;
+            *reinterpret_cast<uint4*>(dst + ((j ^ (k & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<uint4*>(dst + (((j + 1) ^ (k & 7)) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
+        }
+    }
+    // V^T: thread ct (ct < d) converts keys [8kb, 8kb + 8) x dims [8db, 8db + 8)
+#pragma unroll
+    for (int vp = 0; vp < Tg::VPASS; ++vp)
+        if (D >= 128 || ct < D) {
+            const int kb = ct & 7, db = (ct >> 3) + 16 * vp;
+            uint32_t w[8][2];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = 8 * kb + i, key = t0 + k;
+                uint2 x = make_uint2(0, 0);
+                if (k < np * kBS && key >= kmin && key <= kmax)
+                    x = *reinterpret_cast<const uint2*>(stg + tcg::kKeys * D + stg_v_kb<D>(k, kb, db >> 1) +
+                                                        8 * (db & 1));
+                w[i][0] = x.x;
+                w[i][1] = x.y;
+            }
+            uint32_t vt4[8][4];   // [dim][key pair]
+#pragma unroll
+            for (int i2 = 0; i2 < 4; ++i2)
+#pragma unroll
+                for (int hw = 0; hw < 2; ++hw) {
+                    e4m3x4_to_f16x2x2(byte_perm(w[2 * i2][hw], w[2 * i2 + 1][hw], 0x5140u), vt4[4 * hw + 0][i2],
+                                      vt4[4 * hw + 1][i2]);
+                    e4m3x4_to_f16x2x2(byte_perm(w[2 * i2][hw], w[2 * i2 + 1][hw], 0x7362u), vt4[4 * hw + 2][i2],
+                                      vt4[4 * hw + 3][i2]);
+                }
+#pragma unroll
+            for (int dd = 0; dd < 8; ++dd)
+                *reinterpret_cast<uint4*>(vt + (8 * db + dd) * 128 + ((kb ^ dd) << 4)) =
+                    make_uint4(vt4[dd][0], vt4[dd][1], vt4[dd][2], vt4[dd][3]);
+        }
 }
 
 template <int D, int G>
@@ -337,57 +404,8 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
         const int t0 = pgs * kBS;
         const uint8_t* stg = sm + Tg::STG + (st & 1) * Tg::SLOT;
 
-        // ---- 1a. K: thread t converts CH staged chunks (16 dims each) of key t & 63
-        {
-            constexpr int CH = D / 32;                        // 4 at d = 128, 2 at d = 64
-            const int k = t & 63, part = t >> 6;
-#pragma unroll
-            for (int i = 0; i < CH; ++i) {
-                const int c = part * CH + i;                   // staged chunk: dims 16c .. 16c + 15
-                const uint4 x = *reinterpret_cast<const uint4*>(stg + stg_k<D>(k, c));
-                uint32_t f[8];
-                e4m3x4_to_f16x2x2(x.x, f[0], f[1]);
-                e4m3x4_to_f16x2x2(x.y, f[2], f[3]);
-                e4m3x4_to_f16x2x2(x.z, f[4], f[5]);
-                e4m3x4_to_f16x2x2(x.w, f[6], f[7]);
-                const int j = 2 * (c & 3);                     // f16 chunk within the 64-dim block c / 4
-                uint8_t* dst = sm + Tg::KT + (c >> 2) * (tcg::kKeys * 128) + k * 128;
-                *reinterpret_cast<uint4*>(dst + ((j ^ (k & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
-                *reinterpret_cast<uint4*>(dst + (((j + 1) ^ (k & 7)) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
-            }
-        }
-        // ---- 1b. V^T: thread t (t < d) converts keys [8kb, 8kb + 8) x dims [8db, 8db + 8);
-        // keys outside the tile's range (or past the stage's pages) become zeros
-#pragma unroll
-        for (int vp = 0; vp < Tg::VPASS; ++vp)
-        if (D >= 128 || t < D) {
-            const int kb = t & 7, db = (t >> 3) + 16 * vp;
-            uint32_t w[8][2];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int k = 8 * kb + i, key = t0 + k;
-                uint2 x = make_uint2(0, 0);
-                if (k < np * kBS && key >= u.kmin && key <= u.kmax)
-                    x = *reinterpret_cast<const uint2*>(stg + tcg::kKeys * D + stg_v_kb<D>(k, kb, db >> 1) +
-                                                        8 * (db & 1));
-                w[i][0] = x.x;
-                w[i][1] = x.y;
-            }
-            uint32_t vt[8][4];   // [dim][key pair]
-#pragma unroll
-            for (int i2 = 0; i2 < 4; ++i2)
-#pragma unroll
-                for (int hw = 0; hw < 2; ++hw) {
-                    e4m3x4_to_f16x2x2(byte_perm(w[2 * i2][hw], w[2 * i2 + 1][hw], 0x5140u), vt[4 * hw + 0][i2],
-                                      vt[4 * hw + 1][i2]);
-                    e4m3x4_to_f16x2x2(byte_perm(w[2 * i2][hw], w[2 * i2 + 1][hw], 0x7362u), vt[4 * hw + 2][i2],
-                                      vt[4 * hw + 3][i2]);
-                }
-#pragma unroll
-            for (int dd = 0; dd < 8; ++dd)
-                *reinterpret_cast<uint4*>(sm + Tg::VT + (8 * db + dd) * 128 + ((kb ^ dd) << 4)) =
-                    make_uint4(vt[dd][0], vt[dd][1], vt[dd][2], vt[dd][3]);
-        }
+        // ---- 1. the stage's K and V^T operand tiles
+        convert_stage<D>(stg, sm + Tg::KT, sm + Tg::VT, t, t0, np, u.kmin, u.kmax);
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncthreads();
@@ -567,6 +585,398 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// The warp-specialised prefill kernel (d = 128, chunks of at least two tiles).
+//
+// A CTA takes two consecutive query tiles of one (kv head, sequence), 256
+// rows, and one key range; the K and V operand tiles of each stage are built
+// once for both.  The roles run concurrently and hand work over through
+// mbarriers (every wait bounded):
+//   * warps 8-11 (converters): cp.async the fp8 pages of stage s + 2 into a
+//     3-slot staging ring, then convert stage s into one of two f16 K / V^T
+//     slots (once the MMAs of stage s - 2 have finished reading it);
+//   * one thread of warp 12 (the MMA issuer): per stage and tile, S = Q K^T
+//     into the tile's TMEM columns (once the tile's previous fold has read
+//     them), then, once the tile's P is written, O_tile = P V into the same
+//     columns;
+//   * warps 0-3 and 4-7 (one warpgroup per tile, thread = row = TMEM lane):
+//     load the row of S, online softmax in log2 units, write the row of P
+//     (f16) to shared memory; then fold the row of O_tile into the row's FP32
+//     accumulator in TMEM, O = O * alpha + O_tile (the two-level
+//     accumulation).
+// While one tile's warpgroup runs its softmax or fold, the tensor cores work
+// on the other tile, and the converters prepare the next stage.
+namespace ws {
+constexpr int kTiles = 2;                  // query tiles of 128 rows per CTA
+constexpr int kConvWarp0 = 8;              // warps 8-11 convert
+constexpr int kMmaWarp = 12;               // warp 12 issues the MMAs
+constexpr int kThreads = 13 * 32;
+constexpr int kStg = 3;                    // fp8 staging slots
+constexpr int kKv = 2;                     // f16 K / V^T slots
+constexpr int kConvBar = 2;                // named barrier of the converter warps
+}  // namespace ws
+
+template <int D>
+struct WsGeo {
+    static constexpr int NB = D / 64;
+    static constexpr int QTB = NB * 128 * 128;          // one Q tile: 128 rows x d
+    static constexpr int KTB = NB * tcg::kKeys * 128;   // one K tile: 64 keys x d
+    static constexpr int VTB = D * 128;                 // one V^T tile: d rows x 64 keys
+    static constexpr int PTB = 128 * 128;               // one P tile: 128 rows x 64 keys
+    static constexpr int SLOT = 2 * tcg::kKeys * D;     // one fp8 staging slot: K rows, then V rows
+    static constexpr int QT = 0;
+    static constexpr int KT = QT + ws::kTiles * QTB;
+    static constexpr int VT = KT + ws::kKv * KTB;
+    static constexpr int PT = VT + ws::kKv * VTB;
+    static constexpr int STG = PT + ws::kTiles * PTB;
+    static constexpr int SMEM = STG + ws::kStg * SLOT;  // 208 KB
+    // TMEM per tile: S (64 columns) and O_tile (d columns) share [0, d); the
+    // FP32 output accumulator takes [d, 2d)
+    static constexpr uint32_t TC = 2 * D;
+    static constexpr uint32_t COLS = ws::kTiles * TC;   // 512
+    static_assert(D == 128, "the warp-specialised kernel covers d = 128");
+};
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Named barrier over n threads that also ORs a predicate across them.
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+// A bounded mbarrier wait that also gives up as soon as another thread of the
+// CTA has given up (the shared abort flag); the first to run out sets it.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const Args a) {
+    using Wg = WsGeo<D>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t kv_full[ws::kKv], kv_empty[ws::kKv];
+    __shared__ uint64_t s_full[ws::kTiles], p_full[ws::kTiles], o_full[ws::kTiles], o_free[ws::kTiles];
+    __shared__ uint64_t done_bar;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_sh;
+    volatile int* abort_flag = &abort_sh;
+    uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t sb = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int j = 0; j < ws::kKv; ++j) {
+            mbar_init(&kv_full[j], 128);   // the converter threads
+            mbar_init(&kv_empty[j], 1);    // tcgen05.commit
+        }
+        for (int i = 0; i < ws::kTiles; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 128);    // the tile's warpgroup
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_free[i], 128);
+        }
+        mbar_init(&done_bar, 1);
+        abort_sh = 0;
+        fence_barrier_init();
+    }
+    griddep_wait();                // inputs may come from the previous grid on the stream
+    griddep_launch_dependents();
+    const int b = blockIdx.z, hk = blockIdx.y;
+    const int pair = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
+    Unit u[ws::kTiles];
+    if (!make_unit<G>(a, b, 2 * pair, blockIdx.x == 0 && hk == 0 && tid == 0, u[0])) return;
+    const bool has1 = make_unit<G>(a, b, 2 * pair + 1, false, u[1]);
+    // the pair's keys: the first tile's window starts first, the second tile's rows end last
+    const int kmin = u[0].kmin, kmax = has1 ? u[1].kmax : u[0].kmax;
+    const int pg0 = kmin / kBS, np_all = kmax / kBS - pg0 + 1;
+    const int sp0 = pg0 + static_cast<int>(static_cast<int64_t>(split) * np_all / a.splits);
+    const int sp1 = pg0 + static_cast<int>(static_cast<int64_t>(split + 1) * np_all / a.splits);
+    const int nst = (sp1 - sp0 + tcg::kPages - 1) / tcg::kPages;
+    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
+
+    // ---- role set-up: the warpgroups build their Q tiles; the converters
+    // start the first stages' copies
+    const int ti = warp >> 2;                     // the tile of warps 0-7
+    const int tt = tid & 127;                     // row within the tile
+    const Unit& uu = u[ti < ws::kTiles ? ti : 0];
+    const int r = uu.R0 + tt;
+    const bool rv = warp < 8 && (ti == 0 || has1) && r < uu.rows;
+    float cs = 0.f;
+    int pq = 0, lq = 0, wpos0 = 0, wlo1 = 0;
+    if (warp < 8) {
+        // the bf16 row in 16-byte chunks, read twice (its largest magnitude,
+        // then the copy) to keep few of them in registers
+        constexpr int NC = D / 8;
+        const int tok = rv ? r / G : 0, hq = hk * G + (rv ? r % G : 0);
+        const uint4* qrow =
+            reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(uu.q0 + tok) * a.num_q_heads + hq) * D);
+        float qmax = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < NC; ++c) {
+            const uint4 qv = rv ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
+            const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                qmax = fmaxf(qmax, fmaxf(fabsf(bf16_to_f32(w4[e] & 0xFFFF)), fabsf(bf16_to_f32(w4[e] >> 16))));
+        }
+        int shift = 0;
+        if (qmax > 0.f) {
+            const int e = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFF) - 127;
+            shift = max(-100, min(100, 14 - e));
+        }
+        const float up = __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
+#pragma unroll 4
+        for (int c = 0; c < NC; ++c) {
+            const uint4 qv = rv ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
+            const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+            uint32_t f[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                f[e] = pack_f16x2(bf16_to_f32(w4[e] & 0xFFFF) * up, bf16_to_f32(w4[e] >> 16) * up);
+            *reinterpret_cast<uint4*>(sm + Wg::QT + ti * Wg::QTB + (c >> 3) * 16384 + tt * 128 +
+                                      (((c & 7) ^ (tt & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+        }
+        cs = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
+        pq = uu.L - uu.n + (rv ? r / G : 0);
+        lq = (a.window > 0 && pq + 1 > a.window) ? pq + 1 - a.window : 0;
+        // the warp's first position and its last valid row's window start: a
+        // stage of keys in [wlo1, wpos0] is attended in full by every row of the warp
+        const int wr0 = uu.R0 + (warp & 3) * 32;
+        wpos0 = uu.L - uu.n + wr0 / G;
+        const int wpos1 = uu.L - uu.n + max(0, min(wr0 + 31, uu.rows - 1)) / G;
+        wlo1 = (a.window > 0 && wpos1 + 1 > a.window) ? wpos1 + 1 - a.window : 0;
+        if (!(ti == 0 || has1)) wpos0 = -1;       // no valid row: never the fast path
+    } else if (warp < ws::kMmaWarp) {
+        const int ct = tid - ws::kConvWarp0 * 32;
+        for (int s = 0; s < ws::kStg - 1; ++s) {
+            if (s < nst)
+                load_stage_tc<D>(a, bt, hk, sp0 + s * tcg::kPages, min(tcg::kPages, sp1 - sp0 - s * tcg::kPages),
+                                 sb + Wg::STG + s * Wg::SLOT, ct);
+            cp_async_commit();
+        }
+    }
+    if (warp == 0) tc::alloc(&tmem_base, Wg::COLS);
+    tc::fence_proxy_async_smem();  // the Q tiles are read by the tensor cores
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = tmem_base;
+
+    const int ntl = has1 ? 2 : 1;             // tiles with rows (the second one of a pair may have none)
+    float m = -INFINITY, l = 0.f;
+    if (warp < 8 && ti < ntl) {
+        // ---------------------------------------------------------- softmax and fold of tile ti
+        const uint32_t trow = tm + ti * Wg::TC + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        {
+            float z[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) z[j] = 0.f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tc::st32(trow + D + 32 * c, z);
+            tc::wait_st();
+        }
+        uint8_t* prow = sm + Wg::PT + ti * Wg::PTB + tt * 128;
+        for (int st = 0; st < nst; ++st) {
+            bool ok = wait_or_abort(&s_full[ti], st & 1, a.wait_ns, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) break;   // warp-uniform: the TMEM loads below are collective
+            tc::fence_after_sync();
+            const int pgs = sp0 + st * tcg::kPages;
+            const int np = min(tcg::kPages, sp1 - pgs);
+            const int t0 = pgs * kBS;
+            const bool interior = np == tcg::kPages && t0 + tcg::kKeys - 1 <= wpos0 && t0 >= wlo1;
+            float sv[64];
+            tc::ld32(trow, *reinterpret_cast<float(*)[32]>(sv));
+            tc::ld32(trow + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
+            tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv));
+            tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv + 32));
+            float mx = -INFINITY;
+            if (interior) {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    sv[j] *= cs;
+                    mx = fmaxf(mx, sv[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const int key = t0 + j;
+                    const bool valid = j < np * kBS && rv && key >= lq && key <= pq;
+                    sv[j] = valid ? sv[j] * cs : -INFINITY;
+                    mx = fmaxf(mx, sv[j]);
+                }
+            }
+            const float mn = fmaxf(m, mx);
+            const float muse = mn == -INFINITY ? 0.f : mn;
+            const float alpha = fast_exp2(m - muse);
+            m = mn;
+            float ls = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t pw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = fast_exp2(sv[8 * c + 2 * e] - muse), p1 = fast_exp2(sv[8 * c + 2 * e + 1] - muse);
+                    ls += p0 + p1;
+                    pw[e] = pack_f16x2(p0, p1);
+                }
+                *reinterpret_cast<uint4*>(prow + ((c ^ (tt & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            }
+            l = l * alpha + ls;
+            tc::fence_proxy_async_smem();  // P is read by the tensor cores
+            tc::fence_before_sync();
+            mbar_arrive(&p_full[ti]);
+            ok = wait_or_abort(&o_full[ti], st & 1, a.wait_ns, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc::fence_after_sync();
+            // O = O * alpha + O_tile (IEEE FMA, FP32): the two-level accumulation
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                float x[32], y[32];
+                tc::ld32(trow + 32 * c, x);
+                tc::ld32(trow + D + 32 * c, y);
+                tc::wait_ld(x);
+                tc::wait_ld(y);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) y[j] = fmaf(y[j], alpha, x[j]);
+                tc::st32(trow + D + 32 * c, y);
+            }
+            tc::wait_st();
+            tc::fence_before_sync();
+            mbar_arrive(&o_free[ti]);      // the MMA may overwrite S / O_tile
+        }
+    } else if (warp >= 8 && warp < ws::kMmaWarp) {
+        // ---------------------------------------------------------- converters
+        const int ct = tid - ws::kConvWarp0 * 32;
+        for (int st = 0; st < nst; ++st) {
+            const int nxt = st + ws::kStg - 1;
+            if (nxt < nst)
+                load_stage_tc<D>(a, bt, hk, sp0 + nxt * tcg::kPages, min(tcg::kPages, sp1 - sp0 - nxt * tcg::kPages),
+                                 sb + Wg::STG + (nxt % ws::kStg) * Wg::SLOT, ct);
+            cp_async_commit();
+            cp_async_wait<ws::kStg - 1>();   // this thread's copies of stage st have landed
+            const int j = st & 1;
+            // the f16 slot is free once the MMAs of stage st - 2 have completed
+            const bool ok = st < ws::kKv || wait_or_abort(&kv_empty[j], ((st >> 1) + 1) & 1, a.wait_ns, abort_flag);
+            if (named_bar_or(ws::kConvBar, 128, !ok)) break;   // every copy of stage st landed (or all give up)
+            const int pgs = sp0 + st * tcg::kPages;
+            convert_stage<D>(sm + Wg::STG + (st % ws::kStg) * Wg::SLOT, sm + Wg::KT + j * Wg::KTB,
+                             sm + Wg::VT + j * Wg::VTB, ct, pgs * kBS, min(tcg::kPages, sp1 - pgs), kmin, kmax);
+            tc::fence_proxy_async_smem();    // the tiles are read by the tensor cores
+            mbar_arrive(&kv_full[j]);
+            named_bar_sync(ws::kConvBar, 128);  // the staging slot is read before it is refilled
+        }
+        cp_async_wait<0>();
+    } else if (warp == ws::kMmaWarp && lane == 0) {
+        // ---------------------------------------------------------- MMA issuer
+        constexpr uint32_t id_s = tc::idesc_f16_f32(128, tcg::kKeys);
+        constexpr uint32_t id_o = tc::idesc_f16_f32(128, D);
+        const bool stall_cta = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+        for (int st = 0; st < nst; ++st) {
+            const int j = st & 1;
+            if (!wait_or_abort(&kv_full[j], (st >> 1) & 1, a.wait_ns, abort_flag)) break;
+            tc::fence_after_sync();
+            bool ok = true;
+            for (int i = 0; i < ntl && ok; ++i) {
+                if (st > 0 && !wait_or_abort(&o_free[i], (st - 1) & 1, a.wait_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                if (st == a.stall_stage && stall_cta) continue;   // test hook: this tile's S never arrives
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks & 3) * 32;
+                    tc::mma_f16(tm + i * Wg::TC,
+                                tc::desc_k_sw128(sb + Wg::QT + i * Wg::QTB + (ks >> 2) * 16384 + off),
+                                tc::desc_k_sw128(sb + Wg::KT + j * Wg::KTB + (ks >> 2) * (tcg::kKeys * 128) + off),
+                                id_s, ks > 0);
+                }
+                tc::commit(&s_full[i]);
+            }
+            for (int i = 0; i < ntl && ok; ++i) {
+                if (!wait_or_abort(&p_full[i], st & 1, a.wait_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_f16(tm + i * Wg::TC, tc::desc_k_sw128(sb + Wg::PT + i * Wg::PTB + ks * 32),
+                                tc::desc_k_sw128(sb + Wg::VT + j * Wg::VTB + ks * 32), id_o, ks > 0);
+                tc::commit(&o_full[i]);
+            }
+            if (!ok) break;
+            tc::commit(&kv_empty[j]);   // the slot's MMAs (both tiles) have completed
+        }
+        // every MMA this thread issued completes before TMEM is released
+        tc::commit(&done_bar);
+        mbar_wait_bounded(&done_bar, 0, tcg::kWaitNs);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const bool failed = *abort_flag != 0;
+    if (failed) {
+        if (tid == 0) report(a.err, FP8KV_ERR_TIMEOUT);
+    } else if (warp < 8 && (ti == 0 || has1)) {
+        // ---- the rows' outputs (or partials) from the TMEM accumulator; every
+        // thread of the warp loads (tcgen05.ld is collective), valid rows store
+        const uint32_t trow = tm + ti * Wg::TC + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const int tile = 2 * pair + ti;
+        const int64_t unit = (static_cast<int64_t>(b) * a.num_kv_heads + hk) * a.tiles + tile;
+        const float so = l > 0.f ? a.v_scale / l : 0.f;
+        uint4* orow = reinterpret_cast<uint4*>(
+            a.out + (static_cast<int64_t>(uu.q0 + (rv ? r / G : 0)) * a.num_q_heads + hk * G + (rv ? r % G : 0)) * D);
+        const int64_t slot = (unit * a.splits + split) * a.rows + tt;
+        float4* po = reinterpret_cast<float4*>(a.part_o + slot * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            float x[32];
+            tc::ld32(trow + D + 32 * c, x);
+            tc::wait_ld(x);
+            if (!rv) continue;
+            if (a.splits == 1) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    orow[4 * c + i] = make_uint4(pack_bf16x2(x[8 * i] * so, x[8 * i + 1] * so),
+                                                 pack_bf16x2(x[8 * i + 2] * so, x[8 * i + 3] * so),
+                                                 pack_bf16x2(x[8 * i + 4] * so, x[8 * i + 5] * so),
+                                                 pack_bf16x2(x[8 * i + 6] * so, x[8 * i + 7] * so));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) po[8 * c + i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+            }
+        }
+        if (rv && a.splits > 1) a.part_ml[slot] = make_float2(m, l);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::dealloc(tm, Wg::COLS);
+    }
+}
+
 // Combines a unit's split partials row by row in FP32: with M the largest
 // row maximum, weight_s = 2^(m_s - M), out = v_scale * sum_s weight_s o_s /
 // sum_s weight_s l_s, rounded to bf16.  A CTA covers 8 rows of a unit, a
@@ -658,18 +1068,30 @@ struct Plan {
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Query rows per tile for a head dimension: the tcgen05 kernel at d = 64 and
-// 128, the mma.sync kernel at d = 256.
+// Query rows per tile (one TMEM lane each).
 inline int rows_per_tile(int) { return kRowsTC; }
+
+// Query tiles of 128 rows per (sequence, kv head) for a chunk of max_q_len.
+inline int tiles_of(int max_q_len, int G) {
+    return static_cast<int>((static_cast<int64_t>(max_q_len) * G + kRowsTC - 1) / kRowsTC);
+}
+
+// Which kernel runs: the warp-specialised one (two tiles per CTA) at d = 128
+// when a sequence's chunk spans at least two tiles; otherwise
+// paged_prefill_tc_kernel, one tile per CTA (at d = 64 its 56 KB of shared
+// memory let several CTAs share an SM, which measured faster).
+inline bool uses_ws(int D, int tiles) { return D == 128 && tiles >= 2; }
 
 Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D, int window, int sms, int per_sm) {
     Plan pl;
     const int rows = rows_per_tile(D);
-    pl.tiles = static_cast<int>((static_cast<int64_t>(max_q_len) * G + rows - 1) / rows);
+    pl.tiles = tiles_of(max_q_len, G);
+    const int tpc = uses_ws(D, pl.tiles) ? ws::kTiles : 1;   // tiles per CTA
     const int64_t units = static_cast<int64_t>(pl.tiles) * Hkv * batch;
+    const int64_t ctas = static_cast<int64_t>((pl.tiles + tpc - 1) / tpc) * Hkv * batch;
     int64_t pages = (static_cast<int64_t>(max_seq_len) + kBS - 1) / kBS;
-    if (window > 0) pages = std::min<int64_t>(pages, (static_cast<int64_t>(window) + rows) / kBS + 2);
-    pl.splits = choose_splits(units, pages, static_cast<int64_t>(sms) * per_sm);
+    if (window > 0) pages = std::min<int64_t>(pages, (static_cast<int64_t>(window) + rows * tpc) / kBS + 2);
+    pl.splits = choose_splits(ctas, pages, static_cast<int64_t>(sms) * per_sm);
     if (pl.splits > 1) {
         const size_t slots = static_cast<size_t>(units) * pl.splits * rows;
         pl.ml = kHeader;
@@ -679,65 +1101,80 @@ Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D,
     return pl;
 }
 
-// The prefill kernel for (D, G) and its dynamic shared memory.
+// The prefill kernel for (D, G) -- the warp-specialised one when `ws` --,
+// its dynamic shared memory and its threads.
 template <int D, int G>
-void kernel_of(void (**fn)(const Args), size_t* smem) {
+void kernel_of(bool ws_kernel, void (**fn)(const Args), size_t* smem, int* threads) {
+    if constexpr (D == 128) {
+        if (ws_kernel) {
+            *fn = paged_prefill_ws_kernel<D, G>;
+            *smem = static_cast<size_t>(WsGeo<D>::SMEM) + 1024;
+            *threads = ws::kThreads;
+            return;
+        }
+    }
     *fn = paged_prefill_tc_kernel<D, G>;
     *smem = static_cast<size_t>(TcGeo<D>::SMEM) + 1024;
+    *threads = kThreads;
 }
 
 template <int D>
-bool kernel_of_g(int G, void (**fn)(const Args), size_t* smem) {
+bool kernel_of_g(int G, bool ws_kernel, void (**fn)(const Args), size_t* smem, int* threads) {
     switch (G) {
-        case 1: kernel_of<D, 1>(fn, smem); return true;
-        case 2: kernel_of<D, 2>(fn, smem); return true;
-        case 4: kernel_of<D, 4>(fn, smem); return true;
-        case 8: kernel_of<D, 8>(fn, smem); return true;
-        case 16: kernel_of<D, 16>(fn, smem); return true;
+        case 1: kernel_of<D, 1>(ws_kernel, fn, smem, threads); return true;
+        case 2: kernel_of<D, 2>(ws_kernel, fn, smem, threads); return true;
+        case 4: kernel_of<D, 4>(ws_kernel, fn, smem, threads); return true;
+        case 8: kernel_of<D, 8>(ws_kernel, fn, smem, threads); return true;
+        case 16: kernel_of<D, 16>(ws_kernel, fn, smem, threads); return true;
         default: return false;
     }
 }
 
-// Resident CTAs per SM of the prefill kernel for (D, G) on the current
+// Resident CTAs per SM of the prefill kernel for (D, G, ws) on the current
 // device (the occupancy calculator, with the kernel's shared-memory opt-in
 // applied); 0 on failure.  Cached per device.
-int resident_per_sm(int D, int G) {
-    static std::atomic<int> cache[3][5][64] = {};
+int resident_per_sm(int D, int G, bool ws_kernel) {
+    static std::atomic<int> cache[2][3][5][64] = {};
     const int di = D == 64 ? 0 : (D == 128 ? 1 : 2);
     const int gi = G == 1 ? 0 : (G == 2 ? 1 : (G == 4 ? 2 : (G == 8 ? 3 : 4)));
+    const int wi = ws_kernel ? 1 : 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (dev >= 0 && dev < 64) {
-        const int c = cache[di][gi][dev].load(std::memory_order_relaxed);
+        const int c = cache[wi][di][gi][dev].load(std::memory_order_relaxed);
         if (c > 0) return c;
     }
     void (*fn)(const Args) = nullptr;
     size_t smem = 0;
-    const bool ok = D == 64 ? kernel_of_g<64>(G, &fn, &smem)
-                            : (D == 128 ? kernel_of_g<128>(G, &fn, &smem) : kernel_of_g<256>(G, &fn, &smem));
+    int threads = 0;
+    const bool ok = D == 64 ? kernel_of_g<64>(G, ws_kernel, &fn, &smem, &threads)
+                            : (D == 128 ? kernel_of_g<128>(G, ws_kernel, &fn, &smem, &threads)
+                                        : kernel_of_g<256>(G, ws_kernel, &fn, &smem, &threads));
     if (!ok) return 0;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
         return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem) != cudaSuccess || n < 1) return 0;
-    if (dev >= 0 && dev < 64) cache[di][gi][dev].store(n, std::memory_order_relaxed);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess || n < 1) return 0;
+    if (dev >= 0 && dev < 64) cache[wi][di][gi][dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
 template <int D, int G>
 cudaError_t launch(const Args& a, int batch, cudaStream_t s) {
+    const bool ws_kernel = uses_ws(D, a.tiles);
     void (*kernel)(const Args) = nullptr;
     size_t smem = 0;
-    kernel_of<D, G>(&kernel, &smem);
-    static std::atomic<uint64_t> done_mask{0};
+    int threads = 0;
+    kernel_of<D, G>(ws_kernel, &kernel, &smem, &threads);
+    static std::atomic<uint64_t> done_mask[2] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
-    if (bit == 0 || !(done_mask.load(std::memory_order_acquire) & bit)) {
+    if (bit == 0 || !(done_mask[ws_kernel].load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        done_mask.fetch_or(bit, std::memory_order_release);
+        done_mask[ws_kernel].fetch_or(bit, std::memory_order_release);
     }
     // Both grids may start before the previous work on the stream ends; each
     // waits (griddepcontrol.wait) before touching what that work wrote.
@@ -745,9 +1182,11 @@ cudaError_t launch(const Args& a, int batch, cudaStream_t s) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.tiles * a.splits), static_cast<unsigned>(a.num_kv_heads),
+    const int tpc = ws_kernel ? ws::kTiles : 1;
+    const int ctas_x = (a.tiles + tpc - 1) / tpc;
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas_x * a.splits), static_cast<unsigned>(a.num_kv_heads),
                        static_cast<unsigned>(batch));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
@@ -799,7 +1238,7 @@ extern "C" size_t fp8kv_paged_prefill_workspace_size(int batch, int max_q_len, i
     int sms = 0;
     if (fp8kv::device_sms(&sms) != 0) return 0;
     const int G = num_q_heads / num_kv_heads;
-    const int per_sm = resident_per_sm(head_dim, G);
+    const int per_sm = resident_per_sm(head_dim, G, uses_ws(head_dim, tiles_of(max_q_len, G)));
     if (per_sm < 1) return 0;
     return make_plan(batch, max_q_len, max_seq_len, G, num_kv_heads, head_dim, window > 0 ? window : 0, sms, per_sm)
         .total;
@@ -834,7 +1273,7 @@ fp8kv_status prefill_impl(const void* q, int64_t num_q_tokens, const uint8_t* k_
     int sms = 0;
     if (fp8kv::device_sms(&sms) != 0) return FP8KV_ERR_CUDA;
     const int G = num_q_heads / num_kv_heads;
-    const int per_sm = resident_per_sm(head_dim, G);
+    const int per_sm = resident_per_sm(head_dim, G, uses_ws(head_dim, tiles_of(max_q_len, G)));
     if (per_sm < 1) return FP8KV_ERR_CUDA;
     const Plan pl = make_plan(batch, max_q_len, max_seq_len, G, num_kv_heads, head_dim, window > 0 ? window : 0, sms,
                               per_sm);

@@ -263,7 +263,7 @@ fp8kv_status fp8kv_paged_decode_engine(const void* q, const uint8_t* k_cache, co
  *
  * Scores and P.V run on the tensor cores with bf16 operands (P rounded to
  * bf16) and FP32 accumulation, each stage's tile added into FP32 registers.
- * Supported: head_dim in {64, 128}; block_size == 16; g in {1, 2, 4, 8, 16}.
+ * Supported: head_dim in {64, 128, 256}; block_size == 16; g in {1, 2, 4, 8, 16}.
  */
 fp8kv_status fp8kv_paged_decode_bf16(const void* q, const void* k_cache, const void* v_cache,
                                      int64_t num_blocks, const int32_t* block_tables,

@@ -84,7 +84,7 @@ def _bf16(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(d=256), 2), (dict(d=96), 2), (dict(bs=32), 2), (dict(hq=256, hkv=8), 2), (dict(hq=30, hkv=8), 1),
+    (dict(d=96), 2), (dict(bs=32), 2), (dict(hq=256, hkv=8), 2), (dict(hq=30, hkv=8), 1),
     (dict(sm=float("nan")), 1), (dict(q=None), 1), (dict(k=MISALIGNED), 1), (dict(mb=4, msl=128), 1),
     (dict(B=0, q=None, out=None), 0),
 ])

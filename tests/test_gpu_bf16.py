@@ -1,7 +1,8 @@
 """GPU parity of the bf16-cache twin (fp8kv_paged_decode_bf16) against the
 fp64 oracle over the same bf16 values: max|err| <= 8e-3, mean|err| <= 1e-3,
-small cases with ragged tails and windows, every supported head layout, NaN
-garbage in unwritten slots, and the full-size 8x20K and 128K-needle layouts."""
+small cases with ragged tails and windows, every supported head layout
+(d = 64, 128, 256), NaN garbage in unwritten slots, and the full-size 8x20K,
+128K-needle and gemma-like (d = 256) layouts."""
 import numpy as np
 import pytest
 import torch
@@ -61,6 +62,7 @@ def _f64(t):
     ("llama31_8b_b8_20k", [2999, 1234, 16, 4097], (0, 128)),
     ("gptoss20b_b8_16k", [1, 63, 64, 65, 700, 2500], (0, 128, 7)),
     ("llama33_70b_needle_128k", [3000, 40], (0, 16)),
+    ("gemma4e2b_b16_8k32k", [1, 17, 511, 512, 513, 3000], (0, 512, 33)),
 ])
 def test_bf16_small_cases_match_oracle(base, lens, windows):
     shape = workload.small_shape(base, batch=len(lens), len_lo=1, len_hi=1, needle_margin=None)
@@ -72,7 +74,7 @@ def test_bf16_small_cases_match_oracle(base, lens, windows):
         assert_attn_close(_f64(out), oracle_bf16(w, win), f"bf16 {base} window={win}")
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("g", [1, 2, 4, 8, 16])
 def test_bf16_every_supported_head_layout(d, g):
     hkv = 2
@@ -95,7 +97,7 @@ def test_bf16_unwritten_nan_slots_never_leak():
         assert_attn_close(_f64(out), oracle_bf16(w, win), f"bf16 nan-filled window={win}")
 
 
-@pytest.mark.parametrize("name", ["llama31_8b_b8_20k", "llama33_70b_needle_128k"])
+@pytest.mark.parametrize("name", ["llama31_8b_b8_20k", "llama33_70b_needle_128k", "gemma4e2b_b16_8k32k"])
 def test_bf16_full_size_matches_oracle(name):
     w = workload.make_workload(name, seed=0)
     pc = PagedBf16(w)
