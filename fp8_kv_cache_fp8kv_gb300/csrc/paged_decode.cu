@@ -1646,12 +1646,13 @@ __global__ void __launch_bounds__(StreamCfg<D, ES, G>::NW * 32, kCtasPerSm)
                         const float sc_out = l[t][j] > 0.f ? unit_v_scale(a, w.hk) / l[t][j] : 0.f;
                         if (h < G) {
 #pragma unroll
-                            for (int mt = 0; mt < Gm::MT; ++mt)
-#pragma unroll
-                                for (int e2 = 0; e2 < 2; ++e2) {
-                                    const int dim = (mt / Gm::MTH) * Gm::DBOX + Gm::VWD * gid + 2 * (mt % Gm::MTH) + e2;
-                                    out_u[h * D + dim] = f32_to_bf16(o[t][mt][2 * e2 + j] * sc_out);
-                                }
+                            for (int mt = 0; mt < Gm::MT; ++mt) {
+                                // dimensions dim and dim + 1 together (one 4-byte store)
+                                const int dim = (mt / Gm::MTH) * Gm::DBOX + Gm::VWD * gid + 2 * (mt % Gm::MTH);
+                                *reinterpret_cast<uint32_t*>(out_u + h * D + dim) =
+                                    static_cast<uint32_t>(f32_to_bf16(o[t][mt][j] * sc_out)) |
+                                    (static_cast<uint32_t>(f32_to_bf16(o[t][mt][2 + j] * sc_out)) << 16);
+                            }
                         }
                     }
                 } else {
@@ -1854,7 +1855,7 @@ Plan make_plan(int batch, int num_kv_heads, int D, int max_seq_len, int window, 
 // partials per unit are estimated from the plan with every sequence at
 // max_seq_len: a unit of n pages meets at most ceil(n / pages per CTA) + 1
 // CTAs.  Shorter sequences only change the speed of the chosen merge.
-constexpr int64_t kInlineMergeBytes = 32 << 10;
+constexpr int64_t kInlineMergeBytes = 16 << 10;
 
 bool merge_inline(const Plan& p, int batch, int units_per_seq, int G, int D, int max_seq_len, int window) {
     if (p.ctas <= 1 || max_seq_len <= 0) return true;
@@ -2195,6 +2196,21 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
     if (hs && hs->in_bytes > 0 &&
         cudaMemcpyAsync(hs->d_in, hs->h_in, hs->in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return FP8KV_ERR_CUDA;
+    // A host output buffer that the device can address (page-locked memory,
+    // mapped under unified addressing) receives the result directly from the
+    // kernels' stores, across the host link; otherwise the result goes to
+    // `out` and is copied to h_out after the step.
+    bool direct_out = false;
+    if (hs && hs->h_out) {
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, hs->h_out) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+            pa.devicePointer != nullptr && a16(pa.devicePointer)) {
+            out = pa.devicePointer;
+            direct_out = true;
+        } else {
+            (void)cudaGetLastError();  // not a registered host buffer: copy instead
+        }
+    }
     // Batches above kMaxBatch sequences run as consecutive launches on the
     // stream, reusing the workspace.
     for (int b0 = 0; b0 < batch; b0 += kMaxBatch) {
@@ -2255,8 +2271,9 @@ fp8kv_status decode_impl(const void* q, const void* k_new, const void* v_new, co
         }
         if (e != cudaSuccess) return FP8KV_ERR_CUDA;
     }
-    if (hs && cudaMemcpyAsync(hs->h_out, out, static_cast<size_t>(batch) * num_q_heads * head_dim * 2,
-                              cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    if (hs && !direct_out &&
+        cudaMemcpyAsync(hs->h_out, out, static_cast<size_t>(batch) * num_q_heads * head_dim * 2,
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return FP8KV_ERR_CUDA;
     return FP8KV_OK;
 }

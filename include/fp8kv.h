@@ -302,9 +302,13 @@ fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, const void* v_n
  * inputs and output across the host link around the step above.
  *
  * On `stream`, in order: one copy of in_bytes bytes from h_in to d_in, the
- * decode step, one copy of the step's output (batch*num_q_heads*head_dim bf16)
- * from `out` to h_out.  It returns once the three are enqueued; h_out is valid
- * after the caller synchronises the stream.
+ * decode step, and the step's output (batch*num_q_heads*head_dim bf16) into
+ * h_out.  When the device can address h_out (page-locked host memory under
+ * unified addressing, e.g. cudaHostAlloc or a registered buffer) the step's
+ * kernels store the output there directly, across the host link, and `out`
+ * is not written; otherwise the output goes to `out` and one copy moves it
+ * to h_out.  It returns once the work is enqueued; h_out is valid after the
+ * caller synchronises the stream.
  *
  *   h_in    host buffer (page-locked for an asynchronous copy) holding the
  *           step's inputs exactly as they must appear at d_in
