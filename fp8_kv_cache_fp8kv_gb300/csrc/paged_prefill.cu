@@ -226,9 +226,7 @@ __device__ __forceinline__ void load_stage_tc(const Args& a, const int32_t* bt, 
 // V^T tile at vt (d rows x 64 keys).  Keys outside [kmin, kmax] or past the
 // stage's np pages become zeros in V^T (their scores are masked).
 template <int D>
-__device__ __forceinline__ void convert_stage(const uint8_t* stg, uint8_t* kt, uint8_t* vt, int ct, int t0, int np,
-                                              int kmin, int kmax) {
-    using Tg = TcGeo<D>;
+__device__ __forceinline__ void convert_stage_k(const uint8_t* stg, uint8_t* kt, int ct) {
     // K: thread ct converts CH staged chunks (16 dims each) of key ct & 63
     {
         constexpr int CH = D / 32;                        // 8 at d = 256, 4 at 128, 2 at 64
@@ -248,6 +246,12 @@ __device__ __forceinline__ void convert_stage(const uint8_t* stg, uint8_t* kt, u
             *reinterpret_cast<uint4*>(dst + (((j + 1) ^ (k & 7)) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
         }
     }
+}
+
+template <int D>
+__device__ __forceinline__ void convert_stage_v(const uint8_t* stg, uint8_t* vt, int ct, int t0, int np, int kmin,
+                                                int kmax) {
+    using Tg = TcGeo<D>;
     // V^T: thread ct (ct < d) converts keys [8kb, 8kb + 8) x dims [8db, 8db + 8)
 #pragma unroll
     for (int vp = 0; vp < Tg::VPASS; ++vp)
@@ -279,6 +283,13 @@ __device__ __forceinline__ void convert_stage(const uint8_t* stg, uint8_t* kt, u
                 *reinterpret_cast<uint4*>(vt + (8 * db + dd) * 128 + ((kb ^ dd) << 4)) =
                     make_uint4(vt4[dd][0], vt4[dd][1], vt4[dd][2], vt4[dd][3]);
         }
+}
+
+template <int D>
+__device__ __forceinline__ void convert_stage(const uint8_t* stg, uint8_t* kt, uint8_t* vt, int ct, int t0, int np,
+                                              int kmin, int kmax) {
+    convert_stage_k<D>(stg, kt, ct);
+    convert_stage_v<D>(stg, vt, ct, t0, np, kmin, kmax);
 }
 
 template <int D, int G>
@@ -979,6 +990,339 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
     }
 }
 
+// ---------------------------------------------------------------------------
+// The warp-specialised prefill kernel at d = 256: one 128-row tile per CTA.
+// A row's 256 FP32 outputs live in TMEM (columns [256, 512)); S has its own
+// columns [0, 64) and the P.V tile [64, 192), computed in two halves of 128
+// output dimensions.  Roles, handing over through mbarriers (every wait
+// bounded, a shared abort flag ending all of them):
+//   * warps 4-7 (converters): cp.async stage s + 1 into a 2-slot staging
+//     ring; convert stage s's K into the K tile once the score MMAs of stage
+//     s - 1 have finished with it, and its V^T into the V^T tile once the
+//     value MMAs of stage s - 1 have;
+//   * one thread of warp 8 (MMA issuer): S(s) = Q K^T; once P(s) is written,
+//     O_tile = P V^T for output dimensions [0, 128), and, once that half has
+//     been folded, for [128, 256);
+//   * warps 0-3 (thread = row): softmax of S(s) into P(s), then the fold of
+//     each half into the accumulator, O = O * alpha + O_tile.
+// S(s + 1) runs while the rows fold stage s; the conversions run beside both.
+namespace ws256 {
+constexpr int kConvWarp0 = 4;              // warps 4-7 convert
+constexpr int kMmaWarp = 8;                // warp 8 issues the MMAs
+constexpr int kThreads = 9 * 32;
+constexpr int kConvBar = 2;                // named barrier of the converter warps
+constexpr int QTB = 4 * 128 * 128;         // Q tile: 128 rows x 256 dims, 4 atom columns
+constexpr int KTB = 4 * tcg::kKeys * 128;  // K tile: 64 keys x 256 dims
+constexpr int VTB = 256 * 128;             // V^T tile: 256 dims x 64 keys
+constexpr int PTB = 128 * 128;             // P tile: 128 rows x 64 keys
+constexpr int SLOT = 2 * tcg::kKeys * 256; // one fp8 staging slot: K rows, then V rows
+constexpr int QT = 0, KT = QT + QTB, VT = KT + KTB, PT = VT + VTB, STG = PT + PTB;
+constexpr int SMEM = STG + 2 * SLOT;       // 208 KB
+constexpr uint32_t S_COL = 0, OT_COL = 64, OACC_COL = 256, COLS = 512;
+}  // namespace ws256
+
+template <int G>
+__global__ void __launch_bounds__(ws256::kThreads, 1) paged_prefill_ws256_kernel(const Args a) {
+    constexpr int D = 256;
+    using namespace ws256;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t k_full, k_empty, v_full, v_empty, s_full, p_full, o_full[2], o_free, done_bar;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_sh;
+    volatile int* abort_flag = &abort_sh;
+    uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t sb = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        mbar_init(&k_full, 128);
+        mbar_init(&v_full, 128);
+        mbar_init(&k_empty, 1);
+        mbar_init(&v_empty, 1);
+        mbar_init(&s_full, 1);
+        mbar_init(&p_full, 128);
+        mbar_init(&o_full[0], 1);
+        mbar_init(&o_full[1], 1);
+        mbar_init(&o_free, 128);
+        mbar_init(&done_bar, 1);
+        abort_sh = 0;
+        fence_barrier_init();
+    }
+    griddep_wait();                // inputs may come from the previous grid on the stream
+    griddep_launch_dependents();
+    const int b = blockIdx.z, hk = blockIdx.y;
+    const int tile = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
+    Unit u;
+    if (!make_unit<G>(a, b, tile, blockIdx.x == 0 && hk == 0 && tid == 0, u)) return;
+    const int pg0 = u.kmin / kBS, np_all = u.kmax / kBS - pg0 + 1;
+    const int sp0 = pg0 + static_cast<int>(static_cast<int64_t>(split) * np_all / a.splits);
+    const int sp1 = pg0 + static_cast<int>(static_cast<int64_t>(split + 1) * np_all / a.splits);
+    const int nst = (sp1 - sp0 + tcg::kPages - 1) / tcg::kPages;
+    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
+
+    // ---- set-up: the rows build the Q tile; the converters start stage 0's copies
+    const int r = u.R0 + tid;
+    const bool rv = warp < 4 && r < u.rows;
+    float cs = 0.f;
+    int pq = 0, lq = 0, wpos0 = 0, wlo1 = 0;
+    if (warp < 4) {
+        // the bf16 row in 16-byte chunks, read twice (its largest magnitude,
+        // then the copy) to keep few of them in registers
+        constexpr int NC = D / 8;
+        const int tok = rv ? r / G : 0, hq = hk * G + (rv ? r % G : 0);
+        const uint4* qrow =
+            reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(u.q0 + tok) * a.num_q_heads + hq) * D);
+        float qmax = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < NC; ++c) {
+            const uint4 qv = rv ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
+            const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                qmax = fmaxf(qmax, fmaxf(fabsf(bf16_to_f32(w4[e] & 0xFFFF)), fabsf(bf16_to_f32(w4[e] >> 16))));
+        }
+        int shift = 0;
+        if (qmax > 0.f) {
+            const int e = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFF) - 127;
+            shift = max(-100, min(100, 14 - e));
+        }
+        const float up = __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
+#pragma unroll 4
+        for (int c = 0; c < NC; ++c) {
+            const uint4 qv = rv ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
+            const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+            uint32_t f[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                f[e] = pack_f16x2(bf16_to_f32(w4[e] & 0xFFFF) * up, bf16_to_f32(w4[e] >> 16) * up);
+            *reinterpret_cast<uint4*>(sm + QT + (c >> 3) * 16384 + tid * 128 + (((c & 7) ^ (tid & 7)) << 4)) =
+                make_uint4(f[0], f[1], f[2], f[3]);
+        }
+        cs = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
+        pq = u.L - u.n + (rv ? r / G : 0);
+        lq = (a.window > 0 && pq + 1 > a.window) ? pq + 1 - a.window : 0;
+        const int wr0 = u.R0 + warp * 32;
+        wpos0 = u.L - u.n + wr0 / G;
+        const int wpos1 = u.L - u.n + max(0, min(wr0 + 31, u.rows - 1)) / G;
+        wlo1 = (a.window > 0 && wpos1 + 1 > a.window) ? wpos1 + 1 - a.window : 0;
+    } else if (warp < kMmaWarp) {
+        const int ct = tid - kConvWarp0 * 32;
+        if (nst > 0)
+            load_stage_tc<D>(a, bt, hk, sp0, min(tcg::kPages, sp1 - sp0), sb + STG, ct);
+        cp_async_commit();
+    }
+    if (warp == 0) tc::alloc(&tmem_base, COLS);
+    tc::fence_proxy_async_smem();  // the Q tile is read by the tensor cores
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = tmem_base;
+
+    float m = -INFINITY, l = 0.f;
+    if (warp < 4) {
+        // ---------------------------------------------------------- softmax and fold
+        const uint32_t trow = tm + (static_cast<uint32_t>(warp * 32) << 16);
+        {
+            float z[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) z[j] = 0.f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tc::st32(trow + OACC_COL + 32 * c, z);
+            tc::wait_st();
+        }
+        uint8_t* prow = sm + PT + tid * 128;
+        for (int st = 0; st < nst; ++st) {
+            bool ok = wait_or_abort(&s_full, st & 1, a.wait_ns, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) break;   // warp-uniform: the TMEM loads below are collective
+            tc::fence_after_sync();
+            const int pgs = sp0 + st * tcg::kPages;
+            const int np = min(tcg::kPages, sp1 - pgs);
+            const int t0 = pgs * kBS;
+            const bool interior = np == tcg::kPages && t0 + tcg::kKeys - 1 <= wpos0 && t0 >= wlo1;
+            float sv[64];
+            tc::ld32(trow + S_COL, *reinterpret_cast<float(*)[32]>(sv));
+            tc::ld32(trow + S_COL + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
+            tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv));
+            tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv + 32));
+            float mx = -INFINITY;
+            if (interior) {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    sv[j] *= cs;
+                    mx = fmaxf(mx, sv[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const int key = t0 + j;
+                    const bool valid = j < np * kBS && rv && key >= lq && key <= pq;
+                    sv[j] = valid ? sv[j] * cs : -INFINITY;
+                    mx = fmaxf(mx, sv[j]);
+                }
+            }
+            const float mn = fmaxf(m, mx);
+            const float muse = mn == -INFINITY ? 0.f : mn;
+            const float alpha = fast_exp2(m - muse);
+            m = mn;
+            float ls = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t pw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = fast_exp2(sv[8 * c + 2 * e] - muse), p1 = fast_exp2(sv[8 * c + 2 * e + 1] - muse);
+                    ls += p0 + p1;
+                    pw[e] = pack_f16x2(p0, p1);
+                }
+                *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            }
+            l = l * alpha + ls;
+            tc::fence_proxy_async_smem();  // P is read by the tensor cores
+            tc::fence_before_sync();
+            mbar_arrive(&p_full);
+            // O = O * alpha + O_tile (IEEE FMA, FP32), one half of the output dimensions at a time
+            bool okh = true;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                ok = wait_or_abort(&o_full[h], st & 1, a.wait_ns, abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    okh = false;
+                    break;
+                }
+                tc::fence_after_sync();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float x[32], y[32];
+                    tc::ld32(trow + OT_COL + 32 * c, x);
+                    tc::ld32(trow + OACC_COL + 128 * h + 32 * c, y);
+                    tc::wait_ld(x);
+                    tc::wait_ld(y);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) y[j] = fmaf(y[j], alpha, x[j]);
+                    tc::st32(trow + OACC_COL + 128 * h + 32 * c, y);
+                }
+                tc::wait_st();
+                tc::fence_before_sync();
+                mbar_arrive(&o_free);      // the MMA may overwrite O_tile
+            }
+            if (!okh) break;
+        }
+    } else if (warp < kMmaWarp) {
+        // ---------------------------------------------------------- converters
+        const int ct = tid - kConvWarp0 * 32;
+        for (int st = 0; st < nst; ++st) {
+            if (st + 1 < nst)
+                load_stage_tc<D>(a, bt, hk, sp0 + (st + 1) * tcg::kPages,
+                                 min(tcg::kPages, sp1 - sp0 - (st + 1) * tcg::kPages),
+                                 sb + STG + ((st + 1) & 1) * SLOT, ct);
+            cp_async_commit();
+            cp_async_wait<1>();              // this thread's copies of stage st have landed
+            // the K tile is free once the score MMAs of stage st - 1 have completed
+            bool ok = st == 0 || wait_or_abort(&k_empty, (st - 1) & 1, a.wait_ns, abort_flag);
+            if (named_bar_or(kConvBar, 128, !ok)) break;   // every copy of stage st landed (or all give up)
+            const uint8_t* stg = sm + STG + (st & 1) * SLOT;
+            const int pgs = sp0 + st * tcg::kPages;
+            const int np = min(tcg::kPages, sp1 - pgs);
+            convert_stage_k<D>(stg, sm + KT, ct);
+            tc::fence_proxy_async_smem();
+            mbar_arrive(&k_full);
+            // the V^T tile is free once the value MMAs of stage st - 1 have completed
+            ok = st == 0 || wait_or_abort(&v_empty, (st - 1) & 1, a.wait_ns, abort_flag);
+            if (named_bar_or(kConvBar, 128, !ok)) break;
+            convert_stage_v<D>(stg, sm + VT, ct, pgs * kBS, np, u.kmin, u.kmax);
+            tc::fence_proxy_async_smem();
+            mbar_arrive(&v_full);
+            named_bar_sync(kConvBar, 128);   // the staging slot is read before it is refilled
+        }
+        cp_async_wait<0>();
+    } else if (lane == 0) {
+        // ---------------------------------------------------------- MMA issuer
+        constexpr uint32_t id_s = tc::idesc_f16_f32(128, tcg::kKeys);
+        constexpr uint32_t id_o = tc::idesc_f16_f32(128, 128);
+        const bool stall_cta = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+        for (int st = 0; st < nst; ++st) {
+            if (!wait_or_abort(&k_full, st & 1, a.wait_ns, abort_flag)) break;
+            tc::fence_after_sync();
+            // S(st) overwrites S(st - 1), which the rows loaded before writing P(st - 1)
+            if (!(st == a.stall_stage && stall_cta)) {   // test hook: this stage's S never arrives
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks & 3) * 32;
+                    tc::mma_f16(tm + S_COL, tc::desc_k_sw128(sb + QT + (ks >> 2) * 16384 + off),
+                                tc::desc_k_sw128(sb + KT + (ks >> 2) * (tcg::kKeys * 128) + off), id_s, ks > 0);
+                }
+                tc::commit(&s_full);
+            }
+            tc::commit(&k_empty);             // the K tile is free when the score MMAs complete
+            if (!wait_or_abort(&p_full, st & 1, a.wait_ns, abort_flag)) break;
+            if (!wait_or_abort(&v_full, st & 1, a.wait_ns, abort_flag)) break;
+            tc::fence_after_sync();
+            bool ok = true;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                // O_tile is free once the rows have folded the previous half
+                const int f = 2 * st + h;     // this half's fold index
+                if (f > 0 && !wait_or_abort(&o_free, (f - 1) & 1, a.wait_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_f16(tm + OT_COL, tc::desc_k_sw128(sb + PT + ks * 32),
+                                tc::desc_k_sw128(sb + VT + h * 128 * 128 + ks * 32), id_o, ks > 0);
+                tc::commit(&o_full[h]);
+            }
+            if (!ok) break;
+            tc::commit(&v_empty);             // the V^T tile is free when the value MMAs complete
+        }
+        // every MMA this thread issued completes before TMEM is released
+        tc::commit(&done_bar);
+        mbar_wait_bounded(&done_bar, 0, tcg::kWaitNs);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const bool failed = *abort_flag != 0;
+    if (failed) {
+        if (tid == 0) report(a.err, FP8KV_ERR_TIMEOUT);
+    } else if (warp < 4) {
+        // ---- the rows' outputs (or partials) from the TMEM accumulator; every
+        // thread of the warp loads (tcgen05.ld is collective), valid rows store
+        const uint32_t trow = tm + (static_cast<uint32_t>(warp * 32) << 16);
+        const int64_t unit = (static_cast<int64_t>(b) * a.num_kv_heads + hk) * a.tiles + tile;
+        const float so = l > 0.f ? a.v_scale / l : 0.f;
+        uint4* orow = reinterpret_cast<uint4*>(
+            a.out + (static_cast<int64_t>(u.q0 + (rv ? r / G : 0)) * a.num_q_heads + hk * G + (rv ? r % G : 0)) * D);
+        const int64_t slot = (unit * a.splits + split) * a.rows + tid;
+        float4* po = reinterpret_cast<float4*>(a.part_o + slot * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            float x[32];
+            tc::ld32(trow + OACC_COL + 32 * c, x);
+            tc::wait_ld(x);
+            if (!rv) continue;
+            if (a.splits == 1) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    orow[4 * c + i] = make_uint4(pack_bf16x2(x[8 * i] * so, x[8 * i + 1] * so),
+                                                 pack_bf16x2(x[8 * i + 2] * so, x[8 * i + 3] * so),
+                                                 pack_bf16x2(x[8 * i + 4] * so, x[8 * i + 5] * so),
+                                                 pack_bf16x2(x[8 * i + 6] * so, x[8 * i + 7] * so));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) po[8 * c + i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+            }
+        }
+        if (rv && a.splits > 1) a.part_ml[slot] = make_float2(m, l);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::dealloc(tm, COLS);
+    }
+}
+
 // Combines a unit's split partials row by row in FP32: with M the largest
 // row maximum, weight_s = 2^(m_s - M), out = v_scale * sum_s weight_s o_s /
 // sum_s weight_s l_s, rounded to bf16.  A CTA covers 8 rows of a unit, a
@@ -1078,17 +1422,19 @@ inline int tiles_of(int max_q_len, int G) {
     return static_cast<int>((static_cast<int64_t>(max_q_len) * G + kRowsTC - 1) / kRowsTC);
 }
 
-// Which kernel runs: the warp-specialised one (two tiles per CTA) at d = 128
-// when a sequence's chunk spans at least two tiles; otherwise
+// Which kernel runs: 1, the warp-specialised one with two tiles per CTA, at
+// d = 128 when a sequence's chunk spans at least two tiles; 2, the
+// warp-specialised one-tile kernel, at d = 256; else 0,
 // paged_prefill_tc_kernel, one tile per CTA (at d = 64 its 56 KB of shared
 // memory let several CTAs share an SM, which measured faster).
-inline bool uses_ws(int D, int tiles) { return D == 128 && tiles >= 2; }
+inline int kernel_kind(int D, int tiles) { return D == 128 && tiles >= 2 ? 1 : (D == 256 ? 2 : 0); }
+inline int tiles_per_cta(int kind) { return kind == 1 ? ws::kTiles : 1; }
 
 Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D, int window, int sms, int per_sm) {
     Plan pl;
     const int rows = rows_per_tile(D);
     pl.tiles = tiles_of(max_q_len, G);
-    const int tpc = uses_ws(D, pl.tiles) ? ws::kTiles : 1;   // tiles per CTA
+    const int tpc = tiles_per_cta(kernel_kind(D, pl.tiles));
     const int64_t units = static_cast<int64_t>(pl.tiles) * Hkv * batch;
     const int64_t ctas = static_cast<int64_t>((pl.tiles + tpc - 1) / tpc) * Hkv * batch;
     int64_t pages = (static_cast<int64_t>(max_seq_len) + kBS - 1) / kBS;
@@ -1103,15 +1449,23 @@ Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D,
     return pl;
 }
 
-// The prefill kernel for (D, G) -- the warp-specialised one when `ws` --,
-// its dynamic shared memory and its threads.
+// The prefill kernel of a kind (kernel_kind) for (D, G), its dynamic shared
+// memory and its threads.
 template <int D, int G>
-void kernel_of(bool ws_kernel, void (**fn)(const Args), size_t* smem, int* threads) {
+void kernel_of(int kind, void (**fn)(const Args), size_t* smem, int* threads) {
     if constexpr (D == 128) {
-        if (ws_kernel) {
+        if (kind == 1) {
             *fn = paged_prefill_ws_kernel<D, G>;
             *smem = static_cast<size_t>(WsGeo<D>::SMEM) + 1024;
             *threads = ws::kThreads;
+            return;
+        }
+    }
+    if constexpr (D == 256) {
+        if (kind == 2) {
+            *fn = paged_prefill_ws256_kernel<G>;
+            *smem = static_cast<size_t>(ws256::SMEM) + 1024;
+            *threads = ws256::kThreads;
             return;
         }
     }
@@ -1121,25 +1475,25 @@ void kernel_of(bool ws_kernel, void (**fn)(const Args), size_t* smem, int* threa
 }
 
 template <int D>
-bool kernel_of_g(int G, bool ws_kernel, void (**fn)(const Args), size_t* smem, int* threads) {
+bool kernel_of_g(int G, int kind, void (**fn)(const Args), size_t* smem, int* threads) {
     switch (G) {
-        case 1: kernel_of<D, 1>(ws_kernel, fn, smem, threads); return true;
-        case 2: kernel_of<D, 2>(ws_kernel, fn, smem, threads); return true;
-        case 4: kernel_of<D, 4>(ws_kernel, fn, smem, threads); return true;
-        case 8: kernel_of<D, 8>(ws_kernel, fn, smem, threads); return true;
-        case 16: kernel_of<D, 16>(ws_kernel, fn, smem, threads); return true;
+        case 1: kernel_of<D, 1>(kind, fn, smem, threads); return true;
+        case 2: kernel_of<D, 2>(kind, fn, smem, threads); return true;
+        case 4: kernel_of<D, 4>(kind, fn, smem, threads); return true;
+        case 8: kernel_of<D, 8>(kind, fn, smem, threads); return true;
+        case 16: kernel_of<D, 16>(kind, fn, smem, threads); return true;
         default: return false;
     }
 }
 
-// Resident CTAs per SM of the prefill kernel for (D, G, ws) on the current
+// Resident CTAs per SM of the prefill kernel for (D, G, kind) on the current
 // device (the occupancy calculator, with the kernel's shared-memory opt-in
 // applied); 0 on failure.  Cached per device.
-int resident_per_sm(int D, int G, bool ws_kernel) {
-    static std::atomic<int> cache[2][3][5][64] = {};
+int resident_per_sm(int D, int G, int kind) {
+    static std::atomic<int> cache[3][3][5][64] = {};
     const int di = D == 64 ? 0 : (D == 128 ? 1 : 2);
     const int gi = G == 1 ? 0 : (G == 2 ? 1 : (G == 4 ? 2 : (G == 8 ? 3 : 4)));
-    const int wi = ws_kernel ? 1 : 0;
+    const int wi = kind;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (dev >= 0 && dev < 64) {
@@ -1149,9 +1503,9 @@ int resident_per_sm(int D, int G, bool ws_kernel) {
     void (*fn)(const Args) = nullptr;
     size_t smem = 0;
     int threads = 0;
-    const bool ok = D == 64 ? kernel_of_g<64>(G, ws_kernel, &fn, &smem, &threads)
-                            : (D == 128 ? kernel_of_g<128>(G, ws_kernel, &fn, &smem, &threads)
-                                        : kernel_of_g<256>(G, ws_kernel, &fn, &smem, &threads));
+    const bool ok = D == 64 ? kernel_of_g<64>(G, kind, &fn, &smem, &threads)
+                            : (D == 128 ? kernel_of_g<128>(G, kind, &fn, &smem, &threads)
+                                        : kernel_of_g<256>(G, kind, &fn, &smem, &threads));
     if (!ok) return 0;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
         return 0;
@@ -1163,20 +1517,20 @@ int resident_per_sm(int D, int G, bool ws_kernel) {
 
 template <int D, int G>
 cudaError_t launch(const Args& a, int batch, cudaStream_t s) {
-    const bool ws_kernel = uses_ws(D, a.tiles);
+    const int kind = kernel_kind(D, a.tiles);
     void (*kernel)(const Args) = nullptr;
     size_t smem = 0;
     int threads = 0;
-    kernel_of<D, G>(ws_kernel, &kernel, &smem, &threads);
-    static std::atomic<uint64_t> done_mask[2] = {};
+    kernel_of<D, G>(kind, &kernel, &smem, &threads);
+    static std::atomic<uint64_t> done_mask[3] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
-    if (bit == 0 || !(done_mask[ws_kernel].load(std::memory_order_acquire) & bit)) {
+    if (bit == 0 || !(done_mask[kind].load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        done_mask[ws_kernel].fetch_or(bit, std::memory_order_release);
+        done_mask[kind].fetch_or(bit, std::memory_order_release);
     }
     // Both grids may start before the previous work on the stream ends; each
     // waits (griddepcontrol.wait) before touching what that work wrote.
@@ -1184,7 +1538,7 @@ cudaError_t launch(const Args& a, int batch, cudaStream_t s) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    const int tpc = ws_kernel ? ws::kTiles : 1;
+    const int tpc = tiles_per_cta(kind);
     const int ctas_x = (a.tiles + tpc - 1) / tpc;
     cfg.gridDim = dim3(static_cast<unsigned>(ctas_x * a.splits), static_cast<unsigned>(a.num_kv_heads),
                        static_cast<unsigned>(batch));
@@ -1240,7 +1594,7 @@ extern "C" size_t fp8kv_paged_prefill_workspace_size(int batch, int max_q_len, i
     int sms = 0;
     if (fp8kv::device_sms(&sms) != 0) return 0;
     const int G = num_q_heads / num_kv_heads;
-    const int per_sm = resident_per_sm(head_dim, G, uses_ws(head_dim, tiles_of(max_q_len, G)));
+    const int per_sm = resident_per_sm(head_dim, G, kernel_kind(head_dim, tiles_of(max_q_len, G)));
     if (per_sm < 1) return 0;
     return make_plan(batch, max_q_len, max_seq_len, G, num_kv_heads, head_dim, window > 0 ? window : 0, sms, per_sm)
         .total;
@@ -1275,7 +1629,7 @@ fp8kv_status prefill_impl(const void* q, int64_t num_q_tokens, const uint8_t* k_
     int sms = 0;
     if (fp8kv::device_sms(&sms) != 0) return FP8KV_ERR_CUDA;
     const int G = num_q_heads / num_kv_heads;
-    const int per_sm = resident_per_sm(head_dim, G, uses_ws(head_dim, tiles_of(max_q_len, G)));
+    const int per_sm = resident_per_sm(head_dim, G, kernel_kind(head_dim, tiles_of(max_q_len, G)));
     if (per_sm < 1) return FP8KV_ERR_CUDA;
     const Plan pl = make_plan(batch, max_q_len, max_seq_len, G, num_kv_heads, head_dim, window > 0 ? window : 0, sms,
                               per_sm);
