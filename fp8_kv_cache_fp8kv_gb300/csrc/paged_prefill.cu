@@ -991,10 +991,11 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
 }
 
 // ---------------------------------------------------------------------------
-// The warp-specialised prefill kernel at d = 256: one 128-row tile per CTA.
-// A row's 256 FP32 outputs live in TMEM (columns [256, 512)); S has its own
-// columns [0, 64) and the P.V tile [64, 192), computed in two halves of 128
-// output dimensions.  Roles, handing over through mbarriers (every wait
+// The warp-specialised one-tile prefill kernel (used at d = 256; written for
+// d = 64 too): one 128-row tile per CTA.  A row's d FP32 outputs live in TMEM
+// (columns [256, 512) at d = 256, [128, 192) at d = 64); S has its own
+// columns [0, 64) and the P.V tile [64, 64 + min(d, 128)), computed in halves
+// of 128 output dimensions at d = 256.  Roles, handing over through mbarriers (every wait
 // bounded, a shared abort flag ending all of them):
 //   * warps 4-7 (converters): cp.async stage s + 1 into a 2-slot staging
 //     ring; convert stage s's K into the K tile once the score MMAs of stage
@@ -1006,27 +1007,42 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
 //   * warps 0-3 (thread = row): softmax of S(s) into P(s), then the fold of
 //     each half into the accumulator, O = O * alpha + O_tile.
 // S(s + 1) runs while the rows fold stage s; the conversions run beside both.
-namespace ws256 {
+namespace ws1 {
 constexpr int kConvWarp0 = 4;              // warps 4-7 convert
 constexpr int kMmaWarp = 8;                // warp 8 issues the MMAs
 constexpr int kThreads = 9 * 32;
 constexpr int kConvBar = 2;                // named barrier of the converter warps
-constexpr int QTB = 4 * 128 * 128;         // Q tile: 128 rows x 256 dims, 4 atom columns
-constexpr int KTB = 4 * tcg::kKeys * 128;  // K tile: 64 keys x 256 dims
-constexpr int VTB = 256 * 128;             // V^T tile: 256 dims x 64 keys
-constexpr int PTB = 128 * 128;             // P tile: 128 rows x 64 keys
-constexpr int SLOT = 2 * tcg::kKeys * 256; // one fp8 staging slot: K rows, then V rows
-constexpr int QT = 0, KT = QT + QTB, VT = KT + KTB, PT = VT + VTB, STG = PT + PTB;
-constexpr int SMEM = STG + 2 * SLOT;       // 208 KB
-constexpr uint32_t S_COL = 0, OT_COL = 64, OACC_COL = 256, COLS = 512;
-}  // namespace ws256
+}  // namespace ws1
 
-template <int G>
-__global__ void __launch_bounds__(ws256::kThreads, 1) paged_prefill_ws256_kernel(const Args a) {
-    constexpr int D = 256;
-    using namespace ws256;
+template <int D>
+struct Ws1Geo {
+    static constexpr int NB = D / 64;
+    static constexpr int QTB = NB * 128 * 128;          // Q tile: 128 rows x d
+    static constexpr int KTB = NB * tcg::kKeys * 128;   // K tile: 64 keys x d
+    static constexpr int VTB = D * 128;                 // V^T tile: d rows x 64 keys
+    static constexpr int PTB = 128 * 128;               // P tile: 128 rows x 64 keys
+    static constexpr int SLOT = 2 * tcg::kKeys * D;     // one fp8 staging slot: K rows, then V rows
+    static constexpr int QT = 0, KT = QT + QTB, VT = KT + KTB, PT = VT + VTB, STG = PT + PTB;
+    static constexpr int SMEM = STG + 2 * SLOT;         // 208 KB at d = 256, 64 KB at 64
+    static constexpr int ON = D > 128 ? 128 : D;        // output dimensions of one P.V half
+    static constexpr int NH = D / ON;                   // halves: 2 at d = 256, else 1
+    static constexpr uint32_t S_COL = 0, OT_COL = 64;
+    static constexpr uint32_t OACC_COL = D == 256 ? 256 : 128;
+    static constexpr uint32_t COLS = D == 256 ? 512 : 256;
+    static constexpr int kCtasPerSm = D == 64 ? 2 : 1;  // 2 x 64 KB of shared memory and 2 x 256 TMEM columns
+    static_assert(OT_COL + ON <= OACC_COL && OACC_COL + D <= COLS, "TMEM columns");
+    static_assert(D == 64 || D == 256, "the one-tile warp-specialised kernel covers d = 64 and 256");
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(ws1::kThreads, Ws1Geo<D>::kCtasPerSm) paged_prefill_ws1_kernel(const Args a) {
+    using namespace ws1;
+    using Wg = Ws1Geo<D>;
+    constexpr int QT = Wg::QT, KT = Wg::KT, VT = Wg::VT, PT = Wg::PT, STG = Wg::STG, SLOT = Wg::SLOT;
+    constexpr uint32_t S_COL = Wg::S_COL, OT_COL = Wg::OT_COL, OACC_COL = Wg::OACC_COL, COLS = Wg::COLS;
+    constexpr int ON = Wg::ON, NH = Wg::NH;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t k_full, k_empty, v_full, v_empty, s_full, p_full, o_full[2], o_free, done_bar;
+    __shared__ uint64_t k_full, k_empty, v_full, v_empty, s_full, p_full, o_full[NH], o_free, done_bar;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_sh;
     volatile int* abort_flag = &abort_sh;
@@ -1040,8 +1056,7 @@ __global__ void __launch_bounds__(ws256::kThreads, 1) paged_prefill_ws256_kernel
         mbar_init(&v_empty, 1);
         mbar_init(&s_full, 1);
         mbar_init(&p_full, 128);
-        mbar_init(&o_full[0], 1);
-        mbar_init(&o_full[1], 1);
+        for (int h = 0; h < NH; ++h) mbar_init(&o_full[h], 1);
         mbar_init(&o_free, 128);
         mbar_init(&done_bar, 1);
         abort_sh = 0;
@@ -1182,7 +1197,7 @@ __global__ void __launch_bounds__(ws256::kThreads, 1) paged_prefill_ws256_kernel
             // O = O * alpha + O_tile (IEEE FMA, FP32), one half of the output dimensions at a time
             bool okh = true;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < NH; ++h) {
                 ok = wait_or_abort(&o_full[h], st & 1, a.wait_ns, abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) {
                     okh = false;
@@ -1190,15 +1205,15 @@ __global__ void __launch_bounds__(ws256::kThreads, 1) paged_prefill_ws256_kernel
                 }
                 tc::fence_after_sync();
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < ON / 32; ++c) {
                     float x[32], y[32];
                     tc::ld32(trow + OT_COL + 32 * c, x);
-                    tc::ld32(trow + OACC_COL + 128 * h + 32 * c, y);
+                    tc::ld32(trow + OACC_COL + ON * h + 32 * c, y);
                     tc::wait_ld(x);
                     tc::wait_ld(y);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) y[j] = fmaf(y[j], alpha, x[j]);
-                    tc::st32(trow + OACC_COL + 128 * h + 32 * c, y);
+                    tc::st32(trow + OACC_COL + ON * h + 32 * c, y);
                 }
                 tc::wait_st();
                 tc::fence_before_sync();
@@ -1237,7 +1252,7 @@ __global__ void __launch_bounds__(ws256::kThreads, 1) paged_prefill_ws256_kernel
     } else if (lane == 0) {
         // ---------------------------------------------------------- MMA issuer
         constexpr uint32_t id_s = tc::idesc_f16_f32(128, tcg::kKeys);
-        constexpr uint32_t id_o = tc::idesc_f16_f32(128, 128);
+        constexpr uint32_t id_o = tc::idesc_f16_f32(128, ON);
         const bool stall_cta = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
         for (int st = 0; st < nst; ++st) {
             if (!wait_or_abort(&k_full, st & 1, a.wait_ns, abort_flag)) break;
@@ -1258,9 +1273,9 @@ __global__ void __launch_bounds__(ws256::kThreads, 1) paged_prefill_ws256_kernel
             tc::fence_after_sync();
             bool ok = true;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < NH; ++h) {
                 // O_tile is free once the rows have folded the previous half
-                const int f = 2 * st + h;     // this half's fold index
+                const int f = NH * st + h;    // this half's fold index
                 if (f > 0 && !wait_or_abort(&o_free, (f - 1) & 1, a.wait_ns, abort_flag)) {
                     ok = false;
                     break;
@@ -1269,7 +1284,7 @@ __global__ void __launch_bounds__(ws256::kThreads, 1) paged_prefill_ws256_kernel
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     tc::mma_f16(tm + OT_COL, tc::desc_k_sw128(sb + PT + ks * 32),
-                                tc::desc_k_sw128(sb + VT + h * 128 * 128 + ks * 32), id_o, ks > 0);
+                                tc::desc_k_sw128(sb + VT + h * ON * 128 + ks * 32), id_o, ks > 0);
                 tc::commit(&o_full[h]);
             }
             if (!ok) break;
@@ -1425,9 +1440,14 @@ inline int tiles_of(int max_q_len, int G) {
 // Which kernel runs: 1, the warp-specialised one with two tiles per CTA, at
 // d = 128 when a sequence's chunk spans at least two tiles; 2, the
 // warp-specialised one-tile kernel, at d = 256; else 0,
-// paged_prefill_tc_kernel, one tile per CTA (at d = 64 its 56 KB of shared
-// memory let several CTAs share an SM, which measured faster).
-inline int kernel_kind(int D, int tiles) { return D == 128 && tiles >= 2 ? 1 : (D == 256 ? 2 : 0); }
+// paged_prefill_tc_kernel, one tile per CTA.  At d = 64 the one-tile kernel
+// with its phases in turn measured faster than both warp-specialised ones
+// (442 against 407 and 369 TFLOP/s at 2048-token chunks): its 56 KB of shared
+// memory let several CTAs share an SM.
+inline int kernel_kind(int D, int tiles) {
+    if (D == 128) return tiles >= 2 ? 1 : 0;
+    return D == 256 ? 2 : 0;
+}
 inline int tiles_per_cta(int kind) { return kind == 1 ? ws::kTiles : 1; }
 
 Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D, int window, int sms, int per_sm) {
@@ -1463,9 +1483,9 @@ void kernel_of(int kind, void (**fn)(const Args), size_t* smem, int* threads) {
     }
     if constexpr (D == 256) {
         if (kind == 2) {
-            *fn = paged_prefill_ws256_kernel<G>;
-            *smem = static_cast<size_t>(ws256::SMEM) + 1024;
-            *threads = ws256::kThreads;
+            *fn = paged_prefill_ws1_kernel<D, G>;
+            *smem = static_cast<size_t>(Ws1Geo<D>::SMEM) + 1024;
+            *threads = ws1::kThreads;
             return;
         }
     }
