@@ -172,6 +172,26 @@ __device__ __forceinline__ uint32_t swz(int r, int o) {
         return r * 64 + ((((o >> 4) ^ ((r >> 1) & 3)) << 4) | (o & 15));
 }
 
+// The streaming kernel's own layout of a staged page (its cp.async copies and
+// its fragment loads are the only users, so it need not match TMA's): rows of
+// 128 bytes as swz<128>; rows of 64 bytes (d = 64) go in pairs into 128-byte
+// lines whose eight 16-byte chunks are XOR-permuted per line, the halves
+// swapped on every other line.  The score loads (a row pair per quarter-warp)
+// and the value loads (4 rows of 8-byte pieces per instruction) then meet
+// every bank once per wavefront; with swz<64> the value loads of the even
+// rows all fell into banks 0-15.
+template <int ROWB>
+__device__ __forceinline__ uint32_t sswz(int r, int o) {
+    if constexpr (ROWB == 128) {
+        return swz<128>(r, o);
+    } else {
+        const int line = r >> 1;
+        const int c = ((r & 1) << 2) | (o >> 4);
+        const int g = ((line & 1) << 2) | ((line >> 1) & 3);
+        return static_cast<uint32_t>(line * 128 + ((c ^ g) << 4) + (o & 15));
+    }
+}
+
 __device__ __forceinline__ void report(uint32_t* err, uint32_t code) { atomicCAS(err, 0u, code); }
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kNCW * 32) : "memory"); }
@@ -360,10 +380,10 @@ __device__ __forceinline__ void load_v_box(const uint8_t* box, int gid, int tig,
         const int row = 2 * tig + (r & 1) + 8 * (r >> 1);
         if (page_ok) {
             if constexpr (Gm::VW == 16) {
-                const uint4 x = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(row, gid * 16));
+                const uint4 x = *reinterpret_cast<const uint4*>(box + sswz<Gm::ROWB>(row, gid * 16));
                 v[r][0] = x.x; v[r][1] = x.y; v[r][2] = x.z; v[r][3] = x.w;
             } else {
-                const uint2 x = *reinterpret_cast<const uint2*>(box + swz<Gm::ROWB>(row, gid * 8));
+                const uint2 x = *reinterpret_cast<const uint2*>(box + sswz<Gm::ROWB>(row, gid * 8));
                 v[r][0] = x.x; v[r][1] = x.y;
             }
         }
@@ -1137,8 +1157,8 @@ __device__ __forceinline__ void tc_stage(const uint8_t* kst, const uint8_t* vst,
                 uint32_t w0[Gm::KW / 4], w1[Gm::KW / 4];
 #pragma unroll
                 for (int cc = 0; cc < Gm::KW / 16; ++cc) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(gid, tig * Gm::KW + 16 * cc));
-                    const uint4 y = *reinterpret_cast<const uint4*>(box + swz<Gm::ROWB>(gid + 8, tig * Gm::KW + 16 * cc));
+                    const uint4 x = *reinterpret_cast<const uint4*>(box + sswz<Gm::ROWB>(gid, tig * Gm::KW + 16 * cc));
+                    const uint4 y = *reinterpret_cast<const uint4*>(box + sswz<Gm::ROWB>(gid + 8, tig * Gm::KW + 16 * cc));
                     w0[4 * cc + 0] = x.x; w0[4 * cc + 1] = x.y; w0[4 * cc + 2] = x.z; w0[4 * cc + 3] = x.w;
                     w1[4 * cc + 0] = y.x; w1[4 * cc + 1] = y.y; w1[4 * cc + 2] = y.z; w1[4 * cc + 3] = y.w;
                 }
@@ -1480,7 +1500,7 @@ __global__ void __launch_bounds__(StreamCfg<D, ES, G>::NW * 32, kCtasPerSm)
     for (int i = 0; i < CPP; ++i) {
         const int byte = (lane + 32 * i) * 16;
         const int r = byte / Gm::RB, b = byte % Gm::RB;
-        soff[i] = (b / Gm::ROWB) * Gm::BOX + swz<Gm::ROWB>(r, b % Gm::ROWB);
+        soff[i] = (b / Gm::ROWB) * Gm::BOX + sswz<Gm::ROWB>(r, b % Gm::ROWB);
     }
     const uint64_t pol = l2_policy_evict_first();
     const bool appending = ES == 1 && a.k_new != nullptr;
