@@ -606,17 +606,20 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
 //   * warps 8-11 (converters): cp.async the fp8 pages of stage s + 2 into a
 //     3-slot staging ring, then convert stage s into one of two f16 K / V^T
 //     slots (once the MMAs of stage s - 2 have finished reading it);
-//   * one thread of warp 12 (the MMA issuer): per stage and tile, S = Q K^T
-//     into the tile's TMEM columns (once the tile's previous fold has read
-//     them), then, once the tile's P is written, O_tile = P V into the same
-//     columns;
+//   * one thread of warp 12 (the MMA issuer), tile by tile in turn: once the
+//     tile's P of stage s is written, O += P V (A = P read from TMEM) into the
+//     tile's FP32 accumulator in TMEM, then S = Q K^T of stage s + 1 into the
+//     tile's other S buffer;
 //   * warps 0-3 and 4-7 (one warpgroup per tile, thread = row = TMEM lane):
 //     load the row of S, online softmax in log2 units, write the row of P
-//     (f16) to shared memory; then fold the row of O_tile into the row's FP32
-//     accumulator in TMEM, O = O * alpha + O_tile (the two-level
-//     accumulation).
-// While one tile's warpgroup runs its softmax or fold, the tensor cores work
-// on the other tile, and the converters prepare the next stage.
+//     (f16, two per column) over the S just read, in TMEM.  The running
+//     maximum the row's O and l refer to moves only when the stage's maximum
+//     exceeds it by more than 2^8 (so P stays below 2^8); then, before the
+//     stage's P V, the warp rescales its rows of O in TMEM.  The tensor-core
+//     sums of O continue across stages in FP32.
+// The two tiles ping-pong: while one tile's warpgroup runs its softmax, the
+// tensor cores run the other tile's P V and next S, and the converters
+// prepare the next stage.
 namespace ws {
 constexpr int kTiles = 2;                  // query tiles of 128 rows per CTA
 constexpr int kConvWarp0 = 8;              // warps 8-11 convert
@@ -625,6 +628,7 @@ constexpr int kThreads = 13 * 32;
 constexpr int kStg = 3;                    // fp8 staging slots
 constexpr int kKv = 2;                     // f16 K / V^T slots
 constexpr int kConvBar = 2;                // named barrier of the converter warps
+constexpr float kRescaleLog2 = 8.f;        // a row's maximum moves when exceeded by more than this
 }  // namespace ws
 
 template <int D>
@@ -633,16 +637,16 @@ struct WsGeo {
     static constexpr int QTB = NB * 128 * 128;          // one Q tile: 128 rows x d
     static constexpr int KTB = NB * tcg::kKeys * 128;   // one K tile: 64 keys x d
     static constexpr int VTB = D * 128;                 // one V^T tile: d rows x 64 keys
-    static constexpr int PTB = 128 * 128;               // one P tile: 128 rows x 64 keys
     static constexpr int SLOT = 2 * tcg::kKeys * D;     // one fp8 staging slot: K rows, then V rows
     static constexpr int QT = 0;
     static constexpr int KT = QT + ws::kTiles * QTB;
     static constexpr int VT = KT + ws::kKv * KTB;
-    static constexpr int PT = VT + ws::kKv * VTB;
-    static constexpr int STG = PT + ws::kTiles * PTB;
-    static constexpr int SMEM = STG + ws::kStg * SLOT;  // 208 KB
-    // TMEM per tile: S (64 columns) and O_tile (d columns) share [0, d); the
-    // FP32 output accumulator takes [d, 2d)
+    static constexpr int STG = VT + ws::kKv * VTB;
+    static constexpr int SMEM = STG + ws::kStg * SLOT;  // 176 KB
+    // TMEM per tile: two S buffers of 64 columns (stage s in buffer s & 1, its
+    // P written over its first 32 columns), the FP32 output accumulator in
+    // [d, 2d)
+    static constexpr uint32_t SBUF = tcg::kKeys;
     static constexpr uint32_t TC = 2 * D;
     static constexpr uint32_t COLS = ws::kTiles * TC;   // 512
     static_assert(D == 128, "the warp-specialised kernel covers d = 128");
@@ -687,7 +691,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
     using Wg = WsGeo<D>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t kv_full[ws::kKv], kv_empty[ws::kKv];
-    __shared__ uint64_t s_full[ws::kTiles], p_full[ws::kTiles], o_full[ws::kTiles], o_free[ws::kTiles];
+    __shared__ uint64_t s_full[ws::kTiles], p_full[ws::kTiles];
     __shared__ uint64_t done_bar;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_sh;
@@ -703,8 +707,6 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
         for (int i = 0; i < ws::kTiles; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);    // the tile's warpgroup
-            mbar_init(&o_full[i], 1);
-            mbar_init(&o_free[i], 128);
         }
         mbar_init(&done_bar, 1);
         abort_sh = 0;
@@ -808,18 +810,20 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
             for (int c = 0; c < D / 32; ++c) tc::st32(trow + D + 32 * c, z);
             tc::wait_st();
         }
-        uint8_t* prow = sm + Wg::PT + ti * Wg::PTB + tt * 128;
         for (int st = 0; st < nst; ++st) {
-            bool ok = wait_or_abort(&s_full[ti], st & 1, a.wait_ns, abort_flag);
+            // S of stage st is in; its commit also covers the P V of stage
+            // st - 1, so O is complete and P's columns are free
+            const bool ok = wait_or_abort(&s_full[ti], st & 1, a.wait_ns, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) break;   // warp-uniform: the TMEM loads below are collective
             tc::fence_after_sync();
             const int pgs = sp0 + st * tcg::kPages;
             const int np = min(tcg::kPages, sp1 - pgs);
             const int t0 = pgs * kBS;
             const bool interior = np == tcg::kPages && t0 + tcg::kKeys - 1 <= wpos0 && t0 >= wlo1;
+            const uint32_t srow = trow + (st & 1) * Wg::SBUF;
             float sv[64];
-            tc::ld32(trow, *reinterpret_cast<float(*)[32]>(sv));
-            tc::ld32(trow + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
+            tc::ld32(srow, *reinterpret_cast<float(*)[32]>(sv));
+            tc::ld32(srow + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
             tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv));
             tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv + 32));
             float mx = -INFINITY;
@@ -838,44 +842,43 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
                     mx = fmaxf(mx, sv[j]);
                 }
             }
+            // the reference maximum moves only by more than 8 (log2 units);
+            // a row that had none (m = -inf) holds O = 0 and l = 0
             const float mn = fmaxf(m, mx);
-            const float muse = mn == -INFINITY ? 0.f : mn;
-            const float alpha = fast_exp2(m - muse);
-            m = mn;
-            float ls = 0.f;
+            const bool upd = mn > m + ws::kRescaleLog2;
+            const bool held = upd && m != -INFINITY;
+            float alpha = 1.f;
+            if (upd) {
+                alpha = fast_exp2(m - mn);
+                l *= alpha;
+                m = mn;
+            }
+            if (__any_sync(0xffffffffu, held)) {
+                // O = O * alpha for the warp's rows (1 where the row keeps its maximum)
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t pw[4];
+                for (int c = 0; c < D / 32; ++c) {
+                    float x[32];
+                    tc::ld32(trow + D + 32 * c, x);
+                    tc::wait_ld(x);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = fast_exp2(sv[8 * c + 2 * e] - muse), p1 = fast_exp2(sv[8 * c + 2 * e + 1] - muse);
-                    ls += p0 + p1;
-                    pw[e] = pack_f16x2(p0, p1);
+                    for (int j = 0; j < 32; ++j) x[j] *= alpha;
+                    tc::st32(trow + D + 32 * c, x);
                 }
-                *reinterpret_cast<uint4*>(prow + ((c ^ (tt & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
             }
-            l = l * alpha + ls;
-            tc::fence_proxy_async_smem();  // P is read by the tensor cores
-            tc::fence_before_sync();
-            mbar_arrive(&p_full[ti]);
-            ok = wait_or_abort(&o_full[ti], st & 1, a.wait_ns, abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            tc::fence_after_sync();
-            // O = O * alpha + O_tile (IEEE FMA, FP32): the two-level accumulation
+            const float muse = m == -INFINITY ? 0.f : m;
+            float ls = 0.f;
+            float pw[32];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float x[32], y[32];
-                tc::ld32(trow + 32 * c, x);
-                tc::ld32(trow + D + 32 * c, y);
-                tc::wait_ld(x);
-                tc::wait_ld(y);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) y[j] = fmaf(y[j], alpha, x[j]);
-                tc::st32(trow + D + 32 * c, y);
+            for (int j = 0; j < 32; ++j) {
+                const float p0 = fast_exp2(sv[2 * j] - muse), p1 = fast_exp2(sv[2 * j + 1] - muse);
+                ls += p0 + p1;
+                pw[j] = __uint_as_float(pack_f16x2(p0, p1));
             }
+            l += ls;
+            tc::st32(srow, pw);
             tc::wait_st();
             tc::fence_before_sync();
-            mbar_arrive(&o_free[ti]);      // the MMA may overwrite S / O_tile
+            mbar_arrive(&p_full[ti]);      // P (and the rescaled O) are in TMEM
         }
     } else if (warp < ws::kMmaWarp) {
         // ---------------------------------------------------------- converters
@@ -904,42 +907,50 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
         constexpr uint32_t id_s = tc::idesc_f16_f32(128, tcg::kKeys);
         constexpr uint32_t id_o = tc::idesc_f16_f32(128, D);
         const bool stall_cta = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
-        for (int st = 0; st < nst; ++st) {
-            const int j = st & 1;
-            if (!wait_or_abort(&kv_full[j], (st >> 1) & 1, a.wait_ns, abort_flag)) break;
-            tc::fence_after_sync();
-            bool ok = true;
-            for (int i = 0; i < ws::kTiles && ok; ++i) {
-                if (st > 0 && !wait_or_abort(&o_free[i], (st - 1) & 1, a.wait_ns, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
-                if (st == a.stall_stage && stall_cta) continue;   // test hook: this tile's S never arrives
+        // S = Q K^T of stage s for tile i, into the tile's S buffer s & 1
+        auto issue_s = [&](int i, int s) {
+            if (s == a.stall_stage && stall_cta) return;   // test hook: this tile's S never arrives
+            const int j = s & 1;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks & 3) * 32;
-                    tc::mma_f16(tm + i * Wg::TC,
-                                tc::desc_k_sw128(sb + Wg::QT + i * Wg::QTB + (ks >> 2) * 16384 + off),
-                                tc::desc_k_sw128(sb + Wg::KT + j * Wg::KTB + (ks >> 2) * (tcg::kKeys * 128) + off),
-                                id_s, ks > 0);
-                }
-                tc::commit(&s_full[i]);
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t off = (ks & 3) * 32;
+                tc::mma_f16(tm + i * Wg::TC + j * Wg::SBUF,
+                            tc::desc_k_sw128(sb + Wg::QT + i * Wg::QTB + (ks >> 2) * 16384 + off),
+                            tc::desc_k_sw128(sb + Wg::KT + j * Wg::KTB + (ks >> 2) * (tcg::kKeys * 128) + off),
+                            id_s, ks > 0);
             }
-            for (int i = 0; i < ws::kTiles && ok; ++i) {
+            tc::commit(&s_full[i]);
+        };
+        bool ok = nst == 0 || wait_or_abort(&kv_full[0], 0, a.wait_ns, abort_flag);
+        if (ok && nst > 0) {
+            tc::fence_after_sync();
+            for (int i = 0; i < ws::kTiles; ++i) issue_s(i, 0);
+        }
+        for (int st = 0; st < nst && ok; ++st) {
+            const int j = st & 1;
+            for (int i = 0; i < ws::kTiles; ++i) {
                 if (!wait_or_abort(&p_full[i], st & 1, a.wait_ns, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after_sync();
+                // O += P V: P (128 rows x 64 keys) from the S buffer's first 32 columns
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_f16(tm + i * Wg::TC, tc::desc_k_sw128(sb + Wg::PT + i * Wg::PTB + ks * 32),
-                                tc::desc_k_sw128(sb + Wg::VT + j * Wg::VTB + ks * 32), id_o, ks > 0);
-                tc::commit(&o_full[i]);
+                    tc::mma_f16_ts(tm + i * Wg::TC + D, tm + i * Wg::TC + j * Wg::SBUF + ks * 8,
+                                   tc::desc_k_sw128(sb + Wg::VT + j * Wg::VTB + ks * 32), id_o, 1);
+                if (i == ws::kTiles - 1) tc::commit(&kv_empty[j]);   // the slot's MMAs (both tiles) have completed
+                if (st + 1 < nst) {
+                    if (i == 0) {
+                        if (!wait_or_abort(&kv_full[(st + 1) & 1], ((st + 1) >> 1) & 1, a.wait_ns, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
+                    }
+                    issue_s(i, st + 1);
+                }
             }
-            if (!ok) break;
-            tc::commit(&kv_empty[j]);   // the slot's MMAs (both tiles) have completed
         }
         // every MMA this thread issued completes before TMEM is released
         tc::commit(&done_bar);

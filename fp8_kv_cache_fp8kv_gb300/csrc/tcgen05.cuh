@@ -52,6 +52,20 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A * B^T with A (M x K = 16, f16) in tensor memory: row m in
+// lane m, two consecutive K elements per 32-bit column (the lower K index in
+// the low half), so one MMA reads 8 columns from `a_tmem`; B as in mma_f16.
+// Issued by one thread.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrives (once) on `bar` when every tcgen05 operation this thread issued
 // before has completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {
