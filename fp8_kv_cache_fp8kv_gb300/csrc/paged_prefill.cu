@@ -225,7 +225,7 @@ __device__ __forceinline__ void load_stage_tc(const Args& a, const int32_t* bt, 
 // K-major, 128-byte swizzle) and the staged V rows, transposed, into the f16
 // V^T tile at vt (d rows x 64 keys).  Keys outside [kmin, kmax] or past the
 // stage's np pages become zeros in V^T (their scores are masked).
-template <int D>
+template <int D, int KS = tcg::kKeys * 128>   // KS: bytes between the K tile's 128-byte atom columns
 __device__ __forceinline__ void convert_stage_k(const uint8_t* stg, uint8_t* kt, int ct) {
     // K: thread ct converts CH staged chunks (16 dims each) of key ct & 63
     {
@@ -241,7 +241,7 @@ __device__ __forceinline__ void convert_stage_k(const uint8_t* stg, uint8_t* kt,
             e4m3x4_to_f16x2x2(x.z, f[4], f[5]);
             e4m3x4_to_f16x2x2(x.w, f[6], f[7]);
             const int j = 2 * (c & 3);                     // f16 chunk within the 64-dim block c / 4
-            uint8_t* dst = kt + (c >> 2) * (tcg::kKeys * 128) + k * 128;
+            uint8_t* dst = kt + (c >> 2) * KS + k * 128;
             *reinterpret_cast<uint4*>(dst + ((j ^ (k & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
             *reinterpret_cast<uint4*>(dst + (((j + 1) ^ (k & 7)) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
         }
@@ -600,16 +600,20 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
 // The warp-specialised prefill kernel (d = 128, chunks of at least two tiles).
 //
 // A CTA takes two consecutive query tiles of one (kv head, sequence), 256
-// rows, and one key range; the K and V operand tiles of each stage are built
-// once for both.  The roles run concurrently and hand work over through
+// rows, and one key range, walked in stages of 128 keys (two staging
+// granules of 64 keys); each stage's K and V operand tiles are built once for
+// both tiles.  The roles run concurrently and hand work over through
 // mbarriers (every wait bounded):
-//   * warps 8-11 (converters): cp.async the fp8 pages of stage s + 2 into a
-//     3-slot staging ring, then convert stage s into one of two f16 K / V^T
-//     slots (once the MMAs of stage s - 2 have finished reading it);
+//   * warps 8-11 (converters): cp.async the fp8 pages of stage s + 1 into a
+//     two-stage staging ring, then convert stage s's K into the f16 K tile
+//     (once the score MMAs of stage s - 1 have read it) and its V, transposed,
+//     into one of two f16 V^T tiles (once the value MMAs of stage s - 2 have);
 //   * one thread of warp 12 (the MMA issuer), tile by tile in turn: once the
 //     tile's P of stage s is written, O += P V (A = P read from TMEM) into the
-//     tile's FP32 accumulator in TMEM, then S = Q K^T of stage s + 1 into the
-//     tile's other S buffer;
+//     tile's FP32 accumulator in TMEM, then S = Q K^T of stage s + 1 (N = 128
+//     keys) into the tile's S columns.  The tensor cores run the MMAs one
+//     thread issues in issue order, so S(s + 1) overwrites the columns only
+//     after P V of stage s has read P from them;
 //   * warps 0-3 and 4-7 (one warpgroup per tile, thread = row = TMEM lane):
 //     load the row of S, online softmax in log2 units, write the row of P
 //     (f16, two per column) over the S just read, in TMEM.  The running
@@ -625,8 +629,10 @@ constexpr int kTiles = 2;                  // query tiles of 128 rows per CTA
 constexpr int kConvWarp0 = 8;              // warps 8-11 convert
 constexpr int kMmaWarp = 12;               // warp 12 issues the MMAs
 constexpr int kThreads = 13 * 32;
-constexpr int kStg = 3;                    // fp8 staging slots
-constexpr int kKv = 2;                     // f16 K / V^T slots
+constexpr int kKeys = 128;                 // keys per stage
+constexpr int kGran = kKeys / tcg::kKeys;  // staging granules (64 keys, 4 pages) per stage
+constexpr int kPages = kKeys / kBS;        // pages per stage
+constexpr int kStg = 2;                    // stages in the fp8 staging ring
 constexpr int kConvBar = 2;                // named barrier of the converter warps
 constexpr float kRescaleLog2 = 8.f;        // a row's maximum moves when exceeded by more than this
 }  // namespace ws
@@ -635,18 +641,18 @@ template <int D>
 struct WsGeo {
     static constexpr int NB = D / 64;
     static constexpr int QTB = NB * 128 * 128;          // one Q tile: 128 rows x d
-    static constexpr int KTB = NB * tcg::kKeys * 128;   // one K tile: 64 keys x d
-    static constexpr int VTB = D * 128;                 // one V^T tile: d rows x 64 keys
-    static constexpr int SLOT = 2 * tcg::kKeys * D;     // one fp8 staging slot: K rows, then V rows
+    static constexpr int KAT = ws::kKeys * 128;         // one 128-byte atom column of the K tile (128 keys)
+    static constexpr int KTB = NB * KAT;                // the K tile: 128 keys x d
+    static constexpr int VAT = D * 128;                 // one atom column of the V^T tile: d rows x 64 keys
+    static constexpr int VTB = ws::kGran * VAT;         // the V^T tile: d rows x 128 keys
+    static constexpr int GSLOT = 2 * tcg::kKeys * D;    // one fp8 staging granule: 64 K rows, then 64 V rows
     static constexpr int QT = 0;
     static constexpr int KT = QT + ws::kTiles * QTB;
-    static constexpr int VT = KT + ws::kKv * KTB;
-    static constexpr int STG = VT + ws::kKv * VTB;
-    static constexpr int SMEM = STG + ws::kStg * SLOT;  // 176 KB
-    // TMEM per tile: two S buffers of 64 columns (stage s in buffer s & 1, its
-    // P written over its first 32 columns), the FP32 output accumulator in
-    // [d, 2d)
-    static constexpr uint32_t SBUF = tcg::kKeys;
+    static constexpr int VT = KT + KTB;
+    static constexpr int STG = VT + 2 * VTB;
+    static constexpr int SMEM = STG + ws::kStg * ws::kGran * GSLOT;   // 224 KB
+    // TMEM per tile: S in [0, 128) (P written over its first 64 columns), the
+    // FP32 output accumulator in [d, 2d)
     static constexpr uint32_t TC = 2 * D;
     static constexpr uint32_t COLS = ws::kTiles * TC;   // 512
     static_assert(D == 128, "the warp-specialised kernel covers d = 128");
@@ -690,7 +696,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const Args a) {
     using Wg = WsGeo<D>;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t kv_full[ws::kKv], kv_empty[ws::kKv];
+    __shared__ uint64_t k_full, k_empty, v_full[2], v_empty[2];
     __shared__ uint64_t s_full[ws::kTiles], p_full[ws::kTiles];
     __shared__ uint64_t done_bar;
     __shared__ uint32_t tmem_base;
@@ -700,9 +706,11 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int j = 0; j < ws::kKv; ++j) {
-            mbar_init(&kv_full[j], 128);   // the converter threads
-            mbar_init(&kv_empty[j], 1);    // tcgen05.commit
+        mbar_init(&k_full, 128);           // the converter threads
+        mbar_init(&k_empty, 1);            // tcgen05.commit
+        for (int j = 0; j < 2; ++j) {      // one per V^T tile
+            mbar_init(&v_full[j], 128);
+            mbar_init(&v_empty[j], 1);
         }
         for (int i = 0; i < ws::kTiles; ++i) {
             mbar_init(&s_full[i], 1);
@@ -724,7 +732,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
     const int pg0 = kmin / kBS, np_all = kmax / kBS - pg0 + 1;
     const int sp0 = pg0 + static_cast<int>(static_cast<int64_t>(split) * np_all / a.splits);
     const int sp1 = pg0 + static_cast<int>(static_cast<int64_t>(split + 1) * np_all / a.splits);
-    const int nst = (sp1 - sp0 + tcg::kPages - 1) / tcg::kPages;
+    const int nst = (sp1 - sp0 + ws::kPages - 1) / ws::kPages;
     const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
 
     // ---- role set-up: the warpgroups build their Q tiles; the converters
@@ -779,15 +787,21 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
         const int wpos1 = uu.L - uu.n + max(0, min(wr0 + 31, uu.rows - 1)) / G;
         wlo1 = (a.window > 0 && wpos1 + 1 > a.window) ? wpos1 + 1 - a.window : 0;
         if (!(ti == 0 || has1)) wpos0 = -1;       // no valid row: never the fast path
-    } else if (warp < ws::kMmaWarp) {
-        const int ct = tid - ws::kConvWarp0 * 32;
-        for (int s = 0; s < ws::kStg - 1; ++s) {
-            if (s < nst)
-                load_stage_tc<D>(a, bt, hk, sp0 + s * tcg::kPages, min(tcg::kPages, sp1 - sp0 - s * tcg::kPages),
-                                 sb + Wg::STG + s * Wg::SLOT, ct);
-            cp_async_commit();
-        }
     }
+    // the converters' copies of stage s: granule g's pages into staging granule
+    // (s % kStg) * kGran + g; one commit group per stage
+    auto load_stage = [&](int s, int ct) {
+        if (s < nst)
+            for (int g = 0; g < ws::kGran; ++g) {
+                const int pg = sp0 + s * ws::kPages + g * tcg::kPages;
+                const int npg = min(tcg::kPages, sp1 - pg);
+                if (npg > 0)
+                    load_stage_tc<D>(a, bt, hk, pg, npg, sb + Wg::STG + ((s % ws::kStg) * ws::kGran + g) * Wg::GSLOT,
+                                     ct);
+            }
+        cp_async_commit();
+    };
+    if (warp >= ws::kConvWarp0 && warp < ws::kMmaWarp) load_stage(0, tid - ws::kConvWarp0 * 32);
     if (warp == 0) tc::alloc(&tmem_base, Wg::COLS);
     tc::fence_proxy_async_smem();  // the Q tiles are read by the tensor cores
     tc::fence_before_sync();
@@ -816,31 +830,36 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
             const bool ok = wait_or_abort(&s_full[ti], st & 1, a.wait_ns, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) break;   // warp-uniform: the TMEM loads below are collective
             tc::fence_after_sync();
-            const int pgs = sp0 + st * tcg::kPages;
-            const int np = min(tcg::kPages, sp1 - pgs);
+            const int pgs = sp0 + st * ws::kPages;
+            const int nk = min(ws::kPages, sp1 - pgs) * kBS;    // the stage's keys
             const int t0 = pgs * kBS;
-            const bool interior = np == tcg::kPages && t0 + tcg::kKeys - 1 <= wpos0 && t0 >= wlo1;
-            const uint32_t srow = trow + (st & 1) * Wg::SBUF;
-            float sv[64];
-            tc::ld32(srow, *reinterpret_cast<float(*)[32]>(sv));
-            tc::ld32(srow + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
-            tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv));
-            tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv + 32));
+            const bool interior = nk == ws::kKeys && t0 + ws::kKeys - 1 <= wpos0 && t0 >= wlo1;
+            // the row of S in two halves of 64 keys, read twice (its maximum,
+            // then P) to keep 64 values in registers
+            auto load_half = [&](int h, float (&sv)[64]) {
+                tc::ld32(trow + 64 * h, *reinterpret_cast<float(*)[32]>(sv));
+                tc::ld32(trow + 64 * h + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
+                tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv));
+                tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv + 32));
+                if (interior) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) sv[j] *= cs;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) {
+                        const int jj = 64 * h + j, key = t0 + jj;
+                        const bool valid = jj < nk && rv && key >= lq && key <= pq;
+                        sv[j] = valid ? sv[j] * cs : -INFINITY;
+                    }
+                }
+            };
             float mx = -INFINITY;
-            if (interior) {
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float sv[64];
+                load_half(h, sv);
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    sv[j] *= cs;
-                    mx = fmaxf(mx, sv[j]);
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const int key = t0 + j;
-                    const bool valid = j < np * kBS && rv && key >= lq && key <= pq;
-                    sv[j] = valid ? sv[j] * cs : -INFINITY;
-                    mx = fmaxf(mx, sv[j]);
-                }
+                for (int j = 0; j < 64; ++j) mx = fmaxf(mx, sv[j]);
             }
             // the reference maximum moves only by more than 8 (log2 units);
             // a row that had none (m = -inf) holds O = 0 and l = 0
@@ -867,15 +886,22 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
             }
             const float muse = m == -INFINITY ? 0.f : m;
             float ls = 0.f;
-            float pw[32];
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                // P of keys [64h, 64h + 64) goes to columns [32h, 32h + 32),
+                // whose S (keys [32h, 32h + 32)) has been read already
+                float sv[64];
+                load_half(h, sv);
+                float pw[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float p0 = fast_exp2(sv[2 * j] - muse), p1 = fast_exp2(sv[2 * j + 1] - muse);
-                ls += p0 + p1;
-                pw[j] = __uint_as_float(pack_f16x2(p0, p1));
+                for (int j = 0; j < 32; ++j) {
+                    const float p0 = fast_exp2(sv[2 * j] - muse), p1 = fast_exp2(sv[2 * j + 1] - muse);
+                    ls += p0 + p1;
+                    pw[j] = __uint_as_float(pack_f16x2(p0, p1));
+                }
+                tc::st32(trow + 32 * h, pw);
             }
             l += ls;
-            tc::st32(srow, pw);
             tc::wait_st();
             tc::fence_before_sync();
             mbar_arrive(&p_full[ti]);      // P (and the rescaled O) are in TMEM
@@ -884,71 +910,81 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
         // ---------------------------------------------------------- converters
         const int ct = tid - ws::kConvWarp0 * 32;
         for (int st = 0; st < nst; ++st) {
-            const int nxt = st + ws::kStg - 1;
-            if (nxt < nst)
-                load_stage_tc<D>(a, bt, hk, sp0 + nxt * tcg::kPages, min(tcg::kPages, sp1 - sp0 - nxt * tcg::kPages),
-                                 sb + Wg::STG + (nxt % ws::kStg) * Wg::SLOT, ct);
-            cp_async_commit();
-            cp_async_wait<ws::kStg - 1>();   // this thread's copies of stage st have landed
-            const int j = st & 1;
-            // the f16 slot is free once the MMAs of stage st - 2 have completed
-            const bool ok = st < ws::kKv || wait_or_abort(&kv_empty[j], ((st >> 1) + 1) & 1, a.wait_ns, abort_flag);
+            load_stage(st + 1, ct);          // its staging granules were read in iteration st - 1
+            cp_async_wait<1>();              // this thread's copies of stage st have landed
+            const uint8_t* stg = sm + Wg::STG + (st % ws::kStg) * ws::kGran * Wg::GSLOT;
+            const int pgs = sp0 + st * ws::kPages;
+            // the K tile is free once the score MMAs of stage st - 1 have completed
+            bool ok = st == 0 || wait_or_abort(&k_empty, (st - 1) & 1, a.wait_ns, abort_flag);
             if (named_bar_or(ws::kConvBar, 128, !ok)) break;   // every copy of stage st landed (or all give up)
-            const int pgs = sp0 + st * tcg::kPages;
-            convert_stage<D>(sm + Wg::STG + (st % ws::kStg) * Wg::SLOT, sm + Wg::KT + j * Wg::KTB,
-                             sm + Wg::VT + j * Wg::VTB, ct, pgs * kBS, min(tcg::kPages, sp1 - pgs), kmin, kmax);
-            tc::fence_proxy_async_smem();    // the tiles are read by the tensor cores
-            mbar_arrive(&kv_full[j]);
-            named_bar_sync(ws::kConvBar, 128);  // the staging slot is read before it is refilled
+#pragma unroll
+            for (int g = 0; g < ws::kGran; ++g)
+                if (pgs + g * tcg::kPages < sp1)   // an empty granule's keys are masked
+                    convert_stage_k<D, Wg::KAT>(stg + g * Wg::GSLOT, sm + Wg::KT + g * (tcg::kKeys * 128), ct);
+            tc::fence_proxy_async_smem();    // the tile is read by the tensor cores
+            mbar_arrive(&k_full);
+            // V^T tile st & 1 is free once the value MMAs of stage st - 2 have completed
+            const int j = st & 1;
+            ok = st < 2 || wait_or_abort(&v_empty[j], ((st >> 1) + 1) & 1, a.wait_ns, abort_flag);
+            if (named_bar_or(ws::kConvBar, 128, !ok)) break;
+#pragma unroll
+            for (int g = 0; g < ws::kGran; ++g) {
+                const int pg = pgs + g * tcg::kPages;
+                convert_stage_v<D>(stg + g * Wg::GSLOT, sm + Wg::VT + j * Wg::VTB + g * Wg::VAT, ct, pg * kBS,
+                                   min(tcg::kPages, sp1 - pg), kmin, kmax);   // zeros past the range
+            }
+            tc::fence_proxy_async_smem();
+            mbar_arrive(&v_full[j]);
+            named_bar_sync(ws::kConvBar, 128);  // the staging granules are read before they are refilled
         }
         cp_async_wait<0>();
     } else if (lane == 0) {
         // ---------------------------------------------------------- MMA issuer
-        constexpr uint32_t id_s = tc::idesc_f16_f32(128, tcg::kKeys);
+        constexpr uint32_t id_s = tc::idesc_f16_f32(128, ws::kKeys);
         constexpr uint32_t id_o = tc::idesc_f16_f32(128, D);
         const bool stall_cta = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
-        // S = Q K^T of stage s for tile i, into the tile's S buffer s & 1
+        // S = Q K^T of stage s for tile i (N = 128 keys), into the tile's S columns
         auto issue_s = [&](int i, int s) {
             if (s == a.stall_stage && stall_cta) return;   // test hook: this tile's S never arrives
-            const int j = s & 1;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
                 const uint32_t off = (ks & 3) * 32;
-                tc::mma_f16(tm + i * Wg::TC + j * Wg::SBUF,
-                            tc::desc_k_sw128(sb + Wg::QT + i * Wg::QTB + (ks >> 2) * 16384 + off),
-                            tc::desc_k_sw128(sb + Wg::KT + j * Wg::KTB + (ks >> 2) * (tcg::kKeys * 128) + off),
-                            id_s, ks > 0);
+                tc::mma_f16(tm + i * Wg::TC, tc::desc_k_sw128(sb + Wg::QT + i * Wg::QTB + (ks >> 2) * 16384 + off),
+                            tc::desc_k_sw128(sb + Wg::KT + (ks >> 2) * Wg::KAT + off), id_s, ks > 0);
             }
             tc::commit(&s_full[i]);
         };
-        bool ok = nst == 0 || wait_or_abort(&kv_full[0], 0, a.wait_ns, abort_flag);
+        bool ok = nst == 0 || wait_or_abort(&k_full, 0, a.wait_ns, abort_flag);
         if (ok && nst > 0) {
             tc::fence_after_sync();
             for (int i = 0; i < ws::kTiles; ++i) issue_s(i, 0);
+            tc::commit(&k_empty);            // the K tile is free when the score MMAs complete
         }
         for (int st = 0; st < nst && ok; ++st) {
-            const int j = st & 1;
             for (int i = 0; i < ws::kTiles; ++i) {
-                if (!wait_or_abort(&p_full[i], st & 1, a.wait_ns, abort_flag)) {
+                if (!wait_or_abort(&p_full[i], st & 1, a.wait_ns, abort_flag) ||
+                    (i == 0 && !wait_or_abort(&v_full[st & 1], (st >> 1) & 1, a.wait_ns, abort_flag))) {
                     ok = false;
                     break;
                 }
                 tc::fence_after_sync();
-                // O += P V: P (128 rows x 64 keys) from the S buffer's first 32 columns
+                // O += P V: P (128 rows x 128 keys) from the S columns [0, 64)
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_f16_ts(tm + i * Wg::TC + D, tm + i * Wg::TC + j * Wg::SBUF + ks * 8,
-                                   tc::desc_k_sw128(sb + Wg::VT + j * Wg::VTB + ks * 32), id_o, 1);
-                if (i == ws::kTiles - 1) tc::commit(&kv_empty[j]);   // the slot's MMAs (both tiles) have completed
+                for (int ks = 0; ks < ws::kKeys / 16; ++ks)
+                    tc::mma_f16_ts(tm + i * Wg::TC + D, tm + i * Wg::TC + ks * 8,
+                                   tc::desc_k_sw128(sb + Wg::VT + (st & 1) * Wg::VTB + (ks >> 2) * Wg::VAT + (ks & 3) * 32),
+                                   id_o, 1);
+                if (i == ws::kTiles - 1) tc::commit(&v_empty[st & 1]);   // the V^T tile is free when both tiles' P V complete
                 if (st + 1 < nst) {
                     if (i == 0) {
-                        if (!wait_or_abort(&kv_full[(st + 1) & 1], ((st + 1) >> 1) & 1, a.wait_ns, abort_flag)) {
+                        if (!wait_or_abort(&k_full, (st + 1) & 1, a.wait_ns, abort_flag)) {
                             ok = false;
                             break;
                         }
                         tc::fence_after_sync();
                     }
                     issue_s(i, st + 1);
+                    if (i == ws::kTiles - 1) tc::commit(&k_empty);
                 }
             }
         }
