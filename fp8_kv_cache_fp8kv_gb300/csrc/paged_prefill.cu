@@ -765,7 +765,9 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
             const int e = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFF) - 127;
             shift = max(-100, min(100, 14 - e));
         }
-        const float up = __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
+        // a negative score scale goes into Q, so that the row's scale cs is
+        // positive and the maximum of the scaled scores is cs times the raw maximum
+        const float up = (a.score_scale < 0.f ? -1.f : 1.f) * __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
 #pragma unroll 4
         for (int c = 0; c < NC; ++c) {
             const uint4 qv = rv ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
@@ -777,7 +779,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
             *reinterpret_cast<uint4*>(sm + Wg::QT + ti * Wg::QTB + (c >> 3) * 16384 + tt * 128 +
                                       (((c & 7) ^ (tt & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
         }
-        cs = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
+        cs = fabsf(a.score_scale) * __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
         pq = uu.L - uu.n + (rv ? r / G : 0);
         lq = (a.window > 0 && pq + 1 > a.window) ? pq + 1 - a.window : 0;
         // the warp's first position and its last valid row's window start: a
@@ -835,32 +837,33 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
             const int t0 = pgs * kBS;
             const bool interior = nk == ws::kKeys && t0 + ws::kKeys - 1 <= wpos0 && t0 >= wlo1;
             // the row of S in two halves of 64 keys, read twice (its maximum,
-            // then P) to keep 64 values in registers
+            // then P) to keep 64 values in registers; cs >= 0, so the maximum
+            // of the scaled scores is cs times that of the raw ones
             auto load_half = [&](int h, float (&sv)[64]) {
                 tc::ld32(trow + 64 * h, *reinterpret_cast<float(*)[32]>(sv));
                 tc::ld32(trow + 64 * h + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
                 tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv));
                 tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv + 32));
-                if (interior) {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) sv[j] *= cs;
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) {
-                        const int jj = 64 * h + j, key = t0 + jj;
-                        const bool valid = jj < nk && rv && key >= lq && key <= pq;
-                        sv[j] = valid ? sv[j] * cs : -INFINITY;
-                    }
-                }
             };
-            float mx = -INFINITY;
+            auto key_ok = [&](int jj) {
+                const int key = t0 + jj;
+                return jj < nk && rv && key >= lq && key <= pq;
+            };
+            float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
                 float sv[64];
                 load_half(h, sv);
+                if (interior) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) mx = fmaxf(mx, sv[j]);
+                    for (int j = 0; j < 64; ++j) mr[j & 3] = fmaxf(mr[j & 3], sv[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) mr[j & 3] = fmaxf(mr[j & 3], key_ok(64 * h + j) ? sv[j] : -INFINITY);
+                }
             }
+            const float mraw = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
+            const float mx = mraw == -INFINITY ? -INFINITY : mraw * cs;
             // the reference maximum moves only by more than 8 (log2 units);
             // a row that had none (m = -inf) holds O = 0 and l = 0
             const float mn = fmaxf(m, mx);
@@ -884,8 +887,8 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
                     tc::st32(trow + D + 32 * c, x);
                 }
             }
-            const float muse = m == -INFINITY ? 0.f : m;
-            float ls = 0.f;
+            const float nmuse = m == -INFINITY ? 0.f : -m;
+            float lp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
                 // P of keys [64h, 64h + 64) goes to columns [32h, 32h + 32),
@@ -893,14 +896,26 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
                 float sv[64];
                 load_half(h, sv);
                 float pw[32];
+                if (interior) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float p0 = fast_exp2(sv[2 * j] - muse), p1 = fast_exp2(sv[2 * j + 1] - muse);
-                    ls += p0 + p1;
-                    pw[j] = __uint_as_float(pack_f16x2(p0, p1));
+                    for (int j = 0; j < 32; ++j) {
+                        const float p0 = fast_exp2(fmaf(sv[2 * j], cs, nmuse));
+                        const float p1 = fast_exp2(fmaf(sv[2 * j + 1], cs, nmuse));
+                        lp[j & 3] += p0 + p1;
+                        pw[j] = __uint_as_float(pack_f16x2(p0, p1));
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {   // masked keys weigh 0 (also when cs = 0)
+                        const float p0 = key_ok(64 * h + 2 * j) ? fast_exp2(fmaf(sv[2 * j], cs, nmuse)) : 0.f;
+                        const float p1 = key_ok(64 * h + 2 * j + 1) ? fast_exp2(fmaf(sv[2 * j + 1], cs, nmuse)) : 0.f;
+                        lp[j & 3] += p0 + p1;
+                        pw[j] = __uint_as_float(pack_f16x2(p0, p1));
+                    }
                 }
                 tc::st32(trow + 32 * h, pw);
             }
+            const float ls = (lp[0] + lp[1]) + (lp[2] + lp[3]);
             l += ls;
             tc::wait_st();
             tc::fence_before_sync();

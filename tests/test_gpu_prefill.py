@@ -217,3 +217,22 @@ def test_prefill_short_chunk_long_context_splits_the_keys(base):
         got = _run(p, q, qs, window)
         ref = _oracle(p, q, q_lens, window)
         assert_attn_close(got, ref, f"{base} split window={window}")
+
+
+@pytest.mark.parametrize("base", ["llama31_8b_b8_20k", "gptoss20b_b8_16k", "gemma4e2b_b16_8k32k"])
+@pytest.mark.parametrize("sm_scale", [-0.07, 0.0])
+def test_prefill_negative_and_zero_softmax_scale(base, sm_scale):
+    # the softmax scale is any finite number: a negative one reverses the
+    # order of the scores, zero makes every attended key weigh the same
+    lens = [700, 300, 129]
+    q_lens = [200, 64, 129]                     # 200 tokens span several tiles at every g
+    shape = workload.small_shape(base, len(lens), 1, 1, needle_margin=None)
+    w = workload.make_workload(shape, seed=8, lens=lens)
+    w.sm_scale = sm_scale
+    p = Paged(w, seed=8)
+    p.append_all()
+    q, qs = workload.prefill_queries(w, q_lens, seed=8)
+    for window in (0, 50):
+        got = _run(p, q, qs, window)
+        ref = _oracle(p, q, q_lens, window)
+        assert_attn_close(got, ref, f"{base} sm_scale={sm_scale} window={window}")
