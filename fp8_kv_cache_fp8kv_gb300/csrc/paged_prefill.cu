@@ -1162,7 +1162,9 @@ __global__ void __launch_bounds__(ws1::kThreads, Ws1Geo<D>::kCtasPerSm) paged_pr
             const int e = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFF) - 127;
             shift = max(-100, min(100, 14 - e));
         }
-        const float up = __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
+        // a negative score scale goes into Q, so that the row's scale cs is
+        // positive and the maximum of the scaled scores is cs times the raw maximum
+        const float up = (a.score_scale < 0.f ? -1.f : 1.f) * __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
 #pragma unroll 4
         for (int c = 0; c < NC; ++c) {
             const uint4 qv = rv ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
@@ -1174,7 +1176,7 @@ __global__ void __launch_bounds__(ws1::kThreads, Ws1Geo<D>::kCtasPerSm) paged_pr
             *reinterpret_cast<uint4*>(sm + QT + (c >> 3) * 16384 + tid * 128 + (((c & 7) ^ (tid & 7)) << 4)) =
                 make_uint4(f[0], f[1], f[2], f[3]);
         }
-        cs = a.score_scale * __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
+        cs = fabsf(a.score_scale) * __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
         pq = u.L - u.n + (rv ? r / G : 0);
         lq = (a.window > 0 && pq + 1 > a.window) ? pq + 1 - a.window : 0;
         const int wr0 = u.R0 + warp * 32;
@@ -1220,39 +1222,44 @@ __global__ void __launch_bounds__(ws1::kThreads, Ws1Geo<D>::kCtasPerSm) paged_pr
             tc::ld32(trow + S_COL + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
             tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv));
             tc::wait_ld(*reinterpret_cast<float(*)[32]>(sv + 32));
-            float mx = -INFINITY;
+            // cs >= 0: the maximum of the scaled scores is cs times the raw one
+            auto key_ok = [&](int j) {
+                const int key = t0 + j;
+                return j < np * kBS && rv && key >= lq && key <= pq;
+            };
+            float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (interior) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    sv[j] *= cs;
-                    mx = fmaxf(mx, sv[j]);
-                }
+                for (int j = 0; j < 64; ++j) mr[j & 3] = fmaxf(mr[j & 3], sv[j]);
             } else {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const int key = t0 + j;
-                    const bool valid = j < np * kBS && rv && key >= lq && key <= pq;
-                    sv[j] = valid ? sv[j] * cs : -INFINITY;
-                    mx = fmaxf(mx, sv[j]);
-                }
+                for (int j = 0; j < 64; ++j) mr[j & 3] = fmaxf(mr[j & 3], key_ok(j) ? sv[j] : -INFINITY);
             }
+            const float mraw = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
+            const float mx = mraw == -INFINITY ? -INFINITY : mraw * cs;
             const float mn = fmaxf(m, mx);
             const float muse = mn == -INFINITY ? 0.f : mn;
             const float alpha = fast_exp2(m - muse);
             m = mn;
-            float ls = 0.f;
+            float lp[4] = {0.f, 0.f, 0.f, 0.f};
+            auto emit = [&](auto pof) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t pw[4];
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t pw[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = fast_exp2(sv[8 * c + 2 * e] - muse), p1 = fast_exp2(sv[8 * c + 2 * e + 1] - muse);
-                    ls += p0 + p1;
-                    pw[e] = pack_f16x2(p0, p1);
+                    for (int e = 0; e < 4; ++e) {
+                        const float p0 = pof(8 * c + 2 * e), p1 = pof(8 * c + 2 * e + 1);
+                        lp[e] += p0 + p1;
+                        pw[e] = pack_f16x2(p0, p1);
+                    }
+                    *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
                 }
-                *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-            }
-            l = l * alpha + ls;
+            };
+            if (interior)
+                emit([&](int j) { return fast_exp2(fmaf(sv[j], cs, -muse)); });
+            else   // masked keys weigh 0 (also when cs = 0)
+                emit([&](int j) { return key_ok(j) ? fast_exp2(fmaf(sv[j], cs, -muse)) : 0.f; });
+            l = l * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
             tc::fence_proxy_async_smem();  // P is read by the tensor cores
             tc::fence_before_sync();
             mbar_arrive(&p_full);
