@@ -597,7 +597,8 @@ __global__ void __launch_bounds__(128) paged_prefill_tc_kernel(const Args a) {
 }
 
 // ---------------------------------------------------------------------------
-// The warp-specialised prefill kernel (d = 128, chunks of at least two tiles).
+// The warp-specialised prefill kernel (d = 64 and 128, chunks of at least two
+// tiles).
 //
 // A CTA takes two consecutive query tiles of one (kv head, sequence), 256
 // rows, and one key range, walked in stages of 128 keys (two staging
@@ -650,12 +651,13 @@ struct WsGeo {
     static constexpr int KT = QT + ws::kTiles * QTB;
     static constexpr int VT = KT + KTB;
     static constexpr int STG = VT + 2 * VTB;
-    static constexpr int SMEM = STG + ws::kStg * ws::kGran * GSLOT;   // 224 KB
+    static constexpr int SMEM = STG + ws::kStg * ws::kGran * GSLOT;   // 224 KB at d = 128, 112 KB at 64
     // TMEM per tile: S in [0, 128) (P written over its first 64 columns), the
-    // FP32 output accumulator in [d, 2d)
-    static constexpr uint32_t TC = 2 * D;
+    // FP32 output accumulator in [128, 128 + d)
+    static constexpr uint32_t OC = ws::kKeys;
+    static constexpr uint32_t TC = 256;
     static constexpr uint32_t COLS = ws::kTiles * TC;   // 512
-    static_assert(D == 128, "the warp-specialised kernel covers d = 128");
+    static_assert(D == 64 || D == 128, "the warp-specialised two-tile kernel covers d = 64 and 128");
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
@@ -823,7 +825,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
 #pragma unroll
             for (int j = 0; j < 32; ++j) z[j] = 0.f;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) tc::st32(trow + D + 32 * c, z);
+            for (int c = 0; c < D / 32; ++c) tc::st32(trow + Wg::OC + 32 * c, z);
             tc::wait_st();
         }
         for (int st = 0; st < nst; ++st) {
@@ -880,11 +882,11 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     float x[32];
-                    tc::ld32(trow + D + 32 * c, x);
+                    tc::ld32(trow + Wg::OC + 32 * c, x);
                     tc::wait_ld(x);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) x[j] *= alpha;
-                    tc::st32(trow + D + 32 * c, x);
+                    tc::st32(trow + Wg::OC + 32 * c, x);
                 }
             }
             const float nmuse = m == -INFINITY ? 0.f : -m;
@@ -986,7 +988,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
                 // O += P V: P (128 rows x 128 keys) from the S columns [0, 64)
 #pragma unroll
                 for (int ks = 0; ks < ws::kKeys / 16; ++ks)
-                    tc::mma_f16_ts(tm + i * Wg::TC + D, tm + i * Wg::TC + ks * 8,
+                    tc::mma_f16_ts(tm + i * Wg::TC + Wg::OC, tm + i * Wg::TC + ks * 8,
                                    tc::desc_k_sw128(sb + Wg::VT + (st & 1) * Wg::VTB + (ks >> 2) * Wg::VAT + (ks & 3) * 32),
                                    id_o, 1);
                 if (i == ws::kTiles - 1) tc::commit(&v_empty[st & 1]);   // the V^T tile is free when both tiles' P V complete
@@ -1027,7 +1029,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
             float x[32];
-            tc::ld32(trow + D + 32 * c, x);
+            tc::ld32(trow + Wg::OC + 32 * c, x);
             tc::wait_ld(x);
             if (!rv) continue;
             if (a.splits == 1) {
@@ -1514,8 +1516,8 @@ inline int tiles_of(int max_q_len, int G) {
 // (442 against 407 and 369 TFLOP/s at 2048-token chunks): its 56 KB of shared
 // memory let several CTAs share an SM.
 inline int kernel_kind(int D, int tiles) {
-    if (D == 128) return tiles >= 2 ? 1 : 0;
-    return D == 256 ? 2 : 0;
+    if (D == 256) return 2;
+    return tiles >= 2 ? 1 : 0;
 }
 inline int tiles_per_cta(int kind) { return kind == 1 ? ws::kTiles : 1; }
 
@@ -1542,7 +1544,7 @@ Plan make_plan(int batch, int max_q_len, int max_seq_len, int G, int Hkv, int D,
 // memory and its threads.
 template <int D, int G>
 void kernel_of(int kind, void (**fn)(const Args), size_t* smem, int* threads) {
-    if constexpr (D == 128) {
+    if constexpr (D == 64 || D == 128) {
         if (kind == 1) {
             *fn = paged_prefill_ws_kernel<D, G>;
             *smem = static_cast<size_t>(WsGeo<D>::SMEM) + 1024;
