@@ -11,22 +11,26 @@
 // FP32 registers).
 //
 // How: a unit is (tile of 128 query rows, kv head, sequence); a query row is
-// a (token, query head) pair of the kv head's group.  Two kernels on the
+// a (token, query head) pair of the kv head's group.  Three kernels on the
 // 5th-generation tensor cores (tcgen05.mma from swizzled f16 tiles in shared
-// memory, S and the P.V tile in tensor memory, one row per thread (TMEM lane)
-// for the online softmax):
-//  * paged_prefill_ws_kernel (d = 128, chunks of two or more tiles): two
-//    tiles per CTA and warp roles -- converter warps, one MMA-issuing thread,
-//    a softmax-and-fold warpgroup per tile -- that overlap through mbarriers;
-//  * paged_prefill_tc_kernel (d = 64 and 256, and single-tile chunks): one
-//    tile per CTA, its four warps taking each stage's steps in turn.
-// See the comments above them.  Each stage's P.V tile is computed in fresh
-// FP32 accumulators and folded into an FP32 output accumulator (O = O * alpha
-// + tile, IEEE FMA): registers at d <= 128 in the one-tile kernel, tensor
-// memory otherwise.  That is the two-level accumulation.  When the units are
-// too few to fill the GPU, each unit's key range is split over several CTAs
-// whose FP32 partials (row maximum, row sum, unnormalised output) a second
-// kernel merges (split plan: prefill_plan.h).
+// memory, S in tensor memory, one row per thread (TMEM lane) for the online
+// softmax):
+//  * paged_prefill_ws_kernel (d = 64 and 128, chunks of two or more tiles):
+//    two tiles per CTA, 128-key stages, and warp roles -- converter warps,
+//    one MMA-issuing thread, a softmax warpgroup per tile -- that overlap
+//    through mbarriers.  P goes to tensor memory as the value MMA's A
+//    operand, and the tensor cores carry O across stages in FP32;
+//  * paged_prefill_ws1_kernel (d = 256): one tile per CTA with the same kind
+//    of roles; each stage's P.V tile, computed in fresh FP32 accumulators, is
+//    folded into an FP32 accumulator in tensor memory (O = O * alpha + tile,
+//    IEEE FMA);
+//  * paged_prefill_tc_kernel (single-tile chunks at d = 64 and 128): one
+//    tile per CTA, its four warps taking each stage's steps in turn, the
+//    fold into registers.
+// See the comments above them.  When the units are too few to fill the GPU,
+// each unit's key range is split over several CTAs whose FP32 partials (row
+// maximum, row sum, unnormalised output) a second kernel merges (split plan:
+// prefill_plan.h).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -127,7 +131,8 @@ __device__ __forceinline__ bool make_unit(const Args& a, int b, int tile, bool r
 }
 
 // ---------------------------------------------------------------------------
-// The prefill kernel, on the 5th-generation tensor cores (tcgen05).
+// The one-tile prefill kernel, on the 5th-generation tensor cores (tcgen05):
+// single-tile chunks at d = 64 and 128 (written for d = 256 too).
 //
 // A unit is 128 query rows; thread t of the 4 warps owns row t, which is
 // TMEM lane t of both accumulators.  Per stage of 64 keys (4 pages):
@@ -1508,13 +1513,11 @@ inline int tiles_of(int max_q_len, int G) {
     return static_cast<int>((static_cast<int64_t>(max_q_len) * G + kRowsTC - 1) / kRowsTC);
 }
 
-// Which kernel runs: 1, the warp-specialised one with two tiles per CTA, at
-// d = 128 when a sequence's chunk spans at least two tiles; 2, the
-// warp-specialised one-tile kernel, at d = 256; else 0,
-// paged_prefill_tc_kernel, one tile per CTA.  At d = 64 the one-tile kernel
-// with its phases in turn measured faster than both warp-specialised ones
-// (442 against 407 and 369 TFLOP/s at 2048-token chunks): its 56 KB of shared
-// memory let several CTAs share an SM.
+// Which kernel runs: 2, the warp-specialised one-tile kernel, at d = 256;
+// 1, the warp-specialised one with two tiles per CTA, at d = 64 and 128 when
+// a sequence's chunk spans at least two tiles (at d = 64 it measured 617
+// against 442 TFLOP/s for the one-tile kernel at 2048-token chunks); else 0,
+// paged_prefill_tc_kernel, one tile per CTA.
 inline int kernel_kind(int D, int tiles) {
     if (D == 256) return 2;
     return tiles >= 2 ? 1 : 0;
