@@ -683,6 +683,24 @@ __device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
     return r != 0;
 }
 
+// Packed FP32 pairs (sm_100 family): d = a * b + c and d += a, lane by lane,
+// one instruction for two values.
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                          float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add_f32x2(float& d0, float& d1, float a0, float a1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1));
+}
+
 // A bounded mbarrier wait that also gives up as soon as another thread of the
 // CTA has given up (the shared abort flag); the first to run out sets it.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
@@ -905,10 +923,12 @@ __global__ void __launch_bounds__(ws::kThreads, 1) paged_prefill_ws_kernel(const
                 float pw[32];
                 if (interior) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float p0 = fast_exp2(fmaf(sv[2 * j], cs, nmuse));
-                        const float p1 = fast_exp2(fmaf(sv[2 * j + 1], cs, nmuse));
-                        lp[j & 3] += p0 + p1;
+                    for (int j = 0; j < 32; ++j) {   // key pairs in packed FP32 pairs
+                        float x0, x1;
+                        fma_f32x2(x0, x1, sv[2 * j], sv[2 * j + 1], cs, cs, nmuse, nmuse);
+                        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                        if (j & 1) add_f32x2(lp[2], lp[3], p0, p1);
+                        else add_f32x2(lp[0], lp[1], p0, p1);
                         pw[j] = __uint_as_float(pack_f16x2(p0, p1));
                     }
                 } else {
