@@ -1269,23 +1269,34 @@ __global__ void __launch_bounds__(ws1::kThreads, Ws1Geo<D>::kCtasPerSm) paged_pr
             const float alpha = fast_exp2(m - muse);
             m = mn;
             float lp[4] = {0.f, 0.f, 0.f, 0.f};
+            // pof(j, p0, p1): the weights of keys j and j + 1
             auto emit = [&](auto pof) {
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint32_t pw[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float p0 = pof(8 * c + 2 * e), p1 = pof(8 * c + 2 * e + 1);
-                        lp[e] += p0 + p1;
+                        float p0, p1;
+                        pof(8 * c + 2 * e, p0, p1);
+                        add_f32x2(lp[2 * (e & 1)], lp[2 * (e & 1) + 1], p0, p1);
                         pw[e] = pack_f16x2(p0, p1);
                     }
                     *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
                 }
             };
-            if (interior)
-                emit([&](int j) { return fast_exp2(fmaf(sv[j], cs, -muse)); });
-            else   // masked keys weigh 0 (also when cs = 0)
-                emit([&](int j) { return key_ok(j) ? fast_exp2(fmaf(sv[j], cs, -muse)) : 0.f; });
+            if (interior) {
+                emit([&](int j, float& p0, float& p1) {   // key pairs in packed FP32 pairs
+                    float x0, x1;
+                    fma_f32x2(x0, x1, sv[j], sv[j + 1], cs, cs, -muse, -muse);
+                    p0 = fast_exp2(x0);
+                    p1 = fast_exp2(x1);
+                });
+            } else {   // masked keys weigh 0 (also when cs = 0)
+                emit([&](int j, float& p0, float& p1) {
+                    p0 = key_ok(j) ? fast_exp2(fmaf(sv[j], cs, -muse)) : 0.f;
+                    p1 = key_ok(j + 1) ? fast_exp2(fmaf(sv[j + 1], cs, -muse)) : 0.f;
+                });
+            }
             l = l * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
             tc::fence_proxy_async_smem();  // P is read by the tensor cores
             tc::fence_before_sync();
